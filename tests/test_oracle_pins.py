@@ -1,0 +1,381 @@
+"""Pins for the fp64 oracle: things other than the oracle itself that fix
+its results -- worked examples printed on the pages, closed forms, a library
+routine on special cases (numpy.einsum), brute force on tiny inputs and
+mathematical invariants.  CPU only.
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import blocked, chains, worklist
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+# ------------------------------------------------------------ worked examples
+
+def test_ex38_worklist_matches_page():
+    g = gold("ex3_8_matmul_worklist.json")
+    wl = worklist.worklist(g["spec"], g["bounds"])
+    assert len(wl["tuples"]) == g["n_function_specs"]
+    assert len(wl["groups"]) == len(g["output_blocks"])
+    # F_{m,n}: A block (m-th interval of i, n-th of j) = id (m-1)*2+(n-1); B block = n-1.
+    for gi, members in enumerate(g["groups_as_mn"]):
+        got = wl["tuples"][wl["grp_ptr"][gi]:wl["grp_ptr"][gi + 1]]
+        want = [((m - 1) * 2 + (n - 1), n - 1) for m, n in members]
+        assert got == want
+    # output block keys: group id -> (i interval, k interval) -> lo/hi
+    for gi, ob in enumerate(wl["groups"]):
+        bi = ob  # k has one interval, so the output block id is the i interval
+        lo = [g["bounds"]["i"][bi], 0]
+        hi = [g["bounds"]["i"][bi + 1], 256]
+        assert {"lo": lo, "hi": hi} == g["output_blocks"][gi]
+
+
+@pytest.mark.parametrize("case", gold("matmul3d_volumes.json")["cases"])
+def test_matmul3d_closed_forms(case):
+    N, a, b, c = case["N"], case["a"], case["b"], case["c"]
+    wl = worklist.worklist("ij,jk->ik", {"i": oracle.near_equal_bounds(N, a), "j": oracle.near_equal_bounds(N, b),
+                                         "k": oracle.near_equal_bounds(N, c)})
+    assert len(wl["tuples"]) == case["tuples"] == a * b * c
+    assert wl["join_volume"] == case["join"] == (a + c) * N * N
+    assert wl["agg_volume"] == case["agg"] == (b - 1) * N * N
+    assert len(wl["groups"]) == a * c
+    assert all(wl["grp_ptr"][i + 1] - wl["grp_ptr"][i] == b for i in range(a * c))
+
+
+def test_ex54_overlay_atoms():
+    g = gold("ex5_4_overlay.json")
+    prod = [g["producer_row_bounds"], [0, g["cols"]]]
+    cons = [g["consumer_row_bounds"], [0, g["cols"]]]
+    ov = worklist.overlay(prod, cons)
+    assert ov[0] == g["overlay_row_splits"]
+    at = worklist.atoms(prod, cons)
+    assert len(at) == g["n_atoms"]
+    for i in range(len(g["producer_row_bounds"]) - 1):
+        lo, hi = g["producer_row_bounds"][i], g["producer_row_bounds"][i + 1]
+        inside = [a for a in at if a[0][0] >= lo and a[0][1] <= hi]
+        assert len(inside) == g["atoms_per_producer_block"]
+        assert sum(a[0][1] - a[0][0] for a in inside) == hi - lo
+
+
+def test_function_spec_count_is_product_of_intervals():
+    # Section 3.3: prod_s intervals[s] function specifications.
+    b = {"b": [0, 1, 2], "h": [0, 2, 3, 4], "s": [0, 5], "t": [0, 2, 4, 7], "d": [0, 3, 6]}
+    wl = worklist.worklist("bhsd,bhtd->bhst", b)
+    assert len(wl["tuples"]) == 2 * 3 * 1 * 3 * 2
+    assert len(wl["groups"]) == 2 * 3 * 1 * 3
+
+
+# ------------------------------------------- library routine special cases
+
+EINSUM_CASES = [
+    ("ij,jk->ik", [(5, 7), (7, 3)]),
+    ("ij,kj->ik", [(4, 6), (5, 6)]),
+    ("bhsd,bhtd->bhst", [(2, 3, 4, 5), (2, 3, 6, 5)]),
+    ("bhst,bhtd->bhsd", [(2, 2, 3, 4), (2, 2, 4, 5)]),
+    ("ij,j->i", [(4, 9), (9,)]),
+    ("i,j->ij", [(3,), (4,)]),
+    ("ij->j", [(6, 4)]),
+    ("ijk,kl,lm->im", [(2, 3, 4), (4, 5), (5, 2)]),
+    ("ij,ij->", [(3, 4), (3, 4)]),
+]
+
+
+@pytest.mark.parametrize("tier", ["lit", "idx"])
+@pytest.mark.parametrize("spec,shapes", EINSUM_CASES)
+def test_sum_product_equals_numpy_einsum(tier, spec, shapes):
+    r = rng(hash(spec) % 1000)
+    arrs = [r.standard_normal(s) for s in shapes]
+    got = oracle.joinagg(spec, arrs, "product", "sum", tier=tier)
+    want = np.einsum(spec, *arrs)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("tier", ["lit", "idx"])
+def test_max_aggregation_equals_numpy_max(tier):
+    a = rng(3).standard_normal((4, 5, 7))
+    got = oracle.joinagg("bst->bs", [a], "identity", "max", tier=tier)
+    np.testing.assert_array_equal(got, a.max(axis=2))
+
+
+def test_brute_force_dictionary_join_tiny():
+    """A dictionary-of-cells join written out by hand (Section 1's
+    degenerate relational form), independent of orc.c."""
+    r = rng(4)
+    A = r.integers(-3, 4, (3, 4)).astype(float)
+    B = r.integers(-3, 4, (4, 2)).astype(float)
+    RA = {(i, j): A[i, j] for i in range(3) for j in range(4)}
+    RB = {(j, k): B[j, k] for j in range(4) for k in range(2)}
+    groups = {}
+    for (i, j), va in RA.items():
+        for (j2, k), vb in RB.items():
+            if j == j2:
+                groups.setdefault((i, k), []).append(va * vb)
+    want = np.zeros((3, 2))
+    for (i, k), vals in groups.items():
+        want[i, k] = sum(vals)
+    for tier in ("lit", "idx"):
+        assert np.array_equal(oracle.joinagg("ij,jk->ik", [A, B], tier=tier), want)
+
+
+def test_integer_inputs_exact():
+    r = rng(5)
+    A = r.integers(-2, 3, (64, 96)).astype(float)
+    B = r.integers(-2, 3, (96, 80)).astype(float)
+    want = (A.astype(np.int64) @ B.astype(np.int64)).astype(float)
+    assert np.array_equal(oracle.joinagg("ij,jk->ik", [A, B], tier="lit"), want)
+    assert np.array_equal(oracle.joinagg("ij,jk->ik", [A, B], tier="idx"), want)
+
+
+def test_literal_join_counts_joined_tuples():
+    A = np.ones((3, 4))
+    B = np.ones((4, 5))
+    _, nj = oracle.joinagg("ij,jk->ik", [A, B], tier="lit", return_joined=True)
+    assert nj == 3 * 4 * 5
+
+
+# -------------------------------------------------- decomposition invariance
+
+PARTITIONS = [
+    {"i": [0, 10], "j": [0, 9], "k": [0, 8]},
+    {"i": [0, 3, 10], "j": [0, 4, 5, 9], "k": [0, 8]},
+    {"i": [0, 1, 2, 5, 10], "j": [0, 9], "k": [0, 2, 8]},
+    {"i": [0, 5, 10], "j": [0, 3, 6, 9], "k": [0, 4, 8]},
+]
+
+
+@pytest.mark.parametrize("parts", PARTITIONS)
+def test_block_decomposition_invariance_matmul(parts):
+    r = rng(6)
+    X = r.standard_normal((10, 9))
+    Y = r.standard_normal((9, 8))
+    cell = oracle.joinagg("ij,jk->ik", [X, Y])
+    blk = blocked.joinagg_blocked("ij,jk->ik", [X, Y], parts)
+    np.testing.assert_allclose(blk, cell, rtol=1e-12, atol=1e-12)
+    Xi = r.integers(-2, 3, (10, 9)).astype(float)
+    Yi = r.integers(-2, 3, (9, 8)).astype(float)
+    assert np.array_equal(blocked.joinagg_blocked("ij,jk->ik", [Xi, Yi], parts), oracle.joinagg("ij,jk->ik", [Xi, Yi]))
+
+
+def test_block_decomposition_invariance_max_and_causal():
+    r = rng(7)
+    Q = r.standard_normal((1, 2, 9, 3))
+    K = r.standard_normal((1, 2, 9, 3))
+    full = oracle.joinagg("bhsd,bhtd->bhst", [Q, K], pred="ts")
+    parts = {"b": [0, 1], "h": [0, 1, 2], "s": [0, 4, 9], "t": [0, 2, 5, 9], "d": [0, 1, 3]}
+    blk = blocked.joinagg_blocked("bhsd,bhtd->bhst", [Q, K], parts, pred="ts")
+    np.testing.assert_allclose(blk, full, rtol=1e-12, atol=1e-12, equal_nan=True)
+    m_full = oracle.joinagg("bhst->bhs", [full], "identity", "max")
+    m_blk = blocked.joinagg_blocked("bhst->bhs", [full], {"b": [0, 1], "h": [0, 2], "s": [0, 9], "t": [0, 3, 6, 9]},
+                                    "identity", "max")
+    assert np.array_equal(m_full, m_blk)
+
+
+# ------------------------------------------------------------- chain pins
+
+def _ref_masked_attention(Q, K, V, scale, causal):
+    S = np.einsum("bhsd,bhtd->bhst", Q, K) * scale
+    if causal:
+        n = S.shape[-1]
+        S = np.where(np.tril(np.ones((S.shape[-2], n), bool)), S, -np.inf)
+    P = np.exp(S - S.max(-1, keepdims=True))
+    P /= P.sum(-1, keepdims=True)
+    return P, np.einsum("bhst,bhtd->bhsd", P, V)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_against_library_softmax(causal):
+    r = rng(8)
+    Q, K, V = (r.standard_normal((2, 2, 7, 5)) for _ in range(3))
+    out = chains.softmax_attention(Q, K, V, scale=0.4, causal=causal)
+    P, O = _ref_masked_attention(Q, K, V, 0.4, causal)
+    np.testing.assert_allclose(out["O"], O, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(np.nan_to_num(out["P"]), P, rtol=1e-12, atol=1e-12)
+    if causal:
+        assert np.isnan(out["S"][0, 0, 0, 1]) and not np.isnan(out["S"][0, 0, 1, 0])
+
+
+def test_attention_invariants():
+    r = rng(9)
+    Q, K, V = (r.standard_normal((1, 3, 6, 4)) for _ in range(3))
+    out = chains.softmax_attention(Q, K, V)
+    np.testing.assert_allclose(np.nansum(out["P"], axis=-1), 1.0, rtol=1e-14)
+    ones = chains.softmax_attention(Q, K, np.ones_like(V))
+    np.testing.assert_allclose(ones["O"], 1.0, rtol=1e-14)
+    Ksame = np.repeat(K[:, :, :1, :], K.shape[2], axis=2)
+    same = chains.softmax_attention(Q, Ksame, V)
+    np.testing.assert_allclose(same["O"], np.broadcast_to(V.mean(axis=2, keepdims=True), V.shape), rtol=1e-12)
+
+
+def test_silu_special_values():
+    z = np.array([[0.0, 40.0, -40.0, 1.0]])
+    one = np.ones_like(z)
+    h = oracle.joinagg("ik,ik->ik", [z, one], "silu_mul", "none")
+    assert h[0, 0] == 0.0
+    assert abs(h[0, 1] - 40.0) < 1e-12 and abs(h[0, 2]) < 1e-15
+    assert abs(h[0, 3] - 1.0 / (1.0 + np.exp(-1.0))) < 1e-15
+
+
+def test_rmsnorm_invariant():
+    r = rng(10)
+    x = r.standard_normal((5, 16)) * 3.0
+    eps = 1e-6
+    out = chains.rmsnorm(x, np.ones(16), eps)
+    ms = (x ** 2).mean(axis=1)
+    np.testing.assert_allclose(out["ms"], ms, rtol=1e-14)
+    np.testing.assert_allclose((out["y"] ** 2).mean(axis=1), ms / (ms + eps), rtol=1e-12)
+
+
+def test_rope_invariants():
+    r = rng(11)
+    b, s, h, d = 1, 9, 2, 8
+    q = r.standard_normal((b, s, h, d))
+    k = r.standard_normal((b, s, h, d))
+    qr = chains.rope(q, 10000.0)
+    kr = chains.rope(k, 10000.0)
+    # norm of every pair is preserved
+    np.testing.assert_allclose(np.hypot(qr[..., 0::2], qr[..., 1::2]), np.hypot(q[..., 0::2], q[..., 1::2]), rtol=1e-12)
+    # identity at position 0
+    np.testing.assert_allclose(qr[:, 0], q[:, 0], rtol=0, atol=0)
+    # the score of positions (m, n) depends only on m - n: rotate the same vectors at shifted positions
+    qc = np.repeat(q[:, :1], s, axis=1)
+    kc = np.repeat(k[:, :1], s, axis=1)
+    qcr, kcr = chains.rope(qc, 10000.0), chains.rope(kc, 10000.0)
+    sc = np.einsum("bmhd,bnhd->bhmn", qcr, kcr)
+    for dlt in range(-3, 4):
+        vals = [sc[0, 0, m, m - dlt] for m in range(s) if 0 <= m - dlt < s]
+        np.testing.assert_allclose(vals, vals[0], rtol=1e-11)
+    # pair (0, 1) of position 1 is rotated by exactly 1 radian (theta^0)
+    want0 = q[0, 1, 0, 0] * np.cos(1.0) - q[0, 1, 0, 1] * np.sin(1.0)
+    assert abs(qr[0, 1, 0, 0] - want0) < 1e-14
+
+
+def _tiny_block_weights(D, F, seed, zero=()):
+    r = rng(seed)
+    W = {k: r.standard_normal(shape) * 0.2 for k, shape in
+         [("wq", (D, D)), ("wk", (D, D)), ("wv", (D, D)), ("wo", (D, D)), ("w_gate", (D, F)), ("w_up", (D, F)),
+          ("w_down", (F, D))]}
+    W["g1"] = np.ones(D)
+    W["g2"] = np.ones(D)
+    for k in zero:
+        W[k] = np.zeros_like(W[k])
+    return W
+
+
+def test_llama_block_residual_identity():
+    x = rng(12).standard_normal((1, 5, 8))
+    W = _tiny_block_weights(8, 12, 13, zero=("wo", "w_down"))
+    out = chains.llama_block(x, W, n_heads=2)
+    np.testing.assert_array_equal(out["y"], x)
+
+
+def test_llama_block_is_causal():
+    x = rng(14).standard_normal((1, 6, 8))
+    W = _tiny_block_weights(8, 12, 15)
+    y0 = chains.llama_block(x, W, n_heads=2)["y"]
+    x2 = x.copy()
+    x2[0, 4] += 1.0
+    y1 = chains.llama_block(x2, W, n_heads=2)["y"]
+    np.testing.assert_array_equal(y0[0, :4], y1[0, :4])
+    assert np.abs(y0[0, 4:] - y1[0, 4:]).max() > 1e-3
+
+
+def test_llama_block_prefix_sampling_is_exact():
+    """A prefix of the tokens of one sequence gives the same outputs as the
+    full sequence (causal attention only looks back) -- the property that
+    lets full-size parity sample early tokens."""
+    x = rng(16).standard_normal((2, 7, 8))
+    W = _tiny_block_weights(8, 12, 17)
+    full = chains.llama_block(x, W, n_heads=2)["y"]
+    pre = chains.llama_block(x[1:2, :3], W, n_heads=2)["y"]
+    np.testing.assert_allclose(pre[0], full[1, :3], rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------------ exchange
+
+def _dense_to_arena(a, bounds):
+    """Brute-force arena construction: blocks in row-major id order, each
+    block the row-major ravel of its slice."""
+    parts = []
+    for combo in itertools.product(*[range(len(b) - 1) for b in bounds]):
+        sl = tuple(slice(b[i], b[i + 1]) for b, i in zip(bounds, combo))
+        parts.append(a[sl].ravel())
+    return np.concatenate(parts) if parts else a.ravel()
+
+
+TILINGS = [
+    [[0, 12], [0, 10]],
+    [[0, 3, 6, 9, 12], [0, 10]],
+    [[0, 12], [0, 5, 10]],
+    [[0, 4, 8, 12], [0, 2, 7, 10]],
+    [[0, 1, 12], [0, 9, 10]],
+]
+
+
+@pytest.mark.parametrize("src", range(len(TILINGS)))
+@pytest.mark.parametrize("dst", range(len(TILINGS)))
+def test_exchange_matches_slicing_definition(src, dst):
+    a = np.arange(120, dtype=np.int32).reshape(12, 10) * 7 + 3
+    sa = _dense_to_arena(a, TILINGS[src])
+    got = oracle.exchange(sa, (12, 10), TILINGS[src], TILINGS[dst])
+    assert np.array_equal(got, _dense_to_arena(a, TILINGS[dst]))
+    perm = oracle.exchange_perm((12, 10), TILINGS[src], TILINGS[dst])
+    assert np.array_equal(np.sort(perm), np.arange(120))
+    assert np.array_equal(sa[perm], got)
+
+
+def test_exchange_roundtrip_and_composition_rank3():
+    a = np.arange(4 * 6 * 8, dtype=np.uint16).reshape(4, 6, 8)
+    A = [[0, 2, 4], [0, 6], [0, 8]]
+    B = [[0, 4], [0, 3, 6], [0, 2, 4, 8]]
+    C = [[0, 1, 2, 3, 4], [0, 1, 6], [0, 8]]
+    xa = _dense_to_arena(a, A)
+    xb = oracle.exchange(xa, a.shape, A, B)
+    assert np.array_equal(oracle.exchange(xb, a.shape, B, A), xa)
+    assert np.array_equal(oracle.exchange(xb, a.shape, B, C), oracle.exchange(xa, a.shape, A, C))
+
+
+# ---------------------------------------------- pins catch planted mistakes
+
+def test_pins_catch_planted_mistakes():
+    """Each pin must fail on a plausible oracle mistake planted here, on the
+    CPU: a dropped term, a transposed operand, a sign error in the exp map,
+    a missing causal predicate."""
+    r = rng(18)
+    A, B = r.standard_normal((5, 6)), r.standard_normal((6, 4))
+    want = np.einsum("ij,jk->ik", A, B)
+    dropped = oracle.joinagg("ij,jk->ik", [A[:, :5], B[:5, :]])
+    assert not np.allclose(dropped, want)
+    Bt = r.standard_normal((6, 6))
+    transposed = oracle.joinagg("ij,kj->ik", [A, Bt])
+    assert not np.allclose(transposed, np.einsum("ij,jk->ik", A, Bt))
+    Q, K, V = (r.standard_normal((1, 1, 5, 3)) for _ in range(3))
+    S = oracle.joinagg("bhsd,bhtd->bhst", [Q, K])
+    m = oracle.joinagg("bhst->bhs", [S], "identity", "max")
+    E_bad = np.exp(m[..., None] - S)  # exp(m - S) instead of exp(S - m)
+    P_ref, _ = _ref_masked_attention(Q, K, V, 1.0, False)
+    assert not np.allclose(E_bad / E_bad.sum(-1, keepdims=True), P_ref)
+    # without the predicate, a later token changes an earlier output
+    x = rng(19).standard_normal((1, 1, 4, 2))
+    x2 = x.copy()
+    x2[0, 0, 3] += 1.0
+    o1 = chains.softmax_attention(x, x, x, causal=False)["O"]
+    o2 = chains.softmax_attention(x2, x2, x2, causal=False)["O"]
+    assert not np.array_equal(o1[0, 0, 0], o2[0, 0, 0])
+    c1 = chains.softmax_attention(x, x, x, causal=True)["O"]
+    c2 = chains.softmax_attention(x2, x2, x2, causal=True)["O"]
+    assert np.array_equal(c1[0, 0, :3], c2[0, 0, :3])
