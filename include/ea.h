@@ -1,0 +1,265 @@
+/*
+ * ea.h -- C ABI of the GB300 (sm_103a) join-agg library (libea.so).
+ *
+ * The library executes the data-parallel hot path of Einsummable ("Every
+ * Kernel Is a Join: Automatic Multi-GPU Parallelism for AI Computations in
+ * Einsummable") on one GPU:
+ *   - tensor relations: sets of (sub-tensor key, sub-tensor) blocks
+ *     (Section 1; Definitions 3.1, 3.2);
+ *   - one join-agg: join the blocks of the inputs on shared index letters,
+ *     run a per-tuple kernel f, aggregate the outputs that share an output
+ *     block with SUM or MAX, recompose (Definitions 3.5-3.7, Section 3.3);
+ *   - the exchange: re-block a relation from one tiling to another through
+ *     the overlay of the two tilings (Section 5.3).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Plain C types only.  Pointers named dev_* / arena are device pointers;
+ *   all others are host pointers that the call reads (or writes, where
+ *   stated) before it returns and does not keep.
+ * - Every call returns an ea_status; EA_OK is 0.  On failure nothing is
+ *   launched, no output is written, and ea_last_error() returns a message
+ *   for the calling host thread.
+ * - GPU work is enqueued on the caller's CUDA stream (a cudaStream_t passed
+ *   as void*; NULL = the legacy default stream).  No call blocks the host
+ *   except ea_check().
+ * - A relation of rank r over dims[0..r-1] is tiled per dimension d into
+ *   nblocks[d] intervals [b_i, b_{i+1}) with 0 = b_0 <= ... <= b_n = dims[d]
+ *   (Definition 3.2: the blocks cover the tensor and are pairwise disjoint).
+ *   Blocks are numbered row-major over the block grid.  Each block is stored
+ *   row-major (its last dimension contiguous), and the blocks follow one
+ *   another in block-id order in one arena with no padding.  A block's key
+ *   is its tensor type: lower bounds lo[] (inclusive), upper bounds hi[]
+ *   (exclusive) (Definition 3.1).
+ * - Near-equal split (bounds == NULL): b_i = floor(i * n / k).
+ */
+#ifndef EA_H
+#define EA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define EA_ABI_VERSION 1
+
+typedef int ea_status;
+#define EA_OK 0
+#define EA_ERR_SPEC 1        /* malformed spec string or unsupported letter use    */
+#define EA_ERR_SHAPE 2       /* extents disagree between inputs / output           */
+#define EA_ERR_PARTITION 3   /* bounds do not tile, or partitions of a letter differ */
+#define EA_ERR_DTYPE 4       /* dtype not supported for this join-agg              */
+#define EA_ERR_ALLOC 5       /* device or host allocation failed                   */
+#define EA_ERR_CUDA 6        /* a CUDA runtime call failed (message has the name)  */
+#define EA_ERR_ARG 7         /* NULL pointer, bad count, bad enum value            */
+#define EA_ERR_UNSUPPORTED 8 /* valid join-agg this build has no kernel for        */
+#define EA_ERR_DEVICE 9      /* a kernel raised the device error flag (ea_check)   */
+
+typedef struct ea_relation_s *ea_relation; /* opaque handle */
+
+typedef enum { EA_F32 = 0, EA_BF16 = 1 } ea_dtype;
+
+/* Aggregation op (+) of Definition 3.7 step (2).  NONE: every output block
+ * receives exactly one tuple (elementwise joins). */
+typedef enum { EA_AGG_NONE = 0, EA_AGG_SUM = 1, EA_AGG_MAX = 2 } ea_agg;
+
+/* The per-tuple concrete operator f, applied cell by cell to the joined
+ * values v0, v1, v2 (inputs in spec order), computed in fp32:
+ *   PRODUCT     scale * v0 * v1 (* v2)          (SUM of PRODUCT = contraction)
+ *   IDENTITY    scale * v0
+ *   SILU_MUL    v0 / (1 + exp(-v0)) * v1
+ *   ADD         v0 + v1
+ *   EXP_SUB     exp(v0 - v1)
+ *   DIV         v0 / v1
+ *   SQUARE      scale * v0 * v0
+ *   RMS_APPLY   v0 * rsqrt(v1 + eps) * v2
+ *   EXP_SUB_DIV exp(v0 - v1) / v2              (softmax normalisation)
+ *   ROPE        rotation of interleaved pairs (2i, 2i+1) of the last letter
+ *               by the angle from rope_table at the position letter.       */
+typedef enum {
+    EA_MAP_PRODUCT = 0,
+    EA_MAP_IDENTITY = 1,
+    EA_MAP_SILU_MUL = 2,
+    EA_MAP_ADD = 3,
+    EA_MAP_EXP_SUB = 4,
+    EA_MAP_DIV = 5,
+    EA_MAP_SQUARE = 6,
+    EA_MAP_RMS_APPLY = 7,
+    EA_MAP_EXP_SUB_DIV = 8,
+    EA_MAP_ROPE = 9
+} ea_map;
+
+/* Tiling of one tensor dimension.  bounds: nblocks + 1 values, or NULL for
+ * the near-equal split.  Every interval must be non-empty unless the
+ * dimension's extent is 0 (then nblocks must be 1). */
+typedef struct {
+    int32_t nblocks;
+    int32_t reserved;
+    const int64_t *bounds;
+} ea_dim_part;
+
+/* Tiling of one index letter of a spec (Section 3.3: the intervals of a
+ * shardable index).  Same rules as ea_dim_part. */
+typedef struct {
+    char index; /* 'a'..'z' */
+    char reserved[3];
+    int32_t nblocks;
+    const int64_t *bounds;
+} ea_index_part;
+
+/* Options of ea_joinagg_run.  Zero-initialise, then set what is needed.
+ *   out_dtype  dtype of an output the call creates: 0 = the dtype of
+ *              input 0, otherwise 1 + ea_dtype (1 = fp32, 2 = bf16).
+ *   scale, eps map parameters (scale 0 is read as 1).
+ *   pred_lo, pred_hi  cell predicate: a joined tuple is kept only if the
+ *              value of letter pred_lo is <= the value of letter pred_hi
+ *              (causal attention: pred_lo='t', pred_hi='s').  0 = none.
+ *              Tuples of blocks that hold no such cell are dropped from the
+ *              work list.  Output cells the predicate removes are absent:
+ *              a contraction stores -inf in them, an elementwise join 0.
+ *              A contraction whose predicate names a contracted letter
+ *              relies on the operand holding 0 in removed cells.
+ *   rope_pos   ROPE: the position letter.
+ *   rope_table ROPE: device pointer, fp32 [rope_npos][d/2][2] = (cos, sin)
+ *              of angle pos * theta^(-2i/d).  Not owned.               */
+typedef struct {
+    int32_t out_dtype;
+    float scale;
+    float eps;
+    char pred_lo;
+    char pred_hi;
+    char rope_pos;
+    char reserved0;
+    const float *rope_table;
+    int64_t rope_npos;
+    int64_t reserved[4];
+} ea_opts;
+
+/* ------------------------------------------------------------ basics */
+
+int ea_abi_version(void);
+
+/* Last error message of the calling host thread ("" if none). */
+const char *ea_last_error(void);
+
+/* Synchronise `stream`, then report (and clear) any asynchronous CUDA error
+ * and the device error flag that kernels raise when a bounded wait runs out
+ * or a bounds check fails.  Returns EA_ERR_CUDA or EA_ERR_DEVICE on error. */
+ea_status ea_check(void *stream);
+
+/* Free every cached plan (work lists, tensor maps).  Synchronises the
+ * device first.  Plans are otherwise kept for the life of the process. */
+ea_status ea_plan_cache_clear(void);
+
+/* ------------------------------------------------------------ relations */
+
+/* Create a relation: a tensor of `dtype` and extents dims[0..rank-1]
+ * (1 <= rank <= 8) tiled by parts[0..rank-1] (Definitions 3.1, 3.2).
+ * dev_ptr: an existing device arena of at least prod(dims) * elemsize bytes
+ * in the layout described above, borrowed (the caller keeps it alive and
+ * frees it); NULL: the library allocates the arena with cudaMalloc and
+ * frees it in ea_relation_destroy.  The arena must be 16-byte aligned.
+ * *out receives the handle. */
+ea_status ea_relation_create(ea_dtype dtype, int rank, const int64_t *dims, const ea_dim_part *parts, void *dev_ptr,
+                             ea_relation *out);
+
+ea_status ea_relation_destroy(ea_relation rel);
+
+/* dtype, rank, extents (dims: room for 8) and block count. */
+ea_status ea_relation_info(ea_relation rel, int32_t *dtype, int32_t *rank, int64_t *dims, int64_t *nblocks);
+
+/* Block `block_id`: device pointer to its first element and its key
+ * (lo, hi: room for rank values each; either may be NULL). */
+ea_status ea_relation_block(ea_relation rel, int64_t block_id, void **dev_ptr, int64_t *lo, int64_t *hi);
+
+/* Arena pointer and size in bytes. */
+ea_status ea_relation_data(ea_relation rel, void **arena, size_t *bytes);
+
+/* Bounds of dimension `dim` (room for nblocks + 1 values). */
+ea_status ea_relation_bounds(ea_relation rel, int dim, int32_t *nblocks, int64_t *bounds);
+
+/* ------------------------------------------------------------ join-agg */
+
+/* Run one join-agg (Definition 3.7) on the GPU.
+ *   spec      einsum-style "ij,jk->ik": one term per input, letters a-z, no
+ *             letter twice in a term, every output letter in some input.
+ *             Letters in inputs but not in the output are aggregated.
+ *   inputs    n_inputs relations (1..3); term k's letters name the
+ *             dimensions of inputs[k] in order.
+ *   parts     optional per-letter tilings (may be NULL / 0).  A letter
+ *             without an entry takes the tiling of the inputs that hold it;
+ *             all inputs holding a letter must agree with each other and
+ *             with parts (else EA_ERR_PARTITION: re-block with ea_exchange).
+ *   agg, map  the aggregation op and the per-tuple operator.
+ *   opts      may be NULL (defaults).
+ *   out       in/out.  *out == NULL: the call creates the output relation
+ *             (extents from the letters, tiling from the letter tilings,
+ *             arena from cudaMalloc) and stores its handle; otherwise *out
+ *             must have the output's extents and tiling and is overwritten.
+ * Kernel classes, chosen from the spec, map and agg:
+ *   contraction  SUM of PRODUCT over two inputs with >= 1 aggregated letter:
+ *                grouped contraction, the SUM over a group's tuples fused in
+ *                the accumulator (bf16: tcgen05/TMEM/TMA; fp32: FFMA);
+ *   row reduction  SUM/MAX whose aggregated letters are the trailing
+ *                letters of input 0: one warp per output cell, warp-shuffle
+ *                (+) across the row and across the group's tuples;
+ *   elementwise  agg NONE: one output block per tuple, vectorised. */
+ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inputs, const ea_index_part *parts,
+                         int n_parts, ea_agg agg, ea_map map, const ea_opts *opts, void *stream, ea_relation *out);
+
+/* ------------------------------------------------------------ exchange */
+
+/* Re-block `in` into the tiling new_parts[0..rank-1] (Section 5.3: the
+ * overlay of the two tilings gives the atoms; each atom is copied from its
+ * source block into its destination block; every element keeps its global
+ * coordinates).  The copy is bit-exact.  *out == NULL: the call creates the
+ * output relation; otherwise *out must have the same dtype and extents and
+ * the tiling new_parts (new_parts may then be NULL), and must not share
+ * memory with `in`. */
+ea_status ea_exchange(ea_relation in, const ea_dim_part *new_parts, void *stream, ea_relation *out);
+
+/* What the last ea_joinagg_run / ea_exchange of the calling host thread
+ * launched: kernel class (0 exchange, 1 elementwise, 2 row reduction,
+ * 3 SIMT contraction, 4 tcgen05 contraction), kernel launches, work tiles,
+ * aggregation groups and function specifications (tuples).  Any pointer
+ * may be NULL. */
+ea_status ea_last_plan(int32_t *kernel_class, int32_t *launches, int64_t *tiles, int64_t *groups, int64_t *tuples);
+
+/* ------------------------------------------------ host-only planning hooks */
+
+/* The work list of a join-agg, computed on the host exactly as
+ * ea_joinagg_run plans it (no GPU needed).  shapes: the extents of every
+ * input term, concatenated; parts: one entry per letter that is not whole.
+ * pred_lo/pred_hi: the cell predicate letters or 0.
+ * Outputs (each may be NULL to ask only for the counts):
+ *   groups[n_groups]      output block id of each aggregation group
+ *   grp_ptr[n_groups+1]   CSR offsets into tuples
+ *   tuples[n_tuples*n_in] input block ids of each function specification
+ * Order: groups by increasing output block id (row-major over the output
+ * block grid); inside a group, by the interval indices of the aggregated
+ * letters in order of first appearance in the spec.
+ * join_volume: sum over tuples of the cells of their input blocks;
+ * agg_volume: sum over groups of (m - 1) * cells of the output block
+ * (the sub-costs (2) and (3) of Section 4.3).  Capacities cap_groups and
+ * cap_tuples bound what is written; EA_ERR_ARG if too small. */
+ea_status ea_plan_worklist(const char *spec, const int64_t *shapes, const ea_index_part *parts, int n_parts,
+                           char pred_lo, char pred_hi, int64_t cap_groups, int64_t cap_tuples, int64_t *groups,
+                           int64_t *grp_ptr, int64_t *tuples, int64_t *n_groups, int64_t *n_tuples,
+                           int64_t *join_volume, int64_t *agg_volume);
+
+/* The exchange as a permutation (no GPU needed): perm[i] = position in the
+ * source arena of the element at position i of the destination arena. */
+ea_status ea_exchange_permutation(int rank, const int64_t *dims, const ea_dim_part *src_parts,
+                                  const ea_dim_part *dst_parts, int64_t *perm);
+
+/* Number of atoms of the overlay of two tilings (Section 5.3). */
+ea_status ea_overlay_atoms(int rank, const int64_t *dims, const ea_dim_part *src_parts, const ea_dim_part *dst_parts,
+                           int64_t *n_atoms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EA_H */

@@ -1,0 +1,212 @@
+// ea_internal.h -- types shared by the host planner (host.cpp) and the CUDA
+// kernels of libea.so.  Not part of the public ABI (include/ea.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ea.h"
+
+namespace ea {
+
+constexpr int kMaxRank = 8;
+constexpr int kMaxIn = 3;
+constexpr int kViewDims = 6;  // outer (row) dimensions of an elementwise / row-reduction view
+
+// Error flag codes written by kernels into the device error word.
+enum DeviceErr : int {
+    kDevOk = 0,
+    kDevTimeoutProducer = 1,
+    kDevTimeoutMma = 2,
+    kDevTimeoutEpilogue = 3,
+    kDevBounds = 4,
+};
+
+// ---------------------------------------------------------------- exchange
+// One overlay atom (Section 5.3) copied as rows of a contiguous inner run.
+struct XSeg {
+    int64_t src_off;       // element offset of the atom origin in the source arena
+    int64_t dst_off;       // ... in the destination arena
+    int64_t inner;         // contiguous elements per row (merged trailing dims)
+    int64_t rows;          // product of ext[]
+    int64_t ext[4];        // outer extents, outermost first (unused = 1)
+    int64_t sstr[4];       // source strides of the outer dims (elements)
+    int64_t dstr[4];       // destination strides
+    int32_t nd;            // number of outer dims used
+    int32_t vec;           // 1: every row start and length is 16-byte aligned
+};
+
+struct XTile {
+    int32_t seg;
+    int32_t pad;
+    int64_t row0;   // rows [row0, row0 + nrows) of the segment ...
+    int64_t nrows;
+    int64_t col0;   // ... and inner elements [col0, col0 + ncols) of each row
+    int64_t ncols;
+};
+
+// ------------------------------------------------- elementwise / row reduce
+// A strided view of one tuple's blocks: output cells are addressed as
+// (row coordinates over `nd` outer dims) x (inner index < len).
+struct EwItem {
+    int64_t out_base;                  // element offsets into the arenas
+    int64_t in_base[kMaxIn];
+    int64_t len;                       // inner extent
+    int64_t rows;                      // product of ext[]
+    int64_t out_inner;                 // output stride along the inner dim (1 for elementwise)
+    int64_t in_inner[kMaxIn];          // input strides along the inner dim (0 = broadcast)
+    int64_t ext[kViewDims];
+    int64_t ostr[kViewDims];
+    int64_t istr[kMaxIn][kViewDims];
+    // Global coordinates of special letters (predicate lo, predicate hi, rope
+    // position): sdim = index of the outer dim holding it, kViewDims = the
+    // inner dim, -1 = constant (block extent 1); slo = global value at 0.
+    int32_t sdim[3];
+    int16_t vec;                       // 1: vectorised (16-byte) path is safe
+    int16_t nd;                        // outer dims in use
+    int64_t slo[3];
+    int64_t inner_lo;                  // global coordinate of inner index 0
+};
+
+struct EwTile {
+    int32_t item;
+    int32_t pad;
+    int64_t row0;   // rows [row0, row0 + nrows) ...
+    int64_t nrows;
+    int64_t col0;   // ... inner elements [col0, col0 + ncols)
+    int64_t ncols;
+};
+
+// Row reduction: items grouped per output block (CSR over items).
+struct RrGroup {
+    int32_t i0, i1;                    // items [i0, i1) of this output block
+    int32_t pad0, pad1;
+};
+
+struct RrTile {
+    int32_t group;
+    int32_t pad;
+    int64_t row0;
+    int64_t nrows;
+};
+
+// ------------------------------------------------------------ contraction
+// Generic (SIMT) grouped contraction: C[b][m][n] (+)= A[b][m][k] * B[b][k][n].
+struct CtGroup {
+    int64_t c_base;
+    int64_t M, N, nb;                  // extents; nb = batch extent
+    int64_t c_sm, c_sn, c_sb;          // output strides (elements)
+    int64_t m_lo, n_lo;                // global coordinates of m = 0, n = 0 (predicate)
+    int32_t t0, t1;                    // tuples [t0, t1)
+};
+
+struct CtTuple {
+    int64_t a_base, b_base;
+    int64_t K;
+    int64_t a_sm, a_sk, a_sb;
+    int64_t b_sk, b_sn, b_sb;
+};
+
+struct CtTile {
+    int32_t group;
+    int32_t batch;
+    int32_t m0;
+    int32_t n0;
+};
+
+// tcgen05 grouped contraction: operands are described by TMA tensor maps.
+struct TcGroup {
+    int32_t t0, t1;                    // tuples [t0, t1)
+    int32_t out_map;                   // tensor map index of the output block
+    int32_t n_ext;                     // N extent of the output block
+    int64_t m_lo, n_lo;                // predicate coordinates
+};
+
+struct TcTuple {
+    int32_t a_map, b_map;              // tensor map indices
+    int32_t kchunks;                   // ceil(K / 64)
+    int32_t pad;
+};
+
+struct TcTile {
+    int32_t group;
+    int32_t batch;
+    int32_t m0;
+    int32_t n0;
+};
+
+// ------------------------------------------------------------ launchers
+// Each returns cudaSuccess or the launch error.  All take a device error
+// word (int*) for bounded-wait / bounds failures.
+
+cudaError_t launch_exchange(const XSeg *segs, const XTile *tiles, int64_t ntiles, const char *src, char *dst,
+                            int esize, int num_sms, cudaStream_t st);
+
+struct EwParams {
+    const EwItem *items;
+    const EwTile *tiles;
+    int64_t ntiles;
+    const char *in[kMaxIn];
+    int in_dtype[kMaxIn];
+    char *out;
+    int out_dtype;
+    int n_in;
+    int map;
+    float scale, eps;
+    int pred;                          // 1: predicate active
+    const float *rope_table;
+    int64_t rope_npos;
+    int64_t rope_half;                 // pairs per position in rope_table
+    int has_vec, has_scalar;           // which kernel variants have tiles
+    int *err;
+};
+cudaError_t launch_ewise(const EwParams &p, int num_sms, cudaStream_t st);
+
+struct RrParams {
+    const EwItem *items;               // one per (group, tuple)
+    const RrGroup *groups;
+    const RrTile *tiles;
+    int64_t ntiles;
+    const char *in[kMaxIn];
+    int in_dtype[kMaxIn];
+    char *out;
+    int out_dtype;
+    int n_in;
+    int map;
+    int agg;
+    float scale, eps;
+    int pred;
+    int *err;
+};
+cudaError_t launch_rowreduce(const RrParams &p, int num_sms, cudaStream_t st);
+
+struct CtParams {
+    const CtGroup *groups;
+    const CtTuple *tuples;
+    const CtTile *tiles;
+    int64_t ntiles;
+    const char *a, *b;
+    char *c;
+    int a_dtype, b_dtype, c_dtype;
+    float scale;
+    int pred_mode;                     // 0 none; 1 mask n > m; 2 mask m > n
+};
+cudaError_t launch_contract_simt(const CtParams &p, cudaStream_t st);
+
+struct TcParams {
+    const void *tmaps;                 // device array of CUtensorMap (64-byte aligned)
+    const TcGroup *groups;
+    const TcTuple *tuples;
+    const TcTile *tiles;
+    int32_t ntiles;
+    int32_t a_mn_major, b_mn_major;
+    int32_t out_f32;
+    float scale;
+    int32_t pred_mode;
+    int32_t bn;                        // 128 or 256
+    int *err;
+};
+cudaError_t launch_contract_tc(const TcParams &p, int num_sms, cudaStream_t st);
+int tc_smem_bytes(int bn);
+
+}  // namespace ea

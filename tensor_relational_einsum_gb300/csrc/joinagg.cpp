@@ -1,0 +1,1211 @@
+// joinagg.cpp -- ea_joinagg_run and ea_exchange: plan a join-agg (or an
+// exchange) on the host, upload the plan once, cache it, launch the kernel.
+//
+// A join-agg ("Every Kernel Is a Join", Definition 3.7) is executed as:
+//   join       the canonical work list (plan_worklist): one function
+//              specification per combination of letter intervals, grouped
+//              by output block;
+//   aggregate  fused into the kernel that runs the group (the accumulator
+//              of a contraction, the warp reduction of a row reduction);
+//   recompose  zero-copy: the output relation is stored as its blocks.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <unordered_map>
+
+#include "host.h"
+
+namespace ea {
+
+// ----------------------------------------------------------- device context
+
+struct DevCtx {
+    bool init = false;
+    int num_sms = 0;
+    int *err = nullptr;  // device error word (kernels raise it; ea_check reads it)
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+};
+static DevCtx g_ctx[64];
+
+static ea_status get_ctx(DevCtx **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return set_error(EA_ERR_ARG, "device index %d out of range", dev);
+    DevCtx &c = g_ctx[dev];
+    if (!c.init) {
+        e = cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_error(e, "cudaDeviceGetAttribute");
+        e = cudaMalloc((void **)&c.err, 256);
+        if (e != cudaSuccess) return cuda_error(e, "cudaMalloc(error word)");
+        e = cudaMemset(c.err, 0, 256);
+        if (e != cudaSuccess) return cuda_error(e, "cudaMemset(error word)");
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e == cudaSuccess && q == cudaDriverEntryPointSuccess) c.encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+        else cudaGetLastError();
+        c.init = true;
+    }
+    *out = &c;
+    return EA_OK;
+}
+
+// --------------------------------------------------------------- plan blob
+
+struct Blob {
+    std::vector<char> h;
+    size_t add(const void *p, size_t n, size_t align = 128) {
+        size_t off = (h.size() + align - 1) / align * align;
+        h.resize(off + std::max<size_t>(n, 1));
+        if (n) memcpy(h.data() + off, p, n);
+        return off;
+    }
+    template <class T>
+    size_t add_vec(const std::vector<T> &v) {
+        return add(v.data(), v.size() * sizeof(T));
+    }
+};
+
+enum PlanKind { kExchange = 0, kEwise, kRowReduce, kSimt, kTc };
+
+struct DevPlan {
+    int kind = 0;
+    char *dev = nullptr;
+    char *pinned = nullptr;
+    size_t bytes = 0;
+    cudaEvent_t ready = nullptr;
+    cudaStream_t made_on = nullptr;
+    // exchange
+    XSeg *segs = nullptr;
+    XTile *xtiles = nullptr;
+    int64_t nxtiles = 0;
+    const char *xsrc = nullptr;
+    char *xdst = nullptr;
+    int esize = 0;
+    // kernels
+    EwParams ew{};
+    RrParams rr{};
+    CtParams ct{};
+    TcParams tc{};
+    int64_t n_groups = 0, n_tuples = 0;
+};
+
+struct LastPlan {
+    int32_t kind = -1, launches = 0;
+    int64_t tiles = 0, groups = 0, tuples = 0;
+};
+static thread_local LastPlan t_last;
+
+static std::unordered_map<std::string, DevPlan *> g_cache;
+
+static ea_status upload(const Blob &b, cudaStream_t st, DevPlan *p) {
+    p->bytes = b.h.size();
+    cudaError_t e = cudaMalloc((void **)&p->dev, p->bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(EA_ERR_ALLOC, "plan upload: cudaMalloc(%zu): %s", p->bytes, cudaGetErrorString(e));
+    }
+    e = cudaMallocHost((void **)&p->pinned, p->bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(EA_ERR_ALLOC, "plan upload: cudaMallocHost(%zu): %s", p->bytes, cudaGetErrorString(e));
+    }
+    memcpy(p->pinned, b.h.data(), p->bytes);
+    e = cudaMemcpyAsync(p->dev, p->pinned, p->bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_error(e, "plan upload: cudaMemcpyAsync");
+    e = cudaEventCreateWithFlags(&p->ready, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_error(e, "cudaEventCreate");
+    e = cudaEventRecord(p->ready, st);
+    if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord");
+    p->made_on = st;
+    return EA_OK;
+}
+
+static void free_plan(DevPlan *p) {
+    if (!p) return;
+    if (p->dev) cudaFree(p->dev);
+    if (p->pinned) cudaFreeHost(p->pinned);
+    if (p->ready) cudaEventDestroy(p->ready);
+    delete p;
+}
+
+static ea_status plan_ready_on(DevPlan *p, cudaStream_t st) {
+    if (st != p->made_on) {
+        cudaError_t e = cudaStreamWaitEvent(st, p->ready, 0);
+        if (e != cudaSuccess) return cuda_error(e, "cudaStreamWaitEvent(plan upload)");
+    }
+    return EA_OK;
+}
+
+// ------------------------------------------------------------- cache keys
+
+struct Key {
+    std::string s;
+    void raw(const void *p, size_t n) { s.append((const char *)p, n); }
+    template <class T>
+    void v(const T &x) {
+        raw(&x, sizeof x);
+    }
+    void str(const char *c) {
+        s.append(c);
+        s.push_back(0);
+    }
+    void rel(const ea_relation_s *r) {
+        v(r->dtype);
+        v(r->rank);
+        for (int d = 0; d < r->rank; d++) {
+            v(r->dims[d]);
+            int64_t n = (int64_t)r->bounds[d].size();
+            v(n);
+            raw(r->bounds[d].data(), n * sizeof(int64_t));
+        }
+        v(r->arena);
+    }
+};
+
+// ----------------------------------------------------------- block views
+
+struct BlockView {
+    int64_t base = 0;  // element offset of the block in its arena
+    int64_t lo[26], ext[26], str[26];
+    bool has[26];
+};
+
+static void view_of(const ea_relation_s *r, const std::string &term, int64_t bid, BlockView *v) {
+    int64_t iv[kMaxRank], lo[kMaxRank], ext[kMaxRank], str[kMaxRank];
+    block_coords(r, bid, iv);
+    block_box(r, iv, lo, ext);
+    row_major_strides(r->rank, ext, str);
+    for (int l = 0; l < 26; l++) {
+        v->has[l] = false;
+        v->lo[l] = 0;
+        v->ext[l] = 1;
+        v->str[l] = 0;
+    }
+    for (int d = 0; d < r->rank; d++) {
+        int l = term[d] - 'a';
+        v->has[l] = true;
+        v->lo[l] = lo[d];
+        v->ext[l] = ext[d];
+        v->str[l] = str[d];
+    }
+    v->base = r->blk_off[bid];
+}
+
+// Merge a group of letters (outer first) into one dimension for every
+// operand that holds them.  Extent-1 letters are dropped.
+struct Merged {
+    int64_t ext = 1;
+    int64_t str[3] = {0, 0, 0};
+    int single = -1;  // the only letter of extent > 1, if exactly one
+};
+
+static bool merge_letters(const std::string &letters, const BlockView *const *vs, int nv, Merged *m) {
+    std::string keep;
+    const BlockView *ref = nullptr;
+    for (int i = 0; i < nv; i++)
+        if (vs[i]) {
+            ref = vs[i];
+            break;
+        }
+    m->ext = 1;
+    for (int i = 0; i < 3; i++) m->str[i] = 0;
+    for (char c : letters) {
+        if (ref->ext[c - 'a'] == 0) {
+            m->ext = 0;  // empty block: nothing to merge
+            return true;
+        }
+        if (ref->ext[c - 'a'] > 1) keep.push_back(c);
+    }
+    m->single = keep.size() == 1 ? keep[0] - 'a' : -1;
+    if (keep.empty()) return true;
+    for (char c : keep) m->ext *= ref->ext[c - 'a'];
+    for (int i = 0; i < nv; i++) {
+        const BlockView *v = vs[i];
+        if (!v) continue;
+        for (size_t j = 0; j + 1 < keep.size(); j++) {
+            int a = keep[j] - 'a', b = keep[j + 1] - 'a';
+            if (v->str[a] != v->ext[b] * v->str[b]) return false;
+        }
+        m->str[i] = v->str[keep.back() - 'a'];
+    }
+    return true;
+}
+
+// ---------------------------------------------------------- tensor maps
+
+static ea_status encode_map(DevCtx *c, CUtensorMap *map, int dtype, const void *base, uint64_t d0, uint64_t d1,
+                            uint64_t d2, uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1) {
+    if (!c->encode) return set_error(EA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = c->encode(map, dtype == EA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                           const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(EA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return EA_OK;
+}
+
+static bool al16(int64_t elems, size_t es) { return ((uint64_t)elems * es) % 16 == 0; }
+
+// --------------------------------------------------------------- classes
+
+struct JoinCtx {
+    Spec sp;
+    const ea_relation_s *in[kMaxIn];
+    ea_relation_s *out;
+    LetterTilings lt;
+    WorkList wl;
+    ea_agg agg;
+    ea_map map;
+    float scale, eps;
+    char pred_lo, pred_hi;
+    const float *rope_table;
+    int64_t rope_npos;
+    char rope_pos;
+};
+
+// Special letters of an elementwise / row-reduction view.
+static void set_special(EwItem *it, int slot, char letter, const BlockView &ov, const int *dim_of_letter,
+                        int inner_letter) {
+    if (!letter) {
+        it->sdim[slot] = -1;
+        it->slo[slot] = 0;
+        return;
+    }
+    int l = letter - 'a';
+    it->slo[slot] = ov.lo[l];
+    if (l == inner_letter) it->sdim[slot] = kViewDims;
+    else if (dim_of_letter[l] >= 0) it->sdim[slot] = dim_of_letter[l];
+    else it->sdim[slot] = -1;
+}
+
+// Elementwise join: agg NONE, every tuple is one output block.
+static ea_status build_ewise(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan *p) {
+    const Spec &sp = j.sp;
+    int n_in = sp.n_in;
+    std::vector<EwItem> items;
+    std::vector<EwTile> tiles;
+    size_t es_out = elem_size(j.out->dtype);
+    for (size_t g = 0; g < j.wl.groups.size(); g++) {
+        int64_t t = j.wl.grp_ptr[g];
+        if (j.wl.grp_ptr[g + 1] - t != 1) return set_error(EA_ERR_SPEC, "agg NONE needs one tuple per output block");
+        BlockView ov, iv[kMaxIn];
+        view_of(j.out, sp.out, j.wl.groups[g], &ov);
+        for (int k = 0; k < n_in; k++) view_of(j.in[k], sp.term[k], j.wl.tuples[t * n_in + k], &iv[k]);
+        EwItem it;
+        memset(&it, 0, sizeof it);
+        int inner = sp.out.back() - 'a';
+        it.out_base = ov.base;
+        it.len = ov.ext[inner];
+        it.out_inner = ov.str[inner];
+        for (int k = 0; k < n_in; k++) {
+            it.in_base[k] = iv[k].base;
+            it.in_inner[k] = iv[k].has[inner] ? iv[k].str[inner] : 0;
+        }
+        // Row dims: the other output letters with extent > 1; merge neighbours
+        // when every operand agrees; never merge a special letter.
+        int dim_of_letter[26];
+        for (int l = 0; l < 26; l++) dim_of_letter[l] = -1;
+        int nd = 0;
+        char last_c = 0;
+        for (size_t d = 0; d + 1 < sp.out.size(); d++) {
+            char ch = sp.out[d];
+            int l = ch - 'a';
+            if (ov.ext[l] == 1) continue;
+            bool special = ch == j.pred_lo || ch == j.pred_hi || (j.map == EA_MAP_ROPE && ch == j.rope_pos);
+            bool prev_special = last_c && (last_c == j.pred_lo || last_c == j.pred_hi ||
+                                           (j.map == EA_MAP_ROPE && last_c == j.rope_pos));
+            bool can = nd > 0 && !special && !prev_special && it.ostr[nd - 1] == ov.ext[l] * ov.str[l];
+            for (int k = 0; k < n_in && can; k++) {
+                int64_t s = iv[k].has[l] ? iv[k].str[l] : 0;
+                can = it.istr[k][nd - 1] == ov.ext[l] * s;
+            }
+            if (can) {
+                it.ext[nd - 1] *= ov.ext[l];
+                it.ostr[nd - 1] = ov.str[l];
+                for (int k = 0; k < n_in; k++) it.istr[k][nd - 1] = iv[k].has[l] ? iv[k].str[l] : 0;
+            } else {
+                if (nd == kViewDims) return set_error(EA_ERR_UNSUPPORTED, "elementwise view needs more than 6 row dims");
+                it.ext[nd] = ov.ext[l];
+                it.ostr[nd] = ov.str[l];
+                for (int k = 0; k < n_in; k++) it.istr[k][nd] = iv[k].has[l] ? iv[k].str[l] : 0;
+                dim_of_letter[l] = nd;
+                nd++;
+            }
+            last_c = ch;
+        }
+        for (int d = nd; d < kViewDims; d++) it.ext[d] = 1;
+        it.nd = (int16_t)nd;
+        it.inner_lo = ov.lo[inner];
+        it.rows = 1;
+        for (int d = 0; d < kViewDims; d++) it.rows *= it.ext[d];
+        set_special(&it, 0, j.pred_lo, ov, dim_of_letter, inner);
+        set_special(&it, 1, j.pred_hi, ov, dim_of_letter, inner);
+        set_special(&it, 2, j.map == EA_MAP_ROPE ? j.rope_pos : 0, ov, dim_of_letter, inner);
+        bool vec = it.len % 8 == 0 && it.out_inner == 1 && it.out_base % 8 == 0;
+        for (int d = 0; d < nd; d++) vec = vec && it.ostr[d] % 8 == 0;
+        for (int k = 0; k < n_in; k++) {
+            if (it.in_inner[k] == 1) {
+                vec = vec && it.in_base[k] % 8 == 0;
+                for (int d = 0; d < nd; d++) vec = vec && it.istr[k][d] % 8 == 0;
+            } else if (it.in_inner[k] != 0) {
+                vec = false;
+            }
+        }
+        it.vec = vec ? 1 : 0;
+        if (j.map == EA_MAP_ROPE) {
+            if (it.in_inner[0] != 1 || it.len % 2 != 0 || ov.lo[inner] % 2 != 0)
+                return set_error(EA_ERR_UNSUPPORTED, "ROPE needs the pair letter last, contiguous, with even blocks");
+            if (!j.rope_table || it.sdim[2] == kViewDims)
+                return set_error(EA_ERR_ARG, "ROPE needs rope_table and a position letter other than the pair letter");
+            int64_t pos_hi = it.slo[2] + (it.sdim[2] >= 0 ? it.ext[it.sdim[2]] : 1);
+            int64_t pair_hi = (ov.lo[inner] + it.len) / 2;
+            if (pos_hi > j.rope_npos) return set_error(EA_ERR_ARG, "ROPE position beyond rope_npos");
+            (void)pair_hi;
+        }
+        int32_t id = (int32_t)items.size();
+        items.push_back(it);
+        if (it.rows == 0 || it.len == 0) continue;
+        // tiles of about 32K elements
+        const int64_t target = 32768;
+        if (it.len >= target) {
+            for (int64_t r = 0; r < it.rows; r++)
+                for (int64_t c0 = 0; c0 < it.len; c0 += target)
+                    tiles.push_back(EwTile{id, 0, r, 1, c0, std::min(target, it.len - c0)});
+        } else {
+            int64_t per = std::max<int64_t>(1, target / it.len);
+            for (int64_t r = 0; r < it.rows; r += per)
+                tiles.push_back(EwTile{id, 0, r, std::min(per, it.rows - r), 0, it.len});
+        }
+    }
+    (void)es_out;
+    (void)c;
+    Blob b;
+    size_t oi = b.add_vec(items), ot = b.add_vec(tiles);
+    ea_status s = upload(b, st, p);
+    if (s) return s;
+    p->kind = kEwise;
+    EwParams &e = p->ew;
+    e.items = (const EwItem *)(p->dev + oi);
+    e.tiles = (const EwTile *)(p->dev + ot);
+    e.ntiles = (int64_t)tiles.size();
+    for (int k = 0; k < n_in; k++) {
+        e.in[k] = j.in[k]->arena;
+        e.in_dtype[k] = j.in[k]->dtype;
+    }
+    e.out = j.out->arena;
+    e.out_dtype = j.out->dtype;
+    e.n_in = n_in;
+    e.map = j.map;
+    e.scale = j.scale;
+    e.eps = j.eps;
+    e.pred = j.pred_lo ? 1 : 0;
+    e.rope_table = j.rope_table;
+    e.rope_npos = j.rope_npos;
+    e.rope_half = j.lt.t[sp.out.back() - 'a'].extent / 2;
+    e.has_vec = e.has_scalar = 0;
+    for (const EwItem &x : items) {
+        if (x.rows == 0 || x.len == 0) continue;
+        if (x.vec) e.has_vec = 1;
+        else e.has_scalar = 1;
+    }
+    return EA_OK;
+}
+
+// Row reduction: the aggregated letters are the trailing letters of input 0.
+static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan *p) {
+    (void)c;
+    const Spec &sp = j.sp;
+    int n_in = sp.n_in;
+    const std::string &red = sp.contracted;
+    const std::string &t0 = sp.term[0];
+    if (t0.size() < red.size() || t0.substr(t0.size() - red.size()) != red)
+        return set_error(EA_ERR_UNSUPPORTED, "row reduction needs the aggregated letters last in input 0 (\"%s\")",
+                         t0.c_str());
+    for (int k = 1; k < n_in; k++) {
+        const std::string &tk = sp.term[k];
+        bool any = false;
+        for (char ch : red) any |= tk.find(ch) != std::string::npos;
+        if (any && (tk.size() < red.size() || tk.substr(tk.size() - red.size()) != red))
+            return set_error(EA_ERR_UNSUPPORTED, "row reduction: input %d must hold the aggregated letters last", k);
+    }
+    if ((j.pred_lo && red.find(j.pred_lo) != std::string::npos && red.size() != 1) ||
+        (j.pred_hi && red.find(j.pred_hi) != std::string::npos && red.size() != 1))
+        return set_error(EA_ERR_UNSUPPORTED, "a predicate on an aggregated letter needs a single aggregated letter");
+    std::vector<EwItem> items;
+    std::vector<RrGroup> groups;
+    std::vector<RrTile> tiles;
+    int inner_letter = red.size() == 1 ? red[0] - 'a' : -2;
+    for (size_t g = 0; g < j.wl.groups.size(); g++) {
+        BlockView ov;
+        view_of(j.out, sp.out, j.wl.groups[g], &ov);
+        RrGroup G{(int32_t)items.size(), 0, 0, 0};
+        int64_t rows = 1;
+        for (int64_t t = j.wl.grp_ptr[g]; t < j.wl.grp_ptr[g + 1]; t++) {
+            BlockView iv[kMaxIn];
+            for (int k = 0; k < n_in; k++) view_of(j.in[k], sp.term[k], j.wl.tuples[t * n_in + k], &iv[k]);
+            EwItem it;
+            memset(&it, 0, sizeof it);
+            it.out_base = ov.base;
+            it.len = 1;
+            for (char ch : red) it.len *= iv[0].ext[ch - 'a'];
+            it.out_inner = 0;
+            for (int k = 0; k < n_in; k++) {
+                it.in_base[k] = iv[k].base;
+                it.in_inner[k] = iv[k].has[red.back() - 'a'] ? 1 : 0;
+            }
+            int dim_of_letter[26];
+            for (int l = 0; l < 26; l++) dim_of_letter[l] = -1;
+            int nd = 0;
+            for (char ch : sp.out) {
+                int l = ch - 'a';
+                if (ov.ext[l] == 1) continue;
+                if (nd == kViewDims) return set_error(EA_ERR_UNSUPPORTED, "row reduction with more than 6 row dims");
+                it.ext[nd] = ov.ext[l];
+                it.ostr[nd] = ov.str[l];
+                for (int k = 0; k < n_in; k++) it.istr[k][nd] = iv[k].has[l] ? iv[k].str[l] : 0;
+                dim_of_letter[l] = nd;
+                nd++;
+            }
+            for (int d = nd; d < kViewDims; d++) it.ext[d] = 1;
+            it.nd = (int16_t)nd;
+            it.inner_lo = iv[0].lo[red.back() - 'a'];
+            it.rows = 1;
+            for (int d = 0; d < kViewDims; d++) it.rows *= it.ext[d];
+            rows = it.rows;
+            // predicate letters may live in the input only (the reduced letter)
+            BlockView pv = iv[0];
+            for (int l = 0; l < 26; l++)
+                if (!pv.has[l] && ov.has[l]) pv.lo[l] = ov.lo[l];
+            set_special(&it, 0, j.pred_lo, pv, dim_of_letter, inner_letter);
+            set_special(&it, 1, j.pred_hi, pv, dim_of_letter, inner_letter);
+            it.sdim[2] = -1;
+            bool vec = it.len % 8 == 0;
+            for (int k = 0; k < n_in; k++)
+                if (it.in_inner[k] == 1) {
+                    vec = vec && it.in_base[k] % 8 == 0;
+                    for (int d = 0; d < nd; d++) vec = vec && it.istr[k][d] % 8 == 0;
+                }
+            it.vec = vec ? 1 : 0;
+            items.push_back(it);
+        }
+        G.i1 = (int32_t)items.size();
+        int32_t gid = (int32_t)groups.size();
+        groups.push_back(G);
+        const int64_t per = 64;
+        for (int64_t r = 0; r < rows; r += per) tiles.push_back(RrTile{gid, 0, r, std::min(per, rows - r)});
+    }
+    Blob b;
+    size_t oi = b.add_vec(items), og = b.add_vec(groups), ot = b.add_vec(tiles);
+    ea_status s = upload(b, st, p);
+    if (s) return s;
+    p->kind = kRowReduce;
+    RrParams &r = p->rr;
+    r.items = (const EwItem *)(p->dev + oi);
+    r.groups = (const RrGroup *)(p->dev + og);
+    r.tiles = (const RrTile *)(p->dev + ot);
+    r.ntiles = (int64_t)tiles.size();
+    for (int k = 0; k < n_in; k++) {
+        r.in[k] = j.in[k]->arena;
+        r.in_dtype[k] = j.in[k]->dtype;
+    }
+    r.out = j.out->arena;
+    r.out_dtype = j.out->dtype;
+    r.n_in = n_in;
+    r.map = j.map;
+    r.agg = j.agg;
+    r.scale = j.scale;
+    r.eps = j.eps;
+    r.pred = j.pred_lo ? 1 : 0;
+    return EA_OK;
+}
+
+// Contraction: letters grouped as batch (A, B, C), M (A, C), N (B, C), K (A, B).
+struct ContractionViews {
+    std::string batch, M, N, K;
+};
+
+static ea_status contraction_roles(const Spec &sp, ContractionViews *cv) {
+    const std::string &A = sp.term[0], &B = sp.term[1], &C = sp.out;
+    for (char ch : C) {
+        bool a = A.find(ch) != std::string::npos, b = B.find(ch) != std::string::npos;
+        if (a && b) cv->batch.push_back(ch);
+        else if (a) cv->M.push_back(ch);
+        else cv->N.push_back(ch);
+    }
+    for (char ch : A) {
+        bool b = B.find(ch) != std::string::npos, c = C.find(ch) != std::string::npos;
+        if (!c && b) cv->K.push_back(ch);
+        if (!c && !b) return set_error(EA_ERR_UNSUPPORTED, "letter '%c' is aggregated within input 0 only", ch);
+    }
+    for (char ch : B)
+        if (C.find(ch) == std::string::npos && A.find(ch) == std::string::npos)
+            return set_error(EA_ERR_UNSUPPORTED, "letter '%c' is aggregated within input 1 only", ch);
+    return EA_OK;
+}
+
+struct TupleGeom {
+    Merged bt, m, n, k;
+    BlockView a, b, c;
+};
+
+static ea_status tuple_geom(const JoinCtx &j, const ContractionViews &cv, int64_t g, int64_t t, TupleGeom *tg) {
+    view_of(j.in[0], j.sp.term[0], j.wl.tuples[t * 2 + 0], &tg->a);
+    view_of(j.in[1], j.sp.term[1], j.wl.tuples[t * 2 + 1], &tg->b);
+    view_of(j.out, j.sp.out, j.wl.groups[g], &tg->c);
+    const BlockView *abc[3] = {&tg->a, &tg->b, &tg->c};
+    const BlockView *ac[3] = {&tg->a, nullptr, &tg->c};
+    const BlockView *bc[3] = {nullptr, &tg->b, &tg->c};
+    const BlockView *ab[3] = {&tg->a, &tg->b, nullptr};
+    if (!merge_letters(cv.batch, abc, 3, &tg->bt) || !merge_letters(cv.M, ac, 3, &tg->m) ||
+        !merge_letters(cv.N, bc, 3, &tg->n) || !merge_letters(cv.K, ab, 3, &tg->k))
+        return set_error(EA_ERR_UNSUPPORTED, "contraction: a letter group is not contiguous in every operand");
+    return EA_OK;
+}
+
+static int pred_mode_of(const JoinCtx &j, const ContractionViews &cv, int *kpred) {
+    *kpred = 0;
+    if (!j.pred_lo) return 0;
+    auto in = [](const std::string &s, char ch) { return s.find(ch) != std::string::npos; };
+    if (in(cv.K, j.pred_lo) || in(cv.K, j.pred_hi)) {
+        *kpred = 1;  // block filter only; removed cells must hold 0 in the operand
+        return 0;
+    }
+    if (in(cv.N, j.pred_lo) && in(cv.M, j.pred_hi)) return 1;  // mask cells with n > m
+    if (in(cv.M, j.pred_lo) && in(cv.N, j.pred_hi)) return 2;  // mask cells with m > n
+    return -1;
+}
+
+static ea_status build_simt(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cudaStream_t st, DevPlan *p) {
+    (void)c;
+    int kpred = 0;
+    int mode = pred_mode_of(j, cv, &kpred);
+    if (mode < 0) return set_error(EA_ERR_UNSUPPORTED, "contraction: predicate letters must be output letters");
+    std::vector<CtGroup> groups;
+    std::vector<CtTuple> tuples;
+    std::vector<CtTile> tiles;
+    for (size_t g = 0; g < j.wl.groups.size(); g++) {
+        CtGroup G;
+        memset(&G, 0, sizeof G);
+        G.t0 = (int32_t)tuples.size();
+        for (int64_t t = j.wl.grp_ptr[g]; t < j.wl.grp_ptr[g + 1]; t++) {
+            TupleGeom tg;
+            ea_status s = tuple_geom(j, cv, (int64_t)g, t, &tg);
+            if (s) return s;
+            if (t == j.wl.grp_ptr[g]) {
+                G.c_base = tg.c.base;
+                G.M = tg.m.ext;
+                G.N = tg.n.ext;
+                G.nb = tg.bt.ext;
+                G.c_sm = tg.m.str[2];
+                G.c_sn = tg.n.str[2];
+                G.c_sb = tg.bt.str[2];
+                if (mode) {
+                    int lm = mode == 1 ? j.pred_hi - 'a' : j.pred_lo - 'a';
+                    int ln = mode == 1 ? j.pred_lo - 'a' : j.pred_hi - 'a';
+                    if ((tg.m.single >= 0 && tg.m.single != lm) || (tg.n.single >= 0 && tg.n.single != ln) ||
+                        (tg.m.single < 0 && tg.m.ext > 1) || (tg.n.single < 0 && tg.n.ext > 1))
+                        return set_error(EA_ERR_UNSUPPORTED, "contraction predicate needs single-letter M and N");
+                    G.m_lo = tg.c.lo[lm];
+                    G.n_lo = tg.c.lo[ln];
+                }
+            }
+            CtTuple T;
+            T.a_base = tg.a.base;
+            T.b_base = tg.b.base;
+            T.K = tg.k.ext;
+            T.a_sm = tg.m.str[0];
+            T.a_sk = tg.k.str[0];
+            T.a_sb = tg.bt.str[0];
+            T.b_sk = tg.k.str[1];
+            T.b_sn = tg.n.str[1];
+            T.b_sb = tg.bt.str[1];
+            tuples.push_back(T);
+        }
+        G.t1 = (int32_t)tuples.size();
+        int32_t gid = (int32_t)groups.size();
+        groups.push_back(G);
+        for (int64_t bb = 0; bb < G.nb; bb++)
+            for (int64_t n0 = 0; n0 < G.N; n0 += 64)
+                for (int64_t m0 = 0; m0 < G.M; m0 += 64)
+                    tiles.push_back(CtTile{gid, (int32_t)bb, (int32_t)m0, (int32_t)n0});
+    }
+    Blob b;
+    size_t og = b.add_vec(groups), ou = b.add_vec(tuples), ot = b.add_vec(tiles);
+    ea_status s = upload(b, st, p);
+    if (s) return s;
+    p->kind = kSimt;
+    CtParams &q = p->ct;
+    q.groups = (const CtGroup *)(p->dev + og);
+    q.tuples = (const CtTuple *)(p->dev + ou);
+    q.tiles = (const CtTile *)(p->dev + ot);
+    q.ntiles = (int64_t)tiles.size();
+    q.a = j.in[0]->arena;
+    q.b = j.in[1]->arena;
+    q.c = j.out->arena;
+    q.a_dtype = j.in[0]->dtype;
+    q.b_dtype = j.in[1]->dtype;
+    q.c_dtype = j.out->dtype;
+    q.scale = j.scale;
+    q.pred_mode = mode;
+    return EA_OK;
+}
+
+// tcgen05 path: bf16 operands whose blocks TMA can tile.  Returns
+// EA_ERR_UNSUPPORTED (no message) when the SIMT kernel has to run instead.
+struct TcOp {
+    int64_t base, M, K, nb, s_m, s_k, s_b;  // viewed as [nb][M][K] (M = N for operand B)
+    const ea_relation_s *rel;
+};
+
+static int64_t outer_stride(const TcOp &o, int mn) {
+    // stride of the non-contiguous dimension of a 2-D tile, packed if extent 1
+    if (!mn) return o.s_m ? o.s_m : o.K;
+    return o.s_k ? o.s_k : o.M;
+}
+
+static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cudaStream_t st, DevPlan *p) {
+    if (j.in[0]->dtype != EA_BF16 || j.in[1]->dtype != EA_BF16) return EA_ERR_UNSUPPORTED;
+    if (!c->encode) return EA_ERR_UNSUPPORTED;
+    int kpred = 0;
+    int mode = pred_mode_of(j, cv, &kpred);
+    if (mode < 0) return EA_ERR_UNSUPPORTED;
+    const size_t es = 2, esc = elem_size(j.out->dtype);
+    struct GroupGeom {
+        int64_t c_base, M, N, nb, c_sm, c_sb, m_lo, n_lo;
+        int64_t t0, t1;
+    };
+    std::vector<GroupGeom> gg;
+    std::vector<std::pair<TcOp, TcOp>> tg_ops;
+    bool swap = false;
+    int a_mn = -1, b_mn = -1;
+    int64_t maxN = 0;
+    // ---- pass 1: geometry of every tuple; roles and majorness must agree
+    for (size_t g = 0; g < j.wl.groups.size(); g++) {
+        GroupGeom G{};
+        G.t0 = (int64_t)tg_ops.size();
+        for (int64_t t = j.wl.grp_ptr[g]; t < j.wl.grp_ptr[g + 1]; t++) {
+            TupleGeom tg;
+            if (tuple_geom(j, cv, (int64_t)g, t, &tg)) return EA_ERR_UNSUPPORTED;
+            if (tg.k.ext == 0) return EA_ERR_UNSUPPORTED;
+            TcOp A{tg.a.base, tg.m.ext, tg.k.ext, tg.bt.ext, tg.m.str[0], tg.k.str[0], tg.bt.str[0], j.in[0]};
+            TcOp B{tg.b.base, tg.n.ext, tg.k.ext, tg.bt.ext, tg.n.str[1], tg.k.str[1], tg.bt.str[1], j.in[1]};
+            int64_t M = tg.m.ext, N = tg.n.ext, c_sm = tg.m.str[2], c_sn = tg.n.str[2];
+            int64_t m_lo = 0, n_lo = 0;
+            if (mode) {
+                int lm = mode == 1 ? j.pred_hi - 'a' : j.pred_lo - 'a';
+                int ln = mode == 1 ? j.pred_lo - 'a' : j.pred_hi - 'a';
+                if ((tg.m.single >= 0 && tg.m.single != lm) || (tg.n.single >= 0 && tg.n.single != ln) ||
+                    (tg.m.single < 0 && tg.m.ext > 1) || (tg.n.single < 0 && tg.n.ext > 1))
+                    return EA_ERR_UNSUPPORTED;
+                m_lo = tg.c.lo[lm];
+                n_lo = tg.c.lo[ln];
+            }
+            bool sw = !(c_sn == 1 || N == 1);
+            if (sw && !(c_sm == 1 || M == 1)) return EA_ERR_UNSUPPORTED;
+            if (tg_ops.empty()) swap = sw;
+            if (sw != swap) return EA_ERR_UNSUPPORTED;
+            if (swap) {
+                std::swap(A, B);
+                std::swap(M, N);
+                std::swap(c_sm, c_sn);
+                std::swap(m_lo, n_lo);
+            }
+            auto major = [](const TcOp &o) -> int {
+                if (o.s_k == 1 || o.K == 1) return 0;
+                if (o.s_m == 1 || o.M == 1) return 1;
+                return -1;
+            };
+            int am = major(A), bm = major(B);
+            if (am < 0 || bm < 0) return EA_ERR_UNSUPPORTED;
+            if (a_mn < 0) {
+                a_mn = am;
+                b_mn = bm;
+            }
+            if (am != a_mn || bm != b_mn) return EA_ERR_UNSUPPORTED;
+            auto tma_ok = [&](const TcOp &o, int mn) {
+                int64_t row = outer_stride(o, mn);
+                int64_t bstr = o.nb > 1 ? o.s_b : row * (mn ? o.K : o.M);
+                return al16(o.base, es) && al16(row, es) && al16(bstr, es);
+            };
+            if (!tma_ok(A, a_mn) || !tma_ok(B, b_mn)) return EA_ERR_UNSUPPORTED;
+            int64_t crow = c_sm ? c_sm : N;
+            int64_t cb = A.nb > 1 ? tg.bt.str[2] : crow * M;
+            if (!al16(tg.c.base, esc) || !al16(crow, esc) || !al16(cb, esc)) return EA_ERR_UNSUPPORTED;
+            if (t == j.wl.grp_ptr[g]) {
+                G.c_base = tg.c.base;
+                G.M = M;
+                G.N = N;
+                G.nb = A.nb;
+                G.c_sm = crow;
+                G.c_sb = cb;
+                G.m_lo = m_lo;
+                G.n_lo = n_lo;
+            }
+            tg_ops.push_back({A, B});
+            maxN = std::max(maxN, N);
+        }
+        G.t1 = (int64_t)tg_ops.size();
+        gg.push_back(G);
+    }
+    if (tg_ops.empty()) return EA_ERR_UNSUPPORTED;
+    const int bn = maxN <= 128 ? 128 : 256;
+    if (mode && swap) mode = 3 - mode;  // the mask is stated in the swapped roles
+    // ---- pass 2: tensor maps, tuples, tiles
+    std::vector<CUtensorMap> maps;
+    std::vector<TcGroup> groups;
+    std::vector<TcTuple> tuples;
+    std::vector<TcTile> tiles;
+    std::unordered_map<int64_t, int32_t> cache_a, cache_b;
+    auto op_map = [&](const TcOp &o, int mn, int box_rows, std::unordered_map<int64_t, int32_t> &cache,
+                      int32_t *id) -> ea_status {
+        auto it = cache.find(o.base);
+        if (it != cache.end()) {
+            *id = it->second;
+            return EA_OK;
+        }
+        CUtensorMap m;
+        int64_t row = outer_stride(o, mn);
+        int64_t bstr = o.nb > 1 ? o.s_b : row * (mn ? o.K : o.M);
+        const void *ptr = o.rel->arena + o.base * es;
+        ea_status s = !mn ? encode_map(c, &m, EA_BF16, ptr, o.K, o.M, o.nb, row * es, bstr * es, 64, box_rows)
+                          : encode_map(c, &m, EA_BF16, ptr, o.M, o.K, o.nb, row * es, bstr * es, 64, 64);
+        if (s) return s;
+        *id = (int32_t)maps.size();
+        maps.push_back(m);
+        cache[o.base] = *id;
+        return EA_OK;
+    };
+    for (size_t g = 0; g < gg.size(); g++) {
+        const GroupGeom &G = gg[g];
+        TcGroup TG;
+        memset(&TG, 0, sizeof TG);
+        TG.t0 = (int32_t)tuples.size();
+        TG.m_lo = G.m_lo;
+        TG.n_lo = G.n_lo;
+        bool empty = G.M == 0 || G.N == 0 || G.nb == 0;
+        for (int64_t t = G.t0; t < G.t1 && !empty; t++) {
+            const TcOp &A = tg_ops[t].first, &B = tg_ops[t].second;
+            TcTuple T;
+            memset(&T, 0, sizeof T);
+            ea_status s = op_map(A, a_mn, 128, cache_a, &T.a_map);
+            if (s) return s;
+            s = op_map(B, b_mn, bn, cache_b, &T.b_map);
+            if (s) return s;
+            T.kchunks = (int32_t)((A.K + 63) / 64);
+            tuples.push_back(T);
+        }
+        TG.t1 = (int32_t)tuples.size();
+        TG.n_ext = (int32_t)G.N;
+        if (empty) continue;
+        CUtensorMap m;
+        const void *cptr = j.out->arena + G.c_base * esc;
+        ea_status s = encode_map(c, &m, j.out->dtype, cptr, G.N, G.M, G.nb, G.c_sm * esc, G.c_sb * esc,
+                                 (uint32_t)(128 / esc), 128);
+        if (s) return s;
+        TG.out_map = (int32_t)maps.size();
+        maps.push_back(m);
+        int32_t gid = (int32_t)groups.size();
+        groups.push_back(TG);
+        for (int64_t bb = 0; bb < G.nb; bb++)
+            for (int64_t n0 = 0; n0 < G.N; n0 += bn)
+                for (int64_t m0 = 0; m0 < G.M; m0 += 128)
+                    tiles.push_back(TcTile{gid, (int32_t)bb, (int32_t)m0, (int32_t)n0});
+    }
+    if (tiles.size() > (size_t)INT32_MAX) return EA_ERR_UNSUPPORTED;
+    Blob b;
+    size_t om = b.add(maps.data(), maps.size() * sizeof(CUtensorMap), 128);
+    size_t og = b.add_vec(groups), ou = b.add_vec(tuples), ot = b.add_vec(tiles);
+    ea_status s = upload(b, st, p);
+    if (s) return s;
+    p->kind = kTc;
+    TcParams &q = p->tc;
+    q.tmaps = p->dev + om;
+    q.groups = (const TcGroup *)(p->dev + og);
+    q.tuples = (const TcTuple *)(p->dev + ou);
+    q.tiles = (const TcTile *)(p->dev + ot);
+    q.ntiles = (int32_t)tiles.size();
+    q.a_mn_major = a_mn;
+    q.b_mn_major = b_mn;
+    q.out_f32 = j.out->dtype == EA_F32;
+    q.scale = j.scale;
+    q.pred_mode = mode;
+    q.bn = bn;
+    q.err = c->err;
+    return EA_OK;
+}
+
+// ------------------------------------------------------------ launching
+
+static ea_status launch_plan(DevPlan *p, DevCtx *c, cudaStream_t st) {
+    ea_status s = plan_ready_on(p, st);
+    if (s) return s;
+    cudaError_t e = cudaSuccess;
+    t_last = LastPlan{};
+    t_last.kind = p->kind;
+    t_last.groups = p->n_groups;
+    t_last.tuples = p->n_tuples;
+    switch (p->kind) {
+    case kExchange: t_last.tiles = p->nxtiles; t_last.launches = p->nxtiles > 0; break;
+    case kEwise: t_last.tiles = p->ew.ntiles; t_last.launches = p->ew.has_vec + p->ew.has_scalar; break;
+    case kRowReduce: t_last.tiles = p->rr.ntiles; t_last.launches = p->rr.ntiles > 0; break;
+    case kSimt: t_last.tiles = p->ct.ntiles; t_last.launches = p->ct.ntiles > 0; break;
+    case kTc: t_last.tiles = p->tc.ntiles; t_last.launches = p->tc.ntiles > 0; break;
+    }
+    switch (p->kind) {
+    case kExchange:
+        if (p->nxtiles) e = launch_exchange(p->segs, p->xtiles, p->nxtiles, p->xsrc, p->xdst, p->esize, c->num_sms, st);
+        break;
+    case kEwise:
+        p->ew.err = c->err;
+        if (p->ew.ntiles) e = launch_ewise(p->ew, c->num_sms, st);
+        break;
+    case kRowReduce:
+        p->rr.err = c->err;
+        if (p->rr.ntiles) e = launch_rowreduce(p->rr, c->num_sms, st);
+        break;
+    case kSimt:
+        if (p->ct.ntiles) e = launch_contract_simt(p->ct, st);
+        break;
+    case kTc:
+        p->tc.err = c->err;
+        if (p->tc.ntiles) e = launch_contract_tc(p->tc, c->num_sms, st);
+        break;
+    }
+    if (e != cudaSuccess) return cuda_error(e, "kernel launch");
+    return EA_OK;
+}
+
+static bool same_tiling(const ea_relation_s *r, int d, const Tiling &t) { return r->bounds[d] == t.b; }
+
+}  // namespace ea
+
+using namespace ea;
+
+// =================================================================== C ABI
+
+extern "C" {
+
+ea_status ea_exchange(ea_relation in, const ea_dim_part *new_parts, void *stream, ea_relation *out) {
+    set_error(EA_OK, "");
+    if (!in || !out) return set_error(EA_ERR_ARG, "ea_exchange: NULL argument");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevCtx *c;
+    ea_status s = get_ctx(&c);
+    if (s) return s;
+    Tiling src[kMaxRank], dst[kMaxRank];
+    for (int d = 0; d < in->rank; d++) {
+        src[d].extent = in->dims[d];
+        src[d].b = in->bounds[d];
+    }
+    if (new_parts) {
+        for (int d = 0; d < in->rank; d++) {
+            s = make_tiling(in->dims[d], new_parts[d].nblocks, new_parts[d].bounds, &dst[d]);
+            if (s) return s;
+        }
+    } else {
+        if (!*out) return set_error(EA_ERR_ARG, "ea_exchange: need new_parts or an output relation");
+        for (int d = 0; d < in->rank; d++) {
+            dst[d].extent = (*out)->dims[d];
+            dst[d].b = (*out)->bounds[d];
+        }
+    }
+    ea_relation o = *out;
+    if (o) {
+        if (o->dtype != in->dtype || o->rank != in->rank) return set_error(EA_ERR_SHAPE, "ea_exchange: output dtype/rank differ");
+        for (int d = 0; d < in->rank; d++) {
+            if (o->dims[d] != in->dims[d]) return set_error(EA_ERR_SHAPE, "ea_exchange: output extents differ");
+            if (!same_tiling(o, d, dst[d])) return set_error(EA_ERR_PARTITION, "ea_exchange: output tiling differs from new_parts");
+        }
+        if (o->bytes && in->bytes && o->arena < in->arena + in->bytes && in->arena < o->arena + o->bytes)
+            return set_error(EA_ERR_ARG, "ea_exchange: input and output arenas overlap");
+    } else {
+        ea_dim_part parts[kMaxRank];
+        for (int d = 0; d < in->rank; d++) parts[d] = ea_dim_part{dst[d].nblocks(), 0, dst[d].b.data()};
+        s = ea_relation_create((ea_dtype)in->dtype, in->rank, in->dims, parts, nullptr, &o);
+        if (s) return s;
+    }
+    Key k;
+    k.str("X");
+    k.rel(in);
+    k.rel(o);
+    cudaStream_t st = (cudaStream_t)stream;
+    DevPlan *p;
+    auto it = g_cache.find(k.s);
+    if (it != g_cache.end()) {
+        p = it->second;
+    } else {
+        ExchangePlan xp;
+        s = plan_exchange(in->rank, in->dims, src, dst, (int)elem_size(in->dtype), &xp);
+        if (!s) {
+            p = new DevPlan();
+            Blob b;
+            size_t os = b.add_vec(xp.segs), ot = b.add_vec(xp.tiles);
+            s = upload(b, st, p);
+            if (!s) {
+                p->kind = kExchange;
+                p->segs = (XSeg *)(p->dev + os);
+                p->xtiles = (XTile *)(p->dev + ot);
+                p->nxtiles = (int64_t)xp.tiles.size();
+                p->xsrc = in->arena;
+                p->xdst = o->arena;
+                p->esize = (int)elem_size(in->dtype);
+                g_cache[k.s] = p;
+            } else {
+                free_plan(p);
+            }
+        }
+        if (s) {
+            if (!*out) ea_relation_destroy(o);
+            return s;
+        }
+    }
+    s = launch_plan(p, c, st);
+    if (s) {
+        if (!*out) ea_relation_destroy(o);
+        return s;
+    }
+    *out = o;
+    return EA_OK;
+}
+
+ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inputs, const ea_index_part *parts,
+                         int n_parts, ea_agg agg, ea_map map, const ea_opts *opts, void *stream, ea_relation *out) {
+    set_error(EA_OK, "");
+    if (!spec || !inputs || !out) return set_error(EA_ERR_ARG, "ea_joinagg_run: NULL argument");
+    if (n_parts < 0 || (n_parts > 0 && !parts)) return set_error(EA_ERR_ARG, "ea_joinagg_run: bad parts");
+    if (agg < EA_AGG_NONE || agg > EA_AGG_MAX) return set_error(EA_ERR_ARG, "ea_joinagg_run: unknown agg %d", agg);
+    if (map < EA_MAP_PRODUCT || map > EA_MAP_ROPE) return set_error(EA_ERR_ARG, "ea_joinagg_run: unknown map %d", map);
+    std::lock_guard<std::mutex> lk(g_mu);
+    JoinCtx j;
+    ea_status s = parse_spec(spec, &j.sp);
+    if (s) return s;
+    if (n_inputs != j.sp.n_in) return set_error(EA_ERR_ARG, "spec \"%s\" has %d inputs, got %d", spec, j.sp.n_in, n_inputs);
+    static const int arity[] = {-2, 1, 2, 2, 2, 2, 1, 3, 3, 1};  // -2: two or three
+    if ((arity[map] == -2 && n_inputs < 2) || (arity[map] > 0 && arity[map] != n_inputs))
+        return set_error(EA_ERR_ARG, "map %d does not take %d inputs", map, n_inputs);
+    for (int k = 0; k < n_inputs; k++) {
+        if (!inputs[k]) return set_error(EA_ERR_ARG, "input %d is NULL", k);
+        j.in[k] = inputs[k];
+        if ((int)j.sp.term[k].size() != inputs[k]->rank)
+            return set_error(EA_ERR_SHAPE, "input %d has rank %d but term \"%s\"", k, inputs[k]->rank,
+                             j.sp.term[k].c_str());
+    }
+    ea_opts o{};
+    if (opts) o = *opts;
+    j.agg = agg;
+    j.map = map;
+    j.scale = o.scale == 0.0f ? 1.0f : o.scale;
+    j.eps = o.eps;
+    j.pred_lo = o.pred_lo;
+    j.pred_hi = o.pred_hi;
+    j.rope_table = o.rope_table;
+    j.rope_npos = o.rope_npos;
+    j.rope_pos = o.rope_pos;
+    // Letter tilings: from the inputs, which must agree; explicit parts must match.
+    for (int k = 0; k < n_inputs; k++)
+        for (int d = 0; d < inputs[k]->rank; d++) {
+            char ch = j.sp.term[k][d];
+            Tiling &t = j.lt.t[ch - 'a'];
+            if (t.extent >= 0) {
+                if (t.extent != inputs[k]->dims[d])
+                    return set_error(EA_ERR_SHAPE, "letter '%c' has extents %lld and %lld", ch, (long long)t.extent,
+                                     (long long)inputs[k]->dims[d]);
+                if (t.b != inputs[k]->bounds[d])
+                    return set_error(EA_ERR_PARTITION,
+                                     "letter '%c' is tiled differently by two inputs; re-block one with ea_exchange", ch);
+            } else {
+                t.extent = inputs[k]->dims[d];
+                t.b = inputs[k]->bounds[d];
+            }
+        }
+    for (int i = 0; i < n_parts; i++) {
+        char ch = parts[i].index;
+        if (ch < 'a' || ch > 'z' || j.lt.t[ch - 'a'].extent < 0)
+            return set_error(EA_ERR_SPEC, "partition for letter '%c' that the spec does not use", ch);
+        Tiling t;
+        s = make_tiling(j.lt.t[ch - 'a'].extent, parts[i].nblocks, parts[i].bounds, &t);
+        if (s) return s;
+        if (t.b != j.lt.t[ch - 'a'].b)
+            return set_error(EA_ERR_PARTITION, "letter '%c': the inputs are not tiled as requested; re-block with ea_exchange",
+                             ch);
+    }
+    if ((j.pred_lo != 0) != (j.pred_hi != 0)) return set_error(EA_ERR_ARG, "predicate needs two letters");
+    if (j.pred_lo && (j.pred_lo < 'a' || j.pred_lo > 'z' || j.pred_hi < 'a' || j.pred_hi > 'z' ||
+                      j.lt.t[j.pred_lo - 'a'].extent < 0 || j.lt.t[j.pred_hi - 'a'].extent < 0))
+        return set_error(EA_ERR_SPEC, "predicate letters must be letters of the spec");
+    if (map == EA_MAP_ROPE && (j.rope_pos < 'a' || j.rope_pos > 'z' || j.lt.t[j.rope_pos - 'a'].extent < 0))
+        return set_error(EA_ERR_ARG, "ROPE needs rope_pos, a letter of the spec");
+    // Output relation.
+    int odt = o.out_dtype == 0 ? inputs[0]->dtype : o.out_dtype - 1;
+    if (odt != EA_F32 && odt != EA_BF16) return set_error(EA_ERR_DTYPE, "unknown out_dtype %d", o.out_dtype);
+    int64_t odims[kMaxRank];
+    ea_dim_part oparts[kMaxRank];
+    int orank = (int)j.sp.out.size();
+    if (orank == 0) return set_error(EA_ERR_UNSUPPORTED, "a rank-0 output is not supported");
+    for (int d = 0; d < orank; d++) {
+        const Tiling &t = j.lt.t[j.sp.out[d] - 'a'];
+        odims[d] = t.extent;
+        oparts[d] = ea_dim_part{t.nblocks(), 0, t.b.data()};
+    }
+    ea_relation orel = *out;
+    bool created = false;
+    if (orel) {
+        if (orel->rank != orank) return set_error(EA_ERR_SHAPE, "output relation has rank %d, spec wants %d", orel->rank, orank);
+        for (int d = 0; d < orank; d++) {
+            if (orel->dims[d] != odims[d]) return set_error(EA_ERR_SHAPE, "output extent mismatch in dim %d", d);
+            if (!same_tiling(orel, d, j.lt.t[j.sp.out[d] - 'a']))
+                return set_error(EA_ERR_PARTITION, "output relation is tiled differently from the output letters");
+        }
+        for (int k = 0; k < n_inputs; k++)
+            if (orel->bytes && inputs[k]->bytes && orel->arena < inputs[k]->arena + inputs[k]->bytes &&
+                inputs[k]->arena < orel->arena + orel->bytes && orel->arena != inputs[k]->arena)
+                return set_error(EA_ERR_ARG, "output arena partially overlaps input %d", k);
+    }
+    // Classify.
+    int kind;
+    ContractionViews cv;
+    if (agg == EA_AGG_NONE) {
+        if (!j.sp.contracted.empty())
+            return set_error(EA_ERR_SPEC, "agg NONE but letters \"%s\" are aggregated", j.sp.contracted.c_str());
+        kind = kEwise;
+    } else {
+        if (j.sp.contracted.empty())
+            return set_error(EA_ERR_SPEC, "agg %d needs an aggregated letter (use EA_AGG_NONE for a join)", agg);
+        if (map == EA_MAP_PRODUCT && agg == EA_AGG_SUM && n_inputs == 2) {
+            s = contraction_roles(j.sp, &cv);
+            if (s) return s;
+            kind = kSimt;  // or kTc, decided below
+        } else {
+            if (map != EA_MAP_IDENTITY && map != EA_MAP_SQUARE && map != EA_MAP_EXP_SUB && map != EA_MAP_PRODUCT)
+                return set_error(EA_ERR_UNSUPPORTED, "row reduction supports IDENTITY, SQUARE, EXP_SUB, PRODUCT maps");
+            kind = kRowReduce;
+        }
+    }
+    if (odt == EA_BF16 && kind == kRowReduce && agg == EA_AGG_MAX) {
+        // fine: MAX is exact in any dtype
+    }
+    if (!orel) {
+        s = ea_relation_create((ea_dtype)odt, orank, odims, oparts, nullptr, &orel);
+        if (s) return s;
+        created = true;
+    }
+    j.out = orel;
+    DevCtx *c;
+    s = get_ctx(&c);
+    if (s) {
+        if (created) ea_relation_destroy(orel);
+        return s;
+    }
+    Key key;
+    key.str("J");
+    key.str(spec);
+    for (int k = 0; k < n_inputs; k++) key.rel(inputs[k]);
+    key.rel(orel);
+    key.v((int)agg);
+    key.v((int)map);
+    key.v(j.scale);
+    key.v(j.eps);
+    key.v(j.pred_lo);
+    key.v(j.pred_hi);
+    key.v(j.rope_pos);
+    key.v(j.rope_table);
+    key.v(j.rope_npos);
+    cudaStream_t st = (cudaStream_t)stream;
+    DevPlan *p = nullptr;
+    auto it = g_cache.find(key.s);
+    if (it != g_cache.end()) {
+        p = it->second;
+    } else {
+        s = plan_worklist(j.sp, j.lt, j.pred_lo, j.pred_hi, &j.wl);
+        if (!s) {
+            p = new DevPlan();
+            if (kind == kEwise) s = build_ewise(j, c, st, p);
+            else if (kind == kRowReduce) s = build_rowreduce(j, c, st, p);
+            else {
+                s = build_tc(j, cv, c, st, p);
+                if (s == EA_ERR_UNSUPPORTED) {
+                    free_plan(p);
+                    p = new DevPlan();
+                    set_error(EA_OK, "");
+                    s = build_simt(j, cv, c, st, p);
+                }
+            }
+            if (s) {
+                free_plan(p);
+                p = nullptr;
+            } else {
+                p->n_groups = (int64_t)j.wl.groups.size();
+                p->n_tuples = (int64_t)j.wl.tuples.size() / j.sp.n_in;
+                g_cache[key.s] = p;
+            }
+        }
+        if (s) {
+            if (created) ea_relation_destroy(orel);
+            return s;
+        }
+    }
+    s = launch_plan(p, c, st);
+    if (s) {
+        if (created) ea_relation_destroy(orel);
+        return s;
+    }
+    *out = orel;
+    return EA_OK;
+}
+
+ea_status ea_last_plan(int32_t *kernel_class, int32_t *launches, int64_t *tiles, int64_t *groups, int64_t *tuples) {
+    if (kernel_class) *kernel_class = t_last.kind;
+    if (launches) *launches = t_last.launches;
+    if (tiles) *tiles = t_last.tiles;
+    if (groups) *groups = t_last.groups;
+    if (tuples) *tuples = t_last.tuples;
+    return EA_OK;
+}
+
+ea_status ea_check(void *stream) {
+    set_error(EA_OK, "");
+    DevCtx *c;
+    ea_status s;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        s = get_ctx(&c);
+    }
+    if (s) return s;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_error(e, "ea_check: cudaStreamSynchronize");
+    int flag = 0;
+    e = cudaMemcpy(&flag, c->err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_error(e, "ea_check: reading the device error word");
+    if (flag) {
+        int zero = 0;
+        cudaMemcpy(c->err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        return set_error(EA_ERR_DEVICE, "a kernel raised device error %d (%s)", flag,
+                         flag == kDevTimeoutProducer   ? "bounded wait ran out in the TMA producer"
+                         : flag == kDevTimeoutMma      ? "bounded wait ran out in the MMA issuer"
+                         : flag == kDevTimeoutEpilogue ? "bounded wait ran out in the epilogue"
+                         : flag == kDevBounds          ? "bounds check"
+                                                       : "unknown");
+    }
+    return EA_OK;
+}
+
+ea_status ea_plan_cache_clear(void) {
+    set_error(EA_OK, "");
+    std::lock_guard<std::mutex> lk(g_mu);
+    cudaError_t e = cudaDeviceSynchronize();
+    for (auto &kv : g_cache) free_plan(kv.second);
+    g_cache.clear();
+    if (e != cudaSuccess) return cuda_error(e, "ea_plan_cache_clear: cudaDeviceSynchronize");
+    return EA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,439 @@
+// contract_tc.cu -- grouped bf16 contraction on the sm_103a tensor cores
+// (tcgen05.mma with the accumulator in TMEM, operands staged by TMA).
+//
+// "Every Kernel Is a Join", Examples 3.8/3.9 and Definition 3.7: every
+// function specification of a contraction multiplies one block of each
+// input, and the specifications that share an output block are combined by
+// SUM.  One output tile (128 x BN of one output block) accumulates, in the
+// same TMEM accumulator, every k-chunk of every function specification of
+// its group: the SUM aggregation is the MMA's own accumulate, with no
+// partial block in memory and no separate reduction pass.
+//
+// Warp roles (256 threads, one CTA per SM, persistent over tiles):
+//   warp 0   TMA producer: for each tile, each tuple of the group, each
+//            64-wide k-chunk: A tile [128 x 64] and B tile [BN x 64] into a
+//            stage of the smem ring (128-byte swizzle), one mbarrier with
+//            the byte count per stage.
+//   warp 1   MMA issuer (one thread): 4 x tcgen05.mma (K = 16 each) per
+//            stage into the tile's TMEM accumulator; tcgen05.commit frees
+//            the stage; after the last stage of a tile, commit signals the
+//            epilogue.  Two accumulators (2 x BN TMEM columns) let the MMA
+//            of tile i+1 run while the epilogue drains tile i.
+//   warp 2   allocates and frees TMEM.
+//   warps 4-7 epilogue: tcgen05.ld of its 32 rows, scale, predicate mask
+//            (-inf), convert, write 128-byte swizzled rows into a staging
+//            buffer, TMA store (double-buffered).
+// Every mbarrier wait is bounded (2 s of %globaltimer); on time-out the
+// kernel raises the device error word, the other roles leave their loops,
+// the MMA issuer waits for its own MMAs, TMEM is freed and the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "../ea_internal.h"
+
+namespace ea {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 256;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 100000000ull;
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int STAGING = 2 * 16384;
+    static constexpr int CTL = 256;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + STAGING + CTL;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+};
+
+struct SmemCtl {
+    uint64_t full[8];
+    uint64_t empty[8];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+    int ep_ok;
+};
+
+// ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t gtime() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete.  Gives up (returns false) when
+// another role has aborted, or after `limit` ns, raising the abort flag and
+// the device error word with `code`.
+__device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort, int *err, int code,
+                                       uint64_t limit = kTimeoutNs, bool watch_abort = true) {
+    if (mbar_try(b, parity)) return true;
+    const uint64_t t0 = gtime();
+    for (uint32_t i = 1;; i++) {
+        if (mbar_try(b, parity)) return true;
+        if ((i & 31) == 0) {
+            if (watch_abort && *abort) return false;
+            if (gtime() - t0 > limit) {
+                *abort = 1;
+                if (code) atomicCAS(err, 0, code);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, uint64_t *bar, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+        "[%2];" ::"r"(dst),
+        "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const void *map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (>> 4), descriptor version 1 (bits 46-47), 128-byte
+// swizzle (layout code 2 in bits 61-63).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9, 10-12 = 1), operand majors (bit 15 A, bit 16 B; 1 = MN-major),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__device__ __forceinline__ uint32_t make_idesc(int bn, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams p) {
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *stages = smem;
+    uint8_t *staging = smem + C::STAGES * C::STAGE;
+    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(staging + C::STAGING);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const CUtensorMap *maps = reinterpret_cast<const CUtensorMap *>(p.tmaps);
+    volatile int *abort = &ctl->abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; s++) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        for (int a = 0; a < 2; a++) {
+            mbar_init(&ctl->tfull[a], 1);
+            mbar_init(&ctl->tempty[a], 1);
+        }
+        mbar_init(&ctl->mma_done, 1);
+        ctl->abort = 0;
+        ctl->ep_ok = 1;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (warp == 2) tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int stage = 0;
+        uint32_t ph = 0;
+        uint32_t armed = 0, armed_par = 0;  // per stage: a load issued, and its phase parity
+        for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
+            const TcTile T = p.tiles[tile];
+            const TcGroup G = p.groups[T.group];
+            bool ok = true;
+            for (int t = G.t0; t < G.t1 && ok; t++) {
+                const TcTuple U = p.tuples[t];
+                const CUtensorMap *am = maps + U.a_map;
+                const CUtensorMap *bm = maps + U.b_map;
+                for (int kc = 0; kc < U.kchunks; kc++) {
+                    if (!mbar_wait(&ctl->empty[stage], ph ^ 1, abort, p.err, kDevTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = smem_u32(stages + stage * C::STAGE), sb = sa + C::A_BYTES;
+                    uint64_t *fb = &ctl->full[stage];
+                    mbar_expect_tx(fb, C::STAGE);
+                    if (!p.a_mn_major) {
+                        tma_load_3d(sa, am, fb, kc * BK, T.m0, T.batch);
+                    } else {
+                        tma_load_3d(sa, am, fb, T.m0, kc * BK, T.batch);
+                        tma_load_3d(sa + 8192, am, fb, T.m0 + 64, kc * BK, T.batch);
+                    }
+                    if (!p.b_mn_major) {
+                        tma_load_3d(sb, bm, fb, kc * BK, T.n0, T.batch);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; j++) tma_load_3d(sb + j * 8192, bm, fb, T.n0 + 64 * j, kc * BK, T.batch);
+                    }
+                    armed |= 1u << stage;
+                    armed_par = (armed_par & ~(1u << stage)) | (ph << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok) break;
+        }
+        if (*abort) {
+            // Let our own copies land before the CTA can exit.
+            for (int s = 0; s < C::STAGES; s++)
+                if (armed & (1u << s)) mbar_wait(&ctl->full[s], (armed_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        const uint32_t idesc = make_idesc(BN, p.a_mn_major, p.b_mn_major);
+        int stage = 0, acc = 0;
+        uint32_t ph = 0, acc_ph = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
+            const TcTile T = p.tiles[tile];
+            const TcGroup G = p.groups[T.group];
+            if (!mbar_wait(&ctl->tempty[acc], acc_ph ^ 1, abort, p.err, kDevTimeoutMma)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * BN);
+            uint32_t accumulate = 0;
+            for (int t = G.t0; t < G.t1 && ok; t++) {
+                const TcTuple U = p.tuples[t];
+                for (int kc = 0; kc < U.kchunks; kc++) {
+                    if (!mbar_wait(&ctl->full[stage], ph, abort, p.err, kDevTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(stages + stage * C::STAGE), sb = sa + C::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; kk++) {
+                        const uint64_t ad = p.a_mn_major ? sdesc(sa + kk * 2048, 8192, 1024) : sdesc(sa + kk * 32, 16, 1024);
+                        const uint64_t bd = p.b_mn_major ? sdesc(sb + kk * 2048, 8192, 1024) : sdesc(sb + kk * 32, 16, 1024);
+                        umma_bf16(d, ad, bd, idesc, accumulate);
+                        accumulate = 1;
+                    }
+                    umma_commit(&ctl->empty[stage]);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok) break;
+            umma_commit(&ctl->tfull[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_ph ^= 1;
+        }
+        // Every MMA this thread issued has completed once mma_done flips.
+        umma_commit(&ctl->mma_done);
+        mbar_wait(&ctl->mma_done, 0, abort, p.err, kDevTimeoutMma, kTimeoutNs, false);
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue
+        const int ep = threadIdx.x - 128;  // = TMEM lane = row of the tile
+        const int wq = warp & 3;
+        const int CW = p.out_f32 ? 32 : 64;  // columns per 128-byte row chunk
+        int acc = 0, buf = 0;
+        uint32_t acc_ph = 0;
+        for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
+            const TcTile T = p.tiles[tile];
+            const TcGroup G = p.groups[T.group];
+            const CUtensorMap *om = maps + G.out_map;
+            if (ep == 0) ctl->ep_ok = mbar_wait(&ctl->tfull[acc], acc_ph, abort, p.err, kDevTimeoutEpilogue) ? 1 : 0;
+            named_bar(1, 128);
+            if (!ctl->ep_ok) break;
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
+            const int64_t m_g = G.m_lo + T.m0 + ep;
+            for (int c0 = 0; c0 < BN; c0 += CW) {
+                if (T.n0 + c0 >= G.n_ext) break;  // whole chunk past the block edge
+                uint32_t r[64];
+                tmem_ld32(tb + c0, r);
+                if (!p.out_f32) tmem_ld32(tb + c0 + 32, r + 32);
+                tmem_wait_ld();
+                float v[64];
+#pragma unroll
+                for (int j = 0; j < 64; j++) {
+                    if (j < CW) {
+                        float x = __uint_as_float(r[j]) * p.scale;
+                        if (p.pred_mode) {
+                            int64_t n_g = G.n_lo + T.n0 + c0 + j;
+                            if ((p.pred_mode == 1 && n_g > m_g) || (p.pred_mode == 2 && m_g > n_g)) x = -INFINITY;
+                        }
+                        v[j] = x;
+                    }
+                }
+                uint8_t *sbuf = staging + buf * 16384;
+                const uint32_t rowbase = smem_u32(sbuf) + ep * 128;
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    uint32_t w0, w1, w2, w3;
+                    if (p.out_f32) {
+                        w0 = __float_as_uint(v[4 * q + 0]);
+                        w1 = __float_as_uint(v[4 * q + 1]);
+                        w2 = __float_as_uint(v[4 * q + 2]);
+                        w3 = __float_as_uint(v[4 * q + 3]);
+                    } else {
+                        __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
+                        __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
+                        __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
+                        w0 = *reinterpret_cast<uint32_t *>(&h0);
+                        w1 = *reinterpret_cast<uint32_t *>(&h1);
+                        w2 = *reinterpret_cast<uint32_t *>(&h2);
+                        w3 = *reinterpret_cast<uint32_t *>(&h3);
+                    }
+                    const uint32_t addr = rowbase + ((uint32_t)(q ^ (ep & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2),
+                                 "r"(w3)
+                                 : "memory");
+                }
+                fence_proxy_async();
+                named_bar(1, 128);
+                if (ep == 0) {
+                    tma_store_3d(om, smem_u32(sbuf), T.n0 + c0, T.m0, T.batch);
+                    bulk_commit();
+                    bulk_wait_read1();
+                }
+                buf ^= 1;
+                named_bar(1, 128);
+            }
+            tc_fence_before();
+            named_bar(1, 128);
+            if (ep == 0) mbar_arrive(&ctl->tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_ph ^= 1;
+        }
+        if (ep == 0) bulk_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int BN>
+cudaError_t launch_bn(const TcParams &p, int num_sms, cudaStream_t st) {
+    using C = Cfg<BN>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(tc_contract_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    int grid = std::min<int>(p.ntiles, num_sms);
+    tc_contract_kernel<BN><<<grid, kThreads, C::SMEM, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_smem_bytes(int bn) { return bn == 256 ? Cfg<256>::SMEM : Cfg<128>::SMEM; }
+
+cudaError_t launch_contract_tc(const TcParams &p, int num_sms, cudaStream_t st) {
+    if (p.bn == 256) return launch_bn<256>(p, num_sms, st);
+    return launch_bn<128>(p, num_sms, st);
+}
+
+}  // namespace ea

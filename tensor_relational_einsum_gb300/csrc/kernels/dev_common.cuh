@@ -1,0 +1,99 @@
+// dev_common.cuh -- device helpers shared by the join-agg kernels:
+// element loads/stores for fp32 and bf16, and the per-cell operators f of
+// the join-agg maps (computed in fp32).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../ea_internal.h"
+
+namespace ea {
+
+__device__ __forceinline__ float ld_elem(const char *base, int dtype, int64_t i) {
+    if (dtype == EA_F32) return __ldg(reinterpret_cast<const float *>(base) + i);
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i]);
+}
+
+__device__ __forceinline__ void st_elem(char *base, int dtype, int64_t i, float v) {
+    if (dtype == EA_F32) reinterpret_cast<float *>(base)[i] = v;
+    else reinterpret_cast<__nv_bfloat16 *>(base)[i] = __float2bfloat16_rn(v);
+}
+
+// 8 consecutive elements starting at i (16-byte aligned for bf16, 32 for fp32).
+__device__ __forceinline__ void ld8(const char *base, int dtype, int64_t i, float *v) {
+    if (dtype == EA_F32) {
+        const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(base) + i);
+        float4 a = __ldg(p), b = __ldg(p + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+        uint4 u = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(base) + i));
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            float2 f = __bfloat1622float2(h[q]);
+            v[2 * q] = f.x;
+            v[2 * q + 1] = f.y;
+        }
+    }
+}
+
+__device__ __forceinline__ void st8(char *base, int dtype, int64_t i, const float *v) {
+    if (dtype == EA_F32) {
+        float4 *p = reinterpret_cast<float4 *>(reinterpret_cast<float *>(base) + i);
+        p[0] = make_float4(v[0], v[1], v[2], v[3]);
+        p[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+        uint4 u;
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int q = 0; q < 4; q++) h[q] = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(base) + i) = u;
+    }
+}
+
+// The per-cell operator f of a join (v2 = 1 when the join has two inputs).
+__device__ __forceinline__ float cell_map(int map, float v0, float v1, float v2, float scale, float eps) {
+    switch (map) {
+    case EA_MAP_PRODUCT: return scale * v0 * v1 * v2;
+    case EA_MAP_IDENTITY: return scale * v0;
+    case EA_MAP_SILU_MUL: return v0 / (1.0f + expf(-v0)) * v1;
+    case EA_MAP_ADD: return v0 + v1;
+    case EA_MAP_EXP_SUB: return expf(v0 - v1);
+    case EA_MAP_DIV: return v0 / v1;
+    case EA_MAP_SQUARE: return scale * v0 * v0;
+    case EA_MAP_RMS_APPLY: return v0 * rsqrtf(v1 + eps) * v2;
+    case EA_MAP_EXP_SUB_DIV: return expf(v0 - v1) / v2;
+    default: return v0;
+    }
+}
+
+// Decode a row index over the first nd outer dims (innermost last).
+__device__ __forceinline__ void decode_row(const EwItem &it, int64_t r, int64_t *coord) {
+#pragma unroll
+    for (int d = kViewDims - 1; d >= 0; d--) {
+        if (d >= it.nd) {
+            coord[d] = 0;
+            continue;
+        }
+        if (d == 0) {
+            coord[0] = r;
+        } else {
+            int64_t e = it.ext[d];
+            coord[d] = r % e;
+            r /= e;
+        }
+    }
+}
+
+// Global coordinate of special letter `slot` at row coordinates `coord`
+// and inner index `col`.
+__device__ __forceinline__ int64_t special_coord(const EwItem &it, int slot, const int64_t *coord, int64_t col) {
+    int sd = it.sdim[slot];
+    if (sd < 0) return it.slo[slot];
+    if (sd == kViewDims) return it.slo[slot] + col;
+    return it.slo[slot] + coord[sd];
+}
+
+}  // namespace ea

@@ -1,0 +1,172 @@
+"""Tensor relations on the GPU and the two hot-path calls on them.
+
+A ``Relation`` is a tensor stored as its blocks ("Every Kernel Is a Join",
+Section 1: a set of (sub-tensor key, sub-tensor) pairs; Definitions 3.1 and
+3.2: the keys are tensor types that tile the tensor).  Its arena is a torch
+CUDA tensor; libea.so holds the handle.  ``joinagg`` and ``exchange`` call
+the C ABI on the current torch stream.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import AGGS, DTYPES, MAPS, check_status, lib
+
+_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16}
+_NAMES = {0: "f32", 1: "bf16"}
+
+
+def _stream_ptr(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+class Relation:
+    """A tensor of ``dims`` tiled per dimension by ``parts`` (an int = that
+    many near-equal blocks, or an explicit bounds list).
+
+    ``storage``: an existing CUDA tensor holding the arena (borrowed, must
+    have at least prod(dims) elements of the dtype); default: a new one."""
+
+    def __init__(self, dtype: str, dims, parts, storage: torch.Tensor | None = None, device=None):
+        self.dtype = dtype
+        self.dims = tuple(int(d) for d in dims)
+        n = 1
+        for d in self.dims:
+            n *= d
+        if storage is None:
+            storage = torch.empty(max(n, 1), dtype=_TORCH[dtype], device=device or "cuda")
+        else:
+            if storage.dtype != _TORCH[dtype] or storage.numel() < n or not storage.is_cuda:
+                raise ValueError("storage must be a CUDA tensor of the relation's dtype with enough elements")
+            if not storage.is_contiguous():
+                raise ValueError("storage must be contiguous")
+        self.storage = storage
+        arr, keep, bounds = _abi.dim_parts(self.dims, parts)
+        self.bounds = bounds
+        h = ctypes.c_void_p()
+        check_status(lib().ea_relation_create(DTYPES[dtype], len(self.dims), _abi.i64(self.dims), arr,
+                                              ctypes.c_void_p(storage.data_ptr()), ctypes.byref(h)))
+        self.handle = h
+
+    # -- lifetime
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value and _abi._lib is not None:
+            _abi._lib.ea_relation_destroy(h)
+            self.handle = None
+
+    # -- queries
+    @property
+    def nblocks(self) -> int:
+        n = ctypes.c_int64()
+        check_status(lib().ea_relation_info(self.handle, None, None, None, ctypes.byref(n)))
+        return n.value
+
+    @property
+    def parts(self):
+        return [list(b) for b in self.bounds]
+
+    def block(self, i: int):
+        """(device pointer, lo, hi) of block i."""
+        p = ctypes.c_void_p()
+        lo = (ctypes.c_int64 * 8)()
+        hi = (ctypes.c_int64 * 8)()
+        check_status(lib().ea_relation_block(self.handle, i, ctypes.byref(p), lo, hi))
+        r = len(self.dims)
+        return p.value, tuple(lo[:r]), tuple(hi[:r])
+
+    def arena(self) -> torch.Tensor:
+        n = 1
+        for d in self.dims:
+            n *= d
+        return self.storage[:n]
+
+    # -- conversion (all on the GPU, through the exchange kernel)
+    @classmethod
+    def from_dense(cls, t: torch.Tensor, parts, dtype: str | None = None) -> "Relation":
+        """Relation with tiling ``parts`` holding the row-major tensor ``t``."""
+        dtype = dtype or {torch.float32: "f32", torch.bfloat16: "bf16"}[t.dtype]
+        t = t.contiguous()
+        whole = cls(dtype, t.shape, [1] * t.dim(), storage=t.reshape(-1))
+        if all((isinstance(p, int) and p == 1) or (not isinstance(p, int) and len(p) == 2) for p in parts):
+            out = cls(dtype, t.shape, parts)
+            out.storage.copy_(t.reshape(-1)) if t.numel() else None
+            return out
+        return exchange(whole, parts)
+
+    def to_dense(self) -> torch.Tensor:
+        """The tensor, row-major, as a new CUDA tensor."""
+        if all(len(b) == 2 for b in self.bounds):
+            return self.arena().clone().reshape(self.dims)
+        whole = exchange(self, [1] * len(self.dims))
+        return whole.arena().reshape(self.dims)
+
+
+def exchange(rel: Relation, parts, out: Relation | None = None, stream=None) -> Relation:
+    """Re-block ``rel`` into the tiling ``parts`` ("Every Kernel Is a Join",
+    Section 5.3).  Bit-exact."""
+    if out is None:
+        out = Relation(rel.dtype, rel.dims, parts, device=rel.storage.device)
+        arr = None
+    else:
+        arr = None
+    h = ctypes.c_void_p(out.handle.value)
+    check_status(lib().ea_exchange(rel.handle, arr, ctypes.c_void_p(_stream_ptr(stream)), ctypes.byref(h)))
+    return out
+
+
+def _parse(spec: str):
+    lhs, out = spec.split("->")
+    return lhs.split(","), out
+
+
+def output_layout(spec: str, inputs):
+    """Extents and tilings of the output letters, taken from the inputs."""
+    terms, out = _parse(spec)
+    ext, bnd = {}, {}
+    for term, r in zip(terms, inputs):
+        for l, n, b in zip(term, r.dims, r.bounds):
+            ext.setdefault(l, n)
+            bnd.setdefault(l, b)
+    return [ext[l] for l in out], [bnd[l] for l in out]
+
+
+def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Relation | None = None,
+            out_dtype: str | None = None, scale: float = 1.0, eps: float = 0.0, pred: str | None = None,
+            parts: dict | None = None, rope_table: torch.Tensor | None = None, rope_pos: str | None = None,
+            stream=None) -> Relation:
+    """Run one join-agg ("Every Kernel Is a Join", Definition 3.7) with
+    libea.so.  ``pred="ts"`` keeps joined tuples with t <= s."""
+    if out is None:
+        dims, bounds = output_layout(spec, inputs)
+        out = Relation(out_dtype or inputs[0].dtype, dims, bounds, device=inputs[0].storage.device)
+    handles = (ctypes.c_void_p * len(inputs))(*[r.handle.value for r in inputs])
+    ip, n_parts, keep = _abi.index_parts(parts)
+    o = _abi.Opts()
+    o.out_dtype = 0
+    o.scale = scale
+    o.eps = eps
+    if pred:
+        o.pred_lo, o.pred_hi = pred[0].encode(), pred[1].encode()
+    if rope_table is not None:
+        o.rope_table = rope_table.data_ptr()
+        o.rope_npos = rope_table.shape[0]
+        o.rope_pos = rope_pos.encode()
+    h = ctypes.c_void_p(out.handle.value)
+    check_status(lib().ea_joinagg_run(spec.encode(), handles, len(inputs), ip, n_parts, AGGS[agg], MAPS[map],
+                                      ctypes.byref(o), ctypes.c_void_p(_stream_ptr(stream)), ctypes.byref(h)))
+    return out
+
+
+def check(stream=None):
+    """Synchronise the stream and raise on an asynchronous CUDA error or a
+    raised device error flag."""
+    check_status(lib().ea_check(ctypes.c_void_p(_stream_ptr(stream))))
+
+
+def plan_cache_clear():
+    check_status(lib().ea_plan_cache_clear())

@@ -1,0 +1,192 @@
+"""CPU tests of libea.so: it loads and exports every symbol include/ea.h
+declares, and its host planner (no GPU involved) matches the oracle's
+independent enumerators bit-exactly: work lists, exchange permutations,
+overlay atom counts, near-equal tilings, error codes."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import worklist as owl
+from tensor_relational_einsum_gb300 import _abi
+from tensor_relational_einsum_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return _abi.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    hdr = open(os.path.join(ROOT, "include", "ea.h")).read()
+    names = set(re.findall(r"^(?:ea_status|int|const char \*)\s*(ea_[a-z_]+)\s*\(", hdr, re.M))
+    assert {"ea_relation_create", "ea_joinagg_run", "ea_exchange"} <= names
+    for n in sorted(names):
+        assert hasattr(L, n), n
+    assert L.ea_abi_version() == 1
+
+
+def plan(L, spec, shapes, parts, pred=None):
+    ip, n, keep = _abi.index_parts(parts)
+    sh = _abi.i64([x for s in shapes for x in s])
+    ng, nt, jv, av = (ctypes.c_int64() for _ in range(4))
+    pl, ph = (pred[0].encode(), pred[1].encode()) if pred else (b"\0", b"\0")
+    _abi.check_status(L.ea_plan_worklist(spec.encode(), sh, ip, n, pl, ph, 0, 0, None, None, None, ctypes.byref(ng),
+                                         ctypes.byref(nt), ctypes.byref(jv), ctypes.byref(av)))
+    n_in = len(spec.split("->")[0].split(","))
+    g = np.zeros(max(1, ng.value), dtype=np.int64)
+    gp = np.zeros(ng.value + 1, dtype=np.int64)
+    tp = np.zeros(max(1, nt.value * n_in), dtype=np.int64)
+    _abi.check_status(L.ea_plan_worklist(spec.encode(), sh, ip, n, pl, ph, ng.value, nt.value,
+                                         g.ctypes.data_as(_abi.P64), gp.ctypes.data_as(_abi.P64),
+                                         tp.ctypes.data_as(_abi.P64), ctypes.byref(ng), ctypes.byref(nt),
+                                         ctypes.byref(jv), ctypes.byref(av)))
+    tuples = [tuple(int(x) for x in tp[i * n_in:(i + 1) * n_in]) for i in range(nt.value)]
+    return {"groups": [int(x) for x in g[:ng.value]], "grp_ptr": [int(x) for x in gp], "tuples": tuples,
+            "join_volume": jv.value, "agg_volume": av.value}
+
+
+WL_CASES = [
+    ("ij,jk->ik", [(256, 512), (512, 256)], {"i": [0, 128, 256], "j": [0, 256, 512]}, None),
+    ("ij,jk->ik", [(256, 256), (256, 256)], {"i": 4, "j": 4, "k": 4}, None),
+    ("ij,jk->ik", [(10, 9), (9, 8)], {"i": [0, 3, 10], "j": [0, 4, 5, 9], "k": [0, 2, 8]}, None),
+    ("bhsd,bhtd->bhst", [(4, 32, 2048, 128), (4, 32, 2048, 128)], {"b": 4, "h": 32, "t": 4}, None),
+    ("bhst,bhtd->bhsd", [(4, 32, 2048, 2048), (4, 32, 2048, 128)], {"b": 4, "h": 32, "t": 4}, None),
+    ("bshd,bthd->bhst", [(2, 64, 2, 8), (2, 64, 2, 8)], {"b": 2, "h": 2, "s": 4, "t": 4}, "ts"),
+    ("bhst,bthd->bshd", [(2, 2, 64, 64), (2, 64, 2, 8)], {"b": 2, "h": 2, "s": 4, "t": 4}, "ts"),
+    ("bhst->bhs", [(2, 3, 10, 12)], {"h": [0, 1, 3], "t": [0, 5, 12], "s": [0, 7, 10]}, None),
+    ("td,t,d->td", [(12, 8), (12,), (8,)], {"t": 3, "d": 2}, None),
+    ("ijk,kl->ijl", [(3, 4, 5), (5, 6)], {"i": 3, "k": [0, 1, 5], "l": 2}, None),
+]
+
+
+@pytest.mark.parametrize("spec,shapes,parts,pred", WL_CASES)
+def test_worklist_matches_oracle_enumerator(L, spec, shapes, parts, pred):
+    got = plan(L, spec, shapes, parts, pred)
+    ext = oracle.letter_extents(spec, shapes)
+    bounds = {}
+    for l, n in ext.items():
+        p = parts.get(l, 1)
+        bounds[l] = oracle.near_equal_bounds(n, p) if isinstance(p, int) else list(p)
+    want = owl.worklist(spec, bounds, pred)
+    assert got["groups"] == want["groups"]
+    assert got["grp_ptr"] == want["grp_ptr"]
+    assert got["tuples"] == [tuple(t) for t in want["tuples"]]
+    assert got["join_volume"] == want["join_volume"]
+    assert got["agg_volume"] == want["agg_volume"]
+
+
+def test_worklist_golden_example_3_8(L):
+    import json
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "ex3_8_matmul_worklist.json")))
+    got = plan(L, g["spec"], [(256, 512), (512, 256)], g["bounds"])
+    assert len(got["tuples"]) == g["n_function_specs"]
+    assert got["tuples"] == [((m - 1) * 2 + (n - 1), n - 1) for grp in g["groups_as_mn"] for m, n in grp]
+
+
+def test_matmul3d_closed_forms_from_planner(L):
+    import json
+    for c in json.load(open(os.path.join(ROOT, "tests", "golden", "matmul3d_volumes.json")))["cases"]:
+        N = c["N"]
+        got = plan(L, "ij,jk->ik", [(N, N), (N, N)], {"i": c["a"], "j": c["b"], "k": c["c"]})
+        assert len(got["tuples"]) == c["tuples"]
+        assert got["join_volume"] == c["join"] and got["agg_volume"] == c["agg"]
+
+
+def perm(L, dims, src, dst):
+    sa, k1, _ = _abi.dim_parts(dims, src)
+    da, k2, _ = _abi.dim_parts(dims, dst)
+    out = np.empty(int(np.prod(dims)), dtype=np.int64)
+    _abi.check_status(L.ea_exchange_permutation(len(dims), _abi.i64(dims), sa, da, out.ctypes.data_as(_abi.P64)))
+    return out
+
+
+X_CASES = [
+    ((64, 64), [8, 1], [1, 8]),
+    ((64, 64), [8, 1], [4, 2]),
+    ((64, 64), [8, 1], [16, 16]),
+    ((64, 64), [1, 1], [16, 16]),
+    ((12, 10), [[0, 3, 6, 9, 12], [0, 10]], [[0, 4, 8, 12], [0, 2, 7, 10]]),
+    ((4, 6, 8), [[0, 2, 4], [0, 6], [0, 8]], [[0, 4], [0, 3, 6], [0, 2, 4, 8]]),
+    ((2, 16, 4, 8), [2, 1, 1, 1], [2, 1, 4, 1]),
+    ((2, 3, 5, 7, 3), [2, 3, 1, 2, 1], [1, 1, 5, 1, 3]),
+    ((8192, 8), [8, 1], [16, 1]),
+]
+
+
+@pytest.mark.parametrize("dims,src,dst", X_CASES)
+def test_exchange_permutation_matches_oracle(L, dims, src, dst):
+    got = perm(L, dims, src, dst)
+    sb = [oracle.near_equal_bounds(n, p) if isinstance(p, int) else p for n, p in zip(dims, src)]
+    db = [oracle.near_equal_bounds(n, p) if isinstance(p, int) else p for n, p in zip(dims, dst)]
+    want = oracle.exchange_perm(dims, sb, db)
+    assert np.array_equal(got, want)
+    n = ctypes.c_int64()
+    sa, k1, _ = _abi.dim_parts(dims, sb)
+    da, k2, _ = _abi.dim_parts(dims, db)
+    _abi.check_status(L.ea_overlay_atoms(len(dims), _abi.i64(dims), sa, da, ctypes.byref(n)))
+    assert n.value == len(owl.atoms(sb, db))
+
+
+def test_exchange_full_config_permutation(L):
+    """The 8192 x 8192 re-blockings of the exchange workload, bit-exact."""
+    dims = (8192, 8192)
+    for dst in ([1, 8], [4, 2], [16, 16]):
+        got = perm(L, dims, [8, 1], dst)
+        want = oracle.exchange_perm(dims, [oracle.near_equal_bounds(8192, 8), [0, 8192]],
+                                    [oracle.near_equal_bounds(8192, dst[0]), oracle.near_equal_bounds(8192, dst[1])])
+        assert np.array_equal(got, want)
+
+
+def test_near_equal_tiling_of_relations(L):
+    for n, k in [(10, 3), (7, 7), (8192, 8), (11008, 4), (5, 2)]:
+        arr, keep, _ = _abi.dim_parts([n], [k])
+        arr[0].bounds = None  # ask the library for its near-equal split
+        h = ctypes.c_void_p()
+        _abi.check_status(L.ea_relation_create(0, 1, _abi.i64([n]), arr, ctypes.c_void_p(256), ctypes.byref(h)))
+        nb = ctypes.c_int32()
+        b = (ctypes.c_int64 * (k + 1))()
+        _abi.check_status(L.ea_relation_bounds(h, 0, ctypes.byref(nb), b))
+        assert list(b) == oracle.near_equal_bounds(n, k)
+        L.ea_relation_destroy(h)
+
+
+def _fake_rel(L, dtype, dims, parts, addr=4096):
+    arr, keep, _ = _abi.dim_parts(dims, parts)
+    h = ctypes.c_void_p()
+    rc = L.ea_relation_create(dtype, len(dims), _abi.i64(dims), arr, ctypes.c_void_p(addr), ctypes.byref(h))
+    return rc, h
+
+
+def test_error_codes_without_gpu(L):
+    assert _fake_rel(L, 0, (10,), [[0, 5, 4, 10]])[0] == 3          # bounds not a tiling
+    assert _fake_rel(L, 0, (10,), [[0, 5, 11]])[0] == 3             # past the extent
+    assert _fake_rel(L, 0, (3,), [5])[0] == 3                        # empty blocks
+    assert _fake_rel(L, 7, (3,), [1])[0] == 4                        # dtype
+    assert _fake_rel(L, 0, (3,), [1], addr=4097)[0] == 7             # misaligned arena
+    rc, a = _fake_rel(L, 0, (8, 6), [2, 1], 4096)
+    rc2, b = _fake_rel(L, 0, (6, 4), [3, 1], 1 << 20)                # j tiled 3 ways here, 1 way in a
+    rc3, c = _fake_rel(L, 0, (8, 4), [2, 1], 1 << 21)
+    assert rc == rc2 == rc3 == 0
+    hs = (ctypes.c_void_p * 2)(a.value, b.value)
+    out = ctypes.c_void_p(c.value)
+    err = L.ea_joinagg_run(b"ij,jk->ik", hs, 2, None, 0, 1, 0, None, None, ctypes.byref(out))
+    assert err == 3 and b"re-block" in L.ea_last_error()
+    rc5, b1 = _fake_rel(L, 0, (6, 4), [1, 1], 1 << 23)
+    hs = (ctypes.c_void_p * 2)(a.value, b1.value)
+    assert L.ea_joinagg_run(b"ij,jk->", hs, 2, None, 0, 1, 0, None, None, ctypes.byref(out)) == 8
+    assert L.ea_joinagg_run(b"ij,jk-ik", hs, 2, None, 0, 1, 0, None, None, ctypes.byref(out)) == 1
+    assert L.ea_joinagg_run(b"ii,jk->ik", hs, 2, None, 0, 1, 0, None, None, ctypes.byref(out)) == 1
+    assert L.ea_joinagg_run(b"ij,jk->ik", hs, 1, None, 0, 1, 0, None, None, ctypes.byref(out)) == 7
+    assert L.ea_joinagg_run(b"ij,jk->ik", hs, 2, None, 0, 5, 0, None, None, ctypes.byref(out)) == 7
+    rc4, d = _fake_rel(L, 0, (7, 4), [1, 1], 1 << 22)
+    hs2 = (ctypes.c_void_p * 2)(a.value, d.value)
+    assert L.ea_joinagg_run(b"ij,jk->ik", hs2, 2, None, 0, 1, 0, None, None, ctypes.byref(out)) == 2  # j: 6 vs 7
+    for h in (a, b, c, d, b1):
+        L.ea_relation_destroy(h)

@@ -1,0 +1,239 @@
+"""GPU parity: libea.so's kernels against the fp64 oracle, element by
+element, on seeded inputs at sizes that span several tiles with ragged
+tails.  Bars: bit-exact for the exchange and for integer-valued inputs;
+max relative Frobenius error 1e-5 (fp32) and 2e-2 (bf16 inputs, fp32
+accumulation) otherwise."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from oracle import chains
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from tensor_relational_einsum_gb300.build import build
+    build()
+    assert torch.cuda.is_available(), "the GPU parity tests need a CUDA device"
+    yield
+    from tensor_relational_einsum_gb300.relation import check
+    check()
+
+
+from gpu_util import (BF16_TOL, FP32_TOL, arena_bits, bounds_of, dense64, exchange, joinagg, last,  # noqa: E402
+                      max_block_rel_frob, rel, rel_frob, synth_bounds)
+
+
+# ------------------------------------------------------------------ exchange
+
+X_CASES = [
+    ("bf16", (256, 384), [4, 1], [1, 3]),
+    ("bf16", (256, 384), [4, 1], [16, 6]),
+    ("f32", (200, 136), [[0, 8, 100, 200], [0, 136]], [[0, 64, 200], [0, 8, 72, 136]]),
+    ("bf16", (12, 10), [[0, 3, 6, 9, 12], [0, 10]], [[0, 4, 8, 12], [0, 2, 7, 10]]),   # 2-byte runs: scalar path
+    ("bf16", (2, 64, 4, 128), [2, 1, 1, 1], [2, 1, 4, 1]),                              # tokens -> heads
+    ("f32", (3, 5, 7, 9), [3, 1, 7, 1], [1, 5, 1, 3]),
+    ("bf16", (1, 70000), [1, 1], [1, 7]),                                               # one long row
+]
+
+
+@pytest.mark.parametrize("dtype,dims,src,dst", X_CASES)
+def test_exchange_bit_exact(dtype, dims, src, dst):
+    t = synth.make(dtype, dims, "uniform", seed=11, a=-1, b=1)
+    R = rel(t, src)
+    flat = t.host.reshape(-1)
+    whole = [[0, n] for n in dims]
+    want_src = oracle.exchange(flat, dims, whole, bounds_of(dims, src))
+    assert np.array_equal(arena_bits(R).view(flat.dtype), want_src)
+    X = exchange(R, dst)
+    assert last()["kernel"] == "exchange"
+    want_dst = oracle.exchange(flat, dims, whole, bounds_of(dims, dst))
+    assert np.array_equal(arena_bits(X).view(flat.dtype), want_dst)
+    back = exchange(X, src)
+    assert np.array_equal(arena_bits(back).view(flat.dtype), want_src)
+
+
+# ------------------------------------------------------- fp32 contraction (C1)
+
+def test_matmul_fp32_full_config():
+    """fp32 A[256,256] B[256,256] U[-1,1], every index in 4 blocks: 64
+    function specifications in 16 groups of 4, SUM over j-blocks."""
+    A = synth.make("f32", (256, 256), "uniform", 1, -1, 1)
+    B = synth.make("f32", (256, 256), "uniform", 2, -1, 1)
+    RA, RB = rel(A, [4, 4]), rel(B, [4, 4])
+    C = joinagg("ij,jk->ik", [RA, RB])
+    info = last()
+    assert info["kernel"] == "contract_simt" and info["groups"] == 16 and info["tuples"] == 64
+    want = oracle.joinagg("ij,jk->ik", [A.to_f64(), B.to_f64()], tier="lit")
+    err = max_block_rel_frob(dense64(C), want, [synth_bounds(256, 4)] * 2)
+    assert err <= FP32_TOL, err
+
+
+def test_matmul_fp32_integer_exact_any_partition():
+    A = synth.make("f32", (130, 97), "int", 3, -2, 2)
+    B = synth.make("f32", (97, 75), "int", 4, -2, 2)
+    want = oracle.joinagg("ij,jk->ik", [A.to_f64(), B.to_f64()], tier="lit")
+    for pa, pb in [([1, 1], [1, 1]), ([3, 4], [4, 2]), ([[0, 1, 130], [0, 50, 97]], [[0, 50, 97], [0, 70, 75]])]:
+        C = joinagg("ij,jk->ik", [rel(A, pa), rel(B, pb)])
+        assert np.array_equal(dense64(C), want)
+
+
+# ----------------------------------------------------- bf16 tensor-core path
+
+def _bf16_case(spec, shapes, parts_per_input, out_dtype, seeds=(5, 6), dist=("normal", 0.0, 1.0), pred=None,
+               scale=1.0, expect="contract_tc"):
+    ts = [synth.make("bf16", s, dist[0], sd, dist[1], dist[2]) for s, sd in zip(shapes, seeds)]
+    rs = [rel(t, p) for t, p in zip(ts, parts_per_input)]
+    C = joinagg(spec, rs, out_dtype=out_dtype, pred=pred, scale=scale)
+    info = last()
+    assert info["kernel"] == expect, info
+    want = oracle.joinagg(spec, [t.to_f64() for t in ts], scale=scale, pred=pred)
+    return dense64(C), want, C
+
+
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_tc_matmul_ragged_k_major_a_mn_major_b(out_dtype):
+    # M = 320 (3 m-tiles, ragged), K = 200 in blocks 64/72/64, N = 520 (3 n-tiles of 256, ragged)
+    got, want, C = _bf16_case("ij,jk->ik", [(320, 200), (200, 520)], [[1, [0, 64, 136, 200]], [[0, 64, 136, 200], 1]],
+                              out_dtype)
+    err = rel_frob(got, want)
+    assert err <= (1e-5 if out_dtype == "f32" else 5e-3), err
+
+
+def test_tc_integer_exact():
+    got, want, _ = _bf16_case("ij,jk->ik", [(256, 320), (320, 384)], [[2, 5], [5, 3]], "f32", dist=("int", -2, 2))
+    assert np.array_equal(got, want)
+
+
+def test_tc_scores_k_major_both_and_causal_mask():
+    # "bhsd,bhtd->bhst": both operands K-major (d contiguous); t in 3 blocks -> BN 128
+    shapes = [(1, 2, 384, 128), (1, 2, 384, 128)]
+    parts = [[1, 2, 1, 1], [1, 2, 3, 1]]
+    got, want, _ = _bf16_case("bhsd,bhtd->bhst", shapes, parts, "f32", scale=0.125)
+    assert rel_frob(got, want) <= 1e-5
+    got, want, _ = _bf16_case("bhsd,bhtd->bhst", shapes, [[1, 2, 3, 1], [1, 2, 3, 1]], "f32", scale=0.125, pred="ts")
+    present = ~np.isnan(want)
+    assert rel_frob(got, want) <= 1e-5
+    # blocks above the diagonal are not computed; masked cells of diagonal blocks hold -inf
+    for s0 in range(0, 384, 128):
+        blk = got[0, :, s0:s0 + 128, s0:s0 + 128]
+        assert np.all(np.isneginf(blk[~present[0, :, s0:s0 + 128, s0:s0 + 128]]))
+
+
+def test_tc_pv_mn_major_b():
+    # "bhst,bhtd->bhsd": A = P (t contiguous, K-major), B = V (d contiguous, MN-major), 3 t-blocks summed
+    got, want, _ = _bf16_case("bhst,bhtd->bhsd", [(1, 2, 256, 384), (1, 2, 384, 128)],
+                              [[1, 2, 1, 3], [1, 2, 3, 1]], "bf16")
+    assert rel_frob(got, want) <= 5e-3
+
+
+def test_tc_batch_inside_block_and_swapped_roles():
+    # heads in blocks of 2 -> batch dimension of extent 2 inside each block
+    got, want, _ = _bf16_case("bhsd,bhtd->bhst", [(1, 4, 256, 64), (1, 4, 256, 64)], [[1, 2, 1, 1], [1, 2, 2, 1]],
+                              "f32")
+    assert rel_frob(got, want) <= 1e-5
+    # output's contiguous letter comes from input 0 -> operands swap roles
+    got, want, _ = _bf16_case("ij,jk->ki", [(384, 192), (192, 256)], [[1, 3], [3, 1]], "f32")
+    assert rel_frob(got, want) <= 1e-5
+
+
+def test_tc_unaligned_falls_back_to_simt():
+    got, want, _ = _bf16_case("ij,jk->ik", [(70, 45), (45, 33)], [[2, 3], [3, 1]], "f32", expect="contract_simt")
+    assert rel_frob(got, want) <= 1e-5
+
+
+# -------------------------------------------------------------- elementwise
+
+def test_ewise_silu_mul_and_add():
+    G = synth.make("bf16", (96, 1040), "normal", 7, 0, 1)
+    U = synth.make("bf16", (96, 1040), "normal", 8, 0, 1)
+    H = joinagg("ik,ik->ik", [rel(G, [2, 4]), rel(U, [2, 4])], agg="none", map="silu_mul")
+    assert last()["kernel"] == "elementwise"
+    want = oracle.joinagg("ik,ik->ik", [G.to_f64(), U.to_f64()], "silu_mul", "none")
+    assert rel_frob(dense64(H), want) <= 5e-3
+    S = joinagg("ik,ik->ik", [rel(G, [3, 1]), rel(U, [3, 1])], agg="none", map="add", out_dtype="f32")
+    want = oracle.joinagg("ik,ik->ik", [G.to_f64(), U.to_f64()], "add", "none")
+    assert rel_frob(dense64(S), want) <= 1e-6
+
+
+def test_ewise_rms_apply_broadcast_and_scalar_path():
+    x = synth.make("bf16", (64, 264), "normal", 9, 0, 1)
+    ms = synth.make("f32", (64,), "uniform", 10, 0.5, 2.0)
+    g = synth.make("bf16", (264,), "normal", 11, 1, 0.1)
+    want = oracle.joinagg("td,t,d->td", [x.to_f64(), ms.to_f64(), g.to_f64()], "rms_apply", "none", eps=1e-6)
+    for parts in ([2, 1], [[0, 10, 64], [0, 5, 264]]):   # second: 5-wide blocks -> scalar path
+        y = joinagg("td,t,d->td", [rel(x, parts), rel(ms, [parts[0]]), rel(g, [parts[1]])], agg="none",
+                    map="rms_apply", eps=1e-6)
+        assert rel_frob(dense64(y), want) <= 5e-3
+
+
+def test_ewise_softmax_normalise_with_predicate():
+    S = synth.make("f32", (1, 2, 64, 96), "normal", 12, 0, 2)
+    m = synth.make("f32", (1, 2, 64), "normal", 13, 3, 0.1)
+    l = synth.make("f32", (1, 2, 64), "uniform", 14, 5, 9)
+    # cells with t > s are removed: the join keeps t <= s
+    P = joinagg("bhst,bhs,bhs->bhst", [rel(S, [1, 2, 2, 3]), rel(m, [1, 2, 2]), rel(l, [1, 2, 2])], agg="none",
+                map="exp_sub_div", pred="ts")
+    E = oracle.joinagg("bhst,bhs->bhst", [S.to_f64(), m.to_f64()], "exp_sub", "none")
+    want = oracle.joinagg("bhst,bhs->bhst", [E, l.to_f64()], "div", "none")
+    s_idx = np.arange(64)[:, None]
+    t_idx = np.arange(96)[None, :]
+    got = dense64(P)
+    # cells the predicate removes are absent; blocks with no kept cell are not written
+    assert rel_frob(got, np.where(t_idx <= s_idx, want, np.nan)) <= 1e-6
+    # removed cells inside a written block hold 0: s-block [32, 64) x t-block [32, 64)
+    blk = got[..., 32:64, 32:64]
+    assert np.all(blk[..., (t_idx[:, 32:64] > s_idx[32:64, :])] == 0.0)
+
+
+def test_ewise_rope_against_rotation_relation():
+    import torch as T
+    b, s, h, d = 2, 48, 3, 64
+    x = synth.make("bf16", (b, s, h, d), "normal", 15, 0, 1)
+    i = np.arange(d // 2, dtype=np.float64)
+    ang = np.arange(s, dtype=np.float64)[:, None] * (10000.0 ** (-2 * i / d))[None, :]
+    tab = T.tensor(np.stack([np.cos(ang), np.sin(ang)], -1).astype(np.float32), device="cuda")
+    y = joinagg("bshd->bshd", [rel(x, [2, 3, 1, 1])], agg="none", map="rope", rope_table=tab, rope_pos="s")
+    want = chains.rope(x.to_f64(), 10000.0)
+    assert rel_frob(dense64(y), want) <= 5e-3
+
+
+# ------------------------------------------------------------ row reduction
+
+def test_rowreduce_max_sum_square():
+    S = synth.make("f32", (1, 3, 40, 300), "normal", 16, 0, 3)
+    RS = rel(S, [1, 3, 2, [0, 100, 200, 300]])
+    m = joinagg("bhst->bhs", [RS], agg="max", map="identity")
+    assert last()["kernel"] == "rowreduce" and last()["tuples"] == 3 * 2 * 3
+    want_m = oracle.joinagg("bhst->bhs", [S.to_f64()], "identity", "max")
+    assert np.array_equal(dense64(m), want_m)
+    l = joinagg("bhst,bhs->bhs", [RS, m], agg="sum", map="exp_sub")
+    want_l = oracle.joinagg("bhst->bhs", [oracle.joinagg("bhst,bhs->bhst", [S.to_f64(), want_m], "exp_sub", "none")],
+                            "identity", "sum")
+    assert rel_frob(dense64(l), want_l) <= 1e-5
+    x = synth.make("bf16", (70, 264), "normal", 17, 0, 1)
+    ms = joinagg("td->t", [rel(x, [2, 3])], agg="sum", map="square", scale=1.0 / 264, out_dtype="f32")
+    want = oracle.joinagg("td->t", [x.to_f64()], "square", "sum", scale=1.0 / 264)
+    assert rel_frob(dense64(ms), want) <= 1e-5
+
+
+def test_rowreduce_causal_predicate():
+    S = synth.make("f32", (1, 2, 64, 64), "normal", 18, 0, 2)
+    RS = rel(S, [1, 2, 4, 4])
+    m = joinagg("bhst->bhs", [RS], agg="max", map="identity", pred="ts")
+    assert last()["tuples"] == 2 * (1 + 2 + 3 + 4)
+    Sm = np.where(np.tril(np.ones((64, 64), bool)), S.to_f64(), np.nan)
+    want = oracle.joinagg("bhst->bhs", [Sm], "identity", "max")
+    assert np.array_equal(dense64(m), want)
+
+
+# ------------------------------------------------------------ device checks
+
+def test_no_device_error_raised():
+    from tensor_relational_einsum_gb300.relation import check
+    check()
