@@ -1,0 +1,492 @@
+#!/usr/bin/env python
+"""Benchmark of the join-agg hot path on GB300.
+
+A step is one forward pass of the LLaMA-7B-shaped block (batch 8 x 2048
+tokens, d 4096, 32 heads x 128, FFN 11008, RMSNorm, RoPE, causal
+attention, bf16) executed as a graph of join-aggs and one exchange -- every
+row of the hot path: contractions with fused SUM, MAX/SUM row reductions,
+elementwise joins, the re-blocking exchange.  ``value`` is the block's
+algorithmic TFLOP/s (projections and FFN dense, attention over the causal
+join); ``ms_per_step`` is the block forward in ms.  The other workloads
+(fp32 matmul join-agg, the attention chain, the SwiGLU FFN, the exchange
+re-blockings) are timed once each and reported under ``components``.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (a prefix of one sequence; causal attention
+makes a prefix exact).  Under torchrun, N > 1 runs N independent replicas
+(weak scaling, no collective on the data path) and rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "join-agg TFLOP/s & exchange GB/s (% of GB300 roofline); LLaMA-block fwd ms"
+B, S, D, NH, FF = 8, 2048, 4096, 32, 11008
+EPS, THETA = 1e-6, 10000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def block_flops(b=B, s=S, d=D, nh=NH, ff=FF):
+    T = b * s
+    dh = d // nh
+    causal_pairs = b * nh * s * (s + 1) / 2
+    return 2.0 * T * d * d * 4 + 2.0 * T * d * ff * 3 + 2.0 * causal_pairs * dh * 2
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local, dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float, device=None) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+
+class Clocks:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- workloads
+
+def make_block(device):
+    import torch
+
+    import synth
+    from tensor_relational_einsum_gb300.graphs import LlamaBlock
+    W = {}
+    seeds = {"wq": 101, "wk": 102, "wv": 103, "wo": 104, "w_gate": 105, "w_up": 106, "w_down": 107}
+    shapes = {"wq": (D, D), "wk": (D, D), "wv": (D, D), "wo": (D, D), "w_gate": (D, FF), "w_up": (D, FF),
+              "w_down": (FF, D)}
+    for k in seeds:
+        W[k] = synth.make_torch("bf16", shapes[k], "normal", seeds[k], 0.0, 0.02, device=device)
+    W["g1"] = torch.ones(D, dtype=torch.bfloat16, device=device)
+    W["g2"] = torch.ones(D, dtype=torch.bfloat16, device=device)
+    x = synth.make_torch("bf16", (B * S, D), "normal", 100, 0.0, 1.0, device=device)
+    blk = LlamaBlock(B, S, D, NH, FF, W, eps=EPS, theta=THETA, device=device)
+    blk.x.load(x)
+    del W
+    return blk, x
+
+
+def time_region(fn, steps, warmup, dist, device):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    barrier(dist)
+    return s.elapsed_time(e)
+
+
+def bench_components(peaks, device):
+    """Each remaining workload once: median of a few reps after warm-up."""
+    import torch
+
+    import synth
+    from tensor_relational_einsum_gb300.graphs import AttentionChain, Recorder, SwigluFFN
+    from tensor_relational_einsum_gb300.relation import Relation, exchange, joinagg
+    hbm = peaks["hbm_gbs"]
+    out = {}
+
+    def timed(fn, reps=5, warm=3):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            torch.cuda.synchronize()
+            ts.append(s.elapsed_time(e))
+        return statistics.median(ts), min(ts)
+
+    # fp32 matmul join-agg, 256^3, 4x4x4 blocks (launch-latency bound)
+    A = Relation.from_dense(synth.make_torch("f32", (256, 256), "uniform", 1, -1, 1, device=device), [4, 4])
+    Bm = Relation.from_dense(synth.make_torch("f32", (256, 256), "uniform", 2, -1, 1, device=device), [4, 4])
+    C = Relation("f32", (256, 256), [4, 4], device=device)
+    med, mn = timed(lambda: joinagg("ij,jk->ik", [A, Bm], out=C), reps=50, warm=10)
+    out["matmul_fp32_256"] = {"us_per_call": round(med * 1e3, 2), "min_us": round(mn * 1e3, 2),
+                              "tuples": 64, "groups": 16}
+
+    # attention join-agg chain b4 h32 s=t=2048 d128, t in 4 blocks
+    q = synth.make_torch("bf16", (4, 32, 2048, 128), "normal", 11, 0, 1, device=device)
+    k = synth.make_torch("bf16", (4, 32, 2048, 128), "normal", 12, 0, 1, device=device)
+    v = synth.make_torch("bf16", (4, 32, 2048, 128), "normal", 13, 0, 1, device=device)
+    ch = AttentionChain(Relation.from_dense(q, [4, 32, 1, 1]), Relation.from_dense(k, [4, 32, 4, 1]),
+                        Relation.from_dense(v, [4, 32, 4, 1]))
+    del q, k, v
+    rec = Recorder()
+    med, mn = timed(lambda: ch.run())
+    for _ in range(3):
+        ch.run(rec)
+    torch.cuda.synchronize()
+    sm = rec.summary()
+    S_bytes = 4 * 32 * 2048 * 2048 * 4
+    P_bytes = S_bytes // 2
+    qkv_b = 4 * 32 * 2048 * 128 * 2
+    ml = 4 * 32 * 2048 * 4
+    alg = {"attn.scores": 2 * qkv_b + S_bytes, "attn.max": S_bytes + ml, "attn.sumexp": S_bytes + 2 * ml,
+           "attn.normalise": S_bytes + 2 * ml + P_bytes, "attn.values": P_bytes + 2 * qkv_b}
+    per = {}
+    for name, (kind, n, ts) in sm.items():
+        t = statistics.median(ts)
+        gbs = alg[name] / (t * 1e-3) / 1e9
+        per[name] = {"kernel": kind, "ms": round(t, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+    fl = ch.flops()
+    out["attention_chain_b4h32s2048"] = {"ms": round(med, 4), "TFLOP/s": round(fl / (med * 1e-3) / 1e12, 1),
+                                         "alg_bytes_GB": round(sum(alg.values()) / 1e9, 3),
+                                         "frac_hbm_chain": round(sum(alg.values()) / (med * 1e-3) / 1e9 / hbm, 3),
+                                         "join_aggs": per}
+    del ch
+
+    # SwiGLU FFN join-aggs, x[8192, 4096], contracted dims in 4 blocks
+    x = synth.make_torch("bf16", (8192, 4096), "normal", 21, 0, 1, device=device)
+    wg = synth.make_torch("bf16", (4096, 11008), "normal", 22, 0, 0.02, device=device)
+    wu = synth.make_torch("bf16", (4096, 11008), "normal", 23, 0, 0.02, device=device)
+    wd = synth.make_torch("bf16", (11008, 4096), "normal", 24, 0, 0.02, device=device)
+    ffn = SwigluFFN(Relation.from_dense(x, [1, 4]), wg, wu, wd, k_blocks=4)
+    del x, wg, wu, wd
+    med, mn = timed(lambda: ffn.run())
+    rec = Recorder()
+    for _ in range(3):
+        ffn.run(rec=rec)
+    torch.cuda.synchronize()
+    sm = rec.summary()
+    fl = {"ffn.gate_up": 2.0 * 8192 * 4096 * 2 * 11008, "ffn.down": 2.0 * 8192 * 11008 * 4096}
+    per = {}
+    for name, (kind, n, ts) in sm.items():
+        t = statistics.median(ts)
+        if name in fl:
+            tf = fl[name] / (t * 1e-3) / 1e12
+            per[name] = {"kernel": kind, "ms": round(t, 4), "TFLOP/s": round(tf, 1),
+                         "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 3)}
+        else:
+            gb = 8192 * 11008 * 2 * 3 / (t * 1e-3) / 1e9
+            per[name] = {"kernel": kind, "ms": round(t, 4), "GB/s": round(gb, 1), "frac_hbm": round(gb / hbm, 3)}
+    out["swiglu_ffn_8192x4096x11008"] = {"ms": round(med, 4),
+                                         "TFLOP/s": round(ffn.flops() / (med * 1e-3) / 1e12, 1),
+                                         "frac_bf16_peak": round(ffn.flops() / (med * 1e-3) / 1e12 /
+                                                                 peaks["bf16_tflops"], 3),
+                                         "join_aggs": per}
+    del ffn
+
+    # exchange: bf16 8192^2 held as 8x1 row blocks -> 1x8, 4x2, 16x16
+    X = Relation.from_dense(synth.make_torch("bf16", (8192, 8192), "uniform", 31, -1, 1, device=device), [8, 1])
+    nbytes = 8192 * 8192 * 2
+    ex = {}
+    for name, parts in (("1x8", [1, 8]), ("4x2", [4, 2]), ("16x16", [16, 16])):
+        Y = Relation("bf16", (8192, 8192), parts, device=device)
+        med, mn = timed(lambda: exchange(X, None, out=Y), reps=10, warm=3)
+        gbs = 2 * nbytes / (med * 1e-3) / 1e9
+        ex[name] = {"us": round(med * 1e3, 1), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+        del Y
+    out["exchange_bf16_8192sq_from_8x1"] = ex
+    return out
+
+
+class CpuSample:
+    """The oracle on a prefix of one sequence through the full-width block
+    (causal attention only looks back, so the prefix outputs are exact).
+    Inputs are generated once; ``run()`` times the oracle alone."""
+
+    def __init__(self, tokens: int):
+        import numpy as np
+
+        import synth
+        self.tokens = tokens
+        seeds = {"wq": 101, "wk": 102, "wv": 103, "wo": 104, "w_gate": 105, "w_up": 106, "w_down": 107}
+        shapes = {"wq": (D, D), "wk": (D, D), "wv": (D, D), "wo": (D, D), "w_gate": (D, FF), "w_up": (D, FF),
+                  "w_down": (FF, D)}
+        self.W = {k: synth.make_torch("bf16", shapes[k], "normal", seeds[k], 0.0, 0.02, device="cpu").double().numpy()
+                  for k in seeds}
+        self.W["g1"] = np.ones(D)
+        self.W["g2"] = np.ones(D)
+        self.x = synth.make_torch("bf16", (tokens, D), "normal", 100, 0.0, 1.0, device="cpu").double().numpy()
+
+    def run(self):
+        """Returns (seconds, algorithmic flops of the sample, cores used)."""
+        import oracle
+        from oracle import chains
+        t0 = time.time()
+        chains.llama_block(self.x.reshape(1, self.tokens, D), self.W, n_heads=NH, eps=EPS, theta=THETA)
+        return time.time() - t0, block_flops(b=1, s=self.tokens), oracle.threads()
+
+
+# ------------------------------------------------------------------- arms
+
+def run_reference(args, world, rank, dist):
+    if rank != 0:
+        return 0
+    tokens = args.cpu_tokens
+    sample = CpuSample(tokens)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, fl, cores = sample.run()
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = fl * len(times) / total / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / len(times) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"one sequence, first {tokens} tokens, full-width block (causal prefix is exact)"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def config_dict():
+    return {"workload": "llama7b_block_fwd b8 s2048 d4096 h32x128 ffn11008 bf16 causal (join-agg graph)",
+            "batch": B, "seq_len": S, "d_model": D, "heads": NH, "d_ff": FF, "tilings":
+            "tokens: 1 block per sequence; model dim 4 blocks; heads as a batch letter; s, t: 4 blocks",
+            "l2": "inputs larger than L2 (block touches ~10 GB per step)"}
+
+
+def traffic_from_profiles():
+    """dram bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    import hashlib
+    src = os.path.join(ROOT, "tensor_relational_einsum_gb300", "csrc", "kernels", "contract_tc.cu")
+    prof = os.path.join(ROOT, "profiles", "contract_tc_llama_block.md")
+    if not os.path.exists(prof):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    want = None
+    vals = {}
+    for line in open(prof):
+        if line.startswith("source_sha256_16:"):
+            want = line.split(":", 1)[1].strip()
+        if line.startswith("traffic_bytes_per_launch."):
+            k, v = line.split(":", 1)
+            vals[k.split(".", 1)[1].strip()] = float(v)
+    if want != h:
+        return None
+    return vals
+
+
+def run_ours(args, world, rank, local, dist):
+    import torch
+
+    from tensor_relational_einsum_gb300.build import build
+    from tensor_relational_einsum_gb300.graphs import Recorder
+    from tensor_relational_einsum_gb300.relation import Relation, check, exchange
+    build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    peaks, peak_src = load_peaks()
+    blk, x_dev = make_block(device)
+    # warm-up (plans are built and cached on the first pass)
+    for _ in range(args.warmup):
+        blk.run()
+    torch.cuda.synchronize()
+    check()
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    clocks = Clocks(gpu_index)
+    rec = Recorder()
+    clocks.start()
+    ms = time_region(lambda: blk.run(rec), args.steps, 0, dist, device)
+    clk = clocks.stop()
+    check()
+    ms = max_over_ranks(dist, ms, device)
+    ms_step = ms / args.steps
+    flops = block_flops()
+    value = flops * args.steps * world / (ms * 1e-3) / 1e12
+    sm = rec.summary()
+    launches = sum(n * len(ts) for (k, n, ts) in sm.values())
+    # roofline of the dominant kernel: the tcgen05 contraction (dense projection / FFN launches)
+    cf = blk.call_flops()
+    dense = ("qkv", "o_proj", "ffn.gate_up", "ffn.down")
+    tot_f = sum(cf[n] * len(sm[n][2]) for n in dense)
+    tot_t = sum(sum(sm[n][2]) for n in dense)
+    n_l = sum(len(sm[n][2]) for n in dense)
+    achieved = tot_f / (tot_t * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    traffic = traffic_from_profiles()
+    roof = {"kernel": "contract_tc (projection + FFN contractions)", "bound": "tensor",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_src} bf16 sustained", "flops_per_launch": tot_f / n_l,
+            "ms_per_launch": tot_t / n_l,
+            "traffic": (sum(traffic.values()) / len(traffic)) if traffic else None}
+    per_call = {}
+    for name, (kind, n, ts) in sm.items():
+        t = statistics.median(ts)
+        ent = {"kernel": kind, "ms": round(t, 4), "share": round(sum(ts) / ms, 4)}
+        if name in cf:
+            ent["TFLOP/s"] = round(cf[name] / (t * 1e-3) / 1e12, 1)
+        per_call[name] = ent
+    # end to end through host buffers: H2D of the tokens, the block, D2H of the output
+    x_host = torch.empty((B * S, D), dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(x_dev.cpu())
+    y_host = torch.empty((B * S, D), dtype=torch.bfloat16, pin_memory=True)
+    x_stage = torch.empty_like(x_dev)
+    y_whole = Relation("bf16", (B * S, D), [1, 1], device=device)
+    x_whole = Relation("bf16", (B * S, D), [1, 1], storage=x_stage.reshape(-1))
+
+    def e2e_step():
+        x_stage.copy_(x_host, non_blocking=True)
+        exchange(x_whole, None, out=blk.x)
+        blk.run()
+        exchange(blk.y, None, out=y_whole)
+        y_host.copy_(y_whole.arena().reshape(B * S, D), non_blocking=True)
+
+    ms_e2e = time_region(e2e_step, max(2, args.steps // 2), 1, dist, device)
+    ms_e2e = max_over_ranks(dist, ms_e2e, device)
+    n_e2e = max(2, args.steps // 2)
+    e2e = {"value": flops * n_e2e * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "ms_per_step": ms_e2e / n_e2e, "h2d_bytes_per_step": x_host.numel() * 2,
+           "d2h_bytes_per_step": y_host.numel() * 2}
+    check()
+    comps = None
+    cpu = None
+    if rank == 0 and not args.no_components:
+        del blk, x_dev, x_stage, x_whole, y_whole
+        torch.cuda.empty_cache()
+        comps = bench_components(peaks, device)
+        check()
+    if rank == 0 and world == 1 and not args.no_cpu:
+        dt, fl, cores = CpuSample(args.cpu_tokens).run()
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"one sequence, first {args.cpu_tokens} tokens, full-width block; {dt:.1f} s"}
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": config_dict(), "clocks": clk, "e2e": e2e,
+                "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu, "per_join_agg": per_call,
+                "components": comps}
+        print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=32)
+    ap.add_argument("--no-components", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local, dist = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank, dist)
+        return run_ours(args, world, rank, local, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -16,6 +16,11 @@ notes):
     angle pos * theta^(-2i/d_head); written as the contraction
     "bshiq,sipq->bship" with the 2x2 rotation relation R[s, i, p, q].
   * causal attention: the cell predicate t <= s on the score join.
+
+Dense storage order: a relation's letters may be stored in any order (the
+relation is the same set of cells); weight and value relations are stored
+with their aggregated letter last, which keeps the index-nested-loop join
+on contiguous memory.
 """
 from __future__ import annotations
 
@@ -36,17 +41,18 @@ def softmax_attention(Q, K, V, scale: float = 1.0, causal: bool = False, qspec: 
     E = joinagg("bhst,bhs->bhst", [S, m], "exp_sub", "none", tier=tier)
     l = joinagg("bhst->bhs", [E], "identity", "sum", tier=tier)
     P = joinagg("bhst,bhs->bhst", [E, l], "div", "none", tier=tier)
-    O = joinagg(f"bhst,{vspec}->{ospec}", [P, V], "product", "sum", tier=tier)
+    Vt = np.ascontiguousarray(np.transpose(V, [vspec.index(c) for c in "bhdt"]))
+    O = joinagg(f"bhst,bhdt->{ospec}", [P, Vt], "product", "sum", tier=tier)
     return {"S": S, "m": m, "l": l, "E": E, "P": P, "O": O}
 
 
 def swiglu_ffn(x, w_gate, w_up, w_down, tier: str = "idx"):
     """G = x w_gate, U = x w_up (SUM over the model dimension),
     H = SiLU(G) * U (elementwise join), Y = H w_down."""
-    G = joinagg("ij,jk->ik", [x, w_gate], "product", "sum", tier=tier)
-    U = joinagg("ij,jk->ik", [x, w_up], "product", "sum", tier=tier)
+    G = joinagg("ij,kj->ik", [x, np.ascontiguousarray(w_gate.T)], "product", "sum", tier=tier)
+    U = joinagg("ij,kj->ik", [x, np.ascontiguousarray(w_up.T)], "product", "sum", tier=tier)
     H = joinagg("ik,ik->ik", [G, U], "silu_mul", "none", tier=tier)
-    Y = joinagg("ik,kj->ij", [H, w_down], "product", "sum", tier=tier)
+    Y = joinagg("ik,jk->ij", [H, np.ascontiguousarray(w_down.T)], "product", "sum", tier=tier)
     return {"G": G, "U": U, "H": H, "Y": Y}
 
 
@@ -92,7 +98,7 @@ def llama_block(x, W, n_heads: int, eps: float = 1e-6, theta: float = 10000.0, t
     dh = D // n_heads
     xt = x.reshape(b * s, D)
     n1 = rmsnorm(xt, W["g1"], eps, tier)["y"]
-    proj = lambda a, w: joinagg("td,de->te", [a, w], "product", "sum", tier=tier)  # noqa: E731
+    proj = lambda a, w: joinagg("td,ed->te", [a, np.ascontiguousarray(w.T)], "product", "sum", tier=tier)  # noqa: E731
     q = proj(n1, W["wq"]).reshape(b, s, n_heads, dh)
     k = proj(n1, W["wk"]).reshape(b, s, n_heads, dh)
     v = proj(n1, W["wv"]).reshape(b, s, n_heads, dh)

@@ -436,6 +436,29 @@ static void *idx_worker(void *arg) {
             for (int j = 0; j < c->n_inner; j++) inner_count *= sp->ext[c->inner[j]];
             double acc = 0.0;
             int64_t cnt = 0;
+            if (c->n_inner == 1) {
+                /* one aggregated letter: walk it directly (same order as below) */
+                int l = c->inner[0];
+                for (int64_t x = 0; x < inner_count; x++) {
+                    int absent = 0;
+                    for (int k = 0; k < n; k++) {
+                        v[k] = c->ins[k][base[k] + x * c->stride[k][l]];
+                        if (isnan(v[k])) absent = 1;
+                    }
+                    if (absent) continue;
+                    val[l] = x;
+                    if (sp->pred_a >= 0 && !(val[sp->pred_a] + sp->lo[sp->pred_a] <= val[sp->pred_b] + sp->lo[sp->pred_b]))
+                        continue;
+                    double f = apply_map(c->map, v, n, c->scale, c->eps);
+                    if (cnt == 0) acc = f;
+                    else if (c->agg == A_SUM) acc += f;
+                    else if (c->agg == A_MAX) acc = fmax(acc, f);
+                    else atomic_store(&c->err, 1);
+                    cnt++;
+                }
+                c->out[o] = cnt ? acc : NAN;
+                continue;
+            }
             for (int j = 0; j < c->n_inner; j++) val[c->inner[j]] = 0;
             for (int64_t it = 0; it < inner_count; it++) {
                 if (it > 0) {

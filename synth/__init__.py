@@ -157,3 +157,70 @@ def subset_rows(seed: int, n_total: int, n_pick: int) -> np.ndarray:
     """A seeded sorted choice of n_pick distinct indices out of n_total."""
     keys = raw_u64(seed, 0, n_total)
     return np.sort(np.argsort(keys, kind="stable")[:n_pick])
+
+
+# ------------------------------------------------------------ torch variant
+
+def _torch_mix64(z):
+    import torch
+    m1 = 0xBF58476D1CE4E5B9 - (1 << 64)
+    m2 = 0x94D049BB133111EB - (1 << 64)
+
+    def lsr(x, k):
+        return (x >> k) & ((1 << (64 - k)) - 1)
+
+    z = z ^ lsr(z, 30)
+    z = z * m1
+    z = z ^ lsr(z, 27)
+    z = z * m2
+    return z ^ lsr(z, 31)
+
+
+def _signed(v: int) -> int:
+    v &= (1 << 64) - 1
+    return v - (1 << 64) if v >= (1 << 63) else v
+
+
+def _py_mix64(z: int) -> int:
+    mask = (1 << 64) - 1
+    z &= mask
+    z ^= z >> 30
+    z = (z * 0xBF58476D1CE4E5B9) & mask
+    z ^= z >> 27
+    z = (z * 0x94D049BB133111EB) & mask
+    return z ^ (z >> 31)
+
+
+def make_torch(dtype: str, shape, dist: str, seed: int, a: float = 0.0, b: float = 1.0, device="cuda"):
+    """Same stream as ``make`` computed with torch on ``device`` (fast for
+    large tensors).  Uniform and integer draws are bit-identical to
+    ``make``; normals agree except where the last ulp of the fp64 log / cos
+    differs between libraries.  Returns a torch tensor of the dtype."""
+    import torch
+    shape = tuple(int(s) for s in shape)
+    n = 1
+    for s in shape:
+        n *= s
+    base = _signed(_py_mix64(seed))
+    gamma = _signed(0x9E3779B97F4A7C15)
+    out = torch.empty(n, dtype=torch.float64 if dtype == "f64" else torch.float32, device=device)
+    chunk = 1 << 24
+    per = 2 if dist == "normal" else 1
+    for s0 in range(0, n, chunk):
+        c = min(chunk, n - s0)
+        idx = torch.arange(per * s0 + 1, per * (s0 + c) + 1, dtype=torch.int64, device=device)
+        z = _torch_mix64(base + idx * gamma)
+        u = ((z >> 11) & ((1 << 53) - 1)).to(torch.float64) * (2.0 ** -53)
+        if dist == "uniform":
+            v = a + (b - a) * u
+        elif dist == "int":
+            v = a + torch.floor(u * (int(b) - int(a) + 1))
+        elif dist == "normal":
+            u1, u2 = u[0::2], u[1::2]
+            v = a + b * torch.sqrt(-2.0 * torch.log1p(-u1)) * torch.cos(2.0 * torch.pi * u2)
+        else:
+            raise ValueError(dist)
+        out[s0:s0 + c] = v.to(torch.float32)
+    if dtype == "bf16":
+        return out.to(torch.bfloat16).reshape(shape)
+    return out.reshape(shape)

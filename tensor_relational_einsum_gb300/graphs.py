@@ -1,0 +1,234 @@
+"""Workloads of the hot path as graphs of join-aggs and exchanges.
+
+Each class allocates its relations once and ``run()`` enqueues the calls on
+the current stream -- the single-GPU counterpart of compiling a plan into
+one CUDA graph of kernel invocations ("Every Kernel Is a Join", Section 6).
+All arithmetic runs in libea.so.
+
+* ``AttentionChain``  scores -> MAX -> SUM of exp -> normalise -> values
+                      (softmax over t as MAX then SUM aggregations with an
+                      exp map, Section 1's "softmax as join + aggregation").
+* ``SwigluFFN``       gate/up contractions (SUM over model-dim blocks),
+                      SiLU(gate) * up elementwise join, down contraction.
+* ``LlamaBlock``      pre-norm block: RMSNorm, fused QKV contraction, RoPE,
+                      causal attention chain, exchange of the attention
+                      output into the O-projection's tiling, O projection,
+                      residual, RMSNorm, SwiGLU FFN, residual.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import _abi
+from .relation import Relation, exchange, joinagg
+
+
+class Recorder:
+    """Brackets every call with CUDA events on the current stream and notes
+    which kernel class it launched (for per-kernel timing and launch
+    counts)."""
+
+    def __init__(self):
+        self.calls = []  # (name, kernel class, launches, start event, end event)
+
+    def call(self, name, fn):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        lp = _abi.last_plan()
+        self.calls.append((name, lp["kernel"], lp["launches"], s, e))
+
+    def summary(self):
+        """name -> (kernel class, launches per call, list of ms)."""
+        out = {}
+        for name, k, n, s, e in self.calls:
+            ent = out.setdefault(name, [k, n, []])
+            ent[2].append(s.elapsed_time(e))
+        return out
+
+
+def _direct(name, fn):
+    fn()
+
+
+def view(parent: Relation, offset_elems: int, dims, parts) -> Relation:
+    """A relation over a contiguous piece of ``parent``'s arena (zero-copy)."""
+    n = int(np.prod(dims))
+    return Relation(parent.dtype, dims, parts, storage=parent.storage[offset_elems:offset_elems + n])
+
+
+def rope_table(n_pos: int, d_head: int, theta: float, device="cuda") -> torch.Tensor:
+    """fp32 [n_pos, d_head/2, 2] = (cos, sin) of pos * theta^(-2i/d_head),
+    angles evaluated in float64 on the host."""
+    i = np.arange(d_head // 2, dtype=np.float64)
+    inv = np.power(theta, -2.0 * i / d_head)
+    ang = np.arange(n_pos, dtype=np.float64)[:, None] * inv[None, :]
+    tab = np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
+    return torch.from_numpy(tab).to(device)
+
+
+class AttentionChain:
+    """Q, K, V relations [b, h, s|t, d] (bf16) tiled on b and h; t (and the
+    scores' t) in ``t_blocks`` blocks; optional causal predicate t <= s and
+    score scale."""
+
+    def __init__(self, Q: Relation, K: Relation, V: Relation, scale: float = 1.0, causal: bool = False,
+                 qspec: str = "bhsd", kspec: str = "bhtd", vspec: str = "bhtd", ospec: str = "bhsd"):
+        self.Q, self.K, self.V = Q, K, V
+        self.scale, self.pred = scale, ("ts" if causal else None)
+        self.s_spec = f"{qspec},{kspec}->bhst"
+        self.o_spec = f"bhst,{vspec}->{ospec}"
+        ext, bnd = {}, {}
+        for spec, r in ((qspec, Q), (kspec, K), (vspec, V)):
+            for l, n, b in zip(spec, r.dims, r.bounds):
+                ext[l], bnd[l] = n, b
+        dev = Q.storage.device
+        self.S = Relation("f32", [ext[l] for l in "bhst"], [bnd[l] for l in "bhst"], device=dev)
+        self.m = Relation("f32", [ext[l] for l in "bhs"], [bnd[l] for l in "bhs"], device=dev)
+        self.l = Relation("f32", [ext[l] for l in "bhs"], [bnd[l] for l in "bhs"], device=dev)
+        self.P = Relation("bf16", [ext[l] for l in "bhst"], [bnd[l] for l in "bhst"], device=dev)
+        self.O = Relation("bf16", [ext[l] for l in ospec], [bnd[l] for l in ospec], device=dev)
+        self.ext = ext
+
+    def run(self, rec: Recorder | None = None):
+        c = rec.call if rec is not None else _direct
+        c("attn.scores", lambda: joinagg(self.s_spec, [self.Q, self.K], "sum", "product", out=self.S,
+                                         scale=self.scale, pred=self.pred))
+        c("attn.max", lambda: joinagg("bhst->bhs", [self.S], "max", "identity", out=self.m, pred=self.pred))
+        c("attn.sumexp", lambda: joinagg("bhst,bhs->bhs", [self.S, self.m], "sum", "exp_sub", out=self.l,
+                                         pred=self.pred))
+        c("attn.normalise", lambda: joinagg("bhst,bhs,bhs->bhst", [self.S, self.m, self.l], "none", "exp_sub_div",
+                                            out=self.P, pred=self.pred))
+        c("attn.values", lambda: joinagg(self.o_spec, [self.P, self.V], "sum", "product", out=self.O,
+                                         pred=self.pred))
+        return self.O
+
+    def flops(self) -> float:
+        e = self.ext
+        full = 2.0 * e["b"] * e["h"] * e["s"] * e["t"] * e["d"] * 2
+        return full
+
+
+class SwigluFFN:
+    """x [T, D] tiled (t_blocks, 4); w_gate, w_up [D, F] and w_down [F, D];
+    contracted dims in ``k_blocks`` blocks (partial products SUM-aggregate)."""
+
+    def __init__(self, x: Relation, w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
+                 k_blocks: int = 4, out: Relation | None = None):
+        T, D = x.dims
+        F = w_gate.shape[1]
+        tb = x.bounds[0]
+        dev = x.storage.device
+        self.x = x
+        # gate and up share their join: one relation [D, 2, F] (c = 0 gate, 1 up)
+        gu = torch.stack([w_gate, w_up], dim=1).contiguous()
+        self.wgu = Relation.from_dense(gu, [x.bounds[1], 2, k_blocks])
+        self.wd = Relation.from_dense(w_down.contiguous(), [k_blocks, x.bounds[1]])
+        self.gu = Relation("bf16", (2, T, F), [2, tb, k_blocks], device=dev)
+        half = T * F
+        self.G = view(self.gu, 0, (T, F), [tb, k_blocks])
+        self.U = view(self.gu, half, (T, F), [tb, k_blocks])
+        self.H = Relation("bf16", (T, F), [tb, k_blocks], device=dev)
+        self.Y = out if out is not None else Relation("bf16", (T, D), [tb, x.bounds[1]], device=dev)
+        self.T, self.D, self.F = T, D, F
+
+    def run(self, x: Relation | None = None, rec: Recorder | None = None):
+        x = x or self.x
+        c = rec.call if rec is not None else _direct
+        c("ffn.gate_up", lambda: joinagg("td,dcf->ctf", [x, self.wgu], "sum", "product", out=self.gu))
+        c("ffn.silu_mul", lambda: joinagg("tf,tf->tf", [self.G, self.U], "none", "silu_mul", out=self.H))
+        c("ffn.down", lambda: joinagg("tf,fd->td", [self.H, self.wd], "sum", "product", out=self.Y))
+        return self.Y
+
+    def flops(self) -> float:
+        return 2.0 * self.T * self.D * self.F * 3
+
+
+class LlamaBlock:
+    """Pre-norm LLaMA-style block over x [b * s, D] (bf16), tokens tiled one
+    sequence per block and the model dimension in ``d_blocks`` blocks."""
+
+    def __init__(self, b: int, s: int, D: int, n_heads: int, F: int, W: dict, eps: float = 1e-6,
+                 theta: float = 10000.0, d_blocks: int = 4, s_blocks: int = 4, device="cuda"):
+        self.b, self.s, self.D, self.H, self.F = b, s, D, n_heads, F
+        self.dh = D // n_heads
+        T = b * s
+        self.T = T
+        self.eps = eps
+        dev = device
+        db, sb = d_blocks, s_blocks
+        tb = b  # one block of tokens per sequence
+        self.x = Relation("bf16", (T, D), [tb, db], device=dev)
+        self.g1 = Relation.from_dense(W["g1"].contiguous(), [db])
+        self.g2 = Relation.from_dense(W["g2"].contiguous(), [db])
+        wqkv = torch.stack([W["wq"], W["wk"], W["wv"]], dim=1).contiguous()     # [D, 3, D]
+        self.wqkv = Relation.from_dense(wqkv, [db, 3, 1])
+        self.wo = Relation.from_dense(W["wo"].contiguous(), [db, db])
+        self.ms1 = Relation("f32", (T,), [tb], device=dev)
+        self.n1 = Relation("bf16", (T, D), [tb, db], device=dev)
+        self.qkv = Relation("bf16", (3, T, D), [3, tb, 1], device=dev)
+        hd = (b, s, n_heads, self.dh)
+        attn_parts = [b, sb, 1, 1]
+        self.q = view(self.qkv, 0, hd, attn_parts)
+        self.k = view(self.qkv, T * D, hd, attn_parts)
+        self.v = view(self.qkv, 2 * T * D, hd, attn_parts)
+        self.qr = Relation("bf16", hd, attn_parts, device=dev)
+        self.kr = Relation("bf16", hd, attn_parts, device=dev)
+        self.table = rope_table(s, self.dh, theta, device=dev)
+        self.attn = AttentionChain(self.qr, self.kr, self.v, scale=1.0 / math.sqrt(self.dh), causal=True,
+                                   qspec="bshd", kspec="bthd", vspec="bthd", ospec="bshd")
+        # the attention output, seen as [T, D] in blocks of s / s_blocks tokens x all heads ...
+        self.o_tok = view(self.attn.O, 0, (T, D), [b * sb, 1])
+        # ... re-blocked by the exchange into the O projection's contraction tiling
+        self.o_ex = Relation("bf16", (T, D), [tb, db], device=dev)
+        self.a = Relation("bf16", (T, D), [tb, db], device=dev)
+        self.h = Relation("bf16", (T, D), [tb, db], device=dev)
+        self.ms2 = Relation("f32", (T,), [tb], device=dev)
+        self.n2 = Relation("bf16", (T, D), [tb, db], device=dev)
+        self.y = Relation("bf16", (T, D), [tb, db], device=dev)
+        self.ffn = SwigluFFN(self.n2, W["w_gate"], W["w_up"], W["w_down"], k_blocks=db, out=None)
+        self.ffn_out = self.ffn.Y
+
+    def rmsnorm(self, x, ms, g, out, c, tag):
+        c(tag + ".sumsq", lambda: joinagg("td->t", [x], "sum", "square", out=ms, scale=1.0 / self.D))
+        c(tag + ".apply", lambda: joinagg("td,t,d->td", [x, ms, g], "none", "rms_apply", out=out, eps=self.eps))
+
+    def run(self, rec: Recorder | None = None):
+        c = rec.call if rec is not None else _direct
+        self.rmsnorm(self.x, self.ms1, self.g1, self.n1, c, "norm1")
+        c("qkv", lambda: joinagg("td,dce->cte", [self.n1, self.wqkv], "sum", "product", out=self.qkv))
+        c("rope.q", lambda: joinagg("bshd->bshd", [self.q], "none", "rope", out=self.qr, rope_table=self.table,
+                                    rope_pos="s"))
+        c("rope.k", lambda: joinagg("bshd->bshd", [self.k], "none", "rope", out=self.kr, rope_table=self.table,
+                                    rope_pos="s"))
+        self.attn.run(rec)
+        c("exchange.attn_out", lambda: exchange(self.o_tok, None, out=self.o_ex))
+        c("o_proj", lambda: joinagg("te,ed->td", [self.o_ex, self.wo], "sum", "product", out=self.a))
+        c("residual1", lambda: joinagg("td,td->td", [self.x, self.a], "none", "add", out=self.h))
+        self.rmsnorm(self.h, self.ms2, self.g2, self.n2, c, "norm2")
+        self.ffn.run(self.n2, rec)
+        c("residual2", lambda: joinagg("td,td->td", [self.h, self.ffn_out], "none", "add", out=self.y))
+        return self.y
+
+    def call_flops(self) -> dict:
+        """Algorithmic FLOPs of each contraction call."""
+        T, D, F = self.T, self.D, self.F
+        causal_pairs = self.b * self.H * self.s * (self.s + 1) / 2
+        return {"qkv": 2.0 * T * D * 3 * D, "o_proj": 2.0 * T * D * D, "ffn.gate_up": 2.0 * T * D * 2 * F,
+                "ffn.down": 2.0 * T * F * D, "attn.scores": 2.0 * causal_pairs * self.dh,
+                "attn.values": 2.0 * causal_pairs * self.dh}
+
+    def flops(self) -> dict:
+        """Algorithmic FLOPs: projections and FFN dense; attention over the
+        causal join (cells with t <= s)."""
+        T, D, F = self.T, self.D, self.F
+        proj = 2.0 * T * D * D * 4
+        ffn = 2.0 * T * D * F * 3
+        causal_pairs = self.b * self.H * self.s * (self.s + 1) / 2
+        attn = 2.0 * causal_pairs * self.dh * 2
+        return {"proj": proj, "ffn": ffn, "attn": attn, "total": proj + ffn + attn}

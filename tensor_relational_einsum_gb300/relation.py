@@ -98,6 +98,19 @@ class Relation:
             return out
         return exchange(whole, parts)
 
+    def load(self, t: torch.Tensor, stream=None) -> "Relation":
+        """Fill this relation with the row-major tensor ``t`` (same extents
+        and dtype) through the exchange kernel."""
+        t = t.contiguous()
+        if tuple(t.shape) != self.dims or t.dtype != _TORCH[self.dtype]:
+            raise ValueError("load: tensor shape or dtype differs from the relation")
+        if all(len(b) == 2 for b in self.bounds):
+            self.arena().copy_(t.reshape(-1))
+            return self
+        whole = Relation(self.dtype, self.dims, [1] * len(self.dims), storage=t.reshape(-1))
+        exchange(whole, None, out=self, stream=stream)
+        return self
+
     def to_dense(self) -> torch.Tensor:
         """The tensor, row-major, as a new CUDA tensor."""
         if all(len(b) == 2 for b in self.bounds):
