@@ -467,8 +467,55 @@ def run_ours(args, world, rank, local, dist):
     return 0
 
 
+def profile_case(name: str, reps: int):
+    """A small case of one kernel class for ncu captures (a few hundred MB
+    on the device, ``reps`` launches of the kernel of interest)."""
+    import torch
+
+    import synth
+    from tensor_relational_einsum_gb300.build import build
+    from tensor_relational_einsum_gb300.graphs import AttentionChain
+    from tensor_relational_einsum_gb300.relation import Relation, check, exchange, joinagg
+    build()
+    dev = torch.device("cuda", 0)
+    if name == "gemm":   # FFN gate+up contraction: x[8192,4096] . W[4096, 2, 11008], SUM over 4 blocks
+        x = Relation.from_dense(synth.make_torch("bf16", (8192, 4096), "normal", 21, 0, 1, device=dev), [1, 4])
+        w = Relation.from_dense(synth.make_torch("bf16", (4096, 2, 11008), "normal", 22, 0, 0.02, device=dev),
+                                [4, 2, 4])
+        y = Relation("bf16", (2, 8192, 11008), [2, 1, 4], device=dev)
+        fn = lambda: joinagg("td,dcf->ctf", [x, w], out=y)  # noqa: E731
+    elif name == "attn":  # attention chain b1 h32 s=t=2048 d128, t in 4 blocks
+        q, k, v = (synth.make_torch("bf16", (1, 32, 2048, 128), "normal", sd, 0, 1, device=dev) for sd in (1, 2, 3))
+        ch = AttentionChain(Relation.from_dense(q, [1, 32, 1, 1]), Relation.from_dense(k, [1, 32, 4, 1]),
+                            Relation.from_dense(v, [1, 32, 4, 1]))
+        fn = ch.run
+    elif name == "exchange":  # bf16 8192^2: 8x1 row blocks -> 16x16 tiles
+        X = Relation.from_dense(synth.make_torch("bf16", (8192, 8192), "uniform", 31, -1, 1, device=dev), [8, 1])
+        Y = Relation("bf16", (8192, 8192), [16, 16], device=dev)
+        fn = lambda: exchange(X, None, out=Y)  # noqa: E731
+    elif name == "norm":  # RMSNorm over [16384, 4096] bf16, model dim in 4 blocks
+        x = Relation.from_dense(synth.make_torch("bf16", (16384, 4096), "normal", 5, 0, 1, device=dev), [8, 4])
+        g = Relation.from_dense(torch.ones(4096, dtype=torch.bfloat16, device=dev), [4])
+        ms = Relation("f32", (16384,), [8], device=dev)
+        y = Relation("bf16", (16384, 4096), [8, 4], device=dev)
+
+        def fn():
+            joinagg("td->t", [x], "sum", "square", out=ms, scale=1.0 / 4096)
+            joinagg("td,t,d->td", [x, ms, g], "none", "rms_apply", out=y, eps=1e-6)
+    else:
+        raise SystemExit(f"unknown profile case {name!r}")
+    for _ in range(reps):
+        fn()
+    torch.cuda.synchronize()
+    check()
+    print(f"profile case {name}: {reps} runs ok")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile-case", choices=["gemm", "attn", "exchange", "norm"], default=None)
+    ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
@@ -477,6 +524,8 @@ def main():
     ap.add_argument("--no-components", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
+    if args.profile_case:
+        return profile_case(args.profile_case, args.reps)
     args.warmup = max(3, args.warmup)
     world, rank, local, dist = dist_setup(args)
     try:
