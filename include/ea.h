@@ -227,6 +227,28 @@ ea_status ea_exchange(ea_relation in, const ea_dim_part *new_parts, void *stream
  * may be NULL. */
 ea_status ea_last_plan(int32_t *kernel_class, int32_t *launches, int64_t *tiles, int64_t *groups, int64_t *tuples);
 
+/* The exchange for callers that must not allocate device memory.  This
+ * call has no counterpart in the paper.  ea_exchange and ea_joinagg_run
+ * upload their plans into memory they take from cudaMalloc; a process
+ * whose device memory is handed out by its own pool, a latency-sensitive
+ * path that cannot afford cudaMalloc's implicit device-wide
+ * synchronisation, or an embedding that forbids the library from owning
+ * device memory cannot accept that.  ea_exchange_noalloc re-blocks `in`
+ * into the tiling of `out` (same dtype and extents, arenas not
+ * overlapping; create both with ea_relation_create over your own memory)
+ * and calls no cudaMalloc, cudaFree or other allocating routine: its plan
+ * goes into one static device array of 1 MiB inside libea.so, which every
+ * GPU that loads the library holds until the process exits.  A plan larger
+ * than that (about 6000 overlay atoms, or more than 2048 split points in
+ * one dimension) is rejected with EA_ERR_UNSUPPORTED before anything is
+ * launched.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  The plan is copied into the array with
+ * cudaMemcpyAsync on `stream`, then the kernel runs on `stream`.  Every
+ * call shares the one array, so calls whose work overlaps on the GPU
+ * (different streams with no ordering between them) race on it. */
+ea_status ea_exchange_noalloc(ea_relation in, ea_relation out, void *stream);
+
 /* ------------------------------------------------ host-only planning hooks */
 
 /* The work list of a join-agg, computed on the host exactly as

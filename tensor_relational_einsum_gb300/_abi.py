@@ -83,10 +83,11 @@ def lib():
         L.ea_exchange_permutation.argtypes = [ctypes.c_int, P64, ctypes.POINTER(DimPart), ctypes.POINTER(DimPart), P64]
         L.ea_overlay_atoms.argtypes = [ctypes.c_int, P64, ctypes.POINTER(DimPart), ctypes.POINTER(DimPart), P64]
         L.ea_last_plan.argtypes = [P32, P32, P64, P64, P64]
+        L.ea_exchange_noalloc.argtypes = [VP, VP, VP]
         for name in ("ea_check", "ea_plan_cache_clear", "ea_relation_create", "ea_relation_destroy",
                      "ea_relation_info", "ea_relation_block", "ea_relation_data", "ea_relation_bounds",
                      "ea_joinagg_run", "ea_exchange", "ea_plan_worklist", "ea_exchange_permutation",
-                     "ea_overlay_atoms", "ea_last_plan"):
+                     "ea_overlay_atoms", "ea_last_plan", "ea_exchange_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         if L.ea_abi_version() != 1:
             raise ImportError("libea.so ABI version mismatch")
