@@ -232,6 +232,7 @@ def bench_components(peaks, device):
     qkv_b = 4 * 32 * 2048 * 128 * 2
     ml = 4 * 32 * 2048 * 4
     alg = {"attn.scores": 2 * qkv_b + S_bytes, "attn.max": S_bytes + ml, "attn.sumexp": S_bytes + 2 * ml,
+           "attn.stats": S_bytes + 2 * ml,
            "attn.normalise": S_bytes + 2 * ml + P_bytes, "attn.values": P_bytes + 2 * qkv_b}
     per = {}
     for name, (kind, n, ts) in sm.items():

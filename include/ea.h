@@ -62,8 +62,13 @@ typedef struct ea_relation_s *ea_relation; /* opaque handle */
 typedef enum { EA_F32 = 0, EA_BF16 = 1 } ea_dtype;
 
 /* Aggregation op (+) of Definition 3.7 step (2).  NONE: every output block
- * receives exactly one tuple (elementwise joins). */
-typedef enum { EA_AGG_NONE = 0, EA_AGG_SUM = 1, EA_AGG_MAX = 2 } ea_agg;
+ * receives exactly one tuple (elementwise joins).  MAX_SUMEXP: the softmax
+ * statistics as one aggregation with two results -- out = MAX of the
+ * mapped values over the aggregated letters, opts->out2 = SUM over them of
+ * exp(value - max); the same as a MAX join-agg followed by a SUM join-agg
+ * with the EXP_SUB map, computed in one pass with the associative,
+ * commutative merge (m1,l1)+(m2,l2) = (M, l1 e^(m1-M) + l2 e^(m2-M)). */
+typedef enum { EA_AGG_NONE = 0, EA_AGG_SUM = 1, EA_AGG_MAX = 2, EA_AGG_MAX_SUMEXP = 3 } ea_agg;
 
 /* The per-tuple concrete operator f, applied cell by cell to the joined
  * values v0, v1, v2 (inputs in spec order), computed in fp32:
@@ -123,7 +128,10 @@ typedef struct {
  *              relies on the operand holding 0 in removed cells.
  *   rope_pos   ROPE: the position letter.
  *   rope_table ROPE: device pointer, fp32 [rope_npos][d/2][2] = (cos, sin)
- *              of angle pos * theta^(-2i/d).  Not owned.               */
+ *              of angle pos * theta^(-2i/d).  Not owned.
+ *   out2       EA_AGG_MAX_SUMEXP: the relation receiving the SUM of exp;
+ *              same extents and tiling as the output, created by the
+ *              caller.  Ignored otherwise.                               */
 typedef struct {
     int32_t out_dtype;
     float scale;
@@ -134,7 +142,8 @@ typedef struct {
     char reserved0;
     const float *rope_table;
     int64_t rope_npos;
-    int64_t reserved[4];
+    ea_relation out2;
+    int64_t reserved[3];
 } ea_opts;
 
 /* ------------------------------------------------------------ basics */
@@ -202,7 +211,7 @@ ea_status ea_relation_bounds(ea_relation rel, int dim, int32_t *nblocks, int64_t
  *   contraction  SUM of PRODUCT over two inputs with >= 1 aggregated letter:
  *                grouped contraction, the SUM over a group's tuples fused in
  *                the accumulator (bf16: tcgen05/TMEM/TMA; fp32: FFMA);
- *   row reduction  SUM/MAX whose aggregated letters are the trailing
+ *   row reduction  SUM/MAX/MAX_SUMEXP whose aggregated letters are the trailing
  *                letters of input 0: one warp per output cell, warp-shuffle
  *                (+) across the row and across the group's tuples;
  *   elementwise  agg NONE: one output block per tuple, vectorised. */

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(PKG, "libea.so")
 
 F32, BF16 = 0, 1
 DTYPES = {"f32": F32, "bf16": BF16}
-AGGS = {"none": 0, "sum": 1, "max": 2}
+AGGS = {"none": 0, "sum": 1, "max": 2, "max_sumexp": 3}
 MAPS = {"product": 0, "identity": 1, "silu_mul": 2, "add": 3, "exp_sub": 4, "div": 5, "square": 6,
         "rms_apply": 7, "exp_sub_div": 8, "rope": 9}
 STATUS = {0: "EA_OK", 1: "EA_ERR_SPEC", 2: "EA_ERR_SHAPE", 3: "EA_ERR_PARTITION", 4: "EA_ERR_DTYPE",
@@ -42,7 +42,7 @@ class Opts(ctypes.Structure):
     _fields_ = [("out_dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("eps", ctypes.c_float),
                 ("pred_lo", ctypes.c_char), ("pred_hi", ctypes.c_char), ("rope_pos", ctypes.c_char),
                 ("reserved0", ctypes.c_char), ("rope_table", ctypes.c_void_p), ("rope_npos", ctypes.c_int64),
-                ("reserved", ctypes.c_int64 * 4)]
+                ("out2", ctypes.c_void_p), ("reserved", ctypes.c_int64 * 3)]
 
 
 _lib = None

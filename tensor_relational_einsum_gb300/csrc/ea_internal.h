@@ -158,6 +158,7 @@ struct EwParams {
     int64_t rope_npos;
     int64_t rope_half;                 // pairs per position in rope_table
     int has_vec, has_scalar;           // which kernel variants have tiles
+    int stream_mask;                   // bit k: input k runs along the row (else broadcast)
     int *err;
 };
 cudaError_t launch_ewise(const EwParams &p, int num_sms, cudaStream_t st);
@@ -171,11 +172,14 @@ struct RrParams {
     int in_dtype[kMaxIn];
     char *out;
     int out_dtype;
+    char *out2;                        // MAX_SUMEXP: the SUM of exp
+    int out2_dtype;
     int n_in;
     int map;
     int agg;
     float scale, eps;
     int pred;
+    int stream_mask;                   // bit k: input k runs along the row (else broadcast)
     int *err;
 };
 cudaError_t launch_rowreduce(const RrParams &p, int num_sms, cudaStream_t st);

@@ -270,6 +270,7 @@ struct JoinCtx {
     const float *rope_table;
     int64_t rope_npos;
     char rope_pos;
+    ea_relation_s *out2;
 };
 
 // Special letters of an elementwise / row-reduction view.
@@ -374,14 +375,23 @@ static ea_status build_ewise(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan *p)
         int32_t id = (int32_t)items.size();
         items.push_back(it);
         if (it.rows == 0 || it.len == 0) continue;
-        // tiles of about 32K elements
+        // tiles of about 32K cells whose row count is a whole number of the
+        // CTA's row passes (8 warps x rows per warp, as the kernel packs them)
         const int64_t target = 32768;
         if (it.len >= target) {
             for (int64_t r = 0; r < it.rows; r++)
                 for (int64_t c0 = 0; c0 < it.len; c0 += target)
                     tiles.push_back(EwTile{id, 0, r, 1, c0, std::min(target, it.len - c0)});
         } else {
+            const int64_t cpr = it.vec ? it.len / 8 : it.len;
+            int ns = 0;
+            for (int k = 0; k < n_in; k++) ns += sp.term[k].find(sp.out.back()) != std::string::npos;
+            const int64_t u = ns <= 1 ? 4 : 2;
+            int64_t lpr = 32;
+            while (lpr > 1 && lpr * u > cpr) lpr /= 2;
+            const int64_t pass = 8 * (32 / lpr);
             int64_t per = std::max<int64_t>(1, target / it.len);
+            per = std::max<int64_t>(pass, per / pass * pass);
             for (int64_t r = 0; r < it.rows; r += per)
                 tiles.push_back(EwTile{id, 0, r, std::min(per, it.rows - r), 0, it.len});
         }
@@ -412,6 +422,11 @@ static ea_status build_ewise(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan *p)
     e.rope_npos = j.rope_npos;
     e.rope_half = j.lt.t[sp.out.back() - 'a'].extent / 2;
     e.has_vec = e.has_scalar = 0;
+    e.stream_mask = 0;
+    for (int k = 0; k < n_in; k++) {
+        bool runs = sp.term[k].find(sp.out.back()) != std::string::npos;
+        if (runs) e.stream_mask |= 1 << k;
+    }
     for (const EwItem &x : items) {
         if (x.rows == 0 || x.len == 0) continue;
         if (x.vec) e.has_vec = 1;
@@ -500,7 +515,14 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
         G.i1 = (int32_t)items.size();
         int32_t gid = (int32_t)groups.size();
         groups.push_back(G);
-        const int64_t per = 64;
+        // rows per tile: two passes of the CTA's 8 warps, each pass packing
+        // as many rows per warp as the kernel does for this segment length
+        const EwItem &first = items[G.i0];
+        const int64_t chunks = first.vec ? first.len / 8 : first.len;
+        const int64_t u = 4;
+        int64_t lpr = 32;
+        while (lpr > 1 && lpr * u > chunks) lpr /= 2;
+        const int64_t per = 2 * 8 * (32 / lpr);
         for (int64_t r = 0; r < rows; r += per) tiles.push_back(RrTile{gid, 0, r, std::min(per, rows - r)});
     }
     Blob b;
@@ -519,12 +541,17 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
     }
     r.out = j.out->arena;
     r.out_dtype = j.out->dtype;
+    r.out2 = j.out2 ? j.out2->arena : nullptr;
+    r.out2_dtype = j.out2 ? j.out2->dtype : 0;
     r.n_in = n_in;
     r.map = j.map;
     r.agg = j.agg;
     r.scale = j.scale;
     r.eps = j.eps;
     r.pred = j.pred_lo ? 1 : 0;
+    r.stream_mask = 0;
+    for (int k = 0; k < n_in; k++)
+        if (sp.term[k].find(red.back()) != std::string::npos) r.stream_mask |= 1 << k;
     return EA_OK;
 }
 
@@ -815,10 +842,16 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
         maps.push_back(m);
         int32_t gid = (int32_t)groups.size();
         groups.push_back(TG);
+        // Grouped raster: bands of kBand m-tiles, each band swept across all
+        // n-tiles with m fastest, so the tiles in flight at once share a
+        // small set of A rows and B columns that stays in L2.
+        const int64_t kBand = 16;
+        const int64_t nm = (G.M + 127) / 128, nn = (G.N + bn - 1) / bn;
         for (int64_t bb = 0; bb < G.nb; bb++)
-            for (int64_t n0 = 0; n0 < G.N; n0 += bn)
-                for (int64_t m0 = 0; m0 < G.M; m0 += 128)
-                    tiles.push_back(TcTile{gid, (int32_t)bb, (int32_t)m0, (int32_t)n0});
+            for (int64_t mb = 0; mb < nm; mb += kBand)
+                for (int64_t ni = 0; ni < nn; ni++)
+                    for (int64_t mi = mb; mi < std::min(nm, mb + kBand); mi++)
+                        tiles.push_back(TcTile{gid, (int32_t)bb, (int32_t)(mi * 128), (int32_t)(ni * bn)});
     }
     if (tiles.size() > (size_t)INT32_MAX) return EA_ERR_UNSUPPORTED;
     Blob b;
@@ -982,7 +1015,7 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
     set_error(EA_OK, "");
     if (!spec || !inputs || !out) return set_error(EA_ERR_ARG, "ea_joinagg_run: NULL argument");
     if (n_parts < 0 || (n_parts > 0 && !parts)) return set_error(EA_ERR_ARG, "ea_joinagg_run: bad parts");
-    if (agg < EA_AGG_NONE || agg > EA_AGG_MAX) return set_error(EA_ERR_ARG, "ea_joinagg_run: unknown agg %d", agg);
+    if (agg < EA_AGG_NONE || agg > EA_AGG_MAX_SUMEXP) return set_error(EA_ERR_ARG, "ea_joinagg_run: unknown agg %d", agg);
     if (map < EA_MAP_PRODUCT || map > EA_MAP_ROPE) return set_error(EA_ERR_ARG, "ea_joinagg_run: unknown map %d", map);
     std::lock_guard<std::mutex> lk(g_mu);
     JoinCtx j;
@@ -1010,6 +1043,8 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
     j.rope_table = o.rope_table;
     j.rope_npos = o.rope_npos;
     j.rope_pos = o.rope_pos;
+    j.out2 = agg == EA_AGG_MAX_SUMEXP ? o.out2 : nullptr;
+    if (agg == EA_AGG_MAX_SUMEXP && !j.out2) return set_error(EA_ERR_ARG, "MAX_SUMEXP needs opts->out2");
     // Letter tilings: from the inputs, which must agree; explicit parts must match.
     for (int k = 0; k < n_inputs; k++)
         for (int d = 0; d < inputs[k]->rank; d++) {
@@ -1090,8 +1125,13 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
             kind = kRowReduce;
         }
     }
-    if (odt == EA_BF16 && kind == kRowReduce && agg == EA_AGG_MAX) {
-        // fine: MAX is exact in any dtype
+    if (j.out2) {
+        if (j.out2->rank != orank) return set_error(EA_ERR_SHAPE, "out2 has rank %d, the output %d", j.out2->rank, orank);
+        for (int d = 0; d < orank; d++) {
+            if (j.out2->dims[d] != odims[d]) return set_error(EA_ERR_SHAPE, "out2 extent mismatch in dim %d", d);
+            if (!same_tiling(j.out2, d, j.lt.t[j.sp.out[d] - 'a']))
+                return set_error(EA_ERR_PARTITION, "out2 is tiled differently from the output letters");
+        }
     }
     if (!orel) {
         s = ea_relation_create((ea_dtype)odt, orank, odims, oparts, nullptr, &orel);
@@ -1119,6 +1159,7 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
     key.v(j.rope_pos);
     key.v(j.rope_table);
     key.v(j.rope_npos);
+    if (j.out2) key.rel(j.out2);
     cudaStream_t st = (cudaStream_t)stream;
     DevPlan *p = nullptr;
     auto it = g_cache.find(key.s);

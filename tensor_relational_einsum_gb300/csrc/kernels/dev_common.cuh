@@ -69,6 +69,27 @@ __device__ __forceinline__ float cell_map(int map, float v0, float v1, float v2,
     }
 }
 
+// The per-cell operator as a compile-time choice (the hot loops of the
+// elementwise and row-reduction kernels are instantiated per map).  exp and
+// division use the fast hardware approximations (a few ulp), well inside
+// the fp32 and bf16 tolerances of the outputs.
+template <int MAP>
+__device__ __forceinline__ float fmap(float v0, float v1, float v2, float scale, float eps) {
+    if constexpr (MAP == EA_MAP_PRODUCT) return scale * v0 * v1 * v2;
+    else if constexpr (MAP == EA_MAP_IDENTITY) return scale * v0;
+    else if constexpr (MAP == EA_MAP_SILU_MUL) return __fdividef(v0, 1.0f + __expf(-v0)) * v1;
+    else if constexpr (MAP == EA_MAP_ADD) return v0 + v1;
+    else if constexpr (MAP == EA_MAP_EXP_SUB) return __expf(v0 - v1);
+    else if constexpr (MAP == EA_MAP_DIV) return __fdividef(v0, v1);
+    else if constexpr (MAP == EA_MAP_SQUARE) return scale * v0 * v0;
+    else if constexpr (MAP == EA_MAP_RMS_APPLY) return v0 * rsqrtf(v1 + eps) * v2;
+    else if constexpr (MAP == EA_MAP_EXP_SUB_DIV) return __fdividef(__expf(v0 - v1), v2);
+    else return v0;
+}
+
+__device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
 // Decode a row index over the first nd outer dims (innermost last).
 __device__ __forceinline__ void decode_row(const EwItem &it, int64_t r, int64_t *coord) {
 #pragma unroll

@@ -1,16 +1,25 @@
-// rowreduce.cu -- row-reduction join-agg kernel (aggregation SUM or MAX
-// over the trailing letters of input 0).
+// rowreduce.cu -- row-reduction join-agg kernel (aggregation SUM, MAX, or
+// the softmax statistics MAX + SUM of exp, over the trailing letters of
+// input 0).
 //
 // "Every Kernel Is a Join", Section 1 and Definition 3.7: softmax and
 // normalisation are a join (the scores, possibly with a broadcast row
 // statistic) followed by an aggregation over the reduced letters.  When the
 // reduced letters are split into blocks, every output block has one
 // function specification per block of the reduced letters, and step (2)
-// combines their outputs with the aggregation op.  Here one warp owns one
-// output cell: it walks every function specification of the cell's group,
-// maps the row segment 8 cells per lane (16-byte loads), accumulates in
-// fp32, and combines lanes with warp shuffles -- the per-tuple results and
-// their aggregation are fused, with no partial results in memory.
+// combines their outputs with the aggregation op.  One warp owns one output
+// cell: it walks every function specification of the cell's group, streams
+// the row segment with several 16-byte loads in flight per lane,
+// accumulates in fp32 and combines lanes with warp shuffles -- the
+// per-tuple results and their aggregation are fused, with no partial
+// results in memory.  The row loop is instantiated per map, and rows the
+// predicate leaves whole skip the per-cell test.
+//
+// The statistics variant computes m = MAX_t v and l = SUM_t exp(v - m) in
+// one pass with the associative, commutative merge
+//   (m1, l1) (+) (m2, l2) = (M, l1 exp(m1 - M) + l2 exp(m2 - M)),
+//   M = max(m1, m2), identity (-inf, 0),
+// so the scores are read once instead of twice.
 #include <algorithm>
 #include <math.h>
 
@@ -23,82 +32,228 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-__device__ __forceinline__ float agg_op(int agg, float a, float b) { return agg == EA_AGG_MAX ? fmaxf(a, b) : a + b; }
+struct Stats {
+    float m, l;
+};
 
-__global__ void __launch_bounds__(kThreads) rowreduce_kernel(const RrParams p) {
+__device__ __forceinline__ Stats stats_merge(Stats a, Stats b) {
+    const float M = fmaxf(a.m, b.m);
+    if (M == -INFINITY) return Stats{-INFINITY, 0.0f};
+    return Stats{M, a.l * __expf(a.m - M) + b.l * __expf(b.m - M)};
+}
+
+struct Acc {
+    float a;   // SUM / MAX accumulator
+    Stats st;  // statistics accumulator
+};
+
+template <int MAP>
+__device__ __forceinline__ float rmap(const RrParams &p, float x0, float x1, float x2) {
+    if constexpr (MAP >= 0) return fmap<MAP>(x0, x1, x2, p.scale, p.eps);
+    else return cell_map(p.map, x0, x1, x2, p.scale, p.eps);
+}
+
+// Accumulate one row segment of one function specification.  MAP < 0 /
+// MASK < 0: map / streamed inputs read at run time (generic instance).
+template <int MAP, int AGG, int NIN, int MASK>
+__device__ __forceinline__ void rr_seg(const RrParams &p, Acc &acc, const int64_t *ioff, const int64_t *iinn,
+                                       const float *bc, int64_t len, int64_t cmin, int64_t cmax, bool vec, int sl,
+                                       int lpr) {
+    constexpr int NS = MASK < 0 ? NIN : ((MASK & 1) + ((MASK >> 1) & 1) + ((MASK >> 2) & 1));
+    constexpr int U = NS <= 1 ? 4 : 2;
+    const int mask = MASK < 0 ? (p.stream_mask | 1) : MASK;
+    const bool whole = cmin <= 0 && cmax >= len - 1;
+    const int64_t step = (int64_t)lpr * 8;  // cells between a lane's consecutive chunks
+    if (vec) {
+        for (int64_t c0 = (int64_t)sl * 8; c0 < len; c0 += step * U) {
+            float v[U][NS][8];
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int64_t c = c0 + (int64_t)u * step;
+                if (c >= len) continue;
+                int s = 0;
+#pragma unroll
+                for (int k = 0; k < NIN; k++) {
+                    if (MASK >= 0 && !((MASK >> k) & 1)) continue;
+                    if (MASK < 0 && !((mask >> k) & 1)) {
+#pragma unroll
+                        for (int e = 0; e < 8; e++) v[u][k][e] = bc[k];
+                    } else {
+                        ld8(p.in[k], p.in_dtype[k], ioff[k] + c, v[u][MASK < 0 ? k : s]);
+                    }
+                    s++;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int64_t c = c0 + (int64_t)u * step;
+                if (c >= len) continue;
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    float x[3] = {1.0f, 1.0f, 1.0f};
+                    int s = 0;
+#pragma unroll
+                    for (int k = 0; k < NIN; k++) {
+                        if constexpr (MASK < 0) x[k] = v[u][k][e];
+                        else x[k] = ((MASK >> k) & 1) ? v[u][s++][e] : bc[k];
+                    }
+                    f[e] = rmap<MAP>(p, x[0], x[1], x[2]);
+                    if (!whole && (c + e < cmin || c + e > cmax)) f[e] = AGG == EA_AGG_SUM ? 0.0f : -INFINITY;
+                }
+                if constexpr (AGG == EA_AGG_MAX_SUMEXP) {
+                    float mx = f[0];
+#pragma unroll
+                    for (int e = 1; e < 8; e++) mx = fmaxf(mx, f[e]);
+                    if (mx > acc.st.m) {
+                        acc.st.l *= __expf(acc.st.m - mx);  // exp(-inf) = 0 on the first chunk
+                        acc.st.m = mx;
+                    }
+                    if (acc.st.m != -INFINITY) {
+                        float s = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < 8; e++) s += __expf(f[e] - acc.st.m);
+                        acc.st.l += s;
+                    }
+                } else if constexpr (AGG == EA_AGG_MAX) {
+#pragma unroll
+                    for (int e = 0; e < 8; e++) acc.a = fmaxf(acc.a, f[e]);
+                } else {
+                    float s = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < 8; e++) s += f[e];
+                    acc.a += s;
+                }
+            }
+        }
+    } else {
+        for (int64_t c = sl; c < len; c += lpr) {
+            if (c < cmin || c > cmax) continue;
+            float x[3] = {1.0f, 1.0f, 1.0f};
+#pragma unroll
+            for (int k = 0; k < NIN; k++)
+                x[k] = ((mask >> k) & 1) ? ld_elem(p.in[k], p.in_dtype[k], ioff[k] + c * iinn[k]) : bc[k];
+            const float f = rmap<MAP>(p, x[0], x[1], x[2]);
+            if constexpr (AGG == EA_AGG_MAX_SUMEXP) acc.st = stats_merge(acc.st, Stats{f, 1.0f});
+            else if constexpr (AGG == EA_AGG_MAX) acc.a = fmaxf(acc.a, f);
+            else acc.a += f;
+        }
+    }
+}
+
+template <int AGG, int MAP, int NIN, int MASK>
+__global__ void __launch_bounds__(kThreads, 3) rowreduce_kernel(const RrParams p) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const float ident = p.agg == EA_AGG_MAX ? -INFINITY : 0.0f;
+    const int mask = MASK < 0 ? (p.stream_mask | 1) : MASK;
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const RrTile T = p.tiles[t];
         const RrGroup G = p.groups[T.group];
-        for (int64_t rr = warp; rr < T.nrows; rr += kWarps) {
-            const int64_t r = T.row0 + rr;
-            float acc = ident;
+        // lanes per row: a power of two giving each lane about U chunks of
+        // a row segment; short segments pack several rows to a warp
+        constexpr int NSr = MASK < 0 ? NIN : ((MASK & 1) + ((MASK >> 1) & 1) + ((MASK >> 2) & 1));
+        constexpr int Ur = NSr <= 1 ? 4 : 2;
+        const int64_t seg = p.items[G.i0].len;
+        const int64_t chunks = p.items[G.i0].vec ? seg / 8 : seg;
+        int lpr = 32;
+        while (lpr > 1 && (int64_t)lpr * Ur > chunks) lpr /= 2;
+        const int rpw = 32 / lpr;
+        const int sub = lane / lpr, sl = lane % lpr;
+        const int64_t nrows_pad = (T.nrows + rpw - 1) / rpw * rpw;
+        for (int64_t rr0 = (int64_t)warp * rpw; rr0 < nrows_pad; rr0 += (int64_t)kWarps * rpw) {
+            const int64_t rr = rr0 + sub;
+            const bool live = rr < T.nrows;  // lanes past the tile still join the shuffles
+            const int64_t r = T.row0 + (live ? rr : T.nrows - 1);
+            Acc acc;
+            acc.a = AGG == EA_AGG_SUM ? 0.0f : -INFINITY;
+            acc.st = Stats{-INFINITY, 0.0f};
             int64_t coord[kViewDims];
             for (int i = G.i0; i < G.i1; i++) {
                 const EwItem &it = p.items[i];
                 decode_row(it, r, coord);
-                int64_t ioff[kMaxIn];
-                for (int k = 0; k < p.n_in; k++) {
+                const int nd = it.nd;
+                int64_t ioff[NIN], iinn[NIN];
+                float bc[NIN];
+#pragma unroll
+                for (int k = 0; k < NIN; k++) {
                     ioff[k] = it.in_base[k];
-                    for (int d = 0; d < it.nd; d++) ioff[k] += coord[d] * it.istr[k][d];
+                    iinn[k] = it.in_inner[k];
+                    for (int d = 0; d < nd; d++) ioff[k] += coord[d] * it.istr[k][d];
                 }
-                // broadcast operands: one value per row
-                float bc[kMaxIn] = {1.0f, 1.0f, 1.0f};
-                for (int k = 1; k < p.n_in; k++)
-                    if (it.in_inner[k] == 0) bc[k] = ld_elem(p.in[k], p.in_dtype[k], ioff[k]);
+#pragma unroll
+                for (int k = 0; k < NIN; k++)
+                    bc[k] = ((mask >> k) & 1) ? 1.0f : ld_elem(p.in[k], p.in_dtype[k], ioff[k]);
                 const int64_t len = it.len;
-                if (it.vec) {
-                    for (int64_t c0 = (int64_t)lane * 8; c0 < len; c0 += 32 * 8) {
-                        float v[kMaxIn][8];
-                        ld8(p.in[0], p.in_dtype[0], ioff[0] + c0, v[0]);
-                        for (int k = 1; k < kMaxIn; k++) {
-                            if (k < p.n_in && it.in_inner[k] == 1) ld8(p.in[k], p.in_dtype[k], ioff[k] + c0, v[k]);
-                            else
-#pragma unroll
-                                for (int e = 0; e < 8; e++) v[k][e] = bc[k];
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; e++) {
-                            if (p.pred) {
-                                int64_t a = special_coord(it, 0, coord, c0 + e), b = special_coord(it, 1, coord, c0 + e);
-                                if (a > b) continue;
-                            }
-                            acc = agg_op(p.agg, acc, cell_map(p.map, v[0][e], v[1][e], v[2][e], p.scale, p.eps));
-                        }
-                    }
-                } else {
-                    for (int64_t c = lane; c < len; c += 32) {
-                        if (p.pred) {
-                            int64_t a = special_coord(it, 0, coord, c), b = special_coord(it, 1, coord, c);
-                            if (a > b) continue;
-                        }
-                        float v0 = ld_elem(p.in[0], p.in_dtype[0], ioff[0] + c);
-                        float v1 = p.n_in > 1 ? (it.in_inner[1] ? ld_elem(p.in[1], p.in_dtype[1], ioff[1] + c) : bc[1]) : 1.0f;
-                        float v2 = p.n_in > 2 ? (it.in_inner[2] ? ld_elem(p.in[2], p.in_dtype[2], ioff[2] + c) : bc[2]) : 1.0f;
-                        acc = agg_op(p.agg, acc, cell_map(p.map, v0, v1, v2, p.scale, p.eps));
-                    }
+                int64_t cmin = 0, cmax = len - 1;
+                if (p.pred) {
+                    if (it.sdim[0] == kViewDims) cmax = min64(cmax, special_coord(it, 1, coord, 0) - it.slo[0]);
+                    else if (it.sdim[1] == kViewDims) cmin = max64(cmin, special_coord(it, 0, coord, 0) - it.slo[1]);
+                    else if (special_coord(it, 0, coord, 0) > special_coord(it, 1, coord, 0)) cmax = -1;
+                }
+                if (!live) cmax = -1;
+                rr_seg<MAP, AGG, NIN, MASK>(p, acc, ioff, iinn, bc, len, cmin, cmax, it.vec != 0, sl, lpr);
+            }
+            // combine the lanes of each row (xor within aligned groups of lpr lanes)
+            if constexpr (AGG == EA_AGG_MAX_SUMEXP) {
+                for (int o = lpr / 2; o > 0; o >>= 1) {
+                    Stats other{__shfl_xor_sync(0xffffffffu, acc.st.m, o), __shfl_xor_sync(0xffffffffu, acc.st.l, o)};
+                    acc.st = stats_merge(acc.st, other);
+                }
+            } else {
+                for (int o = lpr / 2; o > 0; o >>= 1) {
+                    const float y = __shfl_xor_sync(0xffffffffu, acc.a, o);
+                    acc.a = AGG == EA_AGG_MAX ? fmaxf(acc.a, y) : acc.a + y;
                 }
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc = agg_op(p.agg, acc, __shfl_xor_sync(0xffffffffu, acc, o));
-            if (lane == 0) {
+            if (sl == 0 && live) {
                 const EwItem &it0 = p.items[G.i0];
                 decode_row(it0, r, coord);
                 int64_t ooff = it0.out_base;
                 for (int d = 0; d < it0.nd; d++) ooff += coord[d] * it0.ostr[d];
-                st_elem(p.out, p.out_dtype, ooff, acc);
+                if constexpr (AGG == EA_AGG_MAX_SUMEXP) {
+                    st_elem(p.out, p.out_dtype, ooff, acc.st.m);
+                    st_elem(p.out2, p.out2_dtype, ooff, acc.st.l);
+                } else {
+                    st_elem(p.out, p.out_dtype, ooff, acc.a);
+                }
             }
         }
     }
 }
 
+template <int AGG, int MAP, int NIN, int MASK>
+cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st) {
+    rowreduce_kernel<AGG, MAP, NIN, MASK><<<(unsigned)grid, kThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int AGG>
+cudaError_t generic(const RrParams &p, int64_t grid, cudaStream_t st) {
+    if (p.n_in == 1) return go<AGG, -1, 1, -1>(p, grid, st);
+    if (p.n_in == 2) return go<AGG, -1, 2, -1>(p, grid, st);
+    return go<AGG, -1, 3, -1>(p, grid, st);
+}
+
 }  // namespace
 
+// Specialised instances for the row reductions of the hot path; the rest
+// run the generic instances (map and streamed inputs read at run time).
 cudaError_t launch_rowreduce(const RrParams &p, int num_sms, cudaStream_t st) {
     int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)num_sms * 8);
-    rowreduce_kernel<<<(unsigned)grid, kThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    const int n = p.n_in, m = p.stream_mask | 1;
+    switch (p.agg) {
+    case EA_AGG_MAX_SUMEXP:
+        if (n == 1 && p.map == EA_MAP_IDENTITY) return go<EA_AGG_MAX_SUMEXP, EA_MAP_IDENTITY, 1, 1>(p, grid, st);
+        return generic<EA_AGG_MAX_SUMEXP>(p, grid, st);
+    case EA_AGG_MAX:
+        if (n == 1 && p.map == EA_MAP_IDENTITY) return go<EA_AGG_MAX, EA_MAP_IDENTITY, 1, 1>(p, grid, st);
+        return generic<EA_AGG_MAX>(p, grid, st);
+    default:
+        if (n == 1 && p.map == EA_MAP_SQUARE) return go<EA_AGG_SUM, EA_MAP_SQUARE, 1, 1>(p, grid, st);
+        if (n == 1 && p.map == EA_MAP_IDENTITY) return go<EA_AGG_SUM, EA_MAP_IDENTITY, 1, 1>(p, grid, st);
+        if (n == 2 && m == 1 && p.map == EA_MAP_EXP_SUB) return go<EA_AGG_SUM, EA_MAP_EXP_SUB, 2, 1>(p, grid, st);
+        if (n == 2 && m == 3 && p.map == EA_MAP_PRODUCT) return go<EA_AGG_SUM, EA_MAP_PRODUCT, 2, 3>(p, grid, st);
+        return generic<EA_AGG_SUM>(p, grid, st);
+    }
 }
 
 }  // namespace ea

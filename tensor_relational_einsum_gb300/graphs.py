@@ -78,8 +78,10 @@ class AttentionChain:
     score scale."""
 
     def __init__(self, Q: Relation, K: Relation, V: Relation, scale: float = 1.0, causal: bool = False,
-                 qspec: str = "bhsd", kspec: str = "bhtd", vspec: str = "bhtd", ospec: str = "bhsd"):
+                 qspec: str = "bhsd", kspec: str = "bhtd", vspec: str = "bhtd", ospec: str = "bhsd",
+                 fused_stats: bool = True):
         self.Q, self.K, self.V = Q, K, V
+        self.fused_stats = fused_stats
         self.scale, self.pred = scale, ("ts" if causal else None)
         self.s_spec = f"{qspec},{kspec}->bhst"
         self.o_spec = f"bhst,{vspec}->{ospec}"
@@ -99,9 +101,14 @@ class AttentionChain:
         c = rec.call if rec is not None else _direct
         c("attn.scores", lambda: joinagg(self.s_spec, [self.Q, self.K], "sum", "product", out=self.S,
                                          scale=self.scale, pred=self.pred))
-        c("attn.max", lambda: joinagg("bhst->bhs", [self.S], "max", "identity", out=self.m, pred=self.pred))
-        c("attn.sumexp", lambda: joinagg("bhst,bhs->bhs", [self.S, self.m], "sum", "exp_sub", out=self.l,
-                                         pred=self.pred))
+        if self.fused_stats:
+            # MAX and SUM of exp in one pass over the scores
+            c("attn.stats", lambda: joinagg("bhst->bhs", [self.S], "max_sumexp", "identity", out=self.m,
+                                            out2=self.l, pred=self.pred))
+        else:
+            c("attn.max", lambda: joinagg("bhst->bhs", [self.S], "max", "identity", out=self.m, pred=self.pred))
+            c("attn.sumexp", lambda: joinagg("bhst,bhs->bhs", [self.S, self.m], "sum", "exp_sub", out=self.l,
+                                             pred=self.pred))
         c("attn.normalise", lambda: joinagg("bhst,bhs,bhs->bhst", [self.S, self.m, self.l], "none", "exp_sub_div",
                                             out=self.P, pred=self.pred))
         c("attn.values", lambda: joinagg(self.o_spec, [self.P, self.V], "sum", "product", out=self.O,

@@ -151,9 +151,11 @@ def output_layout(spec: str, inputs):
 def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Relation | None = None,
             out_dtype: str | None = None, scale: float = 1.0, eps: float = 0.0, pred: str | None = None,
             parts: dict | None = None, rope_table: torch.Tensor | None = None, rope_pos: str | None = None,
-            stream=None) -> Relation:
+            out2: Relation | None = None, stream=None) -> Relation:
     """Run one join-agg ("Every Kernel Is a Join", Definition 3.7) with
-    libea.so.  ``pred="ts"`` keeps joined tuples with t <= s."""
+    libea.so.  ``pred="ts"`` keeps joined tuples with t <= s.  With
+    ``agg="max_sumexp"`` the output receives the MAX and ``out2`` the SUM
+    of exp(value - max)."""
     if out is None:
         dims, bounds = output_layout(spec, inputs)
         out = Relation(out_dtype or inputs[0].dtype, dims, bounds, device=inputs[0].storage.device)
@@ -169,6 +171,8 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
         o.rope_table = rope_table.data_ptr()
         o.rope_npos = rope_table.shape[0]
         o.rope_pos = rope_pos.encode()
+    if out2 is not None:
+        o.out2 = out2.handle.value
     h = ctypes.c_void_p(out.handle.value)
     check_status(lib().ea_joinagg_run(spec.encode(), handles, len(inputs), ip, n_parts, AGGS[agg], MAPS[map],
                                       ctypes.byref(o), ctypes.c_void_p(_stream_ptr(stream)), ctypes.byref(h)))

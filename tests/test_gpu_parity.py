@@ -222,6 +222,26 @@ def test_rowreduce_max_sum_square():
     assert rel_frob(dense64(ms), want) <= 1e-5
 
 
+@pytest.mark.parametrize("parts,pred", [([1, 3, 2, [0, 100, 200, 300]], None), ([1, 3, 2, [0, 100, 200, 300]], "ts"),
+                                        ([1, 1, 1, [0, 37, 300]], "ts")])
+def test_rowreduce_fused_softmax_stats(parts, pred):
+    """MAX_SUMEXP against the oracle's two join-aggs: m = MAX_t S and
+    l = SUM_t exp(S - m) (cells with t > s removed when pred is set); the
+    last case has 37-wide blocks (scalar path)."""
+    from tensor_relational_einsum_gb300.relation import Relation
+    S = synth.make("f32", (1, 3, 40, 300), "normal", 19, 0, 3)
+    RS = rel(S, parts)
+    m = Relation("f32", (1, 3, 40), [parts[0], parts[1], parts[2]])
+    l = Relation("f32", (1, 3, 40), [parts[0], parts[1], parts[2]])
+    joinagg("bhst->bhs", [RS], agg="max_sumexp", map="identity", out=m, out2=l, pred=pred)
+    assert last()["kernel"] == "rowreduce"
+    want_m = oracle.joinagg("bhst->bhs", [S.to_f64()], "identity", "max", pred=pred)
+    E = oracle.joinagg("bhst,bhs->bhst", [S.to_f64(), want_m], "exp_sub", "none", pred=pred)
+    want_l = oracle.joinagg("bhst->bhs", [E], "identity", "sum")
+    assert np.array_equal(dense64(m), want_m)
+    assert rel_frob(dense64(l), want_l) <= 1e-5
+
+
 def test_rowreduce_causal_predicate():
     S = synth.make("f32", (1, 2, 64, 64), "normal", 18, 0, 2)
     RS = rel(S, [1, 2, 4, 4])
