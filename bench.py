@@ -494,6 +494,19 @@ def profile_case(name: str, reps: int):
         X = Relation.from_dense(synth.make_torch("bf16", (8192, 8192), "uniform", 31, -1, 1, device=dev), [8, 1])
         Y = Relation("bf16", (8192, 8192), [16, 16], device=dev)
         fn = lambda: exchange(X, None, out=Y)  # noqa: E731
+    elif name == "ffn_ew":  # SiLU(gate) * up over [16384, 11008] and a residual add over [16384, 4096]
+        gu = Relation.from_dense(synth.make_torch("bf16", (2, 16384, 11008), "normal", 7, 0, 1, device=dev), [2, 8, 4])
+        from tensor_relational_einsum_gb300.graphs import view
+        G = view(gu, 0, (16384, 11008), [8, 4])
+        U = view(gu, 16384 * 11008, (16384, 11008), [8, 4])
+        H = Relation("bf16", (16384, 11008), [8, 4], device=dev)
+        a = Relation.from_dense(synth.make_torch("bf16", (16384, 4096), "normal", 8, 0, 1, device=dev), [8, 4])
+        b = Relation.from_dense(synth.make_torch("bf16", (16384, 4096), "normal", 9, 0, 1, device=dev), [8, 4])
+        c = Relation("bf16", (16384, 4096), [8, 4], device=dev)
+
+        def fn():
+            joinagg("tf,tf->tf", [G, U], "none", "silu_mul", out=H)
+            joinagg("td,td->td", [a, b], "none", "add", out=c)
     elif name == "norm":  # RMSNorm over [16384, 4096] bf16, model dim in 4 blocks
         x = Relation.from_dense(synth.make_torch("bf16", (16384, 4096), "normal", 5, 0, 1, device=dev), [8, 4])
         g = Relation.from_dense(torch.ones(4096, dtype=torch.bfloat16, device=dev), [4])
@@ -515,7 +528,7 @@ def profile_case(name: str, reps: int):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["gemm", "attn", "exchange", "norm"], default=None)
+    ap.add_argument("--profile-case", choices=["gemm", "attn", "exchange", "norm", "ffn_ew"], default=None)
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)

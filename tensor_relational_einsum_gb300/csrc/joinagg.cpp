@@ -384,9 +384,14 @@ static ea_status build_ewise(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan *p)
                     tiles.push_back(EwTile{id, 0, r, 1, c0, std::min(target, it.len - c0)});
         } else {
             const int64_t cpr = it.vec ? it.len / 8 : it.len;
-            int ns = 0;
-            for (int k = 0; k < n_in; k++) ns += sp.term[k].find(sp.out.back()) != std::string::npos;
-            const int64_t u = ns <= 1 ? 4 : 2;
+            int ns = 0, bytes = 16;
+            for (int k = 0; k < n_in; k++)
+                if (sp.term[k].find(sp.out.back()) != std::string::npos) {
+                    ns++;
+                    if (j.in[k]->dtype == EA_F32) bytes = 32;
+                }
+            // the kernel's batch: about 128 bytes of streamed inputs per lane
+            const int64_t u = !it.vec ? 4 : std::max<int64_t>(1, (128 / bytes) / std::max(1, ns));
             int64_t lpr = 32;
             while (lpr > 1 && lpr * u > cpr) lpr /= 2;
             const int64_t pass = 8 * (32 / lpr);
@@ -519,7 +524,16 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
         // as many rows per warp as the kernel does for this segment length
         const EwItem &first = items[G.i0];
         const int64_t chunks = first.vec ? first.len / 8 : first.len;
-        const int64_t u = 4;
+        int ns = 0, bytes = 16, dts = 0;
+        for (int k = 0; k < n_in; k++)
+            if (sp.term[k].find(red.back()) != std::string::npos) {
+                ns++;
+                bytes = j.in[k]->dtype == EA_F32 ? std::max(bytes, 32) : bytes;
+                dts |= 1 << j.in[k]->dtype;
+            }
+        if (dts == 3) bytes = 32;  // mixed dtypes: the generic instance batches like fp32
+        // the kernel's batch: about 128 bytes of streamed inputs per lane
+        const int64_t u = std::max<int64_t>(1, (128 / bytes) / std::max(1, ns));
         int64_t lpr = 32;
         while (lpr > 1 && lpr * u > chunks) lpr /= 2;
         const int64_t per = 2 * 8 * (32 / lpr);

@@ -69,6 +69,30 @@ __device__ __forceinline__ float cell_map(int map, float v0, float v1, float v2,
     }
 }
 
+// Raw 16-byte chunk loads (kept packed in registers until used) and their
+// conversion: a bf16 chunk of 8 cells is one uint4, an fp32 chunk two.
+template <bool kBf16>
+__device__ __forceinline__ void ld_raw(const char *base, int64_t i, uint4 *r) {
+    if constexpr (kBf16) {
+        r[0] = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(base) + i));
+    } else {
+        const uint4 *p = reinterpret_cast<const uint4 *>(reinterpret_cast<const float *>(base) + i);
+        r[0] = __ldg(p);
+        r[1] = __ldg(p + 1);
+    }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ float raw_at(const uint4 *r, int e) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(r);
+    if constexpr (kBf16) {
+        const uint32_t x = w[e >> 1];
+        return __uint_as_float((e & 1) ? (x & 0xFFFF0000u) : (x << 16));
+    } else {
+        return __uint_as_float(w[e]);
+    }
+}
+
 // The per-cell operator as a compile-time choice (the hot loops of the
 // elementwise and row-reduction kernels are instantiated per map).  exp and
 // division use the fast hardware approximations (a few ulp), well inside

@@ -47,17 +47,30 @@ __device__ __forceinline__ float apply(const EwParams &p, float x0, float x1, fl
 
 __device__ __forceinline__ bool streams(int mask, int k) { return (mask >> k) & 1; }
 
+// Cells per chunk and chunks per batch: every lane keeps about 128 bytes of
+// streamed inputs in flight (raw, converted only when used).
+template <bool kVec, int NS, int DT>
+struct Batch {
+    static constexpr int V = kVec ? 8 : 1;
+    static constexpr int BYTES = DT == 1 ? 16 : 32;  // one chunk of one input
+    static constexpr int U = !kVec ? 4 : (NS <= 1 ? 128 / BYTES : (128 / BYTES) / NS > 0 ? (128 / BYTES) / NS : 1);
+};
+
 // Stream one row: chunks sl, sl + lpr, ... of V cells, U chunks per batch.
-template <int MAP, bool kVec, int NIN, int MASK>
+// DT: 1 = streamed inputs are bf16, 2 = fp32, 0 = read at run time.
+template <int MAP, bool kVec, int NIN, int MASK, int DT>
 __device__ __forceinline__ void ew_row(const EwParams &p, const Row<NIN> &w, int cpr, int sl, int lpr, bool masked,
                                        int64_t out_inner) {
     constexpr int V = kVec ? 8 : 1;
     constexpr int NS = MASK < 0 ? NIN : ((MASK & 1) + ((MASK >> 1) & 1) + ((MASK >> 2) & 1));
     constexpr int NSV = NS > 0 ? NS : 1;
-    constexpr int U = NS <= 1 ? 4 : 2;
+    constexpr int U = Batch<kVec, NS, DT>::U;
+    constexpr bool kRaw = kVec && DT != 0 && MASK >= 0;
+    constexpr bool kB16 = DT == 1;
     const int mask = MASK < 0 ? p.stream_mask : MASK;
     for (int c0 = sl; c0 < cpr; c0 += lpr * U) {
-        float v[U][NSV][V];
+        uint4 raw[kRaw ? U : 1][kRaw ? NSV : 1][kB16 ? 1 : 2];
+        float v[kRaw ? 1 : U][kRaw ? 1 : NSV][kRaw ? 1 : V];
 #pragma unroll
         for (int u = 0; u < U; u++) {
             const int c = c0 + u * lpr;
@@ -67,7 +80,9 @@ __device__ __forceinline__ void ew_row(const EwParams &p, const Row<NIN> &w, int
 #pragma unroll
             for (int k = 0; k < NIN; k++) {
                 if (MASK >= 0 && !streams(MASK, k)) continue;
-                if (MASK < 0 && !streams(mask, k)) {
+                if constexpr (kRaw) {
+                    ld_raw<kB16>(p.in[k], w.ioff[k] + col, raw[u][s]);
+                } else if (MASK < 0 && !streams(mask, k)) {
 #pragma unroll
                     for (int e = 0; e < V; e++) v[u][k][e] = w.bc[k];
                 } else if (kVec) {
@@ -83,13 +98,17 @@ __device__ __forceinline__ void ew_row(const EwParams &p, const Row<NIN> &w, int
             const int c = c0 + u * lpr;
             if (c >= cpr) continue;
             const int col = c * V;
+            auto val = [&](int s, int k, int e) -> float {
+                if constexpr (kRaw) return raw_at<kB16>(raw[u][s], e);
+                else return v[u][MASK < 0 ? k : s][e];
+            };
             float o[V];
             if constexpr (MAP == EA_MAP_ROPE) {
                 if constexpr (kVec) {
 #pragma unroll
                     for (int e = 0; e < V; e += 2) {
                         const float2 cs = __ldg(w.tab + w.pair0 + ((col + e) >> 1));
-                        const float x0 = v[u][0][e], x1 = v[u][0][e + 1];
+                        const float x0 = val(0, 0, e), x1 = val(0, 0, e + 1);
                         o[e] = x0 * cs.x - x1 * cs.y;
                         o[e + 1] = x0 * cs.y + x1 * cs.x;
                     }
@@ -98,7 +117,8 @@ __device__ __forceinline__ void ew_row(const EwParams &p, const Row<NIN> &w, int
                     const float2 cs = __ldg(w.tab + (g >> 1));
                     const float partner =
                         ld_elem(p.in[0], p.in_dtype[0], w.ioff[0] + (col + ((g & 1) ? -1 : 1)) * w.iinn[0]);
-                    o[0] = (g & 1) ? partner * cs.y + v[u][0][0] * cs.x : v[u][0][0] * cs.x - partner * cs.y;
+                    const float x = val(0, 0, 0);
+                    o[0] = (g & 1) ? partner * cs.y + x * cs.x : x * cs.x - partner * cs.y;
                 }
             } else {
 #pragma unroll
@@ -107,8 +127,9 @@ __device__ __forceinline__ void ew_row(const EwParams &p, const Row<NIN> &w, int
                     int s = 0;
 #pragma unroll
                     for (int k = 0; k < NIN; k++) {
-                        if constexpr (MASK < 0) x[k] = v[u][k][e];
-                        else x[k] = streams(MASK, k) ? v[u][s++][e] : w.bc[k];
+                        if constexpr (MASK < 0) x[k] = val(k, k, e);
+                        else if (streams(MASK, k)) x[k] = val(s++, k, e);
+                        else x[k] = w.bc[k];
                     }
                     o[e] = apply<MAP, NIN, MASK>(p, x[0], x[1], x[2]);
                 }
@@ -124,7 +145,7 @@ __device__ __forceinline__ void ew_row(const EwParams &p, const Row<NIN> &w, int
     }
 }
 
-template <int MAP, bool kVec, int NIN, int MASK>
+template <int MAP, bool kVec, int NIN, int MASK, int DT>
 __global__ void __launch_bounds__(kThreads, 3) ewise_kernel(const EwParams p) {
     constexpr int V = kVec ? 8 : 1;
     __shared__ EwItem sit;
@@ -145,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 3) ewise_kernel(const EwParams p) {
         // the row, so short rows pack several to a warp and every lane keeps
         // several loads in flight
         constexpr int NSr = MASK < 0 ? NIN : ((MASK & 1) + ((MASK >> 1) & 1) + ((MASK >> 2) & 1));
-        constexpr int Ur = NSr <= 1 ? 4 : 2;
+        constexpr int Ur = Batch<kVec, NSr, DT>::U;
         int lpr = 32;
         while (lpr > 1 && lpr * Ur > cpr) lpr /= 2;
         const int rpw = 32 / lpr;             // rows per warp pass
@@ -187,15 +208,28 @@ __global__ void __launch_bounds__(kThreads, 3) ewise_kernel(const EwParams p) {
                 w.tab = reinterpret_cast<const float2 *>(p.rope_table) + special_coord(sit, 2, coord, 0) * p.rope_half;
                 w.pair0 = (sit.inner_lo + T.col0) >> 1;
             }
-            ew_row<MAP, kVec, NIN, MASK>(p, w, cpr, sl, lpr, masked, sit.out_inner);
+            ew_row<MAP, kVec, NIN, MASK, DT>(p, w, cpr, sl, lpr, masked, sit.out_inner);
         }
     }
 }
 
+// DT: the dtype every streamed input shares (1 bf16, 2 fp32), 0 if mixed.
 template <int MAP, int NIN, int MASK>
 cudaError_t go(const EwParams &p, int64_t grid, bool vec, cudaStream_t st) {
-    if (vec) ewise_kernel<MAP, true, NIN, MASK><<<(unsigned)grid, kThreads, 0, st>>>(p);
-    else ewise_kernel<MAP, false, NIN, MASK><<<(unsigned)grid, kThreads, 0, st>>>(p);
+    int dt = -1;
+    for (int k = 0; k < NIN; k++) {
+        if (MASK >= 0 && !((MASK >> k) & 1)) continue;
+        const int d = p.in_dtype[k] == EA_BF16 ? 1 : 2;
+        dt = dt < 0 ? d : (dt == d ? dt : 0);
+    }
+    if (MASK < 0 || dt <= 0 || !vec) {
+        if (vec) ewise_kernel<MAP, true, NIN, MASK, 0><<<(unsigned)grid, kThreads, 0, st>>>(p);
+        else ewise_kernel<MAP, false, NIN, MASK, 0><<<(unsigned)grid, kThreads, 0, st>>>(p);
+    } else if (dt == 1) {
+        ewise_kernel<MAP, true, NIN, MASK, 1><<<(unsigned)grid, kThreads, 0, st>>>(p);
+    } else {
+        ewise_kernel<MAP, true, NIN, MASK, 2><<<(unsigned)grid, kThreads, 0, st>>>(p);
+    }
     return cudaGetLastError();
 }
 

@@ -55,18 +55,29 @@ __device__ __forceinline__ float rmap(const RrParams &p, float x0, float x1, flo
 
 // Accumulate one row segment of one function specification.  MAP < 0 /
 // MASK < 0: map / streamed inputs read at run time (generic instance).
-template <int MAP, int AGG, int NIN, int MASK>
+// Chunks per batch: about 128 bytes of streamed inputs in flight per lane.
+// DT: 1 = streamed inputs bf16, 2 = fp32, 0 = read at run time.
+template <int NS, int DT>
+struct RrBatch {
+    static constexpr int BYTES = DT == 1 ? 16 : 32;
+    static constexpr int U = (128 / BYTES) / (NS > 0 ? NS : 1) > 0 ? (128 / BYTES) / (NS > 0 ? NS : 1) : 1;
+};
+
+template <int MAP, int AGG, int NIN, int MASK, int DT>
 __device__ __forceinline__ void rr_seg(const RrParams &p, Acc &acc, const int64_t *ioff, const int64_t *iinn,
                                        const float *bc, int64_t len, int64_t cmin, int64_t cmax, bool vec, int sl,
                                        int lpr) {
     constexpr int NS = MASK < 0 ? NIN : ((MASK & 1) + ((MASK >> 1) & 1) + ((MASK >> 2) & 1));
-    constexpr int U = NS <= 1 ? 4 : 2;
+    constexpr int U = RrBatch<NS, DT>::U;
+    constexpr bool kRaw = DT != 0 && MASK >= 0;
+    constexpr bool kB16 = DT == 1;
     const int mask = MASK < 0 ? (p.stream_mask | 1) : MASK;
     const bool whole = cmin <= 0 && cmax >= len - 1;
     const int64_t step = (int64_t)lpr * 8;  // cells between a lane's consecutive chunks
     if (vec) {
         for (int64_t c0 = (int64_t)sl * 8; c0 < len; c0 += step * U) {
-            float v[U][NS][8];
+            uint4 raw[kRaw ? U : 1][kRaw ? NS : 1][kB16 ? 1 : 2];
+            float v[kRaw ? 1 : U][kRaw ? 1 : NS][kRaw ? 1 : 8];
 #pragma unroll
             for (int u = 0; u < U; u++) {
                 const int64_t c = c0 + (int64_t)u * step;
@@ -75,7 +86,9 @@ __device__ __forceinline__ void rr_seg(const RrParams &p, Acc &acc, const int64_
 #pragma unroll
                 for (int k = 0; k < NIN; k++) {
                     if (MASK >= 0 && !((MASK >> k) & 1)) continue;
-                    if (MASK < 0 && !((mask >> k) & 1)) {
+                    if constexpr (kRaw) {
+                        ld_raw<kB16>(p.in[k], ioff[k] + c, raw[u][s]);
+                    } else if (MASK < 0 && !((mask >> k) & 1)) {
 #pragma unroll
                         for (int e = 0; e < 8; e++) v[u][k][e] = bc[k];
                     } else {
@@ -95,8 +108,15 @@ __device__ __forceinline__ void rr_seg(const RrParams &p, Acc &acc, const int64_
                     int s = 0;
 #pragma unroll
                     for (int k = 0; k < NIN; k++) {
-                        if constexpr (MASK < 0) x[k] = v[u][k][e];
-                        else x[k] = ((MASK >> k) & 1) ? v[u][s++][e] : bc[k];
+                        if constexpr (MASK < 0) {
+                            x[k] = v[u][k][e];
+                        } else if ((MASK >> k) & 1) {
+                            if constexpr (kRaw) x[k] = raw_at<kB16>(raw[u][s], e);
+                            else x[k] = v[u][s][e];
+                            s++;
+                        } else {
+                            x[k] = bc[k];
+                        }
                     }
                     f[e] = rmap<MAP>(p, x[0], x[1], x[2]);
                     if (!whole && (c + e < cmin || c + e > cmax)) f[e] = AGG == EA_AGG_SUM ? 0.0f : -INFINITY;
@@ -141,7 +161,7 @@ __device__ __forceinline__ void rr_seg(const RrParams &p, Acc &acc, const int64_
     }
 }
 
-template <int AGG, int MAP, int NIN, int MASK>
+template <int AGG, int MAP, int NIN, int MASK, int DT>
 __global__ void __launch_bounds__(kThreads, 3) rowreduce_kernel(const RrParams p) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int mask = MASK < 0 ? (p.stream_mask | 1) : MASK;
@@ -151,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 3) rowreduce_kernel(const RrParams p
         // lanes per row: a power of two giving each lane about U chunks of
         // a row segment; short segments pack several rows to a warp
         constexpr int NSr = MASK < 0 ? NIN : ((MASK & 1) + ((MASK >> 1) & 1) + ((MASK >> 2) & 1));
-        constexpr int Ur = NSr <= 1 ? 4 : 2;
+        constexpr int Ur = RrBatch<NSr, DT>::U;
         const int64_t seg = p.items[G.i0].len;
         const int64_t chunks = p.items[G.i0].vec ? seg / 8 : seg;
         int lpr = 32;
@@ -190,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 3) rowreduce_kernel(const RrParams p
                     else if (special_coord(it, 0, coord, 0) > special_coord(it, 1, coord, 0)) cmax = -1;
                 }
                 if (!live) cmax = -1;
-                rr_seg<MAP, AGG, NIN, MASK>(p, acc, ioff, iinn, bc, len, cmin, cmax, it.vec != 0, sl, lpr);
+                rr_seg<MAP, AGG, NIN, MASK, DT>(p, acc, ioff, iinn, bc, len, cmin, cmax, it.vec != 0, sl, lpr);
             }
             // combine the lanes of each row (xor within aligned groups of lpr lanes)
             if constexpr (AGG == EA_AGG_MAX_SUMEXP) {
@@ -220,9 +240,18 @@ __global__ void __launch_bounds__(kThreads, 3) rowreduce_kernel(const RrParams p
     }
 }
 
+// DT: the dtype every streamed input shares (1 bf16, 2 fp32), 0 if mixed.
 template <int AGG, int MAP, int NIN, int MASK>
 cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st) {
-    rowreduce_kernel<AGG, MAP, NIN, MASK><<<(unsigned)grid, kThreads, 0, st>>>(p);
+    int dt = -1;
+    for (int k = 0; k < NIN; k++) {
+        if (MASK >= 0 && !((MASK >> k) & 1)) continue;
+        const int d = p.in_dtype[k] == EA_BF16 ? 1 : 2;
+        dt = dt < 0 ? d : (dt == d ? dt : 0);
+    }
+    if (MASK < 0 || dt <= 0) rowreduce_kernel<AGG, MAP, NIN, MASK, 0><<<(unsigned)grid, kThreads, 0, st>>>(p);
+    else if (dt == 1) rowreduce_kernel<AGG, MAP, NIN, MASK, 1><<<(unsigned)grid, kThreads, 0, st>>>(p);
+    else rowreduce_kernel<AGG, MAP, NIN, MASK, 2><<<(unsigned)grid, kThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 
