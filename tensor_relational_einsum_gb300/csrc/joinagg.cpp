@@ -391,14 +391,28 @@ static ea_status build_ewise(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan *p)
                     if (j.in[k]->dtype == EA_F32) bytes = 32;
                 }
             // the kernel's batch: about 128 bytes of streamed inputs per lane
-            const int64_t u = !it.vec ? 4 : std::max<int64_t>(1, (128 / bytes) / std::max(1, ns));
+            // (RoPE batches 4 chunks: it also loads the (cos, sin) table)
+            const int64_t u = !it.vec || j.map == EA_MAP_ROPE ? 4 : std::max<int64_t>(1, (128 / bytes) / std::max(1, ns));
             int64_t lpr = 32;
             while (lpr > 1 && lpr * u > cpr) lpr /= 2;
             const int64_t pass = 8 * (32 / lpr);
             int64_t per = std::max<int64_t>(1, target / it.len);
             per = std::max<int64_t>(pass, per / pass * pass);
-            for (int64_t r = 0; r < it.rows; r += per)
-                tiles.push_back(EwTile{id, 0, r, std::min(per, it.rows - r), 0, it.len});
+            // A tile either stays inside one run of the innermost row dim, or
+            // covers whole runs inside one run of the second-innermost dim; the
+            // kernel then addresses its rows with two strides.
+            const int64_t run = it.nd > 0 ? it.ext[it.nd - 1] : 1;
+            const int64_t run2 = it.nd > 1 ? run * it.ext[it.nd - 2] : run;
+            if (run >= per) {
+                for (int64_t r0 = 0; r0 < it.rows; r0 += run)
+                    for (int64_t r = r0; r < r0 + run; r += per)
+                        tiles.push_back(EwTile{id, 0, r, std::min(per, r0 + run - r), 0, it.len});
+            } else {
+                const int64_t perr = std::max<int64_t>(run, per / run * run);
+                for (int64_t r0 = 0; r0 < it.rows; r0 += run2)
+                    for (int64_t r = r0; r < r0 + run2; r += perr)
+                        tiles.push_back(EwTile{id, 0, r, std::min(perr, r0 + run2 - r), 0, it.len});
+            }
         }
     }
     (void)es_out;
@@ -442,7 +456,6 @@ static ea_status build_ewise(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan *p)
 
 // Row reduction: the aggregated letters are the trailing letters of input 0.
 static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan *p) {
-    (void)c;
     const Spec &sp = j.sp;
     int n_in = sp.n_in;
     const std::string &red = sp.contracted;
@@ -463,6 +476,7 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
     std::vector<EwItem> items;
     std::vector<RrGroup> groups;
     std::vector<RrTile> tiles;
+    int64_t max_items = 0;
     int inner_letter = red.size() == 1 ? red[0] - 'a' : -2;
     for (size_t g = 0; g < j.wl.groups.size(); g++) {
         BlockView ov;
@@ -520,8 +534,10 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
         G.i1 = (int32_t)items.size();
         int32_t gid = (int32_t)groups.size();
         groups.push_back(G);
-        // rows per tile: two passes of the CTA's 8 warps, each pass packing
-        // as many rows per warp as the kernel does for this segment length
+        // rows per tile: four passes of the CTA's 8 warps, each pass packing
+        // as many rows per warp as the kernel does for this segment length;
+        // a tile never crosses a run of the innermost row dimension, so the
+        // offsets inside it are linear in the row index
         const EwItem &first = items[G.i0];
         const int64_t chunks = first.vec ? first.len / 8 : first.len;
         int ns = 0, bytes = 16, dts = 0;
@@ -536,8 +552,13 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
         const int64_t u = std::max<int64_t>(1, (128 / bytes) / std::max(1, ns));
         int64_t lpr = 32;
         while (lpr > 1 && lpr * u > chunks) lpr /= 2;
-        const int64_t per = 2 * 8 * (32 / lpr);
-        for (int64_t r = 0; r < rows; r += per) tiles.push_back(RrTile{gid, 0, r, std::min(per, rows - r)});
+        // four CTA passes per tile, or one when the whole reduction has few rows
+        const int64_t pass = 8 * (32 / lpr);
+        const int64_t per = rows * (int64_t)j.wl.groups.size() >= 4 * pass * 8 * c->num_sms ? 4 * pass : pass;
+        const int64_t run = first.nd > 0 ? first.ext[first.nd - 1] : 1;
+        for (int64_t r0 = 0; r0 < rows; r0 += run)
+            for (int64_t r = r0; r < r0 + run; r += per) tiles.push_back(RrTile{gid, 0, r, std::min(per, r0 + run - r)});
+        max_items = std::max<int64_t>(max_items, G.i1 - G.i0);
     }
     Blob b;
     size_t oi = b.add_vec(items), og = b.add_vec(groups), ot = b.add_vec(tiles);
@@ -563,6 +584,8 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
     r.scale = j.scale;
     r.eps = j.eps;
     r.pred = j.pred_lo ? 1 : 0;
+    r.max_items = (int)max_items;
+    r.tile_linear = 1;
     r.stream_mask = 0;
     for (int k = 0; k < n_in; k++)
         if (sp.term[k].find(red.back()) != std::string::npos) r.stream_mask |= 1 << k;

@@ -241,6 +241,136 @@ __global__ void __launch_bounds__(kThreads, 3) rowreduce_kernel(const RrParams p
 }
 
 // DT: the dtype every streamed input shares (1 bf16, 2 fp32), 0 if mixed.
+constexpr int kTileItems = 64;
+
+// Per tuple, the geometry of the current tile: inside a tile every row is
+// one step along the innermost row dimension, so offsets and predicate
+// bounds are linear in the row index.
+template <int NIN>
+struct TileItem {
+    int64_t off[NIN];   // input offsets at the tile's first row
+    int64_t rstr[NIN];  // their change per row
+    int64_t inn[NIN];   // strides along the reduced letters
+    int64_t len;
+    int64_t inner_lo;   // global coordinate of reduced index 0 (predicate)
+    int64_t a0, b0;     // the predicate letters' global values at the first row
+    int32_t da, db;     // their change per row (0 or 1)
+    int32_t mode;       // 0 no predicate, 1 lo letter reduced, 2 hi letter reduced, 3 neither
+    int32_t vec;
+};
+
+template <int AGG, int MAP, int NIN, int MASK, int DT>
+__global__ void __launch_bounds__(kThreads, 3) rowreduce_tile_kernel(const RrParams p) {
+    __shared__ TileItem<NIN> ti[kTileItems];
+    __shared__ int64_t s_out0, s_ostr;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int mask = MASK < 0 ? (p.stream_mask | 1) : MASK;
+    constexpr int NSr = MASK < 0 ? NIN : ((MASK & 1) + ((MASK >> 1) & 1) + ((MASK >> 2) & 1));
+    constexpr int Ur = RrBatch<NSr, DT>::U;
+    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        const RrTile T = p.tiles[t];
+        const RrGroup G = p.groups[T.group];
+        const int n = G.i1 - G.i0;
+        __syncthreads();
+        if (threadIdx.x < n) {
+            const EwItem &it = p.items[G.i0 + threadIdx.x];
+            int64_t cd[kViewDims];
+            decode_row(it, T.row0, cd);
+            const int last = it.nd - 1;
+            TileItem<NIN> q;
+#pragma unroll
+            for (int k = 0; k < NIN; k++) {
+                int64_t o = it.in_base[k];
+                for (int d = 0; d < it.nd; d++) o += cd[d] * it.istr[k][d];
+                q.off[k] = o;
+                q.rstr[k] = last >= 0 ? it.istr[k][last] : 0;
+                q.inn[k] = it.in_inner[k];
+            }
+            q.len = it.len;
+            q.vec = it.vec;
+            q.mode = 0;
+            q.inner_lo = 0;
+            q.a0 = q.b0 = 0;
+            q.da = q.db = 0;
+            if (p.pred) {
+                q.a0 = special_coord(it, 0, cd, 0);
+                q.b0 = special_coord(it, 1, cd, 0);
+                q.da = it.sdim[0] == last && last >= 0 ? 1 : 0;
+                q.db = it.sdim[1] == last && last >= 0 ? 1 : 0;
+                if (it.sdim[0] == kViewDims) {
+                    q.mode = 1;
+                    q.inner_lo = it.slo[0];
+                } else if (it.sdim[1] == kViewDims) {
+                    q.mode = 2;
+                    q.inner_lo = it.slo[1];
+                } else {
+                    q.mode = 3;
+                }
+            }
+            ti[threadIdx.x] = q;
+            if (threadIdx.x == 0) {
+                int64_t o = it.out_base;
+                for (int d = 0; d < it.nd; d++) o += cd[d] * it.ostr[d];
+                s_out0 = o;
+                s_ostr = last >= 0 ? it.ostr[last] : 0;
+            }
+        }
+        __syncthreads();
+        const int64_t chunks = ti[0].vec ? ti[0].len / 8 : ti[0].len;
+        int lpr = 32;
+        while (lpr > 1 && (int64_t)lpr * Ur > chunks) lpr /= 2;
+        const int rpw = 32 / lpr;
+        const int sub = lane / lpr, sl = lane % lpr;
+        const int64_t nrows_pad = (T.nrows + rpw - 1) / rpw * rpw;
+        for (int64_t rr0 = (int64_t)warp * rpw; rr0 < nrows_pad; rr0 += (int64_t)kWarps * rpw) {
+            const int64_t rr = rr0 + sub;
+            const bool live = rr < T.nrows;  // lanes past the tile still join the shuffles
+            const int64_t dr = live ? rr : T.nrows - 1;
+            Acc acc;
+            acc.a = AGG == EA_AGG_SUM ? 0.0f : -INFINITY;
+            acc.st = Stats{-INFINITY, 0.0f};
+            for (int i = 0; i < n; i++) {
+                const TileItem<NIN> &q = ti[i];
+                int64_t ioff[NIN], iinn[NIN];
+                float bc[NIN];
+#pragma unroll
+                for (int k = 0; k < NIN; k++) {
+                    ioff[k] = q.off[k] + dr * q.rstr[k];
+                    iinn[k] = q.inn[k];
+                    bc[k] = ((mask >> k) & 1) ? 1.0f : ld_elem(p.in[k], p.in_dtype[k], ioff[k]);
+                }
+                const int64_t len = q.len;
+                int64_t cmin = 0, cmax = len - 1;
+                if (q.mode == 1) cmax = min64(cmax, q.b0 + q.db * dr - q.inner_lo);
+                else if (q.mode == 2) cmin = max64(cmin, q.a0 + q.da * dr - q.inner_lo);
+                else if (q.mode == 3 && q.a0 + q.da * dr > q.b0 + q.db * dr) cmax = -1;
+                if (!live) cmax = -1;
+                rr_seg<MAP, AGG, NIN, MASK, DT>(p, acc, ioff, iinn, bc, len, cmin, cmax, q.vec != 0, sl, lpr);
+            }
+            if constexpr (AGG == EA_AGG_MAX_SUMEXP) {
+                for (int o = lpr / 2; o > 0; o >>= 1) {
+                    Stats other{__shfl_xor_sync(0xffffffffu, acc.st.m, o), __shfl_xor_sync(0xffffffffu, acc.st.l, o)};
+                    acc.st = stats_merge(acc.st, other);
+                }
+            } else {
+                for (int o = lpr / 2; o > 0; o >>= 1) {
+                    const float y = __shfl_xor_sync(0xffffffffu, acc.a, o);
+                    acc.a = AGG == EA_AGG_MAX ? fmaxf(acc.a, y) : acc.a + y;
+                }
+            }
+            if (sl == 0 && live) {
+                const int64_t ooff = s_out0 + dr * s_ostr;
+                if constexpr (AGG == EA_AGG_MAX_SUMEXP) {
+                    st_elem(p.out, p.out_dtype, ooff, acc.st.m);
+                    st_elem(p.out2, p.out2_dtype, ooff, acc.st.l);
+                } else {
+                    st_elem(p.out, p.out_dtype, ooff, acc.a);
+                }
+            }
+        }
+    }
+}
+
 template <int AGG, int MAP, int NIN, int MASK>
 cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st) {
     int dt = -1;
@@ -249,9 +379,16 @@ cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st) {
         const int d = p.in_dtype[k] == EA_BF16 ? 1 : 2;
         dt = dt < 0 ? d : (dt == d ? dt : 0);
     }
-    if (MASK < 0 || dt <= 0) rowreduce_kernel<AGG, MAP, NIN, MASK, 0><<<(unsigned)grid, kThreads, 0, st>>>(p);
-    else if (dt == 1) rowreduce_kernel<AGG, MAP, NIN, MASK, 1><<<(unsigned)grid, kThreads, 0, st>>>(p);
-    else rowreduce_kernel<AGG, MAP, NIN, MASK, 2><<<(unsigned)grid, kThreads, 0, st>>>(p);
+    const bool tile = p.tile_linear && p.max_items <= kTileItems;
+    if (tile) {
+        if (MASK < 0 || dt <= 0) rowreduce_tile_kernel<AGG, MAP, NIN, MASK, 0><<<(unsigned)grid, kThreads, 0, st>>>(p);
+        else if (dt == 1) rowreduce_tile_kernel<AGG, MAP, NIN, MASK, 1><<<(unsigned)grid, kThreads, 0, st>>>(p);
+        else rowreduce_tile_kernel<AGG, MAP, NIN, MASK, 2><<<(unsigned)grid, kThreads, 0, st>>>(p);
+    } else {
+        if (MASK < 0 || dt <= 0) rowreduce_kernel<AGG, MAP, NIN, MASK, 0><<<(unsigned)grid, kThreads, 0, st>>>(p);
+        else if (dt == 1) rowreduce_kernel<AGG, MAP, NIN, MASK, 1><<<(unsigned)grid, kThreads, 0, st>>>(p);
+        else rowreduce_kernel<AGG, MAP, NIN, MASK, 2><<<(unsigned)grid, kThreads, 0, st>>>(p);
+    }
     return cudaGetLastError();
 }
 
