@@ -8,9 +8,10 @@
 // read once from its source block and written once into its destination
 // block.  The host plans every atom as rows of a contiguous run (XSeg) cut
 // into ~64 KiB tiles (XTile); the kernel is a persistent grid-stride loop
-// over tiles with four 16-byte loads in flight per thread.  The work is a
-// pure HBM stream (no reuse), so the loads bypass L1 and the stores are
-// marked streaming.
+// over tiles: each tile's segment is staged in shared memory, a warp (or a
+// slice of one) copies a row with eight 16-byte loads in flight per lane.
+// The work is a pure HBM stream (no reuse), so the loads bypass L1 and the
+// stores are marked streaming.
 #include <algorithm>
 
 #include "../ea_internal.h"
@@ -19,8 +20,9 @@ namespace ea {
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kUnroll = 4;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnroll = 8;  // 16-byte chunks in flight per lane
 
 __device__ __forceinline__ void seg_row(const XSeg &g, int64_t r, int64_t *so, int64_t *dof) {
     int64_t s = g.src_off, d = g.dst_off;
@@ -35,40 +37,47 @@ __device__ __forceinline__ void seg_row(const XSeg &g, int64_t r, int64_t *so, i
     *dof = d;
 }
 
-__global__ void __launch_bounds__(kThreads) exchange_kernel(const XSeg *__restrict__ segs,
+__global__ void __launch_bounds__(kThreads, 3) exchange_kernel(const XSeg *__restrict__ segs,
                                                             const XTile *__restrict__ tiles, int64_t ntiles,
                                                             const char *__restrict__ src, char *__restrict__ dst,
                                                             int esize) {
+    __shared__ XSeg sg;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const XTile T = tiles[t];
-        const XSeg &g = segs[T.seg];
-        if (g.vec) {
-            // 16-byte chunks: cpr per row.
-            const int64_t cpr = T.ncols * esize / 16;
-            const int64_t n = T.nrows * cpr;
+        __syncthreads();
+        if (threadIdx.x < (int)(sizeof(XSeg) / 8))
+            reinterpret_cast<int64_t *>(&sg)[threadIdx.x] = reinterpret_cast<const int64_t *>(segs + T.seg)[threadIdx.x];
+        __syncthreads();
+        if (sg.vec) {
+            // a warp (or a slice of one, for short rows) copies a row: each
+            // lane keeps kUnroll 16-byte loads in flight before it stores
+            const int cpr = (int)(T.ncols * esize / 16);
+            int lpr = 32;
+            while (lpr > 1 && lpr * kUnroll > cpr) lpr /= 2;
+            const int rpw = 32 / lpr, sub = lane / lpr, sl = lane % lpr;
             const int64_t col_bytes = T.col0 * esize;
-            for (int64_t base = threadIdx.x; base < n; base += (int64_t)kThreads * kUnroll) {
-                uint4 v[kUnroll];
-                int64_t dofs[kUnroll];
+            for (int64_t r = (int64_t)warp * rpw + sub; r < T.nrows; r += (int64_t)kWarps * rpw) {
+                int64_t so, dof;
+                seg_row(sg, T.row0 + r, &so, &dof);
+                const char *sp = src + so * esize + col_bytes;
+                char *dp = dst + dof * esize + col_bytes;
+                for (int c0 = sl; c0 < cpr; c0 += lpr * kUnroll) {
+                    uint4 v[kUnroll];
 #pragma unroll
-                for (int u = 0; u < kUnroll; u++) {
-                    int64_t c = base + (int64_t)u * kThreads;
-                    dofs[u] = -1;
-                    if (c < n) {
-                        int64_t rr = (cpr == 1) ? c : c / cpr;
-                        int64_t q = c - rr * cpr;
-                        int64_t so, dof;
-                        seg_row(g, T.row0 + rr, &so, &dof);
-                        const char *sp = src + so * esize + col_bytes + q * 16;
-                        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
-                                     : "l"(sp));
-                        dofs[u] = dof * esize + col_bytes + q * 16;
+                    for (int u = 0; u < kUnroll; u++) {
+                        const int c = c0 + u * lpr;
+                        if (c < cpr)
+                            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
+                                         : "l"(sp + (int64_t)c * 16));
+                    }
+#pragma unroll
+                    for (int u = 0; u < kUnroll; u++) {
+                        const int c = c0 + u * lpr;
+                        if (c < cpr) __stcs(reinterpret_cast<uint4 *>(dp + (int64_t)c * 16), v[u]);
                     }
                 }
-#pragma unroll
-                for (int u = 0; u < kUnroll; u++)
-                    if (dofs[u] >= 0) __stcs(reinterpret_cast<uint4 *>(dst + dofs[u]), v[u]);
             }
         } else {
             const int64_t n = T.nrows * T.ncols;
@@ -76,7 +85,7 @@ __global__ void __launch_bounds__(kThreads) exchange_kernel(const XSeg *__restri
                 int64_t rr = c / T.ncols;
                 int64_t q = c - rr * T.ncols + T.col0;
                 int64_t so, dof;
-                seg_row(g, T.row0 + rr, &so, &dof);
+                seg_row(sg, T.row0 + rr, &so, &dof);
                 const char *sp = src + (so + q) * esize;
                 char *dp = dst + (dof + q) * esize;
                 if (esize == 4) *reinterpret_cast<uint32_t *>(dp) = *reinterpret_cast<const uint32_t *>(sp);
@@ -90,8 +99,8 @@ __global__ void __launch_bounds__(kThreads) exchange_kernel(const XSeg *__restri
 
 cudaError_t launch_exchange(const XSeg *segs, const XTile *tiles, int64_t ntiles, const char *src, char *dst,
                             int esize, int num_sms, cudaStream_t st) {
-    // Four resident CTAs of 512 threads per SM; persistent over the tiles.
-    int64_t grid = std::min<int64_t>(ntiles, (int64_t)num_sms * 4);
+    // Eight resident CTAs of 256 threads per SM; persistent over the tiles.
+    int64_t grid = std::min<int64_t>(ntiles, (int64_t)num_sms * 8);
     exchange_kernel<<<(unsigned)grid, kThreads, 0, st>>>(segs, tiles, ntiles, src, dst, esize);
     return cudaGetLastError();
 }
