@@ -90,7 +90,7 @@ def max_over_ranks(dist, x: float, device=None) -> float:
 # ----------------------------------------------------------------- clocks
 
 class Clocks:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """nvidia-smi sampled every 25 ms while the timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -107,7 +107,7 @@ class Clocks:
         try:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                                          "--format=csv,noheader,nounits", "-lms", "25"], stdout=self.out,
                                          stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -352,25 +352,23 @@ def config_dict():
 
 
 def traffic_from_profiles():
-    """dram bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+    """DRAM bytes per launch of the dominant kernel (the gate+up contraction)
+    from the committed ncu summary, if it was taken on the current kernel
+    and planner sources; else None."""
     import hashlib
-    src = os.path.join(ROOT, "tensor_relational_einsum_gb300", "csrc", "kernels", "contract_tc.cu")
-    prof = os.path.join(ROOT, "profiles", "contract_tc_llama_block.md")
+    csrc = os.path.join(ROOT, "tensor_relational_einsum_gb300", "csrc")
+    prof = os.path.join(ROOT, "profiles", "contract_tc_ffn_gate_up.md")
     if not os.path.exists(prof):
         return None
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    want = None
-    vals = {}
+    h = hashlib.sha256(open(os.path.join(csrc, "kernels", "contract_tc.cu"), "rb").read() +
+                       open(os.path.join(csrc, "joinagg.cpp"), "rb").read()).hexdigest()[:16]
+    want, val = None, None
     for line in open(prof):
         if line.startswith("source_sha256_16:"):
             want = line.split(":", 1)[1].strip()
-        if line.startswith("traffic_bytes_per_launch."):
-            k, v = line.split(":", 1)
-            vals[k.split(".", 1)[1].strip()] = float(v)
-    if want != h:
-        return None
-    return vals
+        if line.startswith("traffic_bytes_per_launch.ffn_gate_up:"):
+            val = float(line.split(":", 1)[1])
+    return val if want == h else None
 
 
 def run_ours(args, world, rank, local, dist):
@@ -403,26 +401,34 @@ def run_ours(args, world, rank, local, dist):
     value = flops * args.steps * world / (ms * 1e-3) / 1e12
     sm = rec.summary()
     launches = sum(n * len(ts) for (k, n, ts) in sm.values())
-    # roofline of the dominant kernel: the tcgen05 contraction (dense projection / FFN launches)
+    # roofline of the dominant kernel, the tcgen05 contraction, on its
+    # largest launch (the FFN gate+up join-agg): algorithmic flops of one
+    # launch / its mean duration from the CUDA events above
     cf = blk.call_flops()
+    cb = blk.call_bytes()
+    gu = sm["ffn.gate_up"][2]
+    gu_ms = sum(gu) / len(gu)
+    achieved = cf["ffn.gate_up"] / (gu_ms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    roof = {"kernel": "tc_contract_kernel (ffn.gate_up launch: 2 x 16384 x 4096 x 22016)", "bound": "tensor",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_src} bf16 sustained (kernel timed inside the block step)",
+            "flops_per_launch": cf["ffn.gate_up"], "ms_per_launch": round(gu_ms, 4),
+            "traffic": traffic_from_profiles()}
     dense = ("qkv", "o_proj", "ffn.gate_up", "ffn.down")
     tot_f = sum(cf[n] * len(sm[n][2]) for n in dense)
     tot_t = sum(sum(sm[n][2]) for n in dense)
-    n_l = sum(len(sm[n][2]) for n in dense)
-    achieved = tot_f / (tot_t * 1e-3) / 1e12
-    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-    traffic = traffic_from_profiles()
-    roof = {"kernel": "contract_tc (projection + FFN contractions)", "bound": "tensor",
-            "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-            "peak_source": f"{peak_src} bf16 sustained", "flops_per_launch": tot_f / n_l,
-            "ms_per_launch": tot_t / n_l,
-            "traffic": (sum(traffic.values()) / len(traffic)) if traffic else None}
+    roof["all_projection_ffn_launches_TFLOP/s"] = round(tot_f / (tot_t * 1e-3) / 1e12, 1)
     per_call = {}
     for name, (kind, n, ts) in sm.items():
         t = statistics.median(ts)
         ent = {"kernel": kind, "ms": round(t, 4), "share": round(sum(ts) / ms, 4)}
         if name in cf:
             ent["TFLOP/s"] = round(cf[name] / (t * 1e-3) / 1e12, 1)
+        if name in cb and name not in dense:
+            gbs = cb[name] / (t * 1e-3) / 1e9
+            ent["GB/s"] = round(gbs, 1)
+            ent["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 3)
         per_call[name] = ent
     # end to end through host buffers: H2D of the tokens, the block, D2H of the output
     x_host = torch.empty((B * S, D), dtype=torch.bfloat16, pin_memory=True)

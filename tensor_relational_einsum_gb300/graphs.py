@@ -222,6 +222,24 @@ class LlamaBlock:
         c("residual2", lambda: joinagg("td,td->td", [self.h, self.ffn_out], "none", "add", out=self.y))
         return self.y
 
+    def call_bytes(self) -> dict:
+        """Algorithmic bytes of each call: every input relation read once,
+        every output relation written once (written score blocks only)."""
+        T, D, F = self.T, self.D, self.F
+        x = T * D * 2
+        nb = len(self.attn.S.bounds[2]) - 1            # s (and t) blocks
+        sb = self.s // nb
+        kept = nb * (nb + 1) // 2                     # (s, t) blocks the causal filter keeps
+        S = self.b * self.H * kept * sb * sb * 4
+        P = S // 2
+        ml = self.b * self.H * self.s * 4
+        return {"norm1.sumsq": x + T * 4, "norm1.apply": 2 * x + T * 4 + D * 2, "qkv": 4 * x + 3 * D * D * 2,
+                "rope.q": 2 * x, "rope.k": 2 * x, "attn.scores": 2 * x + S, "attn.stats": S + 2 * ml,
+                "attn.normalise": S + 2 * ml + P, "attn.values": P + 2 * x, "exchange.attn_out": 2 * x,
+                "o_proj": 2 * x + D * D * 2, "residual1": 3 * x, "norm2.sumsq": x + T * 4,
+                "norm2.apply": 2 * x + T * 4 + D * 2, "ffn.gate_up": x + 2 * D * F * 2 + 2 * T * F * 2,
+                "ffn.silu_mul": 3 * T * F * 2, "ffn.down": T * F * 2 + F * D * 2 + x, "residual2": 3 * x}
+
     def call_flops(self) -> dict:
         """Algorithmic FLOPs of each contraction call."""
         T, D, F = self.T, self.D, self.F
