@@ -46,6 +46,49 @@ def softmax_attention(Q, K, V, scale: float = 1.0, causal: bool = False, qspec: 
     return {"S": S, "m": m, "l": l, "E": E, "P": P, "O": O}
 
 
+def flash_attention(Q, K, V, group: int = 1, scale: float = 1.0, causal: bool = False, seq_ends=None,
+                    layout: str = "bhsd", tier: str = "idx"):
+    """Flash attention with grouped-query heads and packed sequences
+    ("Every Kernel Is a Join", Example 3.10), as the attention join-aggs of
+    ``softmax_attention``.
+
+    Q: [b, h_q, s, d] (layout "bhsd") or [b, s, h_q, d] ("bshd"); K, V the
+    same with h_kv = h_q / group heads and t in place of s.  Query head h
+    reads key-value head h // group (heads g*m .. g*m+g-1 share head m).
+    ``seq_ends``: increasing positions at which the packed sequences end (the
+    last equals the sequence extent); a query attends only to keys of its own
+    sequence, so the join is taken separately on each sequence's positions.
+    Causal keeps t <= s.  Returns dict O (in ``layout``), m and l ([b, h_q, s];
+    m is the row maximum of the scaled scores, l the row sum of exp(S - m)).
+    """
+    if layout not in ("bhsd", "bshd"):
+        raise ValueError(layout)
+    to_bhsd = (lambda x: x) if layout == "bhsd" else (lambda x: np.transpose(x, (0, 2, 1, 3)))
+    q, k, v = (np.ascontiguousarray(to_bhsd(np.asarray(x, dtype=np.float64))) for x in (Q, K, V))
+    b, hq, s, d = q.shape
+    hk, t = k.shape[1], k.shape[2]
+    if hq != group * hk:
+        raise ValueError("query heads must be group x key-value heads")
+    heads = np.arange(hq) // group
+    kq, vq = k[:, heads], v[:, heads]
+    ends = [s] if seq_ends is None else [int(e) for e in seq_ends]
+    if seq_ends is not None and s != t:
+        raise ValueError("packed sequences need s == t")
+    O = np.zeros((b, hq, s, d))
+    m = np.full((b, hq, s), -np.inf)
+    ell = np.zeros((b, hq, s))
+    lo = 0
+    for e in ends:
+        qs = slice(lo, e)
+        ks = slice(lo, e) if seq_ends is not None else slice(0, t)
+        if e > lo and ks.stop > ks.start:
+            r = softmax_attention(q[:, :, qs], kq[:, :, ks], vq[:, :, ks], scale=scale, causal=causal, tier=tier)
+            O[:, :, qs], m[:, :, qs], ell[:, :, qs] = r["O"], r["m"], r["l"]
+        lo = e
+    O = O if layout == "bhsd" else np.transpose(O, (0, 2, 1, 3))
+    return {"O": np.ascontiguousarray(O), "m": m, "l": ell}
+
+
 def swiglu_ffn(x, w_gate, w_up, w_down, tier: str = "idx"):
     """G = x w_gate, U = x w_up (SUM over the model dimension),
     H = SiLU(G) * U (elementwise join), Y = H w_down."""

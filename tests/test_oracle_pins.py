@@ -221,6 +221,79 @@ def test_attention_invariants():
     np.testing.assert_allclose(same["O"], np.broadcast_to(V.mean(axis=2, keepdims=True), V.shape), rtol=1e-12)
 
 
+def _brute_flash(Q, K, V, group, scale, causal, ends):
+    """Pure-Python loops over one (b, head, query) row at a time ([b, s, h, d])."""
+    import math
+    b, s, hq, d = Q.shape
+    O = np.zeros_like(Q)
+    starts = [0] + list(ends[:-1])
+    for bi in range(b):
+        for h in range(hq):
+            for i in range(s):
+                seg = max(j for j, a in enumerate(starts) if a <= i)
+                keys = [j for j in range(starts[seg], ends[seg]) if not causal or j <= i]
+                sc = [scale * sum(Q[bi, i, h, c] * K[bi, j, h // group, c] for c in range(d)) for j in keys]
+                mx = max(sc)
+                w = [math.exp(x - mx) for x in sc]
+                tot = sum(w)
+                for c in range(d):
+                    O[bi, i, h, c] = sum(wj * V[bi, j, h // group, c] for wj, j in zip(w, keys)) / tot
+    return O
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_flash_attention_brute_force_gqa_packed(causal):
+    r = rng(21)
+    Q = r.standard_normal((2, 9, 4, 3))
+    K, V = r.standard_normal((2, 9, 2, 3)), r.standard_normal((2, 9, 2, 3))
+    ends = [4, 9]
+    out = chains.flash_attention(Q, K, V, group=2, scale=0.7, causal=causal, seq_ends=ends, layout="bshd")
+    np.testing.assert_allclose(out["O"], _brute_flash(Q, K, V, 2, 0.7, causal, ends), rtol=1e-12, atol=1e-13)
+    # the same data in the head-major layout
+    tr = lambda x: np.ascontiguousarray(np.transpose(x, (0, 2, 1, 3)))  # noqa: E731
+    out2 = chains.flash_attention(tr(Q), tr(K), tr(V), group=2, scale=0.7, causal=causal, seq_ends=ends, layout="bhsd")
+    np.testing.assert_allclose(out2["O"], tr(out["O"]), rtol=1e-14)
+
+
+def test_flash_attention_head_groups_and_sequence_boundaries():
+    r = rng(22)
+    b, s, hk, g, d = 1, 10, 3, 4, 2
+    Q = r.standard_normal((b, s, hk * g, d))
+    K = r.standard_normal((b, s, hk, d))
+    # value of key-value head m is the constant m + 1: query head h must read h // g + 1
+    V = np.broadcast_to((np.arange(hk) + 1.0)[None, None, :, None], (b, s, hk, d)).copy()
+    O = chains.flash_attention(Q, K, V, group=g, causal=True, seq_ends=[3, 10], layout="bshd")["O"]
+    np.testing.assert_allclose(O, np.broadcast_to((np.arange(hk * g) // g + 1.0)[None, None, :, None], O.shape),
+                               rtol=1e-13)
+    # identical keys: every query gets the mean of its own sequence's values
+    Ksame = np.zeros_like(K)
+    V2 = r.standard_normal((b, s, hk, d))
+    O2 = chains.flash_attention(Q, Ksame, V2, group=g, seq_ends=[3, 10], layout="bshd")["O"]
+    for lo, hi in ((0, 3), (3, 10)):
+        want = V2[:, lo:hi].mean(axis=1)[:, np.arange(hk * g) // g]
+        np.testing.assert_allclose(O2[:, lo:hi], np.broadcast_to(want[:, None], O2[:, lo:hi].shape), rtol=1e-12)
+    # causal with identical keys: the mean over the sequence's prefix up to the query
+    O3 = chains.flash_attention(Q, Ksame, V2, group=g, causal=True, seq_ends=[3, 10], layout="bshd")["O"]
+    for i in range(s):
+        lo = 0 if i < 3 else 3
+        want = V2[:, lo:i + 1].mean(axis=1)[:, np.arange(hk * g) // g]
+        np.testing.assert_allclose(O3[:, i], want, rtol=1e-12)
+
+
+def test_flash_attention_stats_close_forms():
+    r = rng(23)
+    Q, K = r.standard_normal((1, 2, 5, 3)), r.standard_normal((1, 2, 5, 3))
+    V = r.standard_normal((1, 2, 5, 3))
+    out = chains.flash_attention(Q, K, V, scale=0.5, causal=True)
+    S = 0.5 * np.einsum("bhsd,bhtd->bhst", Q, K)
+    S = np.where(np.tril(np.ones((5, 5), bool)), S, -np.inf)
+    m = S.max(-1)
+    np.testing.assert_allclose(out["m"], m, rtol=1e-14)
+    np.testing.assert_allclose(out["l"], np.exp(S - m[..., None]).sum(-1), rtol=1e-13)
+    # the first query sees only itself: l = 1, m = its own score
+    np.testing.assert_allclose(out["l"][..., 0], 1.0, rtol=1e-15)
+
+
 def test_silu_special_values():
     z = np.array([[0.0, 40.0, -40.0, 1.0]])
     one = np.ones_like(z)
