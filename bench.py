@@ -186,7 +186,7 @@ def bench_components(peaks, device):
     import torch
 
     import synth
-    from tensor_relational_einsum_gb300.graphs import AttentionChain, Recorder, SwigluFFN
+    from tensor_relational_einsum_gb300.graphs import AttentionChain, FusedAttention, Recorder, SwigluFFN
     from tensor_relational_einsum_gb300.relation import Relation, exchange, joinagg
     hbm = peaks["hbm_gbs"]
     out = {}
@@ -244,7 +244,16 @@ def bench_components(peaks, device):
                                          "alg_bytes_GB": round(sum(alg.values()) / 1e9, 3),
                                          "frac_hbm_chain": round(sum(alg.values()) / (med * 1e-3) / 1e9 / hbm, 3),
                                          "join_aggs": per}
+    # the same attention as one join-agg (fused kernel): tensor-bound
+    fa = FusedAttention(ch.Q, ch.K, ch.V, "bhsd,bhtd,bhtd->bhsd", scale=1.0)
     del ch
+    fmed, fmn = timed(lambda: fa.run())
+    tf = fl / (fmed * 1e-3) / 1e12
+    out["attention_fused_b4h32s2048"] = {"ms": round(fmed, 4), "min_ms": round(fmn, 4), "TFLOP/s": round(tf, 1),
+                                         "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 3),
+                                         "alg_bytes_GB": round(4 * qkv_b / 1e9, 3),
+                                         "speedup_vs_chain": round(med / fmed, 2)}
+    del fa
 
     # SwiGLU FFN join-aggs, x[8192, 4096], contracted dims in 4 blocks
     x = synth.make_torch("bf16", (8192, 4096), "normal", 21, 0, 1, device=device)
@@ -425,7 +434,9 @@ def run_ours(args, world, rank, local, dist):
         ent = {"kernel": kind, "ms": round(t, 4), "share": round(sum(ts) / ms, 4)}
         if name in cf:
             ent["TFLOP/s"] = round(cf[name] / (t * 1e-3) / 1e12, 1)
-        if name in cb and name not in dense:
+        if name == "attn.fused":
+            ent["frac_bf16_peak"] = round(cf[name] / (t * 1e-3) / 1e12 / peak, 3)
+        elif name in cb and name not in dense:
             gbs = cb[name] / (t * 1e-3) / 1e9
             ent["GB/s"] = round(gbs, 1)
             ent["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 3)
@@ -496,6 +507,12 @@ def profile_case(name: str, reps: int):
         ch = AttentionChain(Relation.from_dense(q, [1, 32, 1, 1]), Relation.from_dense(k, [1, 32, 4, 1]),
                             Relation.from_dense(v, [1, 32, 4, 1]))
         fn = ch.run
+    elif name == "attn_fused":  # fused causal attention b4 s2048 h32 d128 token-major, s and t in 4 blocks
+        from tensor_relational_einsum_gb300.relation import attention
+        q, k, v = (Relation.from_dense(synth.make_torch("bf16", (4, 2048, 32, 128), "normal", sd, 0, 1, device=dev),
+                                       [4, 4, 1, 1]) for sd in (1, 2, 3))
+        o = Relation("bf16", (4, 2048, 32, 128), [4, 4, 1, 1], device=dev)
+        fn = lambda: attention("bshd,bthd,bthd->bshd", q, k, v, causal=True, out=o)  # noqa: E731
     elif name == "exchange":  # bf16 8192^2: 8x1 row blocks -> 16x16 tiles
         X = Relation.from_dense(synth.make_torch("bf16", (8192, 8192), "uniform", 31, -1, 1, device=dev), [8, 1])
         Y = Relation("bf16", (8192, 8192), [16, 16], device=dev)
@@ -534,7 +551,7 @@ def profile_case(name: str, reps: int):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["gemm", "attn", "exchange", "norm", "ffn_ew"], default=None)
+    ap.add_argument("--profile-case", choices=["gemm", "attn", "attn_fused", "exchange", "norm", "ffn_ew"], default=None)
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)

@@ -218,6 +218,57 @@ ea_status ea_relation_bounds(ea_relation rel, int dim, int32_t *nblocks, int64_t
 ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inputs, const ea_index_part *parts,
                          int n_parts, ea_agg agg, ea_map map, const ea_opts *opts, void *stream, ea_relation *out);
 
+/* ------------------------------------------------- attention join-agg */
+
+/* Options of ea_attention_run; zero-initialise, every field is optional. */
+typedef struct {
+    float scale;             /* score scale, > 0; 0 = 1/sqrt(head dim)                      */
+    int32_t causal;          /* nonzero: a query at position s keeps only keys t <= s        */
+    int32_t n_seq_ends;      /* packed sequences: entries of seq_ends (0: none)              */
+    int32_t reserved0;
+    const int64_t *seq_ends; /* host; increasing end positions, the last = the s extent     */
+    ea_relation m_out;       /* optional f32 relation: row maximum of the scaled scores      */
+    ea_relation l_out;       /* optional f32 relation: row sum of exp(score - maximum)       */
+    int64_t reserved[4];
+} ea_attn_opts;
+
+/* Flash attention as one join-agg ("Every Kernel Is a Join", Example 3.10:
+ * grouped-query heads, packed sequences).
+ *   spec   "bshd,bthd,bthd->bshd" (Q, K, V -> O) or any other letters and
+ *          order with these roles: the last letter of every term is the
+ *          head dimension d (extent 64 or 128, one block); the letter in Q
+ *          but not in K is the query position s, the letter in K but not in
+ *          Q the key position t; the other one or two letters are shared by
+ *          all terms.  K and V have the same term; O has Q's term.  A shared
+ *          letter may have g times as many values in Q as in K (the query
+ *          heads): query head h then reads key-value head floor(h / g), so
+ *          heads g m .. g m + g - 1 share head m.
+ *   q, k, v  bf16 relations.  Tilings: d whole; each shared letter tiled the
+ *          same in all four relations (the grouped letter's Q bounds are g
+ *          times its K bounds); s tiled the same in Q and O, t the same in K
+ *          and V.  Else EA_ERR_PARTITION (re-block with ea_exchange).
+ *   out    *out == NULL: the call creates O (bf16, Q's extents and tiling);
+ *          otherwise *out must match and is overwritten.
+ * Result, per query row (b, s, h):
+ *   O = SUM_t softmax_t(scale Q.K_t) V_t over the kept keys t: those of the
+ *   same packed sequence as s (opts->seq_ends; all keys when none) and, if
+ *   causal, t <= s.  A row that keeps no key gets O = 0 (m = -inf, l = 0).
+ *   m_out / l_out (optional, both or neither): f32 relations over Q's term
+ *   without d, tiled as Q, receiving m = max_t scale Q.K_t and
+ *   l = SUM_t exp(scale Q.K_t - m) over the kept keys.
+ * How it runs: a group is one tile of 128 query positions of one query head,
+ * its tuples the key tiles of 128 keys that the predicate keeps; the
+ * aggregation over t merges (m, l, A) triples, A = SUM exp(S - m) V,
+ * (m1,l1,A1) + (m2,l2,A2) = (M, l1 e^(m1-M) + l2 e^(m2-M), A1 e^(m1-M) +
+ * A2 e^(m2-M)) with M = max(m1, m2), in registers; O = A / l.  Scores are
+ * fp32 from bf16 inputs; the probabilities enter the second product as bf16.
+ * Errors: EA_ERR_SPEC (roles above), EA_ERR_SHAPE, EA_ERR_PARTITION,
+ * EA_ERR_DTYPE (not bf16 / stats not f32), EA_ERR_UNSUPPORTED (head dim not
+ * 64 or 128, a block not 16-byte aligned, no tensor-map encoder),
+ * EA_ERR_ARG (bad seq_ends, scale < 0, one of m_out/l_out). */
+ea_status ea_attention_run(const char *spec, ea_relation q, ea_relation k, ea_relation v, const ea_attn_opts *opts,
+                           void *stream, ea_relation *out);
+
 /* ------------------------------------------------------------ exchange */
 
 /* Re-block `in` into the tiling new_parts[0..rank-1] (Section 5.3: the
@@ -231,7 +282,7 @@ ea_status ea_exchange(ea_relation in, const ea_dim_part *new_parts, void *stream
 
 /* What the last ea_joinagg_run / ea_exchange of the calling host thread
  * launched: kernel class (0 exchange, 1 elementwise, 2 row reduction,
- * 3 SIMT contraction, 4 tcgen05 contraction), kernel launches, work tiles,
+ * 3 SIMT contraction, 4 tcgen05 contraction, 5 attention), kernel launches, work tiles,
  * aggregation groups and function specifications (tuples).  Any pointer
  * may be NULL. */
 ea_status ea_last_plan(int32_t *kernel_class, int32_t *launches, int64_t *tiles, int64_t *groups, int64_t *tuples);

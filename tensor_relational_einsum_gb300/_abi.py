@@ -45,6 +45,12 @@ class Opts(ctypes.Structure):
                 ("out2", ctypes.c_void_p), ("reserved", ctypes.c_int64 * 3)]
 
 
+class AttnOpts(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_float), ("causal", ctypes.c_int32), ("n_seq_ends", ctypes.c_int32),
+                ("reserved0", ctypes.c_int32), ("seq_ends", ctypes.c_void_p), ("m_out", ctypes.c_void_p),
+                ("l_out", ctypes.c_void_p), ("reserved", ctypes.c_int64 * 4)]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -84,10 +90,11 @@ def lib():
         L.ea_overlay_atoms.argtypes = [ctypes.c_int, P64, ctypes.POINTER(DimPart), ctypes.POINTER(DimPart), P64]
         L.ea_last_plan.argtypes = [P32, P32, P64, P64, P64]
         L.ea_exchange_noalloc.argtypes = [VP, VP, VP]
+        L.ea_attention_run.argtypes = [ctypes.c_char_p, VP, VP, VP, ctypes.POINTER(AttnOpts), VP, ctypes.POINTER(VP)]
         for name in ("ea_check", "ea_plan_cache_clear", "ea_relation_create", "ea_relation_destroy",
                      "ea_relation_info", "ea_relation_block", "ea_relation_data", "ea_relation_bounds",
                      "ea_joinagg_run", "ea_exchange", "ea_plan_worklist", "ea_exchange_permutation",
-                     "ea_overlay_atoms", "ea_last_plan", "ea_exchange_noalloc"):
+                     "ea_overlay_atoms", "ea_last_plan", "ea_exchange_noalloc", "ea_attention_run"):
             getattr(L, name).restype = ctypes.c_int
         if L.ea_abi_version() != 1:
             raise ImportError("libea.so ABI version mismatch")
@@ -148,7 +155,7 @@ def index_parts(parts: dict | None):
     return arr, len(parts), keep
 
 
-KERNEL_CLASS = {0: "exchange", 1: "elementwise", 2: "rowreduce", 3: "contract_simt", 4: "contract_tc"}
+KERNEL_CLASS = {0: "exchange", 1: "elementwise", 2: "rowreduce", 3: "contract_simt", 4: "contract_tc", 5: "attention"}
 
 
 def last_plan():

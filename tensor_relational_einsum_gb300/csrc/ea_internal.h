@@ -20,6 +20,8 @@ enum DeviceErr : int {
     kDevTimeoutMma = 2,
     kDevTimeoutEpilogue = 3,
     kDevBounds = 4,
+    kDevTimeoutSoftmax = 5,
+    kDevTimeoutCorrection = 6,
 };
 
 // ---------------------------------------------------------------- exchange
@@ -214,5 +216,52 @@ struct TcParams {
 };
 cudaError_t launch_contract_tc(const TcParams &p, int num_sms, cudaStream_t st);
 int tc_smem_bytes(int bn);
+
+// --------------------------------------------------------------- attention
+// Flash attention as one join-agg: an aggregation group is one tile of 128
+// query positions of one query head; its tuples are the key tiles (128 keys
+// of one K/V block pair) that the predicate keeps, taken in runs.
+struct AtItem {
+    int64_t s_glob0;   // global query position of row 0
+    int64_t o_off;     // element offset in the O arena of row 0, head-dim index 0
+    int64_t o_rstr;    // O element stride between consecutive query positions
+    int64_t ml_off;    // element offset of row 0 in the m and l arenas
+    int64_t ml_rstr;   // their stride between consecutive query positions
+    int32_t q_map;     // tensor map of the Q block
+    int32_t q_c[3];    // map coordinates (dims 1..3) of row 0
+    int32_t nrows;     // valid query rows (<= 128)
+    int32_t r0, r1;    // key-tile runs [r0, r1)
+    int32_t ntiles;    // key tiles over all runs
+};
+
+struct AtRun {
+    int64_t t_glob0;   // global key position of the run's first key
+    int32_t k_map;     // tensor map of the K block (the V block's is k_map + n_kv)
+    int32_t k_c[3];    // map coordinates (dims 1..3) of the run's first key
+    int32_t pos_slot;  // which of k_c steps by 128 from one key tile to the next
+    int32_t ntiles;
+    int32_t nkeys;     // keys in the run (its last tile may be partial)
+    int32_t pad;
+};
+
+struct AtParams {
+    const void *tmaps;       // Q maps, then K maps, then V maps (CUtensorMap, 64-byte aligned)
+    const AtItem *items;     // in the order each CTA runs them
+    const int32_t *cta_ptr;  // CTA x runs items [cta_ptr[x], cta_ptr[x + 1])
+    const AtRun *runs;
+    const int64_t *seq_ends; // packed sequences: end positions (nseq of them), or null
+    char *o;                 // O arena (bf16)
+    float *m_out, *l_out;    // optional row statistics (f32 arenas) or null
+    int32_t ncta;
+    int32_t n_kv;            // number of K (and of V) maps
+    int32_t nseq;
+    int32_t causal;
+    float scale;             // score scale (> 0)
+    float scale_log2;        // scale * log2(e)
+    int32_t d;               // head dimension: 64 or 128
+    int *err;
+};
+cudaError_t launch_attention(const AtParams &p, cudaStream_t st);
+int attention_smem_bytes(int d);
 
 }  // namespace ea

@@ -16,21 +16,15 @@
 #include <algorithm>
 #include <unordered_map>
 
-#include "host.h"
+#include "plan.h"
 
 namespace ea {
 
 // ----------------------------------------------------------- device context
 
-struct DevCtx {
-    bool init = false;
-    int num_sms = 0;
-    int *err = nullptr;  // device error word (kernels raise it; ea_check reads it)
-    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-};
-static DevCtx g_ctx[64];
+DevCtx g_ctx[64];
 
-static ea_status get_ctx(DevCtx **out) {
+ea_status get_ctx(DevCtx **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
@@ -56,53 +50,11 @@ static ea_status get_ctx(DevCtx **out) {
 
 // --------------------------------------------------------------- plan blob
 
-struct Blob {
-    std::vector<char> h;
-    size_t add(const void *p, size_t n, size_t align = 128) {
-        size_t off = (h.size() + align - 1) / align * align;
-        h.resize(off + std::max<size_t>(n, 1));
-        if (n) memcpy(h.data() + off, p, n);
-        return off;
-    }
-    template <class T>
-    size_t add_vec(const std::vector<T> &v) {
-        return add(v.data(), v.size() * sizeof(T));
-    }
-};
+thread_local LastPlan t_last;
 
-enum PlanKind { kExchange = 0, kEwise, kRowReduce, kSimt, kTc };
+std::unordered_map<std::string, DevPlan *> g_cache;
 
-struct DevPlan {
-    int kind = 0;
-    char *dev = nullptr;
-    char *pinned = nullptr;
-    size_t bytes = 0;
-    cudaEvent_t ready = nullptr;
-    cudaStream_t made_on = nullptr;
-    // exchange
-    XSeg *segs = nullptr;
-    XTile *xtiles = nullptr;
-    int64_t nxtiles = 0;
-    const char *xsrc = nullptr;
-    char *xdst = nullptr;
-    int esize = 0;
-    // kernels
-    EwParams ew{};
-    RrParams rr{};
-    CtParams ct{};
-    TcParams tc{};
-    int64_t n_groups = 0, n_tuples = 0;
-};
-
-struct LastPlan {
-    int32_t kind = -1, launches = 0;
-    int64_t tiles = 0, groups = 0, tuples = 0;
-};
-static thread_local LastPlan t_last;
-
-static std::unordered_map<std::string, DevPlan *> g_cache;
-
-static ea_status upload(const Blob &b, cudaStream_t st, DevPlan *p) {
+ea_status upload(const Blob &b, cudaStream_t st, DevPlan *p) {
     p->bytes = b.h.size();
     cudaError_t e = cudaMalloc((void **)&p->dev, p->bytes);
     if (e != cudaSuccess) {
@@ -125,7 +77,7 @@ static ea_status upload(const Blob &b, cudaStream_t st, DevPlan *p) {
     return EA_OK;
 }
 
-static void free_plan(DevPlan *p) {
+void free_plan(DevPlan *p) {
     if (!p) return;
     if (p->dev) cudaFree(p->dev);
     if (p->pinned) cudaFreeHost(p->pinned);
@@ -133,39 +85,13 @@ static void free_plan(DevPlan *p) {
     delete p;
 }
 
-static ea_status plan_ready_on(DevPlan *p, cudaStream_t st) {
+ea_status plan_ready_on(DevPlan *p, cudaStream_t st) {
     if (st != p->made_on) {
         cudaError_t e = cudaStreamWaitEvent(st, p->ready, 0);
         if (e != cudaSuccess) return cuda_error(e, "cudaStreamWaitEvent(plan upload)");
     }
     return EA_OK;
 }
-
-// ------------------------------------------------------------- cache keys
-
-struct Key {
-    std::string s;
-    void raw(const void *p, size_t n) { s.append((const char *)p, n); }
-    template <class T>
-    void v(const T &x) {
-        raw(&x, sizeof x);
-    }
-    void str(const char *c) {
-        s.append(c);
-        s.push_back(0);
-    }
-    void rel(const ea_relation_s *r) {
-        v(r->dtype);
-        v(r->rank);
-        for (int d = 0; d < r->rank; d++) {
-            v(r->dims[d]);
-            int64_t n = (int64_t)r->bounds[d].size();
-            v(n);
-            raw(r->bounds[d].data(), n * sizeof(int64_t));
-        }
-        v(r->arena);
-    }
-};
 
 // ----------------------------------------------------------- block views
 
@@ -915,7 +841,7 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
 
 // ------------------------------------------------------------ launching
 
-static ea_status launch_plan(DevPlan *p, DevCtx *c, cudaStream_t st) {
+ea_status launch_plan(DevPlan *p, DevCtx *c, cudaStream_t st) {
     ea_status s = plan_ready_on(p, st);
     if (s) return s;
     cudaError_t e = cudaSuccess;
@@ -929,6 +855,7 @@ static ea_status launch_plan(DevPlan *p, DevCtx *c, cudaStream_t st) {
     case kRowReduce: t_last.tiles = p->rr.ntiles; t_last.launches = p->rr.ntiles > 0; break;
     case kSimt: t_last.tiles = p->ct.ntiles; t_last.launches = p->ct.ntiles > 0; break;
     case kTc: t_last.tiles = p->tc.ntiles; t_last.launches = p->tc.ntiles > 0; break;
+    case kAttn: t_last.tiles = p->n_groups; t_last.launches = p->at.ncta > 0; break;
     }
     switch (p->kind) {
     case kExchange:
@@ -948,6 +875,10 @@ static ea_status launch_plan(DevPlan *p, DevCtx *c, cudaStream_t st) {
     case kTc:
         p->tc.err = c->err;
         if (p->tc.ntiles) e = launch_contract_tc(p->tc, c->num_sms, st);
+        break;
+    case kAttn:
+        p->at.err = c->err;
+        if (p->at.ncta) e = launch_attention(p->at, st);
         break;
     }
     if (e != cudaSuccess) return cuda_error(e, "kernel launch");
@@ -1271,6 +1202,8 @@ ea_status ea_check(void *stream) {
                          : flag == kDevTimeoutMma      ? "bounded wait ran out in the MMA issuer"
                          : flag == kDevTimeoutEpilogue ? "bounded wait ran out in the epilogue"
                          : flag == kDevBounds          ? "bounds check"
+                         : flag == kDevTimeoutSoftmax  ? "bounded wait ran out in the attention softmax warps"
+                         : flag == kDevTimeoutCorrection ? "bounded wait ran out in the attention output warps"
                                                        : "unknown");
     }
     return EA_OK;

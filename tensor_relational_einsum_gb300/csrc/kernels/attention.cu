@@ -1,0 +1,460 @@
+// attention.cu -- flash attention as one join-agg on the sm_103a tensor
+// cores ("Every Kernel Is a Join", Example 3.10).
+//
+// The join-agg: an aggregation group is one tile of 128 query positions of
+// one query head; its tuples are the key tiles (128 keys of a K/V block
+// pair) the predicate keeps.  Each tuple's kernel computes the scores
+// S = scale Q K^T of the tile, their row maximum m, p = exp(S - m), the
+// row sum l of p and the partial output A = p V.  The group's tuples are
+// aggregated with the merge of (m, l, A) triples
+//     (m1, l1, A1) + (m2, l2, A2) = (M, l1 a1 + l2 a2, A1 a1 + A2 a2),
+//     M = max(m1, m2), a_i = exp(m_i - M),
+// which is associative and commutative; the output block is A / l.  The
+// merge runs on chip, one key tile at a time: A accumulates in TMEM (the
+// MMA's own accumulate), l and m in registers, so no score, probability or
+// partial output ever reaches memory.
+//
+// The reference maximum of a row is only moved when a tile's maximum
+// exceeds it by more than 2^kLazy in exp: until then the exponentials are
+// taken against the older, smaller maximum (values up to 2^kLazy, exact in
+// fp32 and well inside bf16's range), and A and l stay consistent with it,
+// so A / l is unchanged.  Moving it rescales the row of A in TMEM, which is
+// rare after the first tiles.
+//
+// Roles (192 threads, one CTA per SM, persistent over its list of groups):
+//   warp 4     TMA: Q tiles into two buffers (one per group, loaded ahead);
+//              K and V tiles into a ring of two stages (128-byte swizzle,
+//              one [128 x 64] box per 64 head-dim columns).
+//   warp 5     TMEM owner and MMA issuer (one thread).  S_j = Q K_j^T into
+//              one of two TMEM score buffers (columns 0 and 128);
+//              O += P_j V_j into the output accumulator (columns 256..).
+//              S_{j+1} is computed while the softmax of tile j runs.
+//   warps 0-3  one query row per thread (TMEM lane = row): load the row of
+//              S_j, mask (causal, sequence ends, ragged block ends), the
+//              row maximum, p = 2^(S c - m c) with c = scale log2(e), the
+//              row sum, P_j as bf16 into the swizzled A operand of the second
+//              MMA, the rescale of the row of O when the reference maximum
+//              moves; at the end of the group O / l as bf16 to global memory.
+// Every mbarrier wait is bounded (2 s); on time-out the kernel raises the
+// device error word, all roles leave their loops, the copies and MMAs in
+// flight are waited for and TMEM is freed before the CTA exits.
+#include <algorithm>
+
+#include "dev_common.cuh"
+#include "tc_common.cuh"
+
+namespace ea {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kRows = 128;  // query rows of a tile (= TMEM lanes)
+constexpr int kKeys = 128;  // keys of a key tile
+constexpr int kAtThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOCol = 256;  // first TMEM column of the output accumulator
+constexpr float kLazy = 8.0f;    // log2 of the largest exponential taken against a stale maximum
+
+struct AtCtl {
+    uint64_t q_full[2], q_empty[2];
+    uint64_t k_full[2], v_full[2], kv_empty[2];
+    uint64_t s_full[2], s_empty[2];
+    uint64_t p_full, o_done;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int D>
+struct AtCfg {
+    static constexpr int CH = D / 64;            // 64-column (128-byte) chunks of the head dimension
+    static constexpr int TILE = kRows * D * 2;   // one [128 x D] bf16 tile
+    static constexpr int Q_OFF = 0;              // two Q buffers
+    static constexpr int KV_OFF = 2 * TILE;      // stage s: K at KV_OFF + 2 s TILE, V right after
+    static constexpr int P_OFF = KV_OFF + 4 * TILE;
+    static constexpr int CTL_OFF = P_OFF + kRows * kKeys * 2;
+    static constexpr int SMEM = 1024 + CTL_OFF + (int)sizeof(AtCtl);
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// A wait taken by lane 0 for the whole warp; the outcome is the same in
+// every lane, and the warp's later reads are ordered after the wait.
+__device__ __forceinline__ bool warp_wait(uint64_t *b, uint32_t parity, volatile int *abort, int *err, int code) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(b, parity, abort, err, code) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams p) {
+    using C = AtCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    AtCtl *ctl = reinterpret_cast<AtCtl *>(smem + C::CTL_OFF);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const CUtensorMap *maps = reinterpret_cast<const CUtensorMap *>(p.tmaps);
+    volatile int *abort = &ctl->abort;
+    const int i0 = p.cta_ptr[blockIdx.x], i1 = p.cta_ptr[blockIdx.x + 1];
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&ctl->q_full[b], 1);
+            mbar_init(&ctl->q_empty[b], 1);
+            mbar_init(&ctl->k_full[b], 1);
+            mbar_init(&ctl->v_full[b], 1);
+            mbar_init(&ctl->kv_empty[b], 1);
+            mbar_init(&ctl->s_full[b], 1);
+            mbar_init(&ctl->s_empty[b], 4);
+        }
+        mbar_init(&ctl->p_full, 4);
+        mbar_init(&ctl->o_done, 1);
+        mbar_init(&ctl->mma_done, 1);
+        ctl->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (warp == 5) tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            uint32_t ci = 0, ct = 0;
+            uint32_t q_armed = 0, q_par = 0, armed = 0, armed_par = 0;
+            bool ok = true;
+            for (int ii = i0; ii < i1 && ok; ii++) {
+                const AtItem it = p.items[ii];
+                if (it.ntiles == 0) continue;
+                const int qb = ci & 1;
+                const uint32_t qph = (ci >> 1) & 1;
+                if (!mbar_wait(&ctl->q_empty[qb], qph ^ 1, abort, p.err, kDevTimeoutProducer)) {
+                    ok = false;
+                    break;
+                }
+                const CUtensorMap *qm = maps + it.q_map;
+                const uint32_t qs = smem_u32(smem + C::Q_OFF + qb * C::TILE);
+                mbar_expect_tx(&ctl->q_full[qb], C::TILE);
+#pragma unroll
+                for (int c = 0; c < C::CH; c++)
+                    tma_load_4d(qs + c * (kRows * 128), qm, &ctl->q_full[qb], 64 * c, it.q_c[0], it.q_c[1], it.q_c[2]);
+                q_armed |= 1u << qb;
+                q_par = (q_par & ~(1u << qb)) | (qph << qb);
+                ci++;
+                for (int r = it.r0; r < it.r1 && ok; r++) {
+                    const AtRun R = p.runs[r];
+                    const CUtensorMap *km = maps + R.k_map, *vm = maps + R.k_map + p.n_kv;
+                    for (int k = 0; k < R.ntiles; k++) {
+                        const int st = ct & 1;
+                        const uint32_t ph = (ct >> 1) & 1;
+                        if (!mbar_wait(&ctl->kv_empty[st], ph ^ 1, abort, p.err, kDevTimeoutProducer)) {
+                            ok = false;
+                            break;
+                        }
+                        const int step = kKeys * k;
+                        const int c1 = R.k_c[0] + (R.pos_slot == 0 ? step : 0);
+                        const int c2 = R.k_c[1] + (R.pos_slot == 1 ? step : 0);
+                        const int c3 = R.k_c[2] + (R.pos_slot == 2 ? step : 0);
+                        const uint32_t ks = smem_u32(smem + C::KV_OFF + st * 2 * C::TILE), vs = ks + C::TILE;
+                        mbar_expect_tx(&ctl->k_full[st], C::TILE);
+#pragma unroll
+                        for (int c = 0; c < C::CH; c++)
+                            tma_load_4d(ks + c * (kKeys * 128), km, &ctl->k_full[st], 64 * c, c1, c2, c3);
+                        mbar_expect_tx(&ctl->v_full[st], C::TILE);
+#pragma unroll
+                        for (int c = 0; c < C::CH; c++)
+                            tma_load_4d(vs + c * (kKeys * 128), vm, &ctl->v_full[st], 64 * c, c1, c2, c3);
+                        armed |= 1u << st;
+                        armed_par = (armed_par & ~(1u << st)) | (ph << st);
+                        ct++;
+                    }
+                }
+            }
+            if (*abort) {
+                // Let our own copies land before the CTA can exit.
+                for (int s = 0; s < 2; s++) {
+                    if (q_armed & (1u << s)) mbar_wait(&ctl->q_full[s], (q_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
+                    if (armed & (1u << s)) {
+                        mbar_wait(&ctl->k_full[s], (armed_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
+                        mbar_wait(&ctl->v_full[s], (armed_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
+                    }
+                }
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            const uint32_t idesc_s = make_idesc(kRows, kKeys, 0, 0);  // Q (K-major) x K (K-major)
+            const uint32_t idesc_o = make_idesc(kRows, D, 0, 1);      // P (K-major) x V (MN-major)
+            const uint32_t pa = smem_u32(smem + C::P_OFF);
+            const uint32_t od = tmem + kOCol;
+            uint32_t ci = 0, ct = 0;
+            bool ok = true;
+            // O (+)= P_t V_t for key tile t (global tile counter).
+            auto mma_pv = [&](uint32_t t, bool first) -> bool {
+                const int st = t & 1;
+                const uint32_t ph = (t >> 1) & 1;
+                if (!mbar_wait(&ctl->p_full, t & 1, abort, p.err, kDevTimeoutMma)) return false;
+                if (!mbar_wait(&ctl->v_full[st], ph, abort, p.err, kDevTimeoutMma)) return false;
+                tc_fence_after();
+                const uint32_t vb = smem_u32(smem + C::KV_OFF + st * 2 * C::TILE + C::TILE);
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; kk++)
+                    umma_bf16(od, sdesc(pa + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024),
+                              sdesc(vb + kk * 2048, kKeys * 128, 1024), idesc_o, (!first || kk > 0) ? 1u : 0u);
+                umma_commit(&ctl->o_done);
+                umma_commit(&ctl->kv_empty[st]);
+                return true;
+            };
+            for (int ii = i0; ii < i1 && ok; ii++) {
+                const AtItem it = p.items[ii];
+                if (it.ntiles == 0) continue;
+                const int qb = ci & 1;
+                if (!mbar_wait(&ctl->q_full[qb], (ci >> 1) & 1, abort, p.err, kDevTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                ci++;
+                tc_fence_after();
+                const uint32_t qa = smem_u32(smem + C::Q_OFF + qb * C::TILE);
+                for (int j = 0; j < it.ntiles && ok; j++) {
+                    const uint32_t t = ct + j;
+                    const int st = t & 1;
+                    const uint32_t ph = (t >> 1) & 1;
+                    if (!mbar_wait(&ctl->k_full[st], ph, abort, p.err, kDevTimeoutMma) ||
+                        !mbar_wait(&ctl->s_empty[st], ph ^ 1, abort, p.err, kDevTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kb = smem_u32(smem + C::KV_OFF + st * 2 * C::TILE);
+                    const uint32_t d = tmem + (uint32_t)(st * kKeys);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++)
+                        umma_bf16(d, sdesc(qa + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024),
+                                  sdesc(kb + (kk >> 2) * (kKeys * 128) + (kk & 3) * 32, 16, 1024), idesc_s,
+                                  kk > 0 ? 1u : 0u);
+                    umma_commit(&ctl->s_full[st]);
+                    if (j == it.ntiles - 1) umma_commit(&ctl->q_empty[qb]);
+                    if (j > 0 && !mma_pv(t - 1, j == 1)) ok = false;
+                }
+                if (ok && !mma_pv(ct + it.ntiles - 1, it.ntiles == 1)) ok = false;
+                ct += it.ntiles;
+            }
+            // Every MMA this thread issued has completed once mma_done flips.
+            umma_commit(&ctl->mma_done);
+            mbar_wait(&ctl->mma_done, 0, abort, p.err, kDevTimeoutMma, kTimeoutNs, false);
+        }
+    } else {
+        // ------------------------------------------------ softmax and output (warps 0-3)
+        const int row = threadIdx.x;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t orow = lane_base + kOCol;
+        const uint32_t prow = smem_u32(smem + C::P_OFF) + (uint32_t)row * 128;
+        const float c = p.scale_log2;
+        uint32_t ct = 0;
+        bool ok = true;
+        for (int ii = i0; ii < i1 && ok; ii++) {
+            const AtItem it = p.items[ii];
+            const int64_t s_g = it.s_glob0 + row;
+            // keys this row may see: [lo_t, hi_t] (global positions)
+            int64_t lo_t = 0, hi_t = INT64_MAX;
+            if (p.nseq > 0) {
+                int a = 0, b = p.nseq - 1;
+                while (a < b) {
+                    const int mid = (a + b) >> 1;
+                    if (p.seq_ends[mid] > s_g) b = mid;
+                    else a = mid + 1;
+                }
+                lo_t = a > 0 ? p.seq_ends[a - 1] : 0;
+                hi_t = p.seq_ends[a] - 1;
+            }
+            if (p.causal) hi_t = s_g < hi_t ? s_g : hi_t;
+            float m_ref = -INFINITY, m_max = -INFINITY, l = 0.f;  // raw score units
+            int j = 0;
+            for (int r = it.r0; r < it.r1 && ok; r++) {
+                const AtRun R = p.runs[r];
+                for (int k = 0; k < R.ntiles; k++, j++) {
+                    const uint32_t t = ct + j;
+                    const int st = t & 1;
+                    const uint32_t ph = (t >> 1) & 1;
+                    if (!warp_wait(&ctl->s_full[st], ph, abort, p.err, kDevTimeoutSoftmax)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t u[kKeys];
+                    const uint32_t ts = lane_base + (uint32_t)(st * kKeys);
+                    tmem_ld32(ts, u);
+                    tmem_ld32(ts + 32, u + 32);
+                    tmem_ld32(ts + 64, u + 64);
+                    tmem_ld32(ts + 96, u + 96);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->s_empty[st]);
+
+                    const int64_t t0 = R.t_glob0 + (int64_t)kKeys * k;
+                    const int nv = min(kKeys, R.nkeys - kKeys * k);
+                    const int jlo = (int)max64(0, min64(kKeys, lo_t - t0));
+                    const int jhi = (int)max64(-1, min64(nv - 1, hi_t - t0));
+                    if (jlo > 0 || jhi < kKeys - 1) {
+#pragma unroll
+                        for (int q = 0; q < kKeys; q++)
+                            if (q < jlo || q > jhi) u[q] = __float_as_uint(-INFINITY);
+                    }
+                    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+                    for (int q = 0; q < kKeys; q += 4) {
+                        mx0 = fmaxf(mx0, __uint_as_float(u[q]));
+                        mx1 = fmaxf(mx1, __uint_as_float(u[q + 1]));
+                        mx2 = fmaxf(mx2, __uint_as_float(u[q + 2]));
+                        mx3 = fmaxf(mx3, __uint_as_float(u[q + 3]));
+                    }
+                    const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                    m_max = fmaxf(m_max, mx);
+                    // move the reference maximum only when exponentials would pass 2^kLazy
+                    float alpha = 1.f;
+                    if (mx != -INFINITY && (m_ref == -INFINITY || (mx - m_ref) * c > kLazy)) {
+                        alpha = m_ref == -INFINITY ? 0.f : ex2((m_ref - mx) * c);
+                        m_ref = mx;
+                    }
+                    const float base = m_ref == -INFINITY ? 0.f : m_ref * c;
+                    float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                    for (int q = 0; q < kKeys / 2; q++) {
+                        const float e0 = ex2(fmaf(__uint_as_float(u[2 * q]), c, -base));
+                        const float e1 = ex2(fmaf(__uint_as_float(u[2 * q + 1]), c, -base));
+                        l0 += e0;
+                        l1 += e1;
+                        u[q] = pack_bf16(e0, e1);
+                    }
+                    l = fmaf(l, alpha, l0 + l1);
+
+                    // The previous tile's O += P V must be done: it reads the P
+                    // buffer and writes the rows of O a rescale touches.
+                    if (t > 0 && !warp_wait(&ctl->o_done, (t - 1) & 1, abort, p.err, kDevTimeoutSoftmax)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int ch = 0; ch < 2; ch++)
+#pragma unroll
+                        for (int q = 0; q < 8; q++) {
+                            const uint32_t *w = u + ch * 32 + q * 4;
+                            const uint32_t addr = prow + ch * (kRows * 128) + ((uint32_t)(q ^ (row & 7)) << 4);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                                         "r"(w[2]), "r"(w[3])
+                                         : "memory");
+                        }
+                    fence_proxy_async();
+                    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; cc++) {
+                            uint32_t o[32];
+                            tmem_ld32(orow + 32 * cc, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tmem_st32(orow + 32 * cc, o);
+                        }
+                        tmem_wait_st();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->p_full);
+                }
+            }
+            if (!ok) break;
+            ct += it.ntiles;
+            // The group's aggregate is complete once its last O += P V is done.
+            if (it.ntiles > 0 && !warp_wait(&ctl->o_done, (ct - 1) & 1, abort, p.err, kDevTimeoutSoftmax)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.o + (it.o_off + (int64_t)(row < it.nrows ? row : 0) * it.o_rstr) * 2);
+#pragma unroll
+            for (int cc = 0; cc < D / 32; cc++) {
+                uint32_t o[32];
+                if (it.ntiles > 0) {
+                    tmem_ld32(orow + 32 * cc, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i++) o[i] = 0u;
+                }
+                if (row < it.nrows) {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const float *f = reinterpret_cast<const float *>(o + 8 * q);
+                        uint4 w;
+                        w.x = pack_bf16(f[0] * inv, f[1] * inv);
+                        w.y = pack_bf16(f[2] * inv, f[3] * inv);
+                        w.z = pack_bf16(f[4] * inv, f[5] * inv);
+                        w.w = pack_bf16(f[6] * inv, f[7] * inv);
+                        dst[4 * cc + q] = w;
+                    }
+                }
+            }
+            tc_fence_before();
+            if (p.m_out && row < it.nrows) {
+                const int64_t o = it.ml_off + (int64_t)row * it.ml_rstr;
+                p.m_out[o] = m_max * p.scale;
+                p.l_out[o] = m_max == -INFINITY ? 0.f : l * ex2((m_ref - m_max) * c);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const AtParams &p, cudaStream_t st) {
+    using C = AtCfg<D>;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    attention_kernel<D><<<p.ncta, kAtThreads, C::SMEM, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int attention_smem_bytes(int d) { return d == 64 ? AtCfg<64>::SMEM : AtCfg<128>::SMEM; }
+
+cudaError_t launch_attention(const AtParams &p, cudaStream_t st) {
+    if (p.ncta <= 0) return cudaSuccess;
+    if (p.d == 64) return launch_d<64>(p, st);
+    return launch_d<128>(p, st);
+}
+
+}  // namespace ea

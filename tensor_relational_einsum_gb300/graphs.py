@@ -8,10 +8,14 @@ All arithmetic runs in libea.so.
 * ``AttentionChain``  scores -> MAX -> SUM of exp -> normalise -> values
                       (softmax over t as MAX then SUM aggregations with an
                       exp map, Section 1's "softmax as join + aggregation").
+* ``FusedAttention``  the same attention as one join-agg (Example 3.10):
+                      the key tiles of a query tile aggregated with the
+                      merge of (max, sum of exp, weighted sum) triples in one
+                      tcgen05 kernel.
 * ``SwigluFFN``       gate/up contractions (SUM over model-dim blocks),
                       SiLU(gate) * up elementwise join, down contraction.
 * ``LlamaBlock``      pre-norm block: RMSNorm, fused QKV contraction, RoPE,
-                      causal attention chain, exchange of the attention
+                      causal attention (fused, or the chain), exchange of the attention
                       output into the O-projection's tiling, O projection,
                       residual, RMSNorm, SwiGLU FFN, residual.
 """
@@ -23,7 +27,7 @@ import numpy as np
 import torch
 
 from . import _abi
-from .relation import Relation, exchange, joinagg
+from .relation import Relation, attention, exchange, joinagg
 
 
 class Recorder:
@@ -121,6 +125,22 @@ class AttentionChain:
         return full
 
 
+class FusedAttention:
+    """Q [.., s, .., d], K and V [.., t, .., d] (bf16) as one attention
+    join-agg; ``spec`` names the roles ("bshd,bthd,bthd->bshd")."""
+
+    def __init__(self, Q: Relation, K: Relation, V: Relation, spec: str, scale: float = 0.0, causal: bool = False):
+        self.Q, self.K, self.V, self.spec = Q, K, V, spec
+        self.scale, self.causal = scale, causal
+        self.O = Relation("bf16", Q.dims, Q.bounds, device=Q.storage.device)
+
+    def run(self, rec: Recorder | None = None):
+        c = rec.call if rec is not None else _direct
+        c("attn.fused", lambda: attention(self.spec, self.Q, self.K, self.V, scale=self.scale, causal=self.causal,
+                                          out=self.O))
+        return self.O
+
+
 class SwigluFFN:
     """x [T, D] tiled (t_blocks, 4); w_gate, w_up [D, F] and w_down [F, D];
     contracted dims in ``k_blocks`` blocks (partial products SUM-aggregate)."""
@@ -161,7 +181,8 @@ class LlamaBlock:
     sequence per block and the model dimension in ``d_blocks`` blocks."""
 
     def __init__(self, b: int, s: int, D: int, n_heads: int, F: int, W: dict, eps: float = 1e-6,
-                 theta: float = 10000.0, d_blocks: int = 4, s_blocks: int = 4, device="cuda"):
+                 theta: float = 10000.0, d_blocks: int = 4, s_blocks: int = 4, device="cuda",
+                 fused_attention: bool = True):
         self.b, self.s, self.D, self.H, self.F = b, s, D, n_heads, F
         self.dh = D // n_heads
         T = b * s
@@ -187,8 +208,13 @@ class LlamaBlock:
         self.qr = Relation("bf16", hd, attn_parts, device=dev)
         self.kr = Relation("bf16", hd, attn_parts, device=dev)
         self.table = rope_table(s, self.dh, theta, device=dev)
-        self.attn = AttentionChain(self.qr, self.kr, self.v, scale=1.0 / math.sqrt(self.dh), causal=True,
-                                   qspec="bshd", kspec="bthd", vspec="bthd", ospec="bshd")
+        self.fused_attention = fused_attention
+        if fused_attention:
+            self.attn = FusedAttention(self.qr, self.kr, self.v, "bshd,bthd,bthd->bshd", scale=1.0 / math.sqrt(self.dh),
+                                       causal=True)
+        else:
+            self.attn = AttentionChain(self.qr, self.kr, self.v, scale=1.0 / math.sqrt(self.dh), causal=True,
+                                       qspec="bshd", kspec="bthd", vspec="bthd", ospec="bshd")
         # the attention output, seen as [T, D] in blocks of s / s_blocks tokens x all heads ...
         self.o_tok = view(self.attn.O, 0, (T, D), [b * sb, 1])
         # ... re-blocked by the exchange into the O projection's contraction tiling
@@ -227,7 +253,7 @@ class LlamaBlock:
         every output relation written once (written score blocks only)."""
         T, D, F = self.T, self.D, self.F
         x = T * D * 2
-        nb = len(self.attn.S.bounds[2]) - 1            # s (and t) blocks
+        nb = len(self.qr.bounds[1]) - 1                # s (and t) blocks
         sb = self.s // nb
         kept = nb * (nb + 1) // 2                     # (s, t) blocks the causal filter keeps
         S = self.b * self.H * kept * sb * sb * 4
@@ -235,7 +261,8 @@ class LlamaBlock:
         ml = self.b * self.H * self.s * 4
         return {"norm1.sumsq": x + T * 4, "norm1.apply": 2 * x + T * 4 + D * 2, "qkv": 4 * x + 3 * D * D * 2,
                 "rope.q": 2 * x, "rope.k": 2 * x, "attn.scores": 2 * x + S, "attn.stats": S + 2 * ml,
-                "attn.normalise": S + 2 * ml + P, "attn.values": P + 2 * x, "exchange.attn_out": 2 * x,
+                "attn.normalise": S + 2 * ml + P, "attn.values": P + 2 * x, "attn.fused": 4 * x,
+                "exchange.attn_out": 2 * x,
                 "o_proj": 2 * x + D * D * 2, "residual1": 3 * x, "norm2.sumsq": x + T * 4,
                 "norm2.apply": 2 * x + T * 4 + D * 2, "ffn.gate_up": x + 2 * D * F * 2 + 2 * T * F * 2,
                 "ffn.silu_mul": 3 * T * F * 2, "ffn.down": T * F * 2 + F * D * 2 + x, "residual2": 3 * x}
@@ -246,7 +273,7 @@ class LlamaBlock:
         causal_pairs = self.b * self.H * self.s * (self.s + 1) / 2
         return {"qkv": 2.0 * T * D * 3 * D, "o_proj": 2.0 * T * D * D, "ffn.gate_up": 2.0 * T * D * 2 * F,
                 "ffn.down": 2.0 * T * F * D, "attn.scores": 2.0 * causal_pairs * self.dh,
-                "attn.values": 2.0 * causal_pairs * self.dh}
+                "attn.values": 2.0 * causal_pairs * self.dh, "attn.fused": 4.0 * causal_pairs * self.dh}
 
     def flops(self) -> dict:
         """Algorithmic FLOPs: projections and FFN dense; attention over the

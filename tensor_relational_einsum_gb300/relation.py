@@ -179,6 +179,36 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
     return out
 
 
+def attention(spec: str, q: Relation, k: Relation, v: Relation, scale: float = 0.0, causal: bool = False,
+              seq_ends=None, out: Relation | None = None, m_out: Relation | None = None,
+              l_out: Relation | None = None, stream=None) -> Relation:
+    """Flash attention as one join-agg ("Every Kernel Is a Join", Example
+    3.10) with libea.so: ``spec`` such as "bshd,bthd,bthd->bshd"; a shared
+    letter with g times more values in Q than in K groups query heads;
+    ``seq_ends`` lists the end positions of packed sequences; ``scale`` 0
+    means 1/sqrt(head dim).  Optional ``m_out``/``l_out`` (f32 over Q's
+    letters without the head dim) receive the row max and row sum of exp."""
+    if out is None:
+        out = Relation("bf16", q.dims, q.bounds, device=q.storage.device)
+    o = _abi.AttnOpts()
+    o.scale = scale
+    o.causal = 1 if causal else 0
+    keep = None
+    if seq_ends is not None:
+        keep = _abi.i64(list(seq_ends))
+        o.n_seq_ends = len(seq_ends)
+        o.seq_ends = ctypes.cast(keep, ctypes.c_void_p)
+    if m_out is not None:
+        o.m_out = m_out.handle.value
+    if l_out is not None:
+        o.l_out = l_out.handle.value
+    h = ctypes.c_void_p(out.handle.value)
+    check_status(lib().ea_attention_run(spec.encode(), q.handle, k.handle, v.handle, ctypes.byref(o),
+                                        ctypes.c_void_p(_stream_ptr(stream)), ctypes.byref(h)))
+    del keep
+    return out
+
+
 def check(stream=None):
     """Synchronise the stream and raise on an asynchronous CUDA error or a
     raised device error flag."""

@@ -190,3 +190,57 @@ def test_error_codes_without_gpu(L):
     assert L.ea_joinagg_run(b"ij,jk->ik", hs2, 2, None, 0, 1, 0, None, None, ctypes.byref(out)) == 2  # j: 6 vs 7
     for h in (a, b, c, d, b1):
         L.ea_relation_destroy(h)
+
+
+def test_attention_errors_without_gpu(L):
+    """ea_attention_run validates roles, extents, tilings and options before
+    it touches the GPU."""
+    BF, F32 = 1, 0
+    _, q = _fake_rel(L, BF, (2, 256, 8, 128), [2, 2, 1, 1], 1 << 24)
+    _, k = _fake_rel(L, BF, (2, 256, 2, 128), [2, 4, 1, 1], 1 << 25)
+    _, v = _fake_rel(L, BF, (2, 256, 2, 128), [2, 4, 1, 1], 1 << 26)
+    out = ctypes.c_void_p()
+    o = _abi.AttnOpts()
+
+    def run(spec, a=q, b=k, c=v, opts=o):
+        return L.ea_attention_run(spec, a, b, c, ctypes.byref(opts), None, ctypes.byref(out))
+
+    assert run(b"bshd,bthd,bthd") == 1                     # no output term
+    assert run(b"bshd,bthd,bthd->bhsd") == 1               # O must have Q's term
+    assert run(b"bshd,bthd,btdh->bshd") == 1               # V must have K's term
+    assert run(b"bshd,bshd,bshd->bshd") == 1               # no key letter
+    assert run(b"bshd,bthd,bthd->bshd", b=q) == 2          # K extents differ from V
+    _, k3 = _fake_rel(L, BF, (2, 256, 3, 128), [2, 4, 1, 1], 1 << 27)
+    _, v3 = _fake_rel(L, BF, (2, 256, 3, 128), [2, 4, 1, 1], 1 << 28)
+    assert run(b"bshd,bthd,bthd->bshd", b=k3, c=v3) == 2   # 8 query heads over 3 kv heads
+    _, kf = _fake_rel(L, F32, (2, 256, 2, 128), [2, 4, 1, 1], 1 << 27)
+    assert run(b"bshd,bthd,bthd->bshd", b=kf, c=kf) == 4  # K, V not bf16
+    _, kb = _fake_rel(L, BF, (2, 256, 2, 128), [1, 4, 1, 1], 1 << 27)
+    _, vb = _fake_rel(L, BF, (2, 256, 2, 128), [1, 4, 1, 1], 1 << 28)
+    assert run(b"bshd,bthd,bthd->bshd", b=kb, c=vb) == 3   # b tiled differently in Q and K
+    _, kh = _fake_rel(L, BF, (2, 256, 2, 128), [2, 4, 2, 1], 1 << 27)
+    _, vh = _fake_rel(L, BF, (2, 256, 2, 128), [2, 4, 2, 1], 1 << 28)
+    assert run(b"bshd,bthd,bthd->bshd", b=kh, c=vh) == 3   # heads: 2 kv blocks vs 1 query block
+    _, q96 = _fake_rel(L, BF, (2, 256, 8, 96), [2, 2, 1, 1], 1 << 29)
+    _, k96 = _fake_rel(L, BF, (2, 256, 2, 96), [2, 4, 1, 1], 1 << 30)
+    assert run(b"bshd,bthd,bthd->bshd", a=q96, b=k96, c=k96) == 8   # head dim 96
+    bad = _abi.AttnOpts()
+    ends = _abi.i64([100, 90, 256])
+    bad.n_seq_ends, bad.seq_ends = 3, ctypes.cast(ends, ctypes.c_void_p)
+    assert run(b"bshd,bthd,bthd->bshd", opts=bad) == 7     # ends not increasing
+    ends2 = _abi.i64([100, 200])
+    bad.n_seq_ends, bad.seq_ends = 2, ctypes.cast(ends2, ctypes.c_void_p)
+    assert run(b"bshd,bthd,bthd->bshd", opts=bad) == 7     # last end != extent
+    neg = _abi.AttnOpts()
+    neg.scale = -1.0
+    assert run(b"bshd,bthd,bthd->bshd", opts=neg) == 7
+    _, m = _fake_rel(L, F32, (2, 256, 8), [2, 2, 1], 1 << 31)
+    one = _abi.AttnOpts()
+    one.m_out = m.value
+    assert run(b"bshd,bthd,bthd->bshd", opts=one) == 7     # m_out without l_out
+    _, mb = _fake_rel(L, BF, (2, 256, 8), [2, 2, 1], 1 << 32)
+    both = _abi.AttnOpts()
+    both.m_out, both.l_out = mb.value, mb.value
+    assert run(b"bshd,bthd,bthd->bshd", opts=both) == 4    # stats must be f32
+    for h in (q, k, v, k3, v3, kf, kb, vb, kh, vh, q96, k96, m, mb):
+        L.ea_relation_destroy(h)

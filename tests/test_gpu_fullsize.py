@@ -134,6 +134,6 @@ def test_llama_block_full_size_prefix_sample():
     assert rel_frob(got_y, want["y"]) <= BF16_TOL
     got_h = blk.h.to_dense()[seq * S: seq * S + n].double().cpu().numpy()
     assert rel_frob(got_h, want["h"]) <= BF16_TOL
-    got_m = blk.attn.m.to_dense()[seq, :, :n].double().cpu().numpy()
-    assert rel_frob(got_m, want["m"][0]) <= BF16_TOL
+    got_o = blk.attn.O.to_dense()[seq, :n].double().cpu().numpy()
+    assert rel_frob(got_o, want["O"][0]) <= BF16_TOL
     del blk
