@@ -6,10 +6,12 @@
 // it and every tile of 128 query positions, one aggregation group; its
 // tuples are the key tiles of the matching K/V blocks (same shared-letter
 // intervals; key-value head floor(h / g)) that the predicate keeps, stored
-// as runs of consecutive tiles of one block.  Groups are dealt to the CTAs
-// by list scheduling in block order: each group goes to the CTA with the
-// least work so far, which balances the causal triangle and keeps the
-// groups that read the same K/V blocks running at the same time (their
+// as runs of consecutive tiles of one block.  Two neighbouring query tiles
+// of one head form a work item over the union of their key tiles (a tile
+// only one of them keeps is fully masked for the other).  Items are dealt
+// to the CTAs by list scheduling in block order: each goes to the CTA with
+// the least work so far, which balances the causal triangle and keeps the
+// items that read the same K/V blocks running at the same time (their
 // tiles then come from L2).
 #include <cmath>
 
@@ -216,30 +218,38 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
                 int64_t ml_off = ml_base;
                 if (j.m)
                     for (int i = 0; i < nsh; i++) ml_off += (i == 0 ? x0 : x1) * ml_str[qs_pos[i]];
-                // tiles of 128 query positions, last first inside the block
+                // tiles of 128 query positions, last first inside the block, in pairs
                 const int64_t ns = ext[ds];
                 const int64_t ntile_q = (ns + kTileRows - 1) / kTileRows;
-                for (int64_t qt = ntile_q - 1; qt >= 0; qt--) {
+                for (int64_t qt = ntile_q - 1; qt >= 0; qt -= 2) {
                     AtItem it{};
-                    const int64_t s_loc = qt * kTileRows;
-                    it.s_glob0 = lo[ds] + s_loc;
-                    it.nrows = (int32_t)std::min<int64_t>(kTileRows, ns - s_loc);
-                    it.o_off = j.o->blk_off[qb] + q_off + s_loc * str[ds];
-                    it.o_rstr = str[ds];
-                    it.ml_off = j.m ? ml_off + s_loc * ml_str[ds] : 0;
-                    it.ml_rstr = j.m ? ml_str[ds] : 0;
-                    it.q_map = (int32_t)qb;
-                    int32_t qc[3] = {0, 0, 0};
-                    qc[qm.slot[0]] = (int32_t)s_loc;
-                    qc[qm.slot[1]] = (int32_t)(nsh > 0 ? x0 : 0);
-                    qc[qm.slot[2]] = (int32_t)(nsh > 1 ? x1 : 0);
-                    for (int i = 0; i < 3; i++) it.q_c[i] = qc[i];
-                    // keys the rows of this tile may see, as one interval [klo, khi]
-                    int64_t a0, a1, b0, b1;
-                    seg_of(it.s_glob0, &a0, &a1);
-                    seg_of(it.s_glob0 + it.nrows - 1, &b0, &b1);
-                    int64_t klo = a0, khi = b1 == INT64_MAX ? INT64_MAX : b1 - 1;
-                    if (j.causal) khi = std::min<int64_t>(khi, it.s_glob0 + it.nrows - 1);
+                    it.nq = qt >= 1 ? 2 : 1;
+                    int64_t klo = INT64_MAX, khi = INT64_MIN;  // keys either tile may see: one interval per tile
+                    int64_t tlo_k[2], thi_k[2];
+                    for (int xq = 0; xq < it.nq; xq++) {
+                        AtQTile &Q = it.q[xq];
+                        const int64_t s_loc = (qt - xq) * kTileRows;
+                        Q.s_glob0 = lo[ds] + s_loc;
+                        Q.nrows = (int32_t)std::min<int64_t>(kTileRows, ns - s_loc);
+                        Q.o_off = j.o->blk_off[qb] + q_off + s_loc * str[ds];
+                        Q.o_rstr = str[ds];
+                        Q.ml_off = j.m ? ml_off + s_loc * ml_str[ds] : 0;
+                        Q.ml_rstr = j.m ? ml_str[ds] : 0;
+                        Q.q_map = (int32_t)qb;
+                        int32_t qc[3] = {0, 0, 0};
+                        qc[qm.slot[0]] = (int32_t)s_loc;
+                        qc[qm.slot[1]] = (int32_t)(nsh > 0 ? x0 : 0);
+                        qc[qm.slot[2]] = (int32_t)(nsh > 1 ? x1 : 0);
+                        for (int i = 0; i < 3; i++) Q.q_c[i] = qc[i];
+                        int64_t a0, a1, b0, b1;
+                        seg_of(Q.s_glob0, &a0, &a1);
+                        seg_of(Q.s_glob0 + Q.nrows - 1, &b0, &b1);
+                        tlo_k[xq] = a0;
+                        thi_k[xq] = b1 == INT64_MAX ? INT64_MAX : b1 - 1;
+                        if (j.causal) thi_k[xq] = std::min<int64_t>(thi_k[xq], Q.s_glob0 + Q.nrows - 1);
+                        klo = std::min(klo, tlo_k[xq]);
+                        khi = std::max(khi, thi_k[xq]);
+                    }
                     it.r0 = (int32_t)runs.size();
                     const int ntb = (int)k->bounds[ksd].size() - 1;
                     for (int tb = 0; tb < ntb; tb++) {
@@ -250,7 +260,9 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
                         int64_t first = -1, last = -2;
                         for (int64_t kt = 0; kt < nkt; kt++) {
                             const int64_t t0 = tlo + kt * kTileRows, t1 = std::min<int64_t>(thi, t0 + kTileRows) - 1;
-                            if (t1 < klo || t0 > khi) continue;
+                            bool keep = false;
+                            for (int xq = 0; xq < it.nq; xq++) keep = keep || !(t1 < tlo_k[xq] || t0 > thi_k[xq]);
+                            if (!keep) continue;
                             if (first < 0) first = kt;
                             last = kt;
                         }
@@ -271,6 +283,8 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
                         runs.push_back(R);
                         it.ntiles += R.ntiles;
                     }
+                    (void)klo;
+                    (void)khi;
                     it.r1 = (int32_t)runs.size();
                     items.push_back(it);
                 }
@@ -288,7 +302,7 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
             Load l = heap.top();
             heap.pop();
             per[l.second].push_back((int32_t)i);
-            l.first += 4 * (int64_t)items[i].ntiles + 1;  // a key tile ~ 4 units, a group's set-up ~ 1
+            l.first += 4 * (int64_t)items[i].ntiles + 2;  // a key tile ~ 4 units, an item's set-up ~ 2
             heap.push(l);
         }
     }
@@ -299,8 +313,11 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
         for (int32_t i : per[x]) ordered.push_back(items[i]);
         cta_ptr.push_back((int32_t)ordered.size());
     }
-    int64_t ntup = 0;
-    for (const AtItem &it : items) ntup += it.ntiles;
+    int64_t ntup = 0, ngroups = 0;
+    for (const AtItem &it : items) {
+        ntup += (int64_t)it.ntiles * it.nq;
+        ngroups += it.nq;
+    }
 
     std::vector<CUtensorMap> raw(maps.size());
     for (size_t i = 0; i < maps.size(); i++) raw[i] = maps[i].map;
@@ -326,7 +343,7 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
     P.scale = j.scale;
     P.scale_log2 = (float)((double)j.scale * 1.4426950408889634);
     P.d = (int32_t)q->dims[dq_d];
-    p->n_groups = (int64_t)items.size();
+    p->n_groups = ngroups;
     p->n_tuples = ntup;
     return EA_OK;
 }

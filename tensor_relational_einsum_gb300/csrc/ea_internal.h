@@ -220,8 +220,10 @@ int tc_smem_bytes(int bn);
 // --------------------------------------------------------------- attention
 // Flash attention as one join-agg: an aggregation group is one tile of 128
 // query positions of one query head; its tuples are the key tiles (128 keys
-// of one K/V block pair) that the predicate keeps, taken in runs.
-struct AtItem {
+// of one K/V block pair) that the predicate keeps, taken in runs.  A work
+// item holds one or two groups that share their key tiles (two query tiles
+// of the same head), run side by side by the two softmax warpgroups.
+struct AtQTile {
     int64_t s_glob0;   // global query position of row 0
     int64_t o_off;     // element offset in the O arena of row 0, head-dim index 0
     int64_t o_rstr;    // O element stride between consecutive query positions
@@ -230,7 +232,13 @@ struct AtItem {
     int32_t q_map;     // tensor map of the Q block
     int32_t q_c[3];    // map coordinates (dims 1..3) of row 0
     int32_t nrows;     // valid query rows (<= 128)
-    int32_t r0, r1;    // key-tile runs [r0, r1)
+    int32_t pad;
+};
+
+struct AtItem {
+    AtQTile q[2];      // q[1] unused when nq == 1
+    int32_t nq;        // query tiles of the item: 1 or 2
+    int32_t r0, r1;    // key-tile runs [r0, r1), shared by the query tiles
     int32_t ntiles;    // key tiles over all runs
 };
 

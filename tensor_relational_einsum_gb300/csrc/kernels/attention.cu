@@ -21,20 +21,29 @@
 // so A / l is unchanged.  Moving it rescales the row of A in TMEM, which is
 // rare after the first tiles.
 //
-// Roles (192 threads, one CTA per SM, persistent over its list of groups):
-//   warp 4     TMA: Q tiles into two buffers (one per group, loaded ahead);
-//              K and V tiles into a ring of two stages (128-byte swizzle,
-//              one [128 x 64] box per 64 head-dim columns).
-//   warp 5     TMEM owner and MMA issuer (one thread).  S_j = Q K_j^T into
-//              one of two TMEM score buffers (columns 0 and 128);
-//              O += P_j V_j into the output accumulator (columns 256..).
-//              S_{j+1} is computed while the softmax of tile j runs.
-//   warps 0-3  one query row per thread (TMEM lane = row): load the row of
-//              S_j, mask (causal, sequence ends, ragged block ends), the
-//              row maximum, p = 2^(S c - m c) with c = scale log2(e), the
-//              row sum, P_j as bf16 into the swizzled A operand of the second
-//              MMA, the rescale of the row of O when the reference maximum
-//              moves; at the end of the group O / l as bf16 to global memory.
+// A work item is one or two groups that share their key tiles: two query
+// tiles of the same head, X = 0 and X = 1, each with its own softmax
+// warpgroup, score buffer S_X and output accumulator O_X in TMEM (columns
+// S_0 [0, 128), S_1 [128, 256), O_0 [256, 256 + d), O_1 [256 + d, 256 + 2d)).
+// Each K and V tile is loaded once for both, and while one warpgroup works
+// on its scores the tensor cores run the other's products.
+//
+// Roles (320 threads, one CTA per SM, persistent over its list of items):
+//   warp 8     TMA: Q tiles (one buffer per X), K and V tiles into two rings
+//              of two stages each (128-byte swizzle, one [128 x 64] box per
+//              64 head-dim columns); K runs one tile ahead of V.
+//   warp 9     TMEM owner and MMA issuer (one thread).  Per X and key tile
+//              j: S_X = Q_X K_j^T; after the softmax of X has written P_X,
+//              O_X (+)= P_X V_j with P_X read from TMEM, then at once
+//              S_X = Q_X K_{j+1}^T (in order on the tensor pipe, so the
+//              next scores land after P_X has been read).
+//   warps 0-3 (X = 0), 4-7 (X = 1): one query row per thread (TMEM lane =
+//              row): load the row of S_X, mask (causal, sequence ends,
+//              ragged block ends), the row maximum, p = 2^(S c - m c) with
+//              c = scale log2(e), the row sum, P_X as bf16 into the first 64
+//              columns of S_X, the rescale of the row of O_X when the
+//              reference maximum moves; at the end of the item O_X / l as
+//              bf16 to global memory.
 // Every mbarrier wait is bounded (2 s); on time-out the kernel raises the
 // device error word, all roles leave their loops, the copies and MMAs in
 // flight are waited for and TMEM is freed before the CTA exits.
@@ -51,16 +60,15 @@ using namespace tc;
 
 constexpr int kRows = 128;  // query rows of a tile (= TMEM lanes)
 constexpr int kKeys = 128;  // keys of a key tile
-constexpr int kAtThreads = 192;
+constexpr int kAtThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 256;  // first TMEM column of the output accumulator
+constexpr uint32_t kOCol = 256;  // first TMEM column of the output accumulators
 constexpr float kLazy = 8.0f;    // log2 of the largest exponential taken against a stale maximum
 
 struct AtCtl {
     uint64_t q_full[2], q_empty[2];
-    uint64_t k_full[2], v_full[2], kv_empty[2];
-    uint64_t s_full[2], s_empty[2];
-    uint64_t p_full, o_done;
+    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t s_full[2], p_full[2], o_fin[2];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
@@ -70,10 +78,10 @@ template <int D>
 struct AtCfg {
     static constexpr int CH = D / 64;            // 64-column (128-byte) chunks of the head dimension
     static constexpr int TILE = kRows * D * 2;   // one [128 x D] bf16 tile
-    static constexpr int Q_OFF = 0;              // two Q buffers
-    static constexpr int KV_OFF = 2 * TILE;      // stage s: K at KV_OFF + 2 s TILE, V right after
-    static constexpr int P_OFF = KV_OFF + 4 * TILE;
-    static constexpr int CTL_OFF = P_OFF + kRows * kKeys * 2;
+    static constexpr int Q_OFF = 0;              // Q_0, Q_1
+    static constexpr int K_OFF = 2 * TILE;       // two K stages
+    static constexpr int V_OFF = 4 * TILE;       // two V stages
+    static constexpr int CTL_OFF = 6 * TILE;
     static constexpr int SMEM = 1024 + CTL_OFF + (int)sizeof(AtCtl);
 };
 
@@ -114,55 +122,74 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             mbar_init(&ctl->q_full[b], 1);
             mbar_init(&ctl->q_empty[b], 1);
             mbar_init(&ctl->k_full[b], 1);
+            mbar_init(&ctl->k_empty[b], 1);
             mbar_init(&ctl->v_full[b], 1);
-            mbar_init(&ctl->kv_empty[b], 1);
+            mbar_init(&ctl->v_empty[b], 1);
             mbar_init(&ctl->s_full[b], 1);
-            mbar_init(&ctl->s_empty[b], 4);
+            mbar_init(&ctl->p_full[b], 4);
+            mbar_init(&ctl->o_fin[b], 1);
         }
-        mbar_init(&ctl->p_full, 4);
-        mbar_init(&ctl->o_done, 1);
         mbar_init(&ctl->mma_done, 1);
         ctl->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
     }
-    if (warp == 5) tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+    if (warp == 9) tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            uint32_t ci = 0, ct = 0;
-            uint32_t q_armed = 0, q_par = 0, armed = 0, armed_par = 0;
+            // K of tile t is loaded before V of tile t - 1: K is needed first
+            // (S = Q K^T) and its stage frees as soon as those MMAs are done.
+            uint32_t ct = 0, qx[2] = {0, 0};  // key tiles; items per query slot
+            uint32_t q_armed = 0, q_par = 0, k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
+            const CUtensorMap *pv_map = nullptr;  // V of the previous tile, not yet loaded
+            int pv_c1 = 0, pv_c2 = 0, pv_c3 = 0;
             bool ok = true;
-            for (int ii = i0; ii < i1 && ok; ii++) {
-                const AtItem it = p.items[ii];
-                if (it.ntiles == 0) continue;
-                const int qb = ci & 1;
-                const uint32_t qph = (ci >> 1) & 1;
-                if (!mbar_wait(&ctl->q_empty[qb], qph ^ 1, abort, p.err, kDevTimeoutProducer)) {
-                    ok = false;
-                    break;
-                }
-                const CUtensorMap *qm = maps + it.q_map;
-                const uint32_t qs = smem_u32(smem + C::Q_OFF + qb * C::TILE);
-                mbar_expect_tx(&ctl->q_full[qb], C::TILE);
+            auto load_v = [&](uint32_t t) -> bool {
+                const int st = t & 1;
+                const uint32_t ph = (t >> 1) & 1;
+                if (!mbar_wait(&ctl->v_empty[st], ph ^ 1, abort, p.err, kDevTimeoutProducer)) return false;
+                const uint32_t vs = smem_u32(smem + C::V_OFF + st * C::TILE);
+                mbar_expect_tx(&ctl->v_full[st], C::TILE);
 #pragma unroll
                 for (int c = 0; c < C::CH; c++)
-                    tma_load_4d(qs + c * (kRows * 128), qm, &ctl->q_full[qb], 64 * c, it.q_c[0], it.q_c[1], it.q_c[2]);
-                q_armed |= 1u << qb;
-                q_par = (q_par & ~(1u << qb)) | (qph << qb);
-                ci++;
+                    tma_load_4d(vs + c * (kKeys * 128), pv_map, &ctl->v_full[st], 64 * c, pv_c1, pv_c2, pv_c3);
+                v_armed |= 1u << st;
+                v_par = (v_par & ~(1u << st)) | (ph << st);
+                return true;
+            };
+            for (int ii = i0; ii < i1 && ok; ii++) {
+                const AtItem &it = p.items[ii];
+                const int ntiles = it.ntiles, nq = it.nq;
+                if (ntiles == 0) continue;
+                for (int x = 0; x < nq && ok; x++) {
+                    if (!mbar_wait(&ctl->q_empty[x], (qx[x] & 1) ^ 1, abort, p.err, kDevTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const AtQTile &Q = it.q[x];
+                    const CUtensorMap *qm = maps + Q.q_map;
+                    const uint32_t qs = smem_u32(smem + C::Q_OFF + x * C::TILE);
+                    mbar_expect_tx(&ctl->q_full[x], C::TILE);
+#pragma unroll
+                    for (int c = 0; c < C::CH; c++)
+                        tma_load_4d(qs + c * (kRows * 128), qm, &ctl->q_full[x], 64 * c, Q.q_c[0], Q.q_c[1], Q.q_c[2]);
+                    q_armed |= 1u << x;
+                    q_par = (q_par & ~(1u << x)) | ((qx[x] & 1) << x);
+                    qx[x]++;
+                }
                 for (int r = it.r0; r < it.r1 && ok; r++) {
                     const AtRun R = p.runs[r];
                     const CUtensorMap *km = maps + R.k_map, *vm = maps + R.k_map + p.n_kv;
                     for (int k = 0; k < R.ntiles; k++) {
                         const int st = ct & 1;
                         const uint32_t ph = (ct >> 1) & 1;
-                        if (!mbar_wait(&ctl->kv_empty[st], ph ^ 1, abort, p.err, kDevTimeoutProducer)) {
+                        if (!mbar_wait(&ctl->k_empty[st], ph ^ 1, abort, p.err, kDevTimeoutProducer)) {
                             ok = false;
                             break;
                         }
@@ -170,108 +197,134 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                         const int c1 = R.k_c[0] + (R.pos_slot == 0 ? step : 0);
                         const int c2 = R.k_c[1] + (R.pos_slot == 1 ? step : 0);
                         const int c3 = R.k_c[2] + (R.pos_slot == 2 ? step : 0);
-                        const uint32_t ks = smem_u32(smem + C::KV_OFF + st * 2 * C::TILE), vs = ks + C::TILE;
+                        const uint32_t ks = smem_u32(smem + C::K_OFF + st * C::TILE);
                         mbar_expect_tx(&ctl->k_full[st], C::TILE);
 #pragma unroll
                         for (int c = 0; c < C::CH; c++)
                             tma_load_4d(ks + c * (kKeys * 128), km, &ctl->k_full[st], 64 * c, c1, c2, c3);
-                        mbar_expect_tx(&ctl->v_full[st], C::TILE);
-#pragma unroll
-                        for (int c = 0; c < C::CH; c++)
-                            tma_load_4d(vs + c * (kKeys * 128), vm, &ctl->v_full[st], 64 * c, c1, c2, c3);
-                        armed |= 1u << st;
-                        armed_par = (armed_par & ~(1u << st)) | (ph << st);
+                        k_armed |= 1u << st;
+                        k_par = (k_par & ~(1u << st)) | (ph << st);
+                        if (pv_map && !load_v(ct - 1)) {
+                            ok = false;
+                            break;
+                        }
+                        pv_map = vm;
+                        pv_c1 = c1;
+                        pv_c2 = c2;
+                        pv_c3 = c3;
                         ct++;
                     }
                 }
             }
+            if (ok && pv_map) load_v(ct - 1);
             if (*abort) {
                 // Let our own copies land before the CTA can exit.
                 for (int s = 0; s < 2; s++) {
                     if (q_armed & (1u << s)) mbar_wait(&ctl->q_full[s], (q_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
-                    if (armed & (1u << s)) {
-                        mbar_wait(&ctl->k_full[s], (armed_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
-                        mbar_wait(&ctl->v_full[s], (armed_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
-                    }
+                    if (k_armed & (1u << s)) mbar_wait(&ctl->k_full[s], (k_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
+                    if (v_armed & (1u << s)) mbar_wait(&ctl->v_full[s], (v_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             const uint32_t idesc_s = make_idesc(kRows, kKeys, 0, 0);  // Q (K-major) x K (K-major)
-            const uint32_t idesc_o = make_idesc(kRows, D, 0, 1);      // P (K-major) x V (MN-major)
-            const uint32_t pa = smem_u32(smem + C::P_OFF);
-            const uint32_t od = tmem + kOCol;
-            uint32_t ci = 0, ct = 0;
+            const uint32_t idesc_o = make_idesc(kRows, D, 0, 1);      // P (TMEM) x V (MN-major)
+            uint32_t ct = 0, qx[2] = {0, 0}, tx[2] = {0, 0};  // key tiles; items and tiles per query slot
             bool ok = true;
-            // O (+)= P_t V_t for key tile t (global tile counter).
-            auto mma_pv = [&](uint32_t t, bool first) -> bool {
-                const int st = t & 1;
-                const uint32_t ph = (t >> 1) & 1;
-                if (!mbar_wait(&ctl->p_full, t & 1, abort, p.err, kDevTimeoutMma)) return false;
-                if (!mbar_wait(&ctl->v_full[st], ph, abort, p.err, kDevTimeoutMma)) return false;
-                tc_fence_after();
-                const uint32_t vb = smem_u32(smem + C::KV_OFF + st * 2 * C::TILE + C::TILE);
+            // S_x = Q_x K_t^T
+            auto mma_s = [&](int x, uint32_t t) {
+                const uint32_t qa = smem_u32(smem + C::Q_OFF + x * C::TILE);
+                const uint32_t kb = smem_u32(smem + C::K_OFF + (t & 1) * C::TILE);
+                const uint32_t d = tmem + (uint32_t)(x * kKeys);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++)
+                    umma_bf16(d, sdesc(qa + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024),
+                              sdesc(kb + (kk >> 2) * (kKeys * 128) + (kk & 3) * 32, 16, 1024), idesc_s,
+                              kk > 0 ? 1u : 0u);
+                umma_commit(&ctl->s_full[x]);
+            };
+            // O_x (+)= P_x V_t, P_x in the first 64 columns of S_x
+            auto mma_o = [&](int x, uint32_t t, bool first) {
+                const uint32_t vb = smem_u32(smem + C::V_OFF + (t & 1) * C::TILE);
+                const uint32_t pa = tmem + (uint32_t)(x * kKeys);
+                const uint32_t d = tmem + kOCol + (uint32_t)(x * D);
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; kk++)
-                    umma_bf16(od, sdesc(pa + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024),
-                              sdesc(vb + kk * 2048, kKeys * 128, 1024), idesc_o, (!first || kk > 0) ? 1u : 0u);
-                umma_commit(&ctl->o_done);
-                umma_commit(&ctl->kv_empty[st]);
-                return true;
+                    umma_bf16_ts(d, pa + kk * 8, sdesc(vb + kk * 2048, kKeys * 128, 1024), idesc_o,
+                                 (!first || kk > 0) ? 1u : 0u);
             };
             for (int ii = i0; ii < i1 && ok; ii++) {
-                const AtItem it = p.items[ii];
-                if (it.ntiles == 0) continue;
-                const int qb = ci & 1;
-                if (!mbar_wait(&ctl->q_full[qb], (ci >> 1) & 1, abort, p.err, kDevTimeoutMma)) {
+                const AtItem &it = p.items[ii];
+                const int n = it.ntiles, nq = it.nq;
+                if (n == 0) continue;
+                // first scores of the item
+                if (!mbar_wait(&ctl->k_full[ct & 1], (ct >> 1) & 1, abort, p.err, kDevTimeoutMma)) {
                     ok = false;
                     break;
                 }
-                ci++;
-                tc_fence_after();
-                const uint32_t qa = smem_u32(smem + C::Q_OFF + qb * C::TILE);
-                for (int j = 0; j < it.ntiles && ok; j++) {
-                    const uint32_t t = ct + j;
-                    const int st = t & 1;
-                    const uint32_t ph = (t >> 1) & 1;
-                    if (!mbar_wait(&ctl->k_full[st], ph, abort, p.err, kDevTimeoutMma) ||
-                        !mbar_wait(&ctl->s_empty[st], ph ^ 1, abort, p.err, kDevTimeoutMma)) {
+                for (int x = 0; x < nq && ok; x++) {
+                    if (!mbar_wait(&ctl->q_full[x], qx[x] & 1, abort, p.err, kDevTimeoutMma)) {
                         ok = false;
                         break;
                     }
+                    qx[x]++;
                     tc_fence_after();
-                    const uint32_t kb = smem_u32(smem + C::KV_OFF + st * 2 * C::TILE);
-                    const uint32_t d = tmem + (uint32_t)(st * kKeys);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; kk++)
-                        umma_bf16(d, sdesc(qa + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024),
-                                  sdesc(kb + (kk >> 2) * (kKeys * 128) + (kk & 3) * 32, 16, 1024), idesc_s,
-                                  kk > 0 ? 1u : 0u);
-                    umma_commit(&ctl->s_full[st]);
-                    if (j == it.ntiles - 1) umma_commit(&ctl->q_empty[qb]);
-                    if (j > 0 && !mma_pv(t - 1, j == 1)) ok = false;
+                    mma_s(x, ct);
+                    if (n == 1) umma_commit(&ctl->q_empty[x]);
                 }
-                if (ok && !mma_pv(ct + it.ntiles - 1, it.ntiles == 1)) ok = false;
-                ct += it.ntiles;
+                if (!ok) break;
+                umma_commit(&ctl->k_empty[ct & 1]);
+                for (int j = 0; j < n && ok; j++) {
+                    const uint32_t t = ct + j;
+                    for (int x = 0; x < nq; x++) {
+                        if (!mbar_wait(&ctl->p_full[x], (tx[x] + j) & 1, abort, p.err, kDevTimeoutMma) ||
+                            (x == 0 && !mbar_wait(&ctl->v_full[t & 1], (t >> 1) & 1, abort, p.err, kDevTimeoutMma))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        mma_o(x, t, j == 0);
+                        if (j == n - 1) umma_commit(&ctl->o_fin[x]);
+                        if (j + 1 < n) {
+                            if (x == 0 && !mbar_wait(&ctl->k_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort, p.err,
+                                                     kDevTimeoutMma)) {
+                                ok = false;
+                                break;
+                            }
+                            mma_s(x, t + 1);
+                            if (j + 1 == n - 1) umma_commit(&ctl->q_empty[x]);
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(&ctl->v_empty[t & 1]);
+                    if (j + 1 < n) umma_commit(&ctl->k_empty[(t + 1) & 1]);
+                }
+                ct += n;
+                for (int x = 0; x < nq; x++) tx[x] += n;
             }
             // Every MMA this thread issued has completed once mma_done flips.
             umma_commit(&ctl->mma_done);
             mbar_wait(&ctl->mma_done, 0, abort, p.err, kDevTimeoutMma, kTimeoutNs, false);
         }
     } else {
-        // ------------------------------------------------ softmax and output (warps 0-3)
-        const int row = threadIdx.x;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        const uint32_t orow = lane_base + kOCol;
-        const uint32_t prow = smem_u32(smem + C::P_OFF) + (uint32_t)row * 128;
+        // ------------------------------------------------ softmax and output (warps 0-7)
+        const int x = warp >> 2;
+        const int row = threadIdx.x & (kRows - 1);
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t srow = lane_base + (uint32_t)(x * kKeys);
+        const uint32_t orow = lane_base + kOCol + (uint32_t)(x * D);
         const float c = p.scale_log2;
-        uint32_t ct = 0;
+        uint32_t ci = 0, ct = 0;  // items and key tiles of this query slot
         bool ok = true;
         for (int ii = i0; ii < i1 && ok; ii++) {
-            const AtItem it = p.items[ii];
-            const int64_t s_g = it.s_glob0 + row;
+            const AtItem &it = p.items[ii];
+            const int n = it.ntiles;
+            if (x >= it.nq) continue;
+            const AtQTile &Q = it.q[x];
+            const int nrows = Q.nrows;
+            const int64_t s_g = Q.s_glob0 + row;
             // keys this row may see: [lo_t, hi_t] (global positions)
             int64_t lo_t = 0, hi_t = INT64_MAX;
             if (p.nseq > 0) {
@@ -291,23 +344,17 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                 const AtRun R = p.runs[r];
                 for (int k = 0; k < R.ntiles; k++, j++) {
                     const uint32_t t = ct + j;
-                    const int st = t & 1;
-                    const uint32_t ph = (t >> 1) & 1;
-                    if (!warp_wait(&ctl->s_full[st], ph, abort, p.err, kDevTimeoutSoftmax)) {
+                    if (!warp_wait(&ctl->s_full[x], t & 1, abort, p.err, kDevTimeoutSoftmax)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     uint32_t u[kKeys];
-                    const uint32_t ts = lane_base + (uint32_t)(st * kKeys);
-                    tmem_ld32(ts, u);
-                    tmem_ld32(ts + 32, u + 32);
-                    tmem_ld32(ts + 64, u + 64);
-                    tmem_ld32(ts + 96, u + 96);
+                    tmem_ld32(srow, u);
+                    tmem_ld32(srow + 32, u + 32);
+                    tmem_ld32(srow + 64, u + 64);
+                    tmem_ld32(srow + 96, u + 96);
                     tmem_wait_ld();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->s_empty[st]);
 
                     const int64_t t0 = R.t_glob0 + (int64_t)kKeys * k;
                     const int nv = min(kKeys, R.nkeys - kKeys * k);
@@ -345,26 +392,12 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                         u[q] = pack_bf16(e0, e1);
                     }
                     l = fmaf(l, alpha, l0 + l1);
-
-                    // The previous tile's O += P V must be done: it reads the P
-                    // buffer and writes the rows of O a rescale touches.
-                    if (t > 0 && !warp_wait(&ctl->o_done, (t - 1) & 1, abort, p.err, kDevTimeoutSoftmax)) {
-                        ok = false;
-                        break;
-                    }
-#pragma unroll
-                    for (int ch = 0; ch < 2; ch++)
-#pragma unroll
-                        for (int q = 0; q < 8; q++) {
-                            const uint32_t *w = u + ch * 32 + q * 4;
-                            const uint32_t addr = prow + ch * (kRows * 128) + ((uint32_t)(q ^ (row & 7)) << 4);
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                                         "r"(w[2]), "r"(w[3])
-                                         : "memory");
-                        }
-                    fence_proxy_async();
+                    // P over the scores just read (the A operand of O += P V)
+                    tmem_st32(srow, u);
+                    tmem_st32(srow + 32, u + 32);
+                    // The previous O += P V of this query tile has completed: the
+                    // scores of this tile were computed after it, in order.
                     if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                        tc_fence_after();
 #pragma unroll
                         for (int cc = 0; cc < D / 32; cc++) {
                             uint32_t o[32];
@@ -374,34 +407,37 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                             for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                             tmem_st32(orow + 32 * cc, o);
                         }
-                        tmem_wait_st();
                     }
+                    tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->p_full);
+                    if (lane == 0) mbar_arrive(&ctl->p_full[x]);
                 }
             }
             if (!ok) break;
-            ct += it.ntiles;
-            // The group's aggregate is complete once its last O += P V is done.
-            if (it.ntiles > 0 && !warp_wait(&ctl->o_done, (ct - 1) & 1, abort, p.err, kDevTimeoutSoftmax)) {
-                ok = false;
-                break;
+            // The item's aggregate is complete once its last O += P V is done.
+            if (n > 0) {
+                if (!warp_wait(&ctl->o_fin[x], ci & 1, abort, p.err, kDevTimeoutSoftmax)) {
+                    ok = false;
+                    break;
+                }
+                ct += n;
+                ci++;
             }
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.o + (it.o_off + (int64_t)(row < it.nrows ? row : 0) * it.o_rstr) * 2);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.o + (Q.o_off + (int64_t)(row < nrows ? row : 0) * Q.o_rstr) * 2);
 #pragma unroll
             for (int cc = 0; cc < D / 32; cc++) {
                 uint32_t o[32];
-                if (it.ntiles > 0) {
+                if (n > 0) {
                     tmem_ld32(orow + 32 * cc, o);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; i++) o[i] = 0u;
                 }
-                if (row < it.nrows) {
+                if (row < nrows) {
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
                         const float *f = reinterpret_cast<const float *>(o + 8 * q);
@@ -415,8 +451,8 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                 }
             }
             tc_fence_before();
-            if (p.m_out && row < it.nrows) {
-                const int64_t o = it.ml_off + (int64_t)row * it.ml_rstr;
+            if (p.m_out && row < nrows) {
+                const int64_t o = Q.ml_off + (int64_t)row * Q.ml_rstr;
                 p.m_out[o] = m_max * p.scale;
                 p.l_out[o] = m_max == -INFINITY ? 0.f : l * ex2((m_ref - m_max) * c);
             }
@@ -425,7 +461,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
