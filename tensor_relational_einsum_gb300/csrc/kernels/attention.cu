@@ -29,9 +29,9 @@
 // on its scores the tensor cores run the other's products.
 //
 // Roles (320 threads, one CTA per SM, persistent over its list of items):
-//   warp 8     TMA: Q tiles (one buffer per X), K and V tiles into two rings
-//              of two stages each (128-byte swizzle, one [128 x 64] box per
-//              64 head-dim columns); K runs one tile ahead of V.
+//   warp 8     TMA: Q tiles (one buffer per X), K and V tiles into rings of
+//              two and three stages (128-byte swizzle, one [128 x 64] box per
+//              64 head-dim columns).
 //   warp 9     TMEM owner and MMA issuer (one thread).  Per X and key tile
 //              j: S_X = Q_X K_j^T; after the softmax of X has written P_X,
 //              O_X (+)= P_X V_j with P_X read from TMEM, then at once
@@ -63,11 +63,12 @@ constexpr int kKeys = 128;  // keys of a key tile
 constexpr int kAtThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;  // first TMEM column of the output accumulators
-constexpr float kLazy = 8.0f;    // log2 of the largest exponential taken against a stale maximum
+constexpr float kLazy = 16.0f;   // log2 of the largest exponential taken against a stale maximum
+constexpr int kVStages = 3;      // V ring depth (K: two stages)
 
 struct AtCtl {
     uint64_t q_full[2], q_empty[2];
-    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t k_full[2], k_empty[2], v_full[3], v_empty[3];
     uint64_t s_full[2], p_full[2], o_fin[2];
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -80,8 +81,8 @@ struct AtCfg {
     static constexpr int TILE = kRows * D * 2;   // one [128 x D] bf16 tile
     static constexpr int Q_OFF = 0;              // Q_0, Q_1
     static constexpr int K_OFF = 2 * TILE;       // two K stages
-    static constexpr int V_OFF = 4 * TILE;       // two V stages
-    static constexpr int CTL_OFF = 6 * TILE;
+    static constexpr int V_OFF = 4 * TILE;       // three V stages
+    static constexpr int CTL_OFF = 7 * TILE;
     static constexpr int SMEM = 1024 + CTL_OFF + (int)sizeof(AtCtl);
 };
 
@@ -89,6 +90,13 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Maximum of three (the inputs hold no NaN).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -123,11 +131,13 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             mbar_init(&ctl->q_empty[b], 1);
             mbar_init(&ctl->k_full[b], 1);
             mbar_init(&ctl->k_empty[b], 1);
-            mbar_init(&ctl->v_full[b], 1);
-            mbar_init(&ctl->v_empty[b], 1);
             mbar_init(&ctl->s_full[b], 1);
             mbar_init(&ctl->p_full[b], 4);
             mbar_init(&ctl->o_fin[b], 1);
+        }
+        for (int b = 0; b < kVStages; b++) {
+            mbar_init(&ctl->v_full[b], 1);
+            mbar_init(&ctl->v_empty[b], 1);
         }
         mbar_init(&ctl->mma_done, 1);
         ctl->abort = 0;
@@ -143,16 +153,16 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
     if (warp == 8) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            // K of tile t is loaded before V of tile t - 1: K is needed first
-            // (S = Q K^T) and its stage frees as soon as those MMAs are done.
+            // K and V of tile t in that order: O += P V of tile t comes just
+            // before S = Q K^T of tile t + 1 on the tensor pipe.
             uint32_t ct = 0, qx[2] = {0, 0};  // key tiles; items per query slot
             uint32_t q_armed = 0, q_par = 0, k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
-            const CUtensorMap *pv_map = nullptr;  // V of the previous tile, not yet loaded
+            const CUtensorMap *pv_map = nullptr;  // V block of the tile being loaded
             int pv_c1 = 0, pv_c2 = 0, pv_c3 = 0;
             bool ok = true;
             auto load_v = [&](uint32_t t) -> bool {
-                const int st = t & 1;
-                const uint32_t ph = (t >> 1) & 1;
+                const int st = t % kVStages;
+                const uint32_t ph = (t / kVStages) & 1;
                 if (!mbar_wait(&ctl->v_empty[st], ph ^ 1, abort, p.err, kDevTimeoutProducer)) return false;
                 const uint32_t vs = smem_u32(smem + C::V_OFF + st * C::TILE);
                 mbar_expect_tx(&ctl->v_full[st], C::TILE);
@@ -204,26 +214,26 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                             tma_load_4d(ks + c * (kKeys * 128), km, &ctl->k_full[st], 64 * c, c1, c2, c3);
                         k_armed |= 1u << st;
                         k_par = (k_par & ~(1u << st)) | (ph << st);
-                        if (pv_map && !load_v(ct - 1)) {
-                            ok = false;
-                            break;
-                        }
                         pv_map = vm;
                         pv_c1 = c1;
                         pv_c2 = c2;
                         pv_c3 = c3;
+                        if (!load_v(ct)) {
+                            ok = false;
+                            break;
+                        }
                         ct++;
                     }
                 }
             }
-            if (ok && pv_map) load_v(ct - 1);
             if (*abort) {
                 // Let our own copies land before the CTA can exit.
                 for (int s = 0; s < 2; s++) {
                     if (q_armed & (1u << s)) mbar_wait(&ctl->q_full[s], (q_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
                     if (k_armed & (1u << s)) mbar_wait(&ctl->k_full[s], (k_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
-                    if (v_armed & (1u << s)) mbar_wait(&ctl->v_full[s], (v_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
                 }
+                for (int s = 0; s < kVStages; s++)
+                    if (v_armed & (1u << s)) mbar_wait(&ctl->v_full[s], (v_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
             }
         }
     } else if (warp == 9) {
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             };
             // O_x (+)= P_x V_t, P_x in the first 64 columns of S_x
             auto mma_o = [&](int x, uint32_t t, bool first) {
-                const uint32_t vb = smem_u32(smem + C::V_OFF + (t & 1) * C::TILE);
+                const uint32_t vb = smem_u32(smem + C::V_OFF + (t % kVStages) * C::TILE);
                 const uint32_t pa = tmem + (uint32_t)(x * kKeys);
                 const uint32_t d = tmem + kOCol + (uint32_t)(x * D);
 #pragma unroll
@@ -280,7 +290,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                     const uint32_t t = ct + j;
                     for (int x = 0; x < nq; x++) {
                         if (!mbar_wait(&ctl->p_full[x], (tx[x] + j) & 1, abort, p.err, kDevTimeoutMma) ||
-                            (x == 0 && !mbar_wait(&ctl->v_full[t & 1], (t >> 1) & 1, abort, p.err, kDevTimeoutMma))) {
+                            (x == 0 && !mbar_wait(&ctl->v_full[t % kVStages], (t / kVStages) & 1, abort, p.err, kDevTimeoutMma))) {
                             ok = false;
                             break;
                         }
@@ -298,7 +308,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                         }
                     }
                     if (!ok) break;
-                    umma_commit(&ctl->v_empty[t & 1]);
+                    umma_commit(&ctl->v_empty[t % kVStages]);
                     if (j + 1 < n) umma_commit(&ctl->k_empty[(t + 1) & 1]);
                 }
                 ct += n;
@@ -367,13 +377,13 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                     }
                     float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-                    for (int q = 0; q < kKeys; q += 4) {
-                        mx0 = fmaxf(mx0, __uint_as_float(u[q]));
-                        mx1 = fmaxf(mx1, __uint_as_float(u[q + 1]));
-                        mx2 = fmaxf(mx2, __uint_as_float(u[q + 2]));
-                        mx3 = fmaxf(mx3, __uint_as_float(u[q + 3]));
+                    for (int q = 0; q < kKeys; q += 8) {
+                        mx0 = max3(mx0, __uint_as_float(u[q]), __uint_as_float(u[q + 1]));
+                        mx1 = max3(mx1, __uint_as_float(u[q + 2]), __uint_as_float(u[q + 3]));
+                        mx2 = max3(mx2, __uint_as_float(u[q + 4]), __uint_as_float(u[q + 5]));
+                        mx3 = max3(mx3, __uint_as_float(u[q + 6]), __uint_as_float(u[q + 7]));
                     }
-                    const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                    const float mx = fmaxf(max3(mx0, mx1, mx2), mx3);
                     m_max = fmaxf(m_max, mx);
                     // move the reference maximum only when exponentials would pass 2^kLazy
                     float alpha = 1.f;
