@@ -92,6 +92,38 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Packed two-wide fp32 arithmetic (one instruction for two values).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t pack_u32x2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ float lo_f32(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo;
+}
+__device__ __forceinline__ float hi_f32(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return hi;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Maximum of three (the inputs hold no NaN).
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
@@ -392,16 +424,18 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                         m_ref = mx;
                     }
                     const float base = m_ref == -INFINITY ? 0.f : m_ref * c;
-                    float l0 = 0.f, l1 = 0.f;
+                    // two scores per packed f32x2 FMA and add; four running pair-sums
+                    const uint64_t c2 = pack_f32x2(c, c), nb2 = pack_f32x2(-base, -base);
+                    uint64_t ls[4] = {0, 0, 0, 0};
 #pragma unroll
                     for (int q = 0; q < kKeys / 2; q++) {
-                        const float e0 = ex2(fmaf(__uint_as_float(u[2 * q]), c, -base));
-                        const float e1 = ex2(fmaf(__uint_as_float(u[2 * q + 1]), c, -base));
-                        l0 += e0;
-                        l1 += e1;
+                        const uint64_t y = fma_f32x2(pack_u32x2(u[2 * q], u[2 * q + 1]), c2, nb2);
+                        const float e0 = ex2(lo_f32(y)), e1 = ex2(hi_f32(y));
+                        ls[q & 3] = add_f32x2(ls[q & 3], pack_f32x2(e0, e1));
                         u[q] = pack_bf16(e0, e1);
                     }
-                    l = fmaf(l, alpha, l0 + l1);
+                    const uint64_t s01 = add_f32x2(add_f32x2(ls[0], ls[1]), add_f32x2(ls[2], ls[3]));
+                    l = fmaf(l, alpha, lo_f32(s01) + hi_f32(s01));
                     // P over the scores just read (the A operand of O += P V)
                     tmem_st32(srow, u);
                     tmem_st32(srow + 32, u + 32);
