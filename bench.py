@@ -370,6 +370,7 @@ def traffic_from_profiles():
     if not os.path.exists(prof):
         return None
     h = hashlib.sha256(open(os.path.join(csrc, "kernels", "contract_tc.cu"), "rb").read() +
+                       open(os.path.join(csrc, "kernels", "tc_common.cuh"), "rb").read() +
                        open(os.path.join(csrc, "joinagg.cpp"), "rb").read()).hexdigest()[:16]
     want, val = None, None
     for line in open(prof):
