@@ -121,6 +121,8 @@ struct TcGroup {
     int32_t t0, t1;                    // tuples [t0, t1)
     int32_t out_map;                   // tensor map index of the output block
     int32_t n_ext;                     // N extent of the output block
+    int32_t m_ext;                     // M extent (tiles at m0 >= m_ext are padding: computed, not stored)
+    int32_t pad;
     int64_t m_lo, n_lo;                // predicate coordinates
 };
 
@@ -212,6 +214,8 @@ struct TcParams {
     float scale;
     int32_t pred_mode;
     int32_t bn;                        // 128 or 256
+    int32_t cluster;                   // CTAs per cluster sharing each B tile (1 or 2): tiles
+                                       // 2 p and 2 p + 1 have the same group, batch and n0
     int *err;
 };
 cudaError_t launch_contract_tc(const TcParams &p, int num_sms, cudaStream_t st);

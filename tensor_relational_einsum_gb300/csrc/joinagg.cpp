@@ -749,6 +749,11 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
     if (tg_ops.empty()) return EA_ERR_UNSUPPORTED;
     const int bn = maxN <= 128 ? 128 : 256;
     if (mode && swap) mode = 3 - mode;  // the mask is stated in the swapped roles
+    // Clusters of two CTAs share each B tile (multicast) when there are
+    // enough tiles to keep every SM busy in pairs.
+    int64_t est_tiles = 0;
+    for (const GroupGeom &G : gg) est_tiles += G.nb * ((G.M + 127) / 128) * ((G.N + bn - 1) / bn);
+    const int cl = est_tiles >= 2 * (int64_t)c->num_sms ? 2 : 1;
     // ---- pass 2: tensor maps, tuples, tiles
     std::vector<CUtensorMap> maps;
     std::vector<TcGroup> groups;
@@ -788,13 +793,14 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
             memset(&T, 0, sizeof T);
             ea_status s = op_map(A, a_mn, 128, cache_a, &T.a_map);
             if (s) return s;
-            s = op_map(B, b_mn, bn, cache_b, &T.b_map);
+            s = op_map(B, b_mn, bn / cl, cache_b, &T.b_map);
             if (s) return s;
             T.kchunks = (int32_t)((A.K + 63) / 64);
             tuples.push_back(T);
         }
         TG.t1 = (int32_t)tuples.size();
         TG.n_ext = (int32_t)G.N;
+        TG.m_ext = (int32_t)G.M;
         if (empty) continue;
         CUtensorMap m;
         const void *cptr = j.out->arena + G.c_base * esc;
@@ -807,14 +813,20 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
         groups.push_back(TG);
         // Grouped raster: bands of kBand m-tiles, each band swept across all
         // n-tiles with m fastest, so the tiles in flight at once share a
-        // small set of A rows and B columns that stays in L2.
+        // small set of A rows and B columns that stays in L2.  With clusters
+        // the tiles come in pairs of the same n-tile (consecutive m-tiles; a
+        // band with an odd count gets a padding tile past the block's rows).
         const int64_t kBand = 16;
         const int64_t nm = (G.M + 127) / 128, nn = (G.N + bn - 1) / bn;
         for (int64_t bb = 0; bb < G.nb; bb++)
             for (int64_t mb = 0; mb < nm; mb += kBand)
-                for (int64_t ni = 0; ni < nn; ni++)
-                    for (int64_t mi = mb; mi < std::min(nm, mb + kBand); mi++)
+                for (int64_t ni = 0; ni < nn; ni++) {
+                    const int64_t me = std::min(nm, mb + kBand);
+                    for (int64_t mi = mb; mi < me; mi++)
                         tiles.push_back(TcTile{gid, (int32_t)bb, (int32_t)(mi * 128), (int32_t)(ni * bn)});
+                    if (cl == 2 && ((me - mb) & 1))
+                        tiles.push_back(TcTile{gid, (int32_t)bb, (int32_t)(me * 128), (int32_t)(ni * bn)});
+                }
     }
     if (tiles.size() > (size_t)INT32_MAX) return EA_ERR_UNSUPPORTED;
     Blob b;
@@ -835,6 +847,7 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
     q.scale = j.scale;
     q.pred_mode = mode;
     q.bn = bn;
+    q.cluster = cl;
     q.err = c->err;
     return EA_OK;
 }

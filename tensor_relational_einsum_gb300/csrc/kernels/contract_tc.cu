@@ -65,9 +65,16 @@ struct SmemCtl {
 
 // ------------------------------------------------------------------ kernel
 
-template <int BN>
+template <int BN, int CL>
 __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams p) {
     using C = Cfg<BN>;
+    // CL CTAs of a cluster run tiles that share their B tile: each loads
+    // 1/CL of it and multicasts it to all, so L2 serves each B byte once
+    // per cluster; a stage is refilled only when every CTA's MMAs are done
+    // with it (their commits arrive on every CTA's `empty`).
+    constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1);
+    const int rank = CL > 1 ? (int)cluster_rank() : 0;
+    const int nunits = (p.ntiles + CL - 1) / CL, unit0 = blockIdx.x / CL, ustep = gridDim.x / CL;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *stages = smem;
@@ -80,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; s++) {
             mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->empty[s], CL);
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(&ctl->tfull[a], 1);
@@ -95,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
     if (warp == 2) tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
+    if (CL > 1) cluster_sync();  // every CTA's barriers are initialised before any multicast
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
@@ -103,8 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
         int stage = 0;
         uint32_t ph = 0;
         uint32_t armed = 0, armed_par = 0;  // per stage: a load issued, and its phase parity
-        for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
-            const TcTile T = p.tiles[tile];
+        for (int unit = unit0; unit < nunits; unit += ustep) {
+            const TcTile T = p.tiles[unit * CL + rank];
             const TcGroup G = p.groups[T.group];
             bool ok = true;
             for (int t = G.t0; t < G.t1 && ok; t++) {
@@ -125,11 +133,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                         tma_load_3d(sa, am, fb, T.m0, kc * BK, T.batch);
                         tma_load_3d(sa + 8192, am, fb, T.m0 + 64, kc * BK, T.batch);
                     }
-                    if (!p.b_mn_major) {
-                        tma_load_3d(sb, bm, fb, kc * BK, T.n0, T.batch);
-                    } else {
+                    if (CL == 1) {
+                        if (!p.b_mn_major) {
+                            tma_load_3d(sb, bm, fb, kc * BK, T.n0, T.batch);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; j++) tma_load_3d(sb + j * 8192, bm, fb, T.n0 + 64 * j, kc * BK, T.batch);
+                            for (int j = 0; j < BN / 64; j++)
+                                tma_load_3d(sb + j * 8192, bm, fb, T.n0 + 64 * j, kc * BK, T.batch);
+                        }
+                    } else {
+                        // this CTA's 1/CL of the B tile, to every CTA of the cluster
+                        constexpr int ROWS = BN / CL;
+                        if (!p.b_mn_major) {
+                            tma_load_3d_mc(sb + rank * ROWS * 128, bm, fb, kc * BK, T.n0 + rank * ROWS, T.batch, kMask);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < ROWS / 64; j++) {
+                                const int jj = rank * (ROWS / 64) + j;
+                                tma_load_3d_mc(sb + jj * 8192, bm, fb, T.n0 + 64 * jj, kc * BK, T.batch, kMask);
+                            }
+                        }
                     }
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (ph << stage);
@@ -152,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
         int stage = 0, acc = 0;
         uint32_t ph = 0, acc_ph = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
-            const TcTile T = p.tiles[tile];
+        for (int unit = unit0; unit < nunits && ok; unit += ustep) {
+            const TcTile T = p.tiles[unit * CL + rank];
             const TcGroup G = p.groups[T.group];
             if (!mbar_wait(&ctl->tempty[acc], acc_ph ^ 1, abort, p.err, kDevTimeoutMma)) break;
             tc_fence_after();
@@ -175,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                         umma_bf16(d, ad, bd, idesc, accumulate);
                         accumulate = 1;
                     }
-                    umma_commit(&ctl->empty[stage]);
+                    if (CL == 1) umma_commit(&ctl->empty[stage]);
+                    else umma_commit_mc(&ctl->empty[stage], kMask);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         ph ^= 1;
@@ -197,10 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
         const int CW = p.out_f32 ? 32 : 64;  // columns per 128-byte row chunk
         int acc = 0, buf = 0;
         uint32_t acc_ph = 0;
-        for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
-            const TcTile T = p.tiles[tile];
+        for (int unit = unit0; unit < nunits; unit += ustep) {
+            const TcTile T = p.tiles[unit * CL + rank];
             const TcGroup G = p.groups[T.group];
             const CUtensorMap *om = maps + G.out_map;
+            const bool store = T.m0 < G.m_ext;  // a padding tile of a cluster is computed, not stored
             if (ep == 0) ctl->ep_ok = mbar_wait(&ctl->tfull[acc], acc_ph, abort, p.err, kDevTimeoutEpilogue) ? 1 : 0;
             named_bar(1, 128);
             if (!ctl->ep_ok) break;
@@ -208,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
             const uint32_t tb = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
             const int64_t m_g = G.m_lo + T.m0 + ep;
             for (int c0 = 0; c0 < BN; c0 += CW) {
-                if (T.n0 + c0 >= G.n_ext) break;  // whole chunk past the block edge
+                if (T.n0 + c0 >= G.n_ext || !store) break;  // whole chunk past the block edge
                 uint32_t r[64];
                 tmem_ld32(tb + c0, r);
                 if (!p.out_f32) tmem_ld32(tb + c0 + 32, r + 32);
@@ -275,20 +300,40 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
+    if (CL > 1) cluster_sync();  // no CTA leaves while a peer may still signal or fill its shared memory
 }
 
-template <int BN>
+template <int BN, int CL>
 cudaError_t launch_bn(const TcParams &p, int num_sms, cudaStream_t st) {
     using C = Cfg<BN>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(tc_contract_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(tc_contract_kernel<BN, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured[dev] = true;
     }
-    int grid = std::min<int>(p.ntiles, num_sms);
-    tc_contract_kernel<BN><<<grid, kThreads, C::SMEM, st>>>(p);
-    return cudaGetLastError();
+    const int units = (p.ntiles + CL - 1) / CL;
+    const int grid = std::min<int>(units, num_sms / CL) * CL;
+    if (CL == 1) {
+        tc_contract_kernel<BN, CL><<<grid, kThreads, C::SMEM, st>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_contract_kernel<BN, CL>, p);
 }
 
 }  // namespace
@@ -296,8 +341,12 @@ cudaError_t launch_bn(const TcParams &p, int num_sms, cudaStream_t st) {
 int tc_smem_bytes(int bn) { return bn == 256 ? Cfg<256>::SMEM : Cfg<128>::SMEM; }
 
 cudaError_t launch_contract_tc(const TcParams &p, int num_sms, cudaStream_t st) {
-    if (p.bn == 256) return launch_bn<256>(p, num_sms, st);
-    return launch_bn<128>(p, num_sms, st);
+    if (p.cluster == 2) {
+        if (p.bn == 256) return launch_bn<256, 2>(p, num_sms, st);
+        return launch_bn<128, 2>(p, num_sms, st);
+    }
+    if (p.bn == 256) return launch_bn<256, 1>(p, num_sms, st);
+    return launch_bn<128, 1>(p, num_sms, st);
 }
 
 }  // namespace ea
