@@ -316,13 +316,12 @@ cudaError_t launch_bn(const TcParams &p, int num_sms, cudaStream_t st) {
         configured[dev] = true;
     }
     const int units = (p.ntiles + CL - 1) / CL;
-    const int grid = std::min<int>(units, num_sms / CL) * CL;
     if (CL == 1) {
-        tc_contract_kernel<BN, CL><<<grid, kThreads, C::SMEM, st>>>(p);
+        tc_contract_kernel<BN, CL><<<std::min<int>(units, num_sms), kThreads, C::SMEM, st>>>(p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.gridDim = dim3(CL * std::min<int>(units, num_sms / CL), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
@@ -333,6 +332,16 @@ cudaError_t launch_bn(const TcParams &p, int num_sms, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // a persistent grid of no more clusters than can be resident at once
+    static int resident[64] = {};
+    const int di = (dev >= 0 && dev < 64) ? dev : 0;
+    if (resident[di] == 0) {
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, tc_contract_kernel<BN, CL>, &cfg);
+        if (e != cudaSuccess) return e;
+        resident[di] = n > 0 ? n : std::max(1, num_sms / CL);
+    }
+    cfg.gridDim = dim3(CL * std::max(1, std::min(units, resident[di])), 1, 1);
     return cudaLaunchKernelEx(&cfg, tc_contract_kernel<BN, CL>, p);
 }
 

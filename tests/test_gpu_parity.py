@@ -142,6 +142,19 @@ def test_tc_batch_inside_block_and_swapped_roles():
     assert rel_frob(got, want) <= 1e-5
 
 
+@pytest.mark.parametrize("spec,bshape", [("bij,bjk->bik", (16, 256, 1096)), ("bij,bkj->bik", (16, 1096, 256))])
+def test_tc_clusters_with_padding_tiles(spec, bshape):
+    # 16 groups of M = 300 (three m-tiles: a padding tile completes each pair
+    # of a two-CTA cluster), N = 1100 (ragged), K = 256: 320 tiles, enough for
+    # the clustered launch that multicasts each B tile to both CTAs
+    # (B MN-major in the first case, K-major in the second)
+    got, want, _ = _bf16_case(spec, [(16, 300, 256), bshape], [[16, 1, 1], [16, 1, 1]], "f32")
+    assert rel_frob(got, want) <= 1e-5
+    got, want, _ = _bf16_case(spec, [(16, 300, 256), bshape], [[16, 1, 1], [16, 1, 1]], "f32",
+                              dist=("int", -2, 2))
+    assert np.array_equal(got, want)
+
+
 def test_tc_unaligned_falls_back_to_simt():
     got, want, _ = _bf16_case("ij,jk->ik", [(70, 45), (45, 33)], [[2, 3], [3, 1]], "f32", expect="contract_simt")
     assert rel_frob(got, want) <= 1e-5
