@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define EA_ABI_VERSION 1
+#define EA_ABI_VERSION 2
 
 typedef int ea_status;
 #define EA_OK 0
@@ -131,7 +131,27 @@ typedef struct {
  *              of angle pos * theta^(-2i/d).  Not owned.
  *   out2       EA_AGG_MAX_SUMEXP: the relation receiving the SUM of exp;
  *              same extents and tiling as the output, created by the
- *              caller.  Ignored otherwise.                               */
+ *              caller.  Ignored otherwise.
+ *   epi_map, epi_in, epi_pair  an elementwise join fused into a
+ *              contraction (SUM of PRODUCT over two bf16 inputs), applied to
+ *              every aggregated output cell v (after scale) before it is
+ *              stored ("Every Kernel Is a Join", Definition 3.7: the
+ *              contraction's output relation is consumed by the join
+ *              without ever being written):
+ *                EA_MAP_ADD       out = v + epi_in at the same output cell;
+ *                                 epi_in has the output's extents, tiling
+ *                                 and dtype (the residual join "o,o->o").
+ *                EA_MAP_SILU_MUL  epi_pair names a letter of the second
+ *                                 input only, extent 2, one block, absent
+ *                                 from the output term.  The contraction
+ *                                 is computed as if epi_pair were the
+ *                                 output's innermost letter, and each pair
+ *                                 of cells g (epi_pair = 0), u (= 1) is
+ *                                 stored as SiLU(g) * u (the join
+ *                                 "of,of->of" of the two slices).  bf16
+ *                                 output only.
+ *              0 = no epilogue.  A join-agg that does not run on the
+ *              tcgen05 contraction kernel returns EA_ERR_UNSUPPORTED.    */
 typedef struct {
     int32_t out_dtype;
     float scale;
@@ -139,11 +159,14 @@ typedef struct {
     char pred_lo;
     char pred_hi;
     char rope_pos;
-    char reserved0;
+    char epi_pair;
     const float *rope_table;
     int64_t rope_npos;
     ea_relation out2;
-    int64_t reserved[3];
+    ea_relation epi_in;
+    int32_t epi_map;
+    int32_t reserved0;
+    int64_t reserved[1];
 } ea_opts;
 
 /* ------------------------------------------------------------ basics */

@@ -41,8 +41,9 @@ class IndexPart(ctypes.Structure):
 class Opts(ctypes.Structure):
     _fields_ = [("out_dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("eps", ctypes.c_float),
                 ("pred_lo", ctypes.c_char), ("pred_hi", ctypes.c_char), ("rope_pos", ctypes.c_char),
-                ("reserved0", ctypes.c_char), ("rope_table", ctypes.c_void_p), ("rope_npos", ctypes.c_int64),
-                ("out2", ctypes.c_void_p), ("reserved", ctypes.c_int64 * 3)]
+                ("epi_pair", ctypes.c_char), ("rope_table", ctypes.c_void_p), ("rope_npos", ctypes.c_int64),
+                ("out2", ctypes.c_void_p), ("epi_in", ctypes.c_void_p), ("epi_map", ctypes.c_int32),
+                ("reserved0", ctypes.c_int32), ("reserved", ctypes.c_int64 * 1)]
 
 
 class AttnOpts(ctypes.Structure):
@@ -96,7 +97,7 @@ def lib():
                      "ea_joinagg_run", "ea_exchange", "ea_plan_worklist", "ea_exchange_permutation",
                      "ea_overlay_atoms", "ea_last_plan", "ea_exchange_noalloc", "ea_attention_run"):
             getattr(L, name).restype = ctypes.c_int
-        if L.ea_abi_version() != 1:
+        if L.ea_abi_version() != 2:
             raise ImportError("libea.so ABI version mismatch")
         _lib = L
         return _lib

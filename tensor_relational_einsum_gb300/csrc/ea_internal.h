@@ -124,6 +124,8 @@ struct TcGroup {
     int32_t m_ext;                     // M extent (tiles at m0 >= m_ext are padding: computed, not stored)
     int32_t pad;
     int64_t m_lo, n_lo;                // predicate coordinates
+    int64_t e_base, e_sm, e_sb;        // epilogue ADD: element offset of the block in epi_in, row and
+                                       // batch strides (the output's: same extents and tiling)
 };
 
 struct TcTuple {
@@ -216,6 +218,8 @@ struct TcParams {
     int32_t bn;                        // 128 or 256
     int32_t cluster;                   // CTAs per cluster sharing each B tile (1 or 2): tiles
                                        // 2 p and 2 p + 1 have the same group, batch and n0
+    int32_t epi;                       // epilogue join: 0 none, 1 ADD epi_in, 2 SiLU(g) * u of column pairs
+    const char *epi_in;                // epi 1: the joined relation's arena (output dtype)
     int *err;
 };
 cudaError_t launch_contract_tc(const TcParams &p, int num_sms, cudaStream_t st);

@@ -197,6 +197,10 @@ struct JoinCtx {
     int64_t rope_npos;
     char rope_pos;
     ea_relation_s *out2;
+    int epi_map;                 // epilogue join of a contraction: 0, EA_MAP_ADD or EA_MAP_SILU_MUL
+    const ea_relation_s *epi_in; // EA_MAP_ADD: the joined relation (output's extents and tiling)
+    char epi_pair;               // EA_MAP_SILU_MUL: the paired letter (innermost in the planned output)
+    ea_relation_s *user_out;     // the output relation (out is its pre-epilogue view when paired)
 };
 
 // Special letters of an elementwise / row-reduction view.
@@ -802,10 +806,18 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
         TG.n_ext = (int32_t)G.N;
         TG.m_ext = (int32_t)G.M;
         if (empty) continue;
+        // the stored output: the planned one, or its pairs halved (one cell per pair)
+        const int64_t h = j.epi_pair ? 2 : 1;
+        if (j.epi_pair && (G.N % 2 || G.c_base % 2 || G.c_sm % 2 || G.c_sb % 2 || !al16(G.c_base / 2, esc) ||
+                           !al16(G.c_sm / 2, esc) || !al16(G.c_sb / 2, esc)))
+            return EA_ERR_UNSUPPORTED;
+        TG.e_base = G.c_base / h;
+        TG.e_sm = G.c_sm / h;
+        TG.e_sb = G.c_sb / h;
         CUtensorMap m;
-        const void *cptr = j.out->arena + G.c_base * esc;
-        ea_status s = encode_map(c, &m, j.out->dtype, cptr, G.N, G.M, G.nb, G.c_sm * esc, G.c_sb * esc,
-                                 (uint32_t)(128 / esc), 128);
+        const void *cptr = j.out->arena + (G.c_base / h) * esc;
+        ea_status s = encode_map(c, &m, j.out->dtype, cptr, G.N / h, G.M, G.nb, (G.c_sm / h) * esc,
+                                 (G.c_sb / h) * esc, (uint32_t)(128 / esc), 128);
         if (s) return s;
         TG.out_map = (int32_t)maps.size();
         maps.push_back(m);
@@ -848,6 +860,8 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
     q.pred_mode = mode;
     q.bn = bn;
     q.cluster = cl;
+    q.epi = j.epi_map == EA_MAP_ADD ? 1 : j.epi_map == EA_MAP_SILU_MUL ? 2 : 0;
+    q.epi_in = j.epi_in ? j.epi_in->arena : nullptr;
     q.err = c->err;
     return EA_OK;
 }
@@ -1086,6 +1100,42 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
                 inputs[k]->arena < orel->arena + orel->bytes && orel->arena != inputs[k]->arena)
                 return set_error(EA_ERR_ARG, "output arena partially overlaps input %d", k);
     }
+    // Epilogue join of a contraction.
+    j.epi_map = o.epi_map;
+    j.epi_in = o.epi_in;
+    j.epi_pair = 0;
+    if (o.epi_map != 0) {
+        if (!(map == EA_MAP_PRODUCT && agg == EA_AGG_SUM && n_inputs == 2))
+            return set_error(EA_ERR_UNSUPPORTED, "an epilogue join needs a contraction (SUM of PRODUCT, two inputs)");
+        if (j.pred_lo) return set_error(EA_ERR_UNSUPPORTED, "an epilogue join with a predicate is not supported");
+        if (o.epi_map == EA_MAP_ADD) {
+            const ea_relation_s *r = o.epi_in;
+            if (!r) return set_error(EA_ERR_ARG, "epilogue ADD needs epi_in");
+            if (r->rank != orank || r->dtype != (orel ? orel->dtype : odt))
+                return set_error(EA_ERR_SHAPE, "epi_in must have the output's rank and dtype");
+            if (((uintptr_t)r->arena & 15) != 0) return set_error(EA_ERR_UNSUPPORTED, "epi_in arena not 16-byte aligned");
+            for (int d = 0; d < orank; d++) {
+                if (r->dims[d] != odims[d]) return set_error(EA_ERR_SHAPE, "epi_in extent mismatch in dim %d", d);
+                if (!same_tiling(r, d, j.lt.t[j.sp.out[d] - 'a']))
+                    return set_error(EA_ERR_PARTITION, "epi_in is tiled differently from the output letters");
+            }
+        } else if (o.epi_map == EA_MAP_SILU_MUL) {
+            const char pc = o.epi_pair;
+            if (pc < 'a' || pc > 'z') return set_error(EA_ERR_ARG, "epilogue SILU_MUL needs epi_pair, a letter");
+            const Tiling &tp = j.lt.t[pc - 'a'];
+            if (tp.extent != 2 || tp.nblocks() != 1 || j.sp.term[0].find(pc) != std::string::npos ||
+                j.sp.term[1].find(pc) == std::string::npos || j.sp.out.find(pc) != std::string::npos)
+                return set_error(EA_ERR_SPEC, "epi_pair '%c' must be a letter of the second input only, extent 2, one block",
+                                 pc);
+            if ((orel ? orel->dtype : odt) != EA_BF16) return set_error(EA_ERR_DTYPE, "epilogue SILU_MUL writes bf16 only");
+            j.epi_pair = pc;
+            // plan with the paired letter as the innermost output letter
+            j.sp.out.push_back(pc);
+            j.sp.contracted.erase(j.sp.contracted.find(pc), 1);
+        } else {
+            return set_error(EA_ERR_UNSUPPORTED, "epilogue map %d (ADD or SILU_MUL only)", o.epi_map);
+        }
+    }
     // Classify.
     int kind;
     ContractionViews cv;
@@ -1120,6 +1170,32 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
         created = true;
     }
     j.out = orel;
+    j.user_out = orel;
+    // A paired epilogue is planned against the output's pre-epilogue view:
+    // the paired letter appended as the innermost output letter (every cell
+    // doubled, blocks at twice the offsets), which the kernel stores halved.
+    ea_relation_s vout;
+    if (j.epi_pair) {
+        if (orank + 1 > kMaxRank) {
+            if (created) ea_relation_destroy(orel);
+            return set_error(EA_ERR_UNSUPPORTED, "output rank too large for a paired epilogue");
+        }
+        vout.dtype = orel->dtype;
+        vout.rank = orank + 1;
+        for (int d = 0; d < orank; d++) {
+            vout.dims[d] = orel->dims[d];
+            vout.bounds[d] = orel->bounds[d];
+        }
+        vout.dims[orank] = 2;
+        vout.bounds[orank] = {0, 2};
+        vout.nblocks = orel->nblocks;
+        vout.blk_off.resize(orel->blk_off.size());
+        for (size_t i = 0; i < orel->blk_off.size(); i++) vout.blk_off[i] = 2 * orel->blk_off[i];
+        vout.arena = orel->arena;
+        vout.bytes = 2 * orel->bytes;
+        vout.owned = false;
+        j.out = &vout;
+    }
     DevCtx *c;
     s = get_ctx(&c);
     if (s) {
@@ -1141,6 +1217,9 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
     key.v(j.rope_table);
     key.v(j.rope_npos);
     if (j.out2) key.rel(j.out2);
+    key.v(j.epi_map);
+    key.v(j.epi_pair);
+    if (j.epi_in) key.rel(j.epi_in);
     cudaStream_t st = (cudaStream_t)stream;
     DevPlan *p = nullptr;
     auto it = g_cache.find(key.s);
@@ -1154,7 +1233,10 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
             else if (kind == kRowReduce) s = build_rowreduce(j, c, st, p);
             else {
                 s = build_tc(j, cv, c, st, p);
-                if (s == EA_ERR_UNSUPPORTED) {
+                if (s == EA_ERR_UNSUPPORTED && j.epi_map) {
+                    s = set_error(EA_ERR_UNSUPPORTED, "an epilogue join needs the tcgen05 contraction path "
+                                                      "(bf16 operands that TMA can tile)");
+                } else if (s == EA_ERR_UNSUPPORTED) {
                     free_plan(p);
                     p = new DevPlan();
                     set_error(EA_OK, "");

@@ -28,6 +28,7 @@
 // the MMA issuer waits for its own MMAs, TMEM is freed and the CTA exits.
 #include <algorithm>
 
+#include "dev_common.cuh"
 #include "tc_common.cuh"
 
 namespace ea {
@@ -232,7 +233,50 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
             const int64_t m_g = G.m_lo + T.m0 + ep;
-            for (int c0 = 0; c0 < BN; c0 += CW) {
+            // epilogue join SiLU(g) * u over column pairs: 128 planned columns -> 64 stored
+            for (int c0 = 0; p.epi == 2 && c0 < BN; c0 += 128) {
+                if (T.n0 + c0 >= G.n_ext || !store) break;
+                uint8_t *sbuf = staging + buf * 16384;
+                const uint32_t rowbase = smem_u32(sbuf) + ep * 128;
+#pragma unroll
+                for (int hh = 0; hh < 2; hh++) {
+                    uint32_t r[64];
+                    tmem_ld32(tb + c0 + 64 * hh, r);
+                    tmem_ld32(tb + c0 + 64 * hh + 32, r + 32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            float o2[2];
+#pragma unroll
+                            for (int z = 0; z < 2; z++) {
+                                const int jj = 8 * q + 2 * e + z;  // stored column inside the half
+                                const float g = __uint_as_float(r[2 * jj]) * p.scale;
+                                const float u = __uint_as_float(r[2 * jj + 1]) * p.scale;
+                                o2[z] = __fdividef(g, 1.0f + __expf(-g)) * u;
+                            }
+                            __nv_bfloat162 hv = __floats2bfloat162_rn(o2[0], o2[1]);
+                            w[e] = *reinterpret_cast<uint32_t *>(&hv);
+                        }
+                        const uint32_t addr = rowbase + ((uint32_t)((4 * hh + q) ^ (ep & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                                     "r"(w[2]), "r"(w[3])
+                                     : "memory");
+                    }
+                }
+                fence_proxy_async();
+                named_bar(1, 128);
+                if (ep == 0) {
+                    tma_store_3d(om, smem_u32(sbuf), (T.n0 + c0) / 2, T.m0, T.batch);
+                    bulk_commit();
+                    bulk_wait_read1();
+                }
+                buf ^= 1;
+                named_bar(1, 128);
+            }
+            for (int c0 = 0; p.epi != 2 && c0 < BN; c0 += CW) {
                 if (T.n0 + c0 >= G.n_ext || !store) break;  // whole chunk past the block edge
                 uint32_t r[64];
                 tmem_ld32(tb + c0, r);
@@ -248,6 +292,35 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                             if ((p.pred_mode == 1 && n_g > m_g) || (p.pred_mode == 2 && m_g > n_g)) x = -INFINITY;
                         }
                         v[j] = x;
+                    }
+                }
+                if (p.epi == 1 && T.m0 + ep < G.m_ext) {
+                    // epilogue join ADD: the joined relation's cells of this row segment
+                    const int64_t e0 = G.e_base + (int64_t)T.batch * G.e_sb + (int64_t)(T.m0 + ep) * G.e_sm + T.n0 + c0;
+                    const int nvalid = (int)min64((int64_t)CW, (int64_t)G.n_ext - (T.n0 + c0));
+                    if (nvalid == CW) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(p.epi_in + e0 * (p.out_f32 ? 4 : 2));
+#pragma unroll
+                        for (int q = 0; q < 8; q++) {
+                            const uint4 w = __ldg(src + q);
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int e = 0; e < 4; e++) {
+                                if (p.out_f32) {
+                                    v[4 * q + e] += __uint_as_float(ww[e]);
+                                } else {
+                                    v[8 * q + 2 * e] += __uint_as_float(ww[e] << 16);
+                                    v[8 * q + 2 * e + 1] += __uint_as_float(ww[e] & 0xFFFF0000u);
+                                }
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 64; jj++)
+                            if (jj < nvalid) {
+                                if (p.out_f32) v[jj] += reinterpret_cast<const float *>(p.epi_in)[e0 + jj];
+                                else v[jj] += __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.epi_in)[e0 + jj]);
+                            }
                     }
                 }
                 uint8_t *sbuf = staging + buf * 16384;

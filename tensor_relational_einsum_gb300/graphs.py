@@ -16,8 +16,10 @@ All arithmetic runs in libea.so.
                       SiLU(gate) * up elementwise join, down contraction.
 * ``LlamaBlock``      pre-norm block: RMSNorm, fused QKV contraction, RoPE,
                       causal attention (fused, or the chain), exchange of the attention
-                      output into the O-projection's tiling, O projection,
-                      residual, RMSNorm, SwiGLU FFN, residual.
+                      output into the O-projection's tiling, O projection
+                      (+ residual in its epilogue), RMSNorm, SwiGLU FFN
+                      (SiLU * up and the second residual in the contraction
+                      epilogues), or the same with every join unfused.
 """
 from __future__ import annotations
 
@@ -143,23 +145,36 @@ class FusedAttention:
 
 class SwigluFFN:
     """x [T, D] tiled (t_blocks, 4); w_gate, w_up [D, F] and w_down [F, D];
-    contracted dims in ``k_blocks`` blocks (partial products SUM-aggregate)."""
+    contracted dims in ``k_blocks`` blocks (partial products SUM-aggregate).
+
+    fused: gate and up are one weight relation [D, F, 2] (c innermost), and
+    the elementwise join H = SiLU(G) * U runs in the contraction's epilogue
+    over the c pairs, so G and U are never written; the down projection can
+    fuse a residual join (Y = H w_down + residual).  Unfused: the three
+    join-aggs of the chain, with G and U as halves of one [2, T, F] output."""
 
     def __init__(self, x: Relation, w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
-                 k_blocks: int = 4, out: Relation | None = None):
+                 k_blocks: int = 4, out: Relation | None = None, fused: bool = True,
+                 residual: Relation | None = None):
         T, D = x.dims
         F = w_gate.shape[1]
         tb = x.bounds[0]
         dev = x.storage.device
         self.x = x
-        # gate and up share their join: one relation [D, 2, F] (c = 0 gate, 1 up)
-        gu = torch.stack([w_gate, w_up], dim=1).contiguous()
-        self.wgu = Relation.from_dense(gu, [x.bounds[1], 2, k_blocks])
+        self.fused = fused
+        self.residual = residual
+        if fused:
+            self.wgu = Relation.from_dense(torch.stack([w_gate, w_up], dim=2).contiguous(), [x.bounds[1], k_blocks, 1])
+            self.G = self.U = None
+        else:
+            # gate and up share their join: one relation [D, 2, F] (c = 0 gate, 1 up)
+            gu = torch.stack([w_gate, w_up], dim=1).contiguous()
+            self.wgu = Relation.from_dense(gu, [x.bounds[1], 2, k_blocks])
+            self.gu = Relation("bf16", (2, T, F), [2, tb, k_blocks], device=dev)
+            half = T * F
+            self.G = view(self.gu, 0, (T, F), [tb, k_blocks])
+            self.U = view(self.gu, half, (T, F), [tb, k_blocks])
         self.wd = Relation.from_dense(w_down.contiguous(), [k_blocks, x.bounds[1]])
-        self.gu = Relation("bf16", (2, T, F), [2, tb, k_blocks], device=dev)
-        half = T * F
-        self.G = view(self.gu, 0, (T, F), [tb, k_blocks])
-        self.U = view(self.gu, half, (T, F), [tb, k_blocks])
         self.H = Relation("bf16", (T, F), [tb, k_blocks], device=dev)
         self.Y = out if out is not None else Relation("bf16", (T, D), [tb, x.bounds[1]], device=dev)
         self.T, self.D, self.F = T, D, F
@@ -167,9 +182,17 @@ class SwigluFFN:
     def run(self, x: Relation | None = None, rec: Recorder | None = None):
         x = x or self.x
         c = rec.call if rec is not None else _direct
-        c("ffn.gate_up", lambda: joinagg("td,dcf->ctf", [x, self.wgu], "sum", "product", out=self.gu))
-        c("ffn.silu_mul", lambda: joinagg("tf,tf->tf", [self.G, self.U], "none", "silu_mul", out=self.H))
-        c("ffn.down", lambda: joinagg("tf,fd->td", [self.H, self.wd], "sum", "product", out=self.Y))
+        if self.fused:
+            c("ffn.gate_up", lambda: joinagg("td,dfc->tf", [x, self.wgu], "sum", "product", out=self.H,
+                                             epi_map="silu_mul", epi_pair="c"))
+        else:
+            c("ffn.gate_up", lambda: joinagg("td,dcf->ctf", [x, self.wgu], "sum", "product", out=self.gu))
+            c("ffn.silu_mul", lambda: joinagg("tf,tf->tf", [self.G, self.U], "none", "silu_mul", out=self.H))
+        if self.residual is not None:
+            c("ffn.down", lambda: joinagg("tf,fd->td", [self.H, self.wd], "sum", "product", out=self.Y,
+                                          epi_map="add", epi_in=self.residual))
+        else:
+            c("ffn.down", lambda: joinagg("tf,fd->td", [self.H, self.wd], "sum", "product", out=self.Y))
         return self.Y
 
     def flops(self) -> float:
@@ -182,7 +205,7 @@ class LlamaBlock:
 
     def __init__(self, b: int, s: int, D: int, n_heads: int, F: int, W: dict, eps: float = 1e-6,
                  theta: float = 10000.0, d_blocks: int = 4, s_blocks: int = 4, device="cuda",
-                 fused_attention: bool = True):
+                 fused_attention: bool = True, fused_epilogues: bool = True):
         self.b, self.s, self.D, self.H, self.F = b, s, D, n_heads, F
         self.dh = D // n_heads
         T = b * s
@@ -219,12 +242,18 @@ class LlamaBlock:
         self.o_tok = view(self.attn.O, 0, (T, D), [b * sb, 1])
         # ... re-blocked by the exchange into the O projection's contraction tiling
         self.o_ex = Relation("bf16", (T, D), [tb, db], device=dev)
-        self.a = Relation("bf16", (T, D), [tb, db], device=dev)
+        self.a = None if fused_epilogues else Relation("bf16", (T, D), [tb, db], device=dev)
         self.h = Relation("bf16", (T, D), [tb, db], device=dev)
         self.ms2 = Relation("f32", (T,), [tb], device=dev)
         self.n2 = Relation("bf16", (T, D), [tb, db], device=dev)
         self.y = Relation("bf16", (T, D), [tb, db], device=dev)
-        self.ffn = SwigluFFN(self.n2, W["w_gate"], W["w_up"], W["w_down"], k_blocks=db, out=None)
+        self.fused_epilogues = fused_epilogues
+        if fused_epilogues:
+            # residual joins in the O-projection and down-projection epilogues
+            self.ffn = SwigluFFN(self.n2, W["w_gate"], W["w_up"], W["w_down"], k_blocks=db, out=self.y, fused=True,
+                                 residual=self.h)
+        else:
+            self.ffn = SwigluFFN(self.n2, W["w_gate"], W["w_up"], W["w_down"], k_blocks=db, out=None, fused=False)
         self.ffn_out = self.ffn.Y
 
     def rmsnorm(self, x, ms, g, out, c, tag):
@@ -241,11 +270,16 @@ class LlamaBlock:
                                     rope_pos="s"))
         self.attn.run(rec)
         c("exchange.attn_out", lambda: exchange(self.o_tok, None, out=self.o_ex))
-        c("o_proj", lambda: joinagg("te,ed->td", [self.o_ex, self.wo], "sum", "product", out=self.a))
-        c("residual1", lambda: joinagg("td,td->td", [self.x, self.a], "none", "add", out=self.h))
+        if self.fused_epilogues:
+            c("o_proj", lambda: joinagg("te,ed->td", [self.o_ex, self.wo], "sum", "product", out=self.h,
+                                        epi_map="add", epi_in=self.x))
+        else:
+            c("o_proj", lambda: joinagg("te,ed->td", [self.o_ex, self.wo], "sum", "product", out=self.a))
+            c("residual1", lambda: joinagg("td,td->td", [self.x, self.a], "none", "add", out=self.h))
         self.rmsnorm(self.h, self.ms2, self.g2, self.n2, c, "norm2")
         self.ffn.run(self.n2, rec)
-        c("residual2", lambda: joinagg("td,td->td", [self.h, self.ffn_out], "none", "add", out=self.y))
+        if not self.fused_epilogues:
+            c("residual2", lambda: joinagg("td,td->td", [self.h, self.ffn_out], "none", "add", out=self.y))
         return self.y
 
     def call_bytes(self) -> dict:
@@ -259,13 +293,16 @@ class LlamaBlock:
         S = self.b * self.H * kept * sb * sb * 4
         P = S // 2
         ml = self.b * self.H * self.s * 4
+        fe = self.fused_epilogues
         return {"norm1.sumsq": x + T * 4, "norm1.apply": 2 * x + T * 4 + D * 2, "qkv": 4 * x + 3 * D * D * 2,
                 "rope.q": 2 * x, "rope.k": 2 * x, "attn.scores": 2 * x + S, "attn.stats": S + 2 * ml,
                 "attn.normalise": S + 2 * ml + P, "attn.values": P + 2 * x, "attn.fused": 4 * x,
                 "exchange.attn_out": 2 * x,
-                "o_proj": 2 * x + D * D * 2, "residual1": 3 * x, "norm2.sumsq": x + T * 4,
-                "norm2.apply": 2 * x + T * 4 + D * 2, "ffn.gate_up": x + 2 * D * F * 2 + 2 * T * F * 2,
-                "ffn.silu_mul": 3 * T * F * 2, "ffn.down": T * F * 2 + F * D * 2 + x, "residual2": 3 * x}
+                "o_proj": (3 if fe else 2) * x + D * D * 2, "residual1": 3 * x, "norm2.sumsq": x + T * 4,
+                "norm2.apply": 2 * x + T * 4 + D * 2,
+                "ffn.gate_up": x + 2 * D * F * 2 + (1 if fe else 2) * T * F * 2,
+                "ffn.silu_mul": 3 * T * F * 2, "ffn.down": T * F * 2 + F * D * 2 + (2 if fe else 1) * x,
+                "residual2": 3 * x}
 
     def call_flops(self) -> dict:
         """Algorithmic FLOPs of each contraction call."""

@@ -151,11 +151,15 @@ def output_layout(spec: str, inputs):
 def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Relation | None = None,
             out_dtype: str | None = None, scale: float = 1.0, eps: float = 0.0, pred: str | None = None,
             parts: dict | None = None, rope_table: torch.Tensor | None = None, rope_pos: str | None = None,
-            out2: Relation | None = None, stream=None) -> Relation:
+            out2: Relation | None = None, epi_map: str | None = None, epi_in: Relation | None = None,
+            epi_pair: str | None = None, stream=None) -> Relation:
     """Run one join-agg ("Every Kernel Is a Join", Definition 3.7) with
     libea.so.  ``pred="ts"`` keeps joined tuples with t <= s.  With
     ``agg="max_sumexp"`` the output receives the MAX and ``out2`` the SUM
-    of exp(value - max)."""
+    of exp(value - max).  A contraction may fuse an elementwise join into
+    its epilogue: ``epi_map="add", epi_in=R`` stores value + R;
+    ``epi_map="silu_mul", epi_pair="c"`` plans letter c (extent 2, second
+    input only) as the innermost output letter and stores SiLU(c=0) * (c=1)."""
     if out is None:
         dims, bounds = output_layout(spec, inputs)
         out = Relation(out_dtype or inputs[0].dtype, dims, bounds, device=inputs[0].storage.device)
@@ -173,6 +177,12 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
         o.rope_pos = rope_pos.encode()
     if out2 is not None:
         o.out2 = out2.handle.value
+    if epi_map is not None:
+        o.epi_map = MAPS[epi_map]
+        if epi_in is not None:
+            o.epi_in = epi_in.handle.value
+        if epi_pair:
+            o.epi_pair = epi_pair.encode()
     h = ctypes.c_void_p(out.handle.value)
     check_status(lib().ea_joinagg_run(spec.encode(), handles, len(inputs), ip, n_parts, AGGS[agg], MAPS[map],
                                       ctypes.byref(o), ctypes.c_void_p(_stream_ptr(stream)), ctypes.byref(h)))

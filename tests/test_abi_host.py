@@ -29,7 +29,7 @@ def test_exports_every_declared_symbol(L):
     assert {"ea_relation_create", "ea_joinagg_run", "ea_exchange"} <= names
     for n in sorted(names):
         assert hasattr(L, n), n
-    assert L.ea_abi_version() == 1
+    assert L.ea_abi_version() == 2
 
 
 def plan(L, spec, shapes, parts, pred=None):
@@ -244,3 +244,36 @@ def test_attention_errors_without_gpu(L):
     assert run(b"bshd,bthd,bthd->bshd", opts=both) == 4    # stats must be f32
     for h in (q, k, v, k3, v3, kf, kb, vb, kh, vh, q96, k96, m, mb):
         L.ea_relation_destroy(h)
+
+
+def test_epilogue_join_errors_without_gpu(L):
+    """The epilogue options of a contraction are validated before any GPU
+    work: ADD needs epi_in of the output's shape and tiling; SILU_MUL needs
+    a pair letter of the second input only, extent 2, one block."""
+    BF = 1
+    _, x = _fake_rel(L, BF, (256, 128), [2, 1], 1 << 24)
+    _, w = _fake_rel(L, BF, (128, 64, 2), [1, 1, 1], 1 << 25)
+    _, h = _fake_rel(L, BF, (256, 64), [2, 1], 1 << 26)
+    _, wrong = _fake_rel(L, BF, (256, 64), [4, 1], 1 << 27)
+    hs = (ctypes.c_void_p * 2)(x.value, w.value)
+    out = ctypes.c_void_p(h.value)
+    o = _abi.Opts()
+    o.epi_map = _abi.MAPS["silu_mul"]
+    o.epi_pair = b"z"  # not a letter of the spec
+    assert L.ea_joinagg_run(b"td,dfc->tf", hs, 2, None, 0, 1, 0, ctypes.byref(o), None, ctypes.byref(out)) == 1
+    o.epi_pair = b"d"  # the contracted letter: in both inputs
+    assert L.ea_joinagg_run(b"td,dfc->tf", hs, 2, None, 0, 1, 0, ctypes.byref(o), None, ctypes.byref(out)) == 1
+    o2 = _abi.Opts()
+    o2.epi_map = _abi.MAPS["add"]
+    assert L.ea_joinagg_run(b"td,dfc->tfc", hs, 2, None, 0, 1, 0, ctypes.byref(o2), None,
+                            ctypes.byref(ctypes.c_void_p())) == 7  # ADD without epi_in
+    _, h3 = _fake_rel(L, BF, (256, 64, 2), [2, 1, 1], 1 << 28)
+    _, r3 = _fake_rel(L, BF, (256, 64, 2), [4, 1, 1], 1 << 29)
+    o2.epi_in = r3.value
+    out3 = ctypes.c_void_p(h3.value)
+    assert L.ea_joinagg_run(b"td,dfc->tfc", hs, 2, None, 0, 1, 0, ctypes.byref(o2), None, ctypes.byref(out3)) == 3
+    o3 = _abi.Opts()
+    o3.epi_map = _abi.MAPS["exp_sub"]
+    assert L.ea_joinagg_run(b"td,dfc->tfc", hs, 2, None, 0, 1, 0, ctypes.byref(o3), None, ctypes.byref(out3)) == 8
+    for r in (x, w, h, wrong, h3, r3):
+        L.ea_relation_destroy(r)

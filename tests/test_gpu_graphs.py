@@ -48,16 +48,18 @@ def test_attention_chain_causal_small():
     assert rel_frob(dense64(ch.O), want["O"]) <= BF16_TOL
 
 
-def test_swiglu_ffn_small():
+@pytest.mark.parametrize("fused", [True, False])
+def test_swiglu_ffn_small(fused):
     from tensor_relational_einsum_gb300.graphs import SwigluFFN
     T, D, F = 256, 512, 768
     x = synth.make("bf16", (T, D), "normal", 31, 0, 1)
     wg, wu = (synth.make("bf16", (D, F), "normal", sd, 0, 0.02) for sd in (32, 33))
     wd = synth.make("bf16", (F, D), "normal", 34, 0, 0.02)
-    ffn = SwigluFFN(rel(x, [1, 4]), to_device(wg), to_device(wu), to_device(wd), k_blocks=4)
+    ffn = SwigluFFN(rel(x, [1, 4]), to_device(wg), to_device(wu), to_device(wd), k_blocks=4, fused=fused)
     ffn.run()
     want = chains.swiglu_ffn(x.to_f64(), wg.to_f64(), wu.to_f64(), wd.to_f64())
-    for k in ("G", "U", "H", "Y"):
+    # fused: G and U are never written (SiLU * up runs in the contraction's epilogue)
+    for k in (("H", "Y") if fused else ("G", "U", "H", "Y")):
         assert rel_frob(dense64(getattr(ffn, k)), want[k]) <= BF16_TOL, k
 
 
@@ -71,12 +73,14 @@ def _block_weights(D, F, seed0):
     return W
 
 
-def test_llama_block_small():
+@pytest.mark.parametrize("fused", [True, False])
+def test_llama_block_small(fused):
     from tensor_relational_einsum_gb300.graphs import LlamaBlock
     b, s, D, H, F = 2, 256, 256, 2, 512
     W = _block_weights(D, F, 40)
     x = synth.make("bf16", (b * s, D), "normal", 50, 0, 1)
-    blk = LlamaBlock(b, s, D, H, F, {k: to_device(v) for k, v in W.items()})
+    blk = LlamaBlock(b, s, D, H, F, {k: to_device(v) for k, v in W.items()}, fused_attention=fused,
+                     fused_epilogues=fused)
     blk.x.load(to_device(x))
     blk.run()
     Wd = {k: v.to_f64() for k, v in W.items()}

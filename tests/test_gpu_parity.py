@@ -155,6 +155,59 @@ def test_tc_clusters_with_padding_tiles(spec, bshape):
     assert np.array_equal(got, want)
 
 
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_tc_epilogue_add(out_dtype):
+    # C = A B + R with the residual join fused: ragged M, K in blocks, ragged N
+    A = synth.make("bf16", (320, 200), "normal", 61, 0, 1)
+    B = synth.make("bf16", (200, 520), "normal", 62, 0, 1)
+    R = synth.make(out_dtype, (320, 520), "normal", 63, 0, 1)
+    C = joinagg("ij,jk->ik", [rel(A, [1, [0, 64, 136, 200]]), rel(B, [[0, 64, 136, 200], 1])], out_dtype=out_dtype,
+                epi_map="add", epi_in=rel(R, [1, 1]))
+    assert last()["kernel"] == "contract_tc"
+    P = oracle.joinagg("ij,jk->ik", [A.to_f64(), B.to_f64()])
+    want = oracle.joinagg("ik,ik->ik", [P, R.to_f64()], "add", "none")
+    assert rel_frob(dense64(C), want) <= (1e-5 if out_dtype == "f32" else 5e-3)
+
+
+def test_tc_epilogue_add_clustered_integer_exact():
+    # 16 groups (cluster launch, padding tiles): C = A B + R exactly in integer mode
+    A = synth.make("bf16", (16, 300, 256), "int", 64, -2, 2)
+    B = synth.make("bf16", (16, 256, 1096), "int", 65, -2, 2)
+    R = synth.make("f32", (16, 300, 1096), "int", 66, -100, 100)
+    C = joinagg("bij,bjk->bik", [rel(A, [16, 1, 1]), rel(B, [16, 1, 1])], out_dtype="f32", epi_map="add",
+                epi_in=rel(R, [16, 1, 1]))
+    P = oracle.joinagg("bij,bjk->bik", [A.to_f64(), B.to_f64()])
+    want = oracle.joinagg("bik,bik->bik", [P, R.to_f64()], "add", "none")
+    assert np.array_equal(dense64(C), want)
+
+
+def _swiglu_pair_case(T, D, F, xp, wp, hp, rows=None):
+    x = synth.make("bf16", (T, D), "normal", 67, 0, 1)
+    w = synth.make("bf16", (D, F, 2), "normal", 68, 0, 0.05)
+    H = joinagg("td,dfc->tf", [rel(x, xp), rel(w, wp)], epi_map="silu_mul", epi_pair="c")
+    assert last()["kernel"] == "contract_tc"
+    xs = x.to_f64() if rows is None else x.to_f64()[rows]
+    wf = w.to_f64()
+    G = oracle.joinagg("td,fd->tf", [xs, np.ascontiguousarray(wf[:, :, 0].T)])
+    U = oracle.joinagg("td,fd->tf", [xs, np.ascontiguousarray(wf[:, :, 1].T)])
+    want = oracle.joinagg("tf,tf->tf", [G, U], "silu_mul", "none")
+    got = dense64(H) if rows is None else dense64(H)[rows]
+    return got, want
+
+
+def test_tc_epilogue_silu_pairs():
+    # H = SiLU(x Wg) * (x Wu) with gate and up interleaved along c: ragged T, F in 3 blocks
+    got, want = _swiglu_pair_case(300, 256, 600, [1, 2], [2, 3, 1], None)
+    assert rel_frob(got, want) <= BF16_TOL
+
+
+def test_tc_epilogue_silu_pairs_clustered_sampled_rows():
+    # 4096 tokens x 1536 FFN columns: a clustered launch; 64 seeded rows against the oracle
+    rows = [int(r) for r in synth.subset_rows(404, 4096, 64)]
+    got, want = _swiglu_pair_case(4096, 512, 1536, [2, 2], [2, 4, 1], rows)
+    assert rel_frob(got, want) <= BF16_TOL
+
+
 def test_tc_unaligned_falls_back_to_simt():
     got, want, _ = _bf16_case("ij,jk->ik", [(70, 45), (45, 33)], [[2, 3], [3, 1]], "f32", expect="contract_simt")
     assert rel_frob(got, want) <= 1e-5
