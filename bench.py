@@ -425,9 +425,9 @@ def run_ours(args, world, rank, local, dist):
             "peak_source": f"{peak_src} bf16 sustained (kernel timed inside the block step)",
             "flops_per_launch": cf["ffn.gate_up"], "ms_per_launch": round(gu_ms, 4),
             "traffic": traffic_from_profiles()}
-    dense = ("qkv", "o_proj", "ffn.gate_up", "ffn.down")
-    tot_f = sum(cf[n] * len(sm[n][2]) for n in dense)
-    tot_t = sum(sum(sm[n][2]) for n in dense)
+    dense = ("qkv", "qkv.v", "o_proj", "ffn.gate_up", "ffn.down")
+    tot_f = sum(cf[n] * len(sm[n][2]) for n in dense if n in sm)
+    tot_t = sum(sum(sm[n][2]) for n in dense if n in sm)
     roof["all_projection_ffn_launches_TFLOP/s"] = round(tot_f / (tot_t * 1e-3) / 1e12, 1)
     per_call = {}
     for name, (kind, n, ts) in sm.items():

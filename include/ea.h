@@ -126,9 +126,15 @@ typedef struct {
  *              a contraction stores -inf in them, an elementwise join 0.
  *              A contraction whose predicate names a contracted letter
  *              relies on the operand holding 0 in removed cells.
- *   rope_pos   ROPE: the position letter.
+ *   rope_pos   ROPE: the position letter.  The position of a cell is the
+ *              value of that letter modulo rope_npos (sequences of rope_npos
+ *              positions packed end to end); the elementwise join requires
+ *              values below rope_npos.
  *   rope_table ROPE: device pointer, fp32 [rope_npos][d/2][2] = (cos, sin)
  *              of angle pos * theta^(-2i/d).  Not owned.
+ *   rope_dim   ROPE: d, the period of the pairs along the last letter (the
+ *              head dimension when that letter merges heads and head dims);
+ *              0 = the last letter's extent.
  *   out2       EA_AGG_MAX_SUMEXP: the relation receiving the SUM of exp;
  *              same extents and tiling as the output, created by the
  *              caller.  Ignored otherwise.
@@ -141,6 +147,11 @@ typedef struct {
  *                EA_MAP_ADD       out = v + epi_in at the same output cell;
  *                                 epi_in has the output's extents, tiling
  *                                 and dtype (the residual join "o,o->o").
+ *                EA_MAP_ROPE      the rotation of the ROPE map applied to
+ *                                 the output's interleaved column pairs
+ *                                 (rope_pos: the output's row letter;
+ *                                 pairs along its last letter, period
+ *                                 rope_dim).
  *                EA_MAP_SILU_MUL  epi_pair names a letter of the second
  *                                 input only, extent 2, one block, absent
  *                                 from the output term.  The contraction
@@ -165,7 +176,7 @@ typedef struct {
     ea_relation out2;
     ea_relation epi_in;
     int32_t epi_map;
-    int32_t reserved0;
+    int32_t rope_dim;
     int64_t reserved[1];
 } ea_opts;
 

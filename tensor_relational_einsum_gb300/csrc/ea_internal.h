@@ -126,6 +126,7 @@ struct TcGroup {
     int64_t m_lo, n_lo;                // predicate coordinates
     int64_t e_base, e_sm, e_sb;        // epilogue ADD: element offset of the block in epi_in, row and
                                        // batch strides (the output's: same extents and tiling)
+    int64_t r_lo, c_lo;                // epilogue ROPE: global position of row 0, global column 0
 };
 
 struct TcTuple {
@@ -218,8 +219,12 @@ struct TcParams {
     int32_t bn;                        // 128 or 256
     int32_t cluster;                   // CTAs per cluster sharing each B tile (1 or 2): tiles
                                        // 2 p and 2 p + 1 have the same group, batch and n0
-    int32_t epi;                       // epilogue join: 0 none, 1 ADD epi_in, 2 SiLU(g) * u of column pairs
+    int32_t epi;                       // epilogue join: 0 none, 1 ADD epi_in, 2 SiLU(g) * u of column pairs,
+                                       // 3 ROPE rotation of column pairs
     const char *epi_in;                // epi 1: the joined relation's arena (output dtype)
+    const float *rope_table;           // epi 3: [rope_npos][rope_half][2] = (cos, sin)
+    int64_t rope_npos;
+    int32_t rope_half;                 // pairs per period along the columns
     int *err;
 };
 cudaError_t launch_contract_tc(const TcParams &p, int num_sms, cudaStream_t st);

@@ -199,6 +199,7 @@ struct JoinCtx {
     ea_relation_s *out2;
     int epi_map;                 // epilogue join of a contraction: 0, EA_MAP_ADD or EA_MAP_SILU_MUL
     const ea_relation_s *epi_in; // EA_MAP_ADD: the joined relation (output's extents and tiling)
+    int rope_dim;                // ROPE: pair period along the last letter (0 = its extent)
     char epi_pair;               // EA_MAP_SILU_MUL: the paired letter (innermost in the planned output)
     ea_relation_s *user_out;     // the output relation (out is its pre-epilogue view when paired)
 };
@@ -674,7 +675,7 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
     if (mode < 0) return EA_ERR_UNSUPPORTED;
     const size_t es = 2, esc = elem_size(j.out->dtype);
     struct GroupGeom {
-        int64_t c_base, M, N, nb, c_sm, c_sb, m_lo, n_lo;
+        int64_t c_base, M, N, nb, c_sm, c_sb, m_lo, n_lo, r_lo, e_lo;
         int64_t t0, t1;
     };
     std::vector<GroupGeom> gg;
@@ -734,7 +735,17 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
             int64_t crow = c_sm ? c_sm : N;
             int64_t cb = A.nb > 1 ? tg.bt.str[2] : crow * M;
             if (!al16(tg.c.base, esc) || !al16(crow, esc) || !al16(cb, esc)) return EA_ERR_UNSUPPORTED;
+            int64_t r_lo = 0, e_lo = 0;
+            if (j.epi_map == EA_MAP_ROPE) {
+                // rows: the position letter; columns: the output's last letter
+                const int lr = j.rope_pos - 'a', le = j.sp.out.back() - 'a';
+                if (swap || (tg.m.single != lr && M > 1) || (tg.n.single != le && N > 1)) return EA_ERR_UNSUPPORTED;
+                r_lo = tg.c.lo[lr];
+                e_lo = tg.c.lo[le];
+            }
             if (t == j.wl.grp_ptr[g]) {
+                G.r_lo = r_lo;
+                G.e_lo = e_lo;
                 G.c_base = tg.c.base;
                 G.M = M;
                 G.N = N;
@@ -814,6 +825,8 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
         TG.e_base = G.c_base / h;
         TG.e_sm = G.c_sm / h;
         TG.e_sb = G.c_sb / h;
+        TG.r_lo = G.r_lo;
+        TG.c_lo = G.e_lo;
         CUtensorMap m;
         const void *cptr = j.out->arena + (G.c_base / h) * esc;
         ea_status s = encode_map(c, &m, j.out->dtype, cptr, G.N / h, G.M, G.nb, (G.c_sm / h) * esc,
@@ -860,8 +873,11 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
     q.pred_mode = mode;
     q.bn = bn;
     q.cluster = cl;
-    q.epi = j.epi_map == EA_MAP_ADD ? 1 : j.epi_map == EA_MAP_SILU_MUL ? 2 : 0;
+    q.epi = j.epi_map == EA_MAP_ADD ? 1 : j.epi_map == EA_MAP_SILU_MUL ? 2 : j.epi_map == EA_MAP_ROPE ? 3 : 0;
     q.epi_in = j.epi_in ? j.epi_in->arena : nullptr;
+    q.rope_table = j.rope_table;
+    q.rope_npos = j.rope_npos;
+    q.rope_half = (int32_t)((j.rope_dim ? j.rope_dim : j.lt.t[j.sp.out.back() - 'a'].extent) / 2);
     q.err = c->err;
     return EA_OK;
 }
@@ -1038,6 +1054,7 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
     j.rope_table = o.rope_table;
     j.rope_npos = o.rope_npos;
     j.rope_pos = o.rope_pos;
+    j.rope_dim = o.rope_dim;
     j.out2 = agg == EA_AGG_MAX_SUMEXP ? o.out2 : nullptr;
     if (agg == EA_AGG_MAX_SUMEXP && !j.out2) return set_error(EA_ERR_ARG, "MAX_SUMEXP needs opts->out2");
     // Letter tilings: from the inputs, which must agree; explicit parts must match.
@@ -1074,6 +1091,8 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
         return set_error(EA_ERR_SPEC, "predicate letters must be letters of the spec");
     if (map == EA_MAP_ROPE && (j.rope_pos < 'a' || j.rope_pos > 'z' || j.lt.t[j.rope_pos - 'a'].extent < 0))
         return set_error(EA_ERR_ARG, "ROPE needs rope_pos, a letter of the spec");
+    if (map == EA_MAP_ROPE && j.rope_dim && j.rope_dim != j.lt.t[j.sp.out.back() - 'a'].extent)
+        return set_error(EA_ERR_UNSUPPORTED, "the elementwise ROPE join takes pairs over the whole last letter");
     // Output relation.
     int odt = o.out_dtype == 0 ? inputs[0]->dtype : o.out_dtype - 1;
     if (odt != EA_F32 && odt != EA_BF16) return set_error(EA_ERR_DTYPE, "unknown out_dtype %d", o.out_dtype);
@@ -1119,6 +1138,16 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
                 if (!same_tiling(r, d, j.lt.t[j.sp.out[d] - 'a']))
                     return set_error(EA_ERR_PARTITION, "epi_in is tiled differently from the output letters");
             }
+        } else if (o.epi_map == EA_MAP_ROPE) {
+            const char last = j.sp.out.back();
+            const int64_t ext = j.lt.t[last - 'a'].extent;
+            const int64_t period = o.rope_dim ? o.rope_dim : ext;
+            if (!o.rope_table || o.rope_npos <= 0 || j.rope_pos < 'a' || j.rope_pos > 'z' ||
+                j.sp.out.find(j.rope_pos) == std::string::npos || j.rope_pos == last)
+                return set_error(EA_ERR_ARG, "epilogue ROPE needs rope_table, rope_npos and rope_pos, an output letter "
+                                             "other than the last");
+            if (period <= 0 || period % 2 || ext % period)
+                return set_error(EA_ERR_ARG, "rope_dim must be even and divide the last letter's extent");
         } else if (o.epi_map == EA_MAP_SILU_MUL) {
             const char pc = o.epi_pair;
             if (pc < 'a' || pc > 'z') return set_error(EA_ERR_ARG, "epilogue SILU_MUL needs epi_pair, a letter");
@@ -1219,6 +1248,7 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
     if (j.out2) key.rel(j.out2);
     key.v(j.epi_map);
     key.v(j.epi_pair);
+    key.v(j.rope_dim);
     if (j.epi_in) key.rel(j.epi_in);
     cudaStream_t st = (cudaStream_t)stream;
     DevPlan *p = nullptr;

@@ -294,6 +294,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                         v[j] = x;
                     }
                 }
+                if (p.epi == 3 && T.m0 + ep < G.m_ext) {
+                    // epilogue join ROPE: rotate the interleaved column pairs of this row
+                    // by the angles of its position (rows = positions, packed sequences)
+                    const int64_t pos = (G.r_lo + T.m0 + ep) % p.rope_npos;
+                    const float2 *tab = reinterpret_cast<const float2 *>(p.rope_table) + pos * p.rope_half;
+                    int ip = (int)(((G.c_lo + T.n0 + c0) >> 1) % p.rope_half);
+#pragma unroll
+                    for (int q = 0; q < 32; q++) {
+                        if (2 * q < CW) {
+                            const float2 cs = __ldg(tab + ip);
+                            const float x0 = v[2 * q], x1 = v[2 * q + 1];
+                            v[2 * q] = x0 * cs.x - x1 * cs.y;
+                            v[2 * q + 1] = x0 * cs.y + x1 * cs.x;
+                            if (++ip == p.rope_half) ip = 0;
+                        }
+                    }
+                }
                 if (p.epi == 1 && T.m0 + ep < G.m_ext) {
                     // epilogue join ADD: the joined relation's cells of this row segment
                     const int64_t e0 = G.e_base + (int64_t)T.batch * G.e_sb + (int64_t)(T.m0 + ep) * G.e_sm + T.n0 + c0;

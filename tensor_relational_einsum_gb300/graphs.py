@@ -14,7 +14,8 @@ All arithmetic runs in libea.so.
                       tcgen05 kernel.
 * ``SwigluFFN``       gate/up contractions (SUM over model-dim blocks),
                       SiLU(gate) * up elementwise join, down contraction.
-* ``LlamaBlock``      pre-norm block: RMSNorm, fused QKV contraction, RoPE,
+* ``LlamaBlock``      pre-norm block: RMSNorm, Q,K contraction with RoPE in its
+                      epilogue and V contraction (or fused QKV then RoPE),
                       causal attention (fused, or the chain), exchange of the attention
                       output into the O-projection's tiling, O projection
                       (+ residual in its epilogue), RMSNorm, SwiGLU FFN
@@ -217,8 +218,13 @@ class LlamaBlock:
         self.x = Relation("bf16", (T, D), [tb, db], device=dev)
         self.g1 = Relation.from_dense(W["g1"].contiguous(), [db])
         self.g2 = Relation.from_dense(W["g2"].contiguous(), [db])
-        wqkv = torch.stack([W["wq"], W["wk"], W["wv"]], dim=1).contiguous()     # [D, 3, D]
-        self.wqkv = Relation.from_dense(wqkv, [db, 3, 1])
+        if fused_epilogues:
+            # Q and K in one contraction with RoPE in its epilogue, V in another
+            self.wqk = Relation.from_dense(torch.stack([W["wq"], W["wk"]], dim=1).contiguous(), [db, 2, 1])
+            self.wv = Relation.from_dense(W["wv"].contiguous(), [db, 1])
+        else:
+            wqkv = torch.stack([W["wq"], W["wk"], W["wv"]], dim=1).contiguous()     # [D, 3, D]
+            self.wqkv = Relation.from_dense(wqkv, [db, 3, 1])
         self.wo = Relation.from_dense(W["wo"].contiguous(), [db, db])
         self.ms1 = Relation("f32", (T,), [tb], device=dev)
         self.n1 = Relation("bf16", (T, D), [tb, db], device=dev)
@@ -228,9 +234,15 @@ class LlamaBlock:
         self.q = view(self.qkv, 0, hd, attn_parts)
         self.k = view(self.qkv, T * D, hd, attn_parts)
         self.v = view(self.qkv, 2 * T * D, hd, attn_parts)
-        self.qr = Relation("bf16", hd, attn_parts, device=dev)
-        self.kr = Relation("bf16", hd, attn_parts, device=dev)
+        self.qk_out = view(self.qkv, 0, (2, T, D), [2, tb, 1])
+        self.v_out = view(self.qkv, 2 * T * D, (T, D), [tb, 1])
+        if fused_epilogues:
+            self.qr, self.kr = self.q, self.k      # rotated in place by the epilogue
+        else:
+            self.qr = Relation("bf16", hd, attn_parts, device=dev)
+            self.kr = Relation("bf16", hd, attn_parts, device=dev)
         self.table = rope_table(s, self.dh, theta, device=dev)
+        self.fused_epilogues = fused_epilogues
         self.fused_attention = fused_attention
         if fused_attention:
             self.attn = FusedAttention(self.qr, self.kr, self.v, "bshd,bthd,bthd->bshd", scale=1.0 / math.sqrt(self.dh),
@@ -247,7 +259,6 @@ class LlamaBlock:
         self.ms2 = Relation("f32", (T,), [tb], device=dev)
         self.n2 = Relation("bf16", (T, D), [tb, db], device=dev)
         self.y = Relation("bf16", (T, D), [tb, db], device=dev)
-        self.fused_epilogues = fused_epilogues
         if fused_epilogues:
             # residual joins in the O-projection and down-projection epilogues
             self.ffn = SwigluFFN(self.n2, W["w_gate"], W["w_up"], W["w_down"], k_blocks=db, out=self.y, fused=True,
@@ -263,11 +274,16 @@ class LlamaBlock:
     def run(self, rec: Recorder | None = None):
         c = rec.call if rec is not None else _direct
         self.rmsnorm(self.x, self.ms1, self.g1, self.n1, c, "norm1")
-        c("qkv", lambda: joinagg("td,dce->cte", [self.n1, self.wqkv], "sum", "product", out=self.qkv))
-        c("rope.q", lambda: joinagg("bshd->bshd", [self.q], "none", "rope", out=self.qr, rope_table=self.table,
-                                    rope_pos="s"))
-        c("rope.k", lambda: joinagg("bshd->bshd", [self.k], "none", "rope", out=self.kr, rope_table=self.table,
-                                    rope_pos="s"))
+        if self.fused_epilogues:
+            c("qkv", lambda: joinagg("td,dce->cte", [self.n1, self.wqk], "sum", "product", out=self.qk_out,
+                                     epi_map="rope", rope_table=self.table, rope_pos="t", rope_dim=self.dh))
+            c("qkv.v", lambda: joinagg("td,de->te", [self.n1, self.wv], "sum", "product", out=self.v_out))
+        else:
+            c("qkv", lambda: joinagg("td,dce->cte", [self.n1, self.wqkv], "sum", "product", out=self.qkv))
+            c("rope.q", lambda: joinagg("bshd->bshd", [self.q], "none", "rope", out=self.qr, rope_table=self.table,
+                                        rope_pos="s"))
+            c("rope.k", lambda: joinagg("bshd->bshd", [self.k], "none", "rope", out=self.kr, rope_table=self.table,
+                                        rope_pos="s"))
         self.attn.run(rec)
         c("exchange.attn_out", lambda: exchange(self.o_tok, None, out=self.o_ex))
         if self.fused_epilogues:
@@ -294,7 +310,8 @@ class LlamaBlock:
         P = S // 2
         ml = self.b * self.H * self.s * 4
         fe = self.fused_epilogues
-        return {"norm1.sumsq": x + T * 4, "norm1.apply": 2 * x + T * 4 + D * 2, "qkv": 4 * x + 3 * D * D * 2,
+        return {"norm1.sumsq": x + T * 4, "norm1.apply": 2 * x + T * 4 + D * 2,
+                "qkv": (3 * x + 2 * D * D * 2) if fe else (4 * x + 3 * D * D * 2), "qkv.v": 2 * x + D * D * 2,
                 "rope.q": 2 * x, "rope.k": 2 * x, "attn.scores": 2 * x + S, "attn.stats": S + 2 * ml,
                 "attn.normalise": S + 2 * ml + P, "attn.values": P + 2 * x, "attn.fused": 4 * x,
                 "exchange.attn_out": 2 * x,
@@ -308,7 +325,8 @@ class LlamaBlock:
         """Algorithmic FLOPs of each contraction call."""
         T, D, F = self.T, self.D, self.F
         causal_pairs = self.b * self.H * self.s * (self.s + 1) / 2
-        return {"qkv": 2.0 * T * D * 3 * D, "o_proj": 2.0 * T * D * D, "ffn.gate_up": 2.0 * T * D * 2 * F,
+        qkv = 2.0 * T * D * (2 if self.fused_epilogues else 3) * D
+        return {"qkv": qkv, "qkv.v": 2.0 * T * D * D, "o_proj": 2.0 * T * D * D, "ffn.gate_up": 2.0 * T * D * 2 * F,
                 "ffn.down": 2.0 * T * F * D, "attn.scores": 2.0 * causal_pairs * self.dh,
                 "attn.values": 2.0 * causal_pairs * self.dh, "attn.fused": 4.0 * causal_pairs * self.dh}
 

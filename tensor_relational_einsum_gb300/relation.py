@@ -152,12 +152,14 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
             out_dtype: str | None = None, scale: float = 1.0, eps: float = 0.0, pred: str | None = None,
             parts: dict | None = None, rope_table: torch.Tensor | None = None, rope_pos: str | None = None,
             out2: Relation | None = None, epi_map: str | None = None, epi_in: Relation | None = None,
-            epi_pair: str | None = None, stream=None) -> Relation:
+            epi_pair: str | None = None, rope_dim: int = 0, stream=None) -> Relation:
     """Run one join-agg ("Every Kernel Is a Join", Definition 3.7) with
     libea.so.  ``pred="ts"`` keeps joined tuples with t <= s.  With
     ``agg="max_sumexp"`` the output receives the MAX and ``out2`` the SUM
     of exp(value - max).  A contraction may fuse an elementwise join into
     its epilogue: ``epi_map="add", epi_in=R`` stores value + R;
+    ``epi_map="rope"`` rotates the output's column pairs (``rope_table``,
+    ``rope_pos`` the row letter, pairs of period ``rope_dim``);
     ``epi_map="silu_mul", epi_pair="c"`` plans letter c (extent 2, second
     input only) as the innermost output letter and stores SiLU(c=0) * (c=1)."""
     if out is None:
@@ -175,6 +177,7 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
         o.rope_table = rope_table.data_ptr()
         o.rope_npos = rope_table.shape[0]
         o.rope_pos = rope_pos.encode()
+        o.rope_dim = rope_dim
     if out2 is not None:
         o.out2 = out2.handle.value
     if epi_map is not None:

@@ -208,6 +208,25 @@ def test_tc_epilogue_silu_pairs_clustered_sampled_rows():
     assert rel_frob(got, want) <= BF16_TOL
 
 
+def test_tc_epilogue_rope():
+    # Q,K projection with RoPE in the epilogue: 2 sequences x 160 positions
+    # (tokens in one block per sequence), 2 heads of 128, model dim 128 in 2 blocks
+    from tensor_relational_einsum_gb300.graphs import rope_table
+    S, NS, H, DH, DM = 160, 2, 2, 128, 128
+    T, E = NS * S, H * DH
+    x = synth.make("bf16", (T, DM), "normal", 71, 0, 1)
+    w = synth.make("bf16", (DM, 2, E), "normal", 72, 0, 0.1)
+    tab = rope_table(S, DH, 10000.0)
+    out = joinagg("td,dce->cte", [rel(x, [NS, 2]), rel(w, [2, 2, 1])], epi_map="rope", rope_table=tab, rope_pos="t",
+                  rope_dim=DH)
+    assert last()["kernel"] == "contract_tc"
+    got = dense64(out)
+    for c in range(2):
+        P = oracle.joinagg("td,ed->te", [x.to_f64(), np.ascontiguousarray(w.to_f64()[:, c, :].T)])
+        want = chains.rope(P.reshape(NS, S, H, DH), 10000.0).reshape(T, E)
+        assert rel_frob(got[c], want) <= BF16_TOL, c
+
+
 def test_tc_unaligned_falls_back_to_simt():
     got, want, _ = _bf16_case("ij,jk->ik", [(70, 45), (45, 33)], [[2, 3], [3, 1]], "f32", expect="contract_simt")
     assert rel_frob(got, want) <= 1e-5
