@@ -442,32 +442,76 @@ def run_ours(args, world, rank, local, dist):
             ent["GB/s"] = round(gbs, 1)
             ent["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 3)
         per_call[name] = ent
-    # end to end through host buffers: H2D of the tokens, the block, D2H of the output
-    x_host = torch.empty((B * S, D), dtype=torch.bfloat16, pin_memory=True)
-    x_host.copy_(x_dev.cpu())
-    y_host = torch.empty((B * S, D), dtype=torch.bfloat16, pin_memory=True)
-    x_stage = torch.empty_like(x_dev)
-    y_whole = Relation("bf16", (B * S, D), [1, 1], device=device)
-    x_whole = Relation("bf16", (B * S, D), [1, 1], storage=x_stage.reshape(-1))
+    # End to end through host buffers, pipelined as a server runs it: while
+    # step i computes on one stream, a copy stream brings in step i+1's tokens
+    # (pinned host -> device) and returns step i-1's output (device -> host),
+    # with two pinned host buffers and two device stages each way.  Every
+    # step's own copies are inside the timed region.
+    nbuf = 2
+    x_host = [torch.empty((B * S, D), dtype=torch.bfloat16, pin_memory=True) for _ in range(nbuf)]
+    xd = x_dev.cpu()
+    for h in x_host:
+        h.copy_(xd)
+    y_host = [torch.empty((B * S, D), dtype=torch.bfloat16, pin_memory=True) for _ in range(nbuf)]
+    x_stage = [torch.empty_like(x_dev) for _ in range(nbuf)]
+    x_whole = [Relation("bf16", (B * S, D), [1, 1], storage=xs.reshape(-1)) for xs in x_stage]
+    y_whole = [Relation("bf16", (B * S, D), [1, 1], device=device) for _ in range(nbuf)]
+    comp, copy = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    h2d = [torch.cuda.Event() for _ in range(nbuf)]
+    done = [torch.cuda.Event() for _ in range(nbuf)]
+    d2h = [torch.cuda.Event() for _ in range(nbuf)]
 
-    def e2e_step():
-        x_stage.copy_(x_host, non_blocking=True)
-        exchange(x_whole, None, out=blk.x)
-        blk.run()
-        exchange(blk.y, None, out=y_whole)
-        y_host.copy_(y_whole.arena().reshape(B * S, D), non_blocking=True)
+    def e2e_steps(n):
+        with torch.cuda.stream(copy):
+            x_stage[0].copy_(x_host[0], non_blocking=True)
+            h2d[0].record(copy)
+        for i in range(n):
+            b = i % nbuf
+            if i + 1 < n:  # next step's tokens, once step i + 1 - nbuf has read that stage
+                nb_ = (i + 1) % nbuf
+                with torch.cuda.stream(copy):
+                    if i + 1 >= nbuf:
+                        copy.wait_event(done[nb_])
+                    x_stage[nb_].copy_(x_host[nb_], non_blocking=True)
+                    h2d[nb_].record(copy)
+            with torch.cuda.stream(comp):
+                comp.wait_event(h2d[b])
+                if i >= nbuf:
+                    comp.wait_event(d2h[b])  # step i - nbuf's output has left y_whole[b]
+                exchange(x_whole[b], None, out=blk.x)
+                blk.run()
+                exchange(blk.y, None, out=y_whole[b])
+                done[b].record(comp)
+            with torch.cuda.stream(copy):
+                copy.wait_event(done[b])
+                y_host[b].copy_(y_whole[b].arena().reshape(B * S, D), non_blocking=True)
+                d2h[b].record(copy)
 
-    ms_e2e = time_region(e2e_step, max(2, args.steps // 2), 1, dist, device)
-    ms_e2e = max_over_ranks(dist, ms_e2e, device)
-    n_e2e = max(2, args.steps // 2)
+    n_e2e = max(4, args.steps)
+    e2e_steps(2)  # warm-up
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(copy)
+    with torch.cuda.stream(comp):
+        comp.wait_event(es)
+    e2e_steps(n_e2e)
+    with torch.cuda.stream(copy):
+        copy.wait_stream(comp)
+        ee.record(copy)
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms_e2e = max_over_ranks(dist, es.elapsed_time(ee), device)
     e2e = {"value": flops * n_e2e * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
-           "ms_per_step": ms_e2e / n_e2e, "h2d_bytes_per_step": x_host.numel() * 2,
-           "d2h_bytes_per_step": y_host.numel() * 2}
+           "ms_per_step": ms_e2e / n_e2e, "h2d_bytes_per_step": x_host[0].numel() * 2,
+           "d2h_bytes_per_step": y_host[0].numel() * 2,
+           "pipelined": "copies of step i+1 (in) and i-1 (out) overlap step i's compute; 2 buffers each way"}
     check()
     comps = None
     cpu = None
     if rank == 0 and not args.no_components:
-        del blk, x_dev, x_stage, x_whole, y_whole
+        del blk, x_dev, x_stage, x_whole, y_whole, x_host, y_host
         torch.cuda.empty_cache()
         comps = bench_components(peaks, device)
         check()
