@@ -541,12 +541,12 @@ def profile_case(name: str, reps: int):
     from tensor_relational_einsum_gb300.relation import Relation, check, exchange, joinagg
     build()
     dev = torch.device("cuda", 0)
-    if name == "gemm":   # FFN gate+up contraction: x[8192,4096] . W[4096, 2, 11008], SUM over 4 blocks
+    if name == "gemm":   # FFN gate+up contraction with SiLU * up in its epilogue: x[8192,4096] . W[4096, 11008, 2]
         x = Relation.from_dense(synth.make_torch("bf16", (8192, 4096), "normal", 21, 0, 1, device=dev), [1, 4])
-        w = Relation.from_dense(synth.make_torch("bf16", (4096, 2, 11008), "normal", 22, 0, 0.02, device=dev),
-                                [4, 2, 4])
-        y = Relation("bf16", (2, 8192, 11008), [2, 1, 4], device=dev)
-        fn = lambda: joinagg("td,dcf->ctf", [x, w], out=y)  # noqa: E731
+        w = Relation.from_dense(synth.make_torch("bf16", (4096, 11008, 2), "normal", 22, 0, 0.02, device=dev),
+                                [4, 4, 1])
+        y = Relation("bf16", (8192, 11008), [1, 4], device=dev)
+        fn = lambda: joinagg("td,dfc->tf", [x, w], out=y, epi_map="silu_mul", epi_pair="c")  # noqa: E731
     elif name == "attn":  # attention chain b1 h32 s=t=2048 d128, t in 4 blocks
         q, k, v = (synth.make_torch("bf16", (1, 32, 2048, 128), "normal", sd, 0, 1, device=dev) for sd in (1, 2, 3))
         ch = AttentionChain(Relation.from_dense(q, [1, 32, 1, 1]), Relation.from_dense(k, [1, 32, 4, 1]),
