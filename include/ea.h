@@ -162,7 +162,16 @@ typedef struct {
  *                                 "of,of->of" of the two slices).  bf16
  *                                 output only.
  *              0 = no epilogue.  A join-agg that does not run on the
- *              tcgen05 contraction kernel returns EA_ERR_UNSUPPORTED.    */
+ *              tcgen05 contraction kernel returns EA_ERR_UNSUPPORTED.
+ *   row_rms    a contraction's row scale (with or without epi_map): an f32
+ *              relation over one letter, the output's row letter (its
+ *              only letter of input 0 kept in the output, other than
+ *              batch letters of extent 1 per block), tiled as that letter;
+ *              every aggregated cell of row r is multiplied by
+ *              rsqrt(row_rms[r] + eps) before the epilogue join.  This is
+ *              RMSNorm's apply join pushed through the SUM over the
+ *              contracted letter (sum_d x[r,d] s[r] W[d,e] = s[r] sum_d
+ *              x[r,d] W[d,e]); a gain over d belongs in the weight.        */
 typedef struct {
     int32_t out_dtype;
     float scale;
@@ -177,7 +186,7 @@ typedef struct {
     ea_relation epi_in;
     int32_t epi_map;
     int32_t rope_dim;
-    int64_t reserved[1];
+    ea_relation row_rms;
 } ea_opts;
 
 /* ------------------------------------------------------------ basics */

@@ -43,7 +43,7 @@ class Opts(ctypes.Structure):
                 ("pred_lo", ctypes.c_char), ("pred_hi", ctypes.c_char), ("rope_pos", ctypes.c_char),
                 ("epi_pair", ctypes.c_char), ("rope_table", ctypes.c_void_p), ("rope_npos", ctypes.c_int64),
                 ("out2", ctypes.c_void_p), ("epi_in", ctypes.c_void_p), ("epi_map", ctypes.c_int32),
-                ("rope_dim", ctypes.c_int32), ("reserved", ctypes.c_int64 * 1)]
+                ("rope_dim", ctypes.c_int32), ("row_rms", ctypes.c_void_p)]
 
 
 class AttnOpts(ctypes.Structure):

@@ -126,7 +126,7 @@ struct TcGroup {
     int64_t m_lo, n_lo;                // predicate coordinates
     int64_t e_base, e_sm, e_sb;        // epilogue ADD: element offset of the block in epi_in, row and
                                        // batch strides (the output's: same extents and tiling)
-    int64_t r_lo, c_lo;                // epilogue ROPE: global position of row 0, global column 0
+    int64_t r_lo, c_lo;                // global row index of row 0 (ROPE position, row scale), global column 0
 };
 
 struct TcTuple {
@@ -222,6 +222,8 @@ struct TcParams {
     int32_t epi;                       // epilogue join: 0 none, 1 ADD epi_in, 2 SiLU(g) * u of column pairs,
                                        // 3 ROPE rotation of column pairs
     const char *epi_in;                // epi 1: the joined relation's arena (output dtype)
+    const float *row_rms;              // row scale rsqrt(row_rms[global row] + eps), or null
+    float eps;
     const float *rope_table;           // epi 3: [rope_npos][rope_half][2] = (cos, sin)
     int64_t rope_npos;
     int32_t rope_half;                 // pairs per period along the columns

@@ -200,6 +200,8 @@ struct JoinCtx {
     int epi_map;                 // epilogue join of a contraction: 0, EA_MAP_ADD or EA_MAP_SILU_MUL
     const ea_relation_s *epi_in; // EA_MAP_ADD: the joined relation (output's extents and tiling)
     int rope_dim;                // ROPE: pair period along the last letter (0 = its extent)
+    const ea_relation_s *row_rms;  // contraction row scale rsqrt(row_rms[row] + eps), or null
+    char row_letter;             // the output letter of input 0 only (rows of the contraction)
     char epi_pair;               // EA_MAP_SILU_MUL: the paired letter (innermost in the planned output)
     ea_relation_s *user_out;     // the output relation (out is its pre-epilogue view when paired)
 };
@@ -743,6 +745,13 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
                 r_lo = tg.c.lo[lr];
                 e_lo = tg.c.lo[le];
             }
+            if (j.row_rms) {
+                // rows: the row letter, global index = the row_rms element (a rank-1 arena is dense)
+                const int lr = j.row_letter - 'a';
+                if (swap || (tg.m.single != lr && M > 1)) return EA_ERR_UNSUPPORTED;
+                if (j.epi_map == EA_MAP_ROPE && j.rope_pos != j.row_letter) return EA_ERR_UNSUPPORTED;
+                r_lo = tg.c.lo[lr];
+            }
             if (t == j.wl.grp_ptr[g]) {
                 G.r_lo = r_lo;
                 G.e_lo = e_lo;
@@ -875,6 +884,8 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
     q.cluster = cl;
     q.epi = j.epi_map == EA_MAP_ADD ? 1 : j.epi_map == EA_MAP_SILU_MUL ? 2 : j.epi_map == EA_MAP_ROPE ? 3 : 0;
     q.epi_in = j.epi_in ? j.epi_in->arena : nullptr;
+    q.row_rms = j.row_rms ? (const float *)j.row_rms->arena : nullptr;
+    q.eps = j.eps;
     q.rope_table = j.rope_table;
     q.rope_npos = j.rope_npos;
     q.rope_half = (int32_t)((j.rope_dim ? j.rope_dim : j.lt.t[j.sp.out.back() - 'a'].extent) / 2);
@@ -1119,6 +1130,25 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
                 inputs[k]->arena < orel->arena + orel->bytes && orel->arena != inputs[k]->arena)
                 return set_error(EA_ERR_ARG, "output arena partially overlaps input %d", k);
     }
+    // Row scale of a contraction.
+    j.row_rms = o.row_rms;
+    j.row_letter = 0;
+    if (o.row_rms) {
+        if (!(map == EA_MAP_PRODUCT && agg == EA_AGG_SUM && n_inputs == 2))
+            return set_error(EA_ERR_UNSUPPORTED, "row_rms needs a contraction (SUM of PRODUCT, two inputs)");
+        for (char ch : j.sp.out)
+            if (j.sp.term[0].find(ch) != std::string::npos && j.sp.term[1].find(ch) == std::string::npos) {
+                if (j.row_letter) return set_error(EA_ERR_UNSUPPORTED, "row_rms needs exactly one row letter");
+                j.row_letter = ch;
+            }
+        if (!j.row_letter) return set_error(EA_ERR_SPEC, "row_rms: the output has no letter of input 0 only");
+        const ea_relation_s *r = o.row_rms;
+        const Tiling &tr = j.lt.t[j.row_letter - 'a'];
+        if (r->rank != 1 || r->dtype != EA_F32) return set_error(EA_ERR_SHAPE, "row_rms must be a rank-1 f32 relation");
+        if (r->dims[0] != tr.extent) return set_error(EA_ERR_SHAPE, "row_rms extent differs from letter '%c'", j.row_letter);
+        if (r->bounds[0] != tr.b) return set_error(EA_ERR_PARTITION, "row_rms is tiled unlike letter '%c'", j.row_letter);
+        if (j.pred_lo) return set_error(EA_ERR_UNSUPPORTED, "row_rms with a predicate is not supported");
+    }
     // Epilogue join of a contraction.
     j.epi_map = o.epi_map;
     j.epi_in = o.epi_in;
@@ -1249,6 +1279,7 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
     key.v(j.epi_map);
     key.v(j.epi_pair);
     key.v(j.rope_dim);
+    if (j.row_rms) key.rel(j.row_rms);
     if (j.epi_in) key.rel(j.epi_in);
     cudaStream_t st = (cudaStream_t)stream;
     DevPlan *p = nullptr;
@@ -1263,7 +1294,7 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
             else if (kind == kRowReduce) s = build_rowreduce(j, c, st, p);
             else {
                 s = build_tc(j, cv, c, st, p);
-                if (s == EA_ERR_UNSUPPORTED && j.epi_map) {
+                if (s == EA_ERR_UNSUPPORTED && (j.epi_map || j.row_rms)) {
                     s = set_error(EA_ERR_UNSUPPORTED, "an epilogue join needs the tcgen05 contraction path "
                                                       "(bf16 operands that TMA can tile)");
                 } else if (s == EA_ERR_UNSUPPORTED) {

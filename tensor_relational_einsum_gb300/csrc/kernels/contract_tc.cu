@@ -233,6 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
             const int64_t m_g = G.m_lo + T.m0 + ep;
+            // the row's scale: scale, times rsqrt(row_rms + eps) for a fused RMSNorm apply
+            const float sc = (p.row_rms && T.m0 + ep < G.m_ext)
+                                 ? p.scale * rsqrtf(__ldg(p.row_rms + G.r_lo + T.m0 + ep) + p.eps)
+                                 : p.scale;
             // epilogue join SiLU(g) * u over column pairs: 128 planned columns -> 64 stored
             for (int c0 = 0; p.epi == 2 && c0 < BN; c0 += 128) {
                 if (T.n0 + c0 >= G.n_ext || !store) break;
@@ -253,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
 #pragma unroll
                             for (int z = 0; z < 2; z++) {
                                 const int jj = 8 * q + 2 * e + z;  // stored column inside the half
-                                const float g = __uint_as_float(r[2 * jj]) * p.scale;
-                                const float u = __uint_as_float(r[2 * jj + 1]) * p.scale;
+                                const float g = __uint_as_float(r[2 * jj]) * sc;
+                                const float u = __uint_as_float(r[2 * jj + 1]) * sc;
                                 o2[z] = __fdividef(g, 1.0f + __expf(-g)) * u;
                             }
                             __nv_bfloat162 hv = __floats2bfloat162_rn(o2[0], o2[1]);
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
 #pragma unroll
                 for (int j = 0; j < 64; j++) {
                     if (j < CW) {
-                        float x = __uint_as_float(r[j]) * p.scale;
+                        float x = __uint_as_float(r[j]) * sc;
                         if (p.pred_mode) {
                             int64_t n_g = G.n_lo + T.n0 + c0 + j;
                             if ((p.pred_mode == 1 && n_g > m_g) || (p.pred_mode == 2 && m_g > n_g)) x = -INFINITY;

@@ -156,7 +156,8 @@ class SwigluFFN:
 
     def __init__(self, x: Relation, w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
                  k_blocks: int = 4, out: Relation | None = None, fused: bool = True,
-                 residual: Relation | None = None):
+                 residual: Relation | None = None, gain: Relation | None = None,
+                 row_rms: Relation | None = None, eps: float = 0.0):
         T, D = x.dims
         F = w_gate.shape[1]
         tb = x.bounds[0]
@@ -164,8 +165,11 @@ class SwigluFFN:
         self.x = x
         self.fused = fused
         self.residual = residual
+        self.row_rms, self.eps = row_rms, eps
         if fused:
             self.wgu = Relation.from_dense(torch.stack([w_gate, w_up], dim=2).contiguous(), [x.bounds[1], k_blocks, 1])
+            if gain is not None:  # an RMSNorm gain over the contracted letter, folded into the weight once
+                self.wgu = joinagg("dfc,d->dfc", [self.wgu, gain], "none", "product")
             self.G = self.U = None
         else:
             # gate and up share their join: one relation [D, 2, F] (c = 0 gate, 1 up)
@@ -185,7 +189,7 @@ class SwigluFFN:
         c = rec.call if rec is not None else _direct
         if self.fused:
             c("ffn.gate_up", lambda: joinagg("td,dfc->tf", [x, self.wgu], "sum", "product", out=self.H,
-                                             epi_map="silu_mul", epi_pair="c"))
+                                             epi_map="silu_mul", epi_pair="c", row_rms=self.row_rms, eps=self.eps))
         else:
             c("ffn.gate_up", lambda: joinagg("td,dcf->ctf", [x, self.wgu], "sum", "product", out=self.gu))
             c("ffn.silu_mul", lambda: joinagg("tf,tf->tf", [self.G, self.U], "none", "silu_mul", out=self.H))
@@ -219,15 +223,18 @@ class LlamaBlock:
         self.g1 = Relation.from_dense(W["g1"].contiguous(), [db])
         self.g2 = Relation.from_dense(W["g2"].contiguous(), [db])
         if fused_epilogues:
-            # Q and K in one contraction with RoPE in its epilogue, V in another
-            self.wqk = Relation.from_dense(torch.stack([W["wq"], W["wk"]], dim=1).contiguous(), [db, 2, 1])
-            self.wv = Relation.from_dense(W["wv"].contiguous(), [db, 1])
+            # Q and K in one contraction with RoPE in its epilogue, V in another;
+            # RMSNorm's gain folded into the weights, its row scale in the epilogues
+            wqk = Relation.from_dense(torch.stack([W["wq"], W["wk"]], dim=1).contiguous(), [db, 2, 1])
+            self.wqk = joinagg("dce,d->dce", [wqk, self.g1], "none", "product")
+            self.wv = joinagg("de,d->de", [Relation.from_dense(W["wv"].contiguous(), [db, 1]), self.g1], "none",
+                              "product")
         else:
             wqkv = torch.stack([W["wq"], W["wk"], W["wv"]], dim=1).contiguous()     # [D, 3, D]
             self.wqkv = Relation.from_dense(wqkv, [db, 3, 1])
         self.wo = Relation.from_dense(W["wo"].contiguous(), [db, db])
         self.ms1 = Relation("f32", (T,), [tb], device=dev)
-        self.n1 = Relation("bf16", (T, D), [tb, db], device=dev)
+        self.n1 = None if fused_epilogues else Relation("bf16", (T, D), [tb, db], device=dev)
         self.qkv = Relation("bf16", (3, T, D), [3, tb, 1], device=dev)
         hd = (b, s, n_heads, self.dh)
         attn_parts = [b, sb, 1, 1]
@@ -257,12 +264,12 @@ class LlamaBlock:
         self.a = None if fused_epilogues else Relation("bf16", (T, D), [tb, db], device=dev)
         self.h = Relation("bf16", (T, D), [tb, db], device=dev)
         self.ms2 = Relation("f32", (T,), [tb], device=dev)
-        self.n2 = Relation("bf16", (T, D), [tb, db], device=dev)
+        self.n2 = None if fused_epilogues else Relation("bf16", (T, D), [tb, db], device=dev)
         self.y = Relation("bf16", (T, D), [tb, db], device=dev)
         if fused_epilogues:
             # residual joins in the O-projection and down-projection epilogues
-            self.ffn = SwigluFFN(self.n2, W["w_gate"], W["w_up"], W["w_down"], k_blocks=db, out=self.y, fused=True,
-                                 residual=self.h)
+            self.ffn = SwigluFFN(self.h, W["w_gate"], W["w_up"], W["w_down"], k_blocks=db, out=self.y, fused=True,
+                                 residual=self.h, gain=self.g2, row_rms=self.ms2, eps=eps)
         else:
             self.ffn = SwigluFFN(self.n2, W["w_gate"], W["w_up"], W["w_down"], k_blocks=db, out=None, fused=False)
         self.ffn_out = self.ffn.Y
@@ -273,12 +280,15 @@ class LlamaBlock:
 
     def run(self, rec: Recorder | None = None):
         c = rec.call if rec is not None else _direct
-        self.rmsnorm(self.x, self.ms1, self.g1, self.n1, c, "norm1")
         if self.fused_epilogues:
-            c("qkv", lambda: joinagg("td,dce->cte", [self.n1, self.wqk], "sum", "product", out=self.qk_out,
-                                     epi_map="rope", rope_table=self.table, rope_pos="t", rope_dim=self.dh))
-            c("qkv.v", lambda: joinagg("td,de->te", [self.n1, self.wv], "sum", "product", out=self.v_out))
+            c("norm1.sumsq", lambda: joinagg("td->t", [self.x], "sum", "square", out=self.ms1, scale=1.0 / self.D))
+            c("qkv", lambda: joinagg("td,dce->cte", [self.x, self.wqk], "sum", "product", out=self.qk_out,
+                                     epi_map="rope", rope_table=self.table, rope_pos="t", rope_dim=self.dh,
+                                     row_rms=self.ms1, eps=self.eps))
+            c("qkv.v", lambda: joinagg("td,de->te", [self.x, self.wv], "sum", "product", out=self.v_out,
+                                       row_rms=self.ms1, eps=self.eps))
         else:
+            self.rmsnorm(self.x, self.ms1, self.g1, self.n1, c, "norm1")
             c("qkv", lambda: joinagg("td,dce->cte", [self.n1, self.wqkv], "sum", "product", out=self.qkv))
             c("rope.q", lambda: joinagg("bshd->bshd", [self.q], "none", "rope", out=self.qr, rope_table=self.table,
                                         rope_pos="s"))
@@ -292,8 +302,12 @@ class LlamaBlock:
         else:
             c("o_proj", lambda: joinagg("te,ed->td", [self.o_ex, self.wo], "sum", "product", out=self.a))
             c("residual1", lambda: joinagg("td,td->td", [self.x, self.a], "none", "add", out=self.h))
-        self.rmsnorm(self.h, self.ms2, self.g2, self.n2, c, "norm2")
-        self.ffn.run(self.n2, rec)
+        if self.fused_epilogues:
+            c("norm2.sumsq", lambda: joinagg("td->t", [self.h], "sum", "square", out=self.ms2, scale=1.0 / self.D))
+            self.ffn.run(self.h, rec)
+        else:
+            self.rmsnorm(self.h, self.ms2, self.g2, self.n2, c, "norm2")
+            self.ffn.run(self.n2, rec)
         if not self.fused_epilogues:
             c("residual2", lambda: joinagg("td,td->td", [self.h, self.ffn_out], "none", "add", out=self.y))
         return self.y

@@ -152,7 +152,8 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
             out_dtype: str | None = None, scale: float = 1.0, eps: float = 0.0, pred: str | None = None,
             parts: dict | None = None, rope_table: torch.Tensor | None = None, rope_pos: str | None = None,
             out2: Relation | None = None, epi_map: str | None = None, epi_in: Relation | None = None,
-            epi_pair: str | None = None, rope_dim: int = 0, stream=None) -> Relation:
+            epi_pair: str | None = None, rope_dim: int = 0, row_rms: Relation | None = None,
+            stream=None) -> Relation:
     """Run one join-agg ("Every Kernel Is a Join", Definition 3.7) with
     libea.so.  ``pred="ts"`` keeps joined tuples with t <= s.  With
     ``agg="max_sumexp"`` the output receives the MAX and ``out2`` the SUM
@@ -160,6 +161,7 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
     its epilogue: ``epi_map="add", epi_in=R`` stores value + R;
     ``epi_map="rope"`` rotates the output's column pairs (``rope_table``,
     ``rope_pos`` the row letter, pairs of period ``rope_dim``);
+    ``row_rms=ms`` multiplies every row r by rsqrt(ms[r] + eps) first;
     ``epi_map="silu_mul", epi_pair="c"`` plans letter c (extent 2, second
     input only) as the innermost output letter and stores SiLU(c=0) * (c=1)."""
     if out is None:
@@ -180,6 +182,8 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
         o.rope_dim = rope_dim
     if out2 is not None:
         o.out2 = out2.handle.value
+    if row_rms is not None:
+        o.row_rms = row_rms.handle.value
     if epi_map is not None:
         o.epi_map = MAPS[epi_map]
         if epi_in is not None:

@@ -85,7 +85,8 @@ def test_llama_block_small(fused):
     blk.run()
     Wd = {k: v.to_f64() for k, v in W.items()}
     want = chains.llama_block(x.to_f64().reshape(b, s, D), Wd, n_heads=H, eps=1e-6, theta=10000.0)
-    assert rel_frob(dense64(blk.n1), want["n1"]) <= BF16_TOL
+    if not fused:  # fused: RMSNorm's apply runs in the projections' epilogues (n1 is never written)
+        assert rel_frob(dense64(blk.n1), want["n1"]) <= BF16_TOL
     assert rel_frob(dense64(blk.qr), want["q"]) <= BF16_TOL
     assert rel_frob(dense64(blk.attn.O), want["O"]) <= BF16_TOL
     assert rel_frob(dense64(blk.h), want["h"]) <= BF16_TOL
