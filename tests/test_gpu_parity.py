@@ -227,6 +227,34 @@ def test_tc_epilogue_rope():
         assert rel_frob(got[c], want) <= BF16_TOL, c
 
 
+@pytest.mark.parametrize("epi", [None, "silu_mul"])
+def test_tc_row_rms(epi):
+    # RMSNorm's apply pushed through the contraction: rows scaled by rsqrt(ms + eps)
+    # (ms from the oracle, passed as an f32 relation over the row letter)
+    eps = 1e-6
+    x = synth.make("bf16", (300, 256), "normal", 73, 0, 1)
+    xo = x.to_f64()
+    ms = oracle.joinagg("td->t", [xo], "square", "sum", scale=1.0 / 256)
+    ms_rel = rel(synth.Tensor(ms.astype(np.float32), "f32", (300,)), [2])
+    n = oracle.joinagg("td,t,d->td", [xo, ms, np.ones(256)], "rms_apply", "none", eps=eps)
+    if epi is None:
+        w = synth.make("bf16", (256, 384), "normal", 74, 0, 0.1)
+        out = joinagg("td,de->te", [rel(x, [2, 2]), rel(w, [2, 1])], row_rms=ms_rel, eps=eps, out_dtype="f32")
+        want = oracle.joinagg("td,ed->te", [n, np.ascontiguousarray(w.to_f64().T)])
+        tol = 1e-5
+    else:
+        w = synth.make("bf16", (256, 192, 2), "normal", 74, 0, 0.1)
+        out = joinagg("td,dfc->tf", [rel(x, [2, 2]), rel(w, [2, 1, 1])], row_rms=ms_rel, eps=eps,
+                      epi_map="silu_mul", epi_pair="c")
+        wf = w.to_f64()
+        G = oracle.joinagg("td,fd->tf", [n, np.ascontiguousarray(wf[:, :, 0].T)])
+        U = oracle.joinagg("td,fd->tf", [n, np.ascontiguousarray(wf[:, :, 1].T)])
+        want = oracle.joinagg("tf,tf->tf", [G, U], "silu_mul", "none")
+        tol = BF16_TOL
+    assert last()["kernel"] == "contract_tc"
+    assert rel_frob(dense64(out), want) <= tol
+
+
 def test_tc_unaligned_falls_back_to_simt():
     got, want, _ = _bf16_case("ij,jk->ik", [(70, 45), (45, 33)], [[2, 3], [3, 1]], "f32", expect="contract_simt")
     assert rel_frob(got, want) <= 1e-5
