@@ -85,7 +85,17 @@ void free_plan(DevPlan *p) {
     delete p;
 }
 
+// Order the plan's upload before work on `st`.  Once the upload is known to
+// have completed (queried on any later use), no CUDA call is made at all, so
+// a cached plan can be launched inside a CUDA-graph capture.
 ea_status plan_ready_on(DevPlan *p, cudaStream_t st) {
+    if (p->uploaded) return EA_OK;
+    cudaError_t q = cudaEventQuery(p->ready);
+    if (q == cudaSuccess) {
+        p->uploaded = true;
+        return EA_OK;
+    }
+    if (q != cudaErrorNotReady) return cuda_error(q, "cudaEventQuery(plan upload)");
     if (st != p->made_on) {
         cudaError_t e = cudaStreamWaitEvent(st, p->ready, 0);
         if (e != cudaSuccess) return cuda_error(e, "cudaStreamWaitEvent(plan upload)");

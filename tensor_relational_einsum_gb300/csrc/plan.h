@@ -47,6 +47,7 @@ struct DevPlan {
     size_t bytes = 0;
     cudaEvent_t ready = nullptr;
     cudaStream_t made_on = nullptr;
+    bool uploaded = false;  // the upload is known complete: no stream needs to wait for it
     // exchange
     XSeg *segs = nullptr;
     XTile *xtiles = nullptr;

@@ -63,6 +63,26 @@ def _direct(name, fn):
     fn()
 
 
+def capture(fn, warmup: int = 2) -> "torch.cuda.CUDAGraph":
+    """Record ``fn``'s libea launches into one CUDA graph ("Every Kernel Is a
+    Join", Section 6: every plan is compiled to a CUDA graph and executed
+    directly).  ``fn`` runs ``warmup`` times first on a side stream, which
+    builds, uploads and caches every plan, so the capture itself makes no
+    allocation or synchronisation; ``graph.replay()`` then launches the same
+    kernels with the same arguments on the current stream."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        fn()
+    return g
+
+
 def view(parent: Relation, offset_elems: int, dims, parts) -> Relation:
     """A relation over a contiguous piece of ``parent``'s arena (zero-copy)."""
     n = int(np.prod(dims))
