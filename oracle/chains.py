@@ -89,6 +89,22 @@ def flash_attention(Q, K, V, group: int = 1, scale: float = 1.0, causal: bool = 
     return {"O": np.ascontiguousarray(O), "m": m, "l": ell}
 
 
+def matrix_chain(mats, paren, tier: str = "idx"):
+    """The product of a chain of matrices in a fixed parenthesization ("Every
+    Kernel Is a Join", Section 7: the matrix-chain workloads), every multiply
+    the contraction join-agg "ij,jk->ik".
+
+    mats: list of 2-D arrays M1..Mn; paren: nested pairs of 1-based matrix
+    indices, e.g. ((1, 2), 3).  Returns the product (fp64).
+    """
+    def ev(node):
+        if isinstance(node, int):
+            return np.asarray(mats[node - 1], dtype=np.float64)
+        left, right = ev(node[0]), ev(node[1])
+        return joinagg("ij,kj->ik", [left, np.ascontiguousarray(right.T)], "product", "sum", tier=tier)
+    return ev(paren)
+
+
 def swiglu_ffn(x, w_gate, w_up, w_down, tier: str = "idx"):
     """G = x w_gate, U = x w_up (SUM over the model dimension),
     H = SiLU(G) * U (elementwise join), Y = H w_down."""

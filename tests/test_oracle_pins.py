@@ -294,6 +294,21 @@ def test_flash_attention_stats_close_forms():
     np.testing.assert_allclose(out["l"][..., 0], 1.0, rtol=1e-15)
 
 
+def test_matrix_chain_against_library_and_associativity():
+    r = rng(31)
+    dims = [5, 7, 3, 6, 4, 8]
+    mats = [r.standard_normal((dims[i], dims[i + 1])) for i in range(5)]
+    paren = ((1, 2), ((3, 4), 5))  # chain B's shape
+    got = chains.matrix_chain(mats, paren)
+    np.testing.assert_allclose(got, np.linalg.multi_dot(mats), rtol=1e-12, atol=1e-12)
+    other = chains.matrix_chain(mats, ((((1, 2), 3), 4), 5))
+    np.testing.assert_allclose(got, other, rtol=1e-12, atol=1e-12)
+    # a transposed operand (a plausible mistake) changes the result
+    bad = [m.copy() for m in mats]
+    bad[2] = np.ascontiguousarray(mats[2][::-1])
+    assert not np.allclose(chains.matrix_chain(bad, paren), got)
+
+
 def test_silu_special_values():
     z = np.array([[0.0, 40.0, -40.0, 1.0]])
     one = np.ones_like(z)
