@@ -211,8 +211,12 @@ def bench_components(peaks, device):
     Bm = Relation.from_dense(synth.make_torch("f32", (256, 256), "uniform", 2, -1, 1, device=device), [4, 4])
     C = Relation("f32", (256, 256), [4, 4], device=device)
     med, mn = timed(lambda: joinagg("ij,jk->ik", [A, Bm], out=C), reps=50, warm=10)
+    from tensor_relational_einsum_gb300.graphs import capture
+    g1 = capture(lambda: joinagg("ij,jk->ik", [A, Bm], out=C))
+    gmed, gmn = timed(g1.replay, reps=50, warm=10)
     out["matmul_fp32_256"] = {"us_per_call": round(med * 1e3, 2), "min_us": round(mn * 1e3, 2),
-                              "tuples": 64, "groups": 16}
+                              "us_per_call_cuda_graph": round(gmed * 1e3, 2), "tuples": 64, "groups": 16}
+    del g1
 
     # attention join-agg chain b4 h32 s=t=2048 d128, t in 4 blocks
     q = synth.make_torch("bf16", (4, 32, 2048, 128), "normal", 11, 0, 1, device=device)
@@ -285,6 +289,23 @@ def bench_components(peaks, device):
                                                                  peaks["bf16_tflops"], 3),
                                          "join_aggs": per}
     del ffn
+
+    # the matrix chains A-E (the pages' second workload family), bf16
+    from tensor_relational_einsum_gb300.graphs import CHAINS, MatrixChain
+    chains_out = {}
+    for name, (dims, paren) in CHAINS.items():
+        mats = [synth.make_torch("bf16", (dims[i], dims[i + 1]), "normal", 400 + i, 0.0,
+                                 1.0 if i == 0 else 1.0 / math.sqrt(dims[i]), device=device)
+                for i in range(len(dims) - 1)]
+        mc = MatrixChain(mats, paren)
+        del mats
+        cmed, cmn = timed(mc.run, reps=3, warm=1)
+        tf = mc.flop / (cmed * 1e-3) / 1e12
+        chains_out[name] = {"ms": round(cmed, 3), "TFLOP/s": round(tf, 1), "tflop": round(mc.flop / 1e12, 3),
+                            "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 3)}
+        del mc
+        torch.cuda.empty_cache()
+    out["matrix_chains_bf16"] = chains_out
 
     # exchange: bf16 8192^2 held as 8x1 row blocks -> 1x8, 4x2, 16x16
     X = Relation.from_dense(synth.make_torch("bf16", (8192, 8192), "uniform", 31, -1, 1, device=device), [8, 1])

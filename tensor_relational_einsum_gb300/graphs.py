@@ -14,6 +14,9 @@ All arithmetic runs in libea.so.
                       tcgen05 kernel.
 * ``SwigluFFN``       gate/up contractions (SUM over model-dim blocks),
                       SiLU(gate) * up elementwise join, down contraction.
+* ``MatrixChain``     the pages' matrix-chain workloads (chains A-E): a
+                      fixed parenthesization, every multiply one contraction
+                      join-agg over near-equal blocks.
 * ``LlamaBlock``      pre-norm block: RMSNorm, Q,K contraction with RoPE in its
                       epilogue and V contraction (or fused QKV then RoPE),
                       causal attention (fused, or the chain), exchange of the attention
@@ -222,6 +225,68 @@ class SwigluFFN:
 
     def flops(self) -> float:
         return 2.0 * self.T * self.D * self.F * 3
+
+
+# The matrix chains of the evaluation ("Every Kernel Is a Join", Section 7):
+# dimensions d0..dn (matrix i is d[i-1] x d[i]) and the fixed parenthesization.
+def _alt(ends, a, b, n):
+    return [ends] + [a if i % 2 == 0 else b for i in range(n - 1)] + [ends]
+
+
+def _necked(ends, neck, inner, n):
+    return [ends, neck] + [inner] * (n - 3) + [neck, ends]
+
+
+def _right_nested(lo, hi):
+    node = (hi - 1, hi)
+    for i in range(hi - 2, lo - 1, -1):
+        node = (i, node)
+    return node
+
+
+CHAINS = {
+    "A": (_alt(10240, 16384, 6144, 9), (((1, 2), ((3, 4), ((5, 6), (7, 8)))), 9)),
+    "B": (_alt(9216, 20480, 5120, 5), ((1, 2), ((3, 4), 5))),
+    "C": ([10240, 12288, 32768, 2048], (1, (2, 3))),
+    "D": (_necked(24576, 1536, 20480, 9), ((1, _right_nested(2, 8)), 9)),
+    "E": (_necked(49152, 1024, 20480, 13), ((1, _right_nested(2, 12)), 13)),
+}
+
+
+def chain_blocks(d: int, block: int = 4096) -> int:
+    """Near-equal blocks of about ``block`` along a chain dimension."""
+    return max(1, round(d / block))
+
+
+class MatrixChain:
+    """A chain of bf16 matrices multiplied in a fixed parenthesization, every
+    multiply the contraction join-agg "ij,jk->ik" (SUM over the contracted
+    dimension's blocks fused in the accumulator); every dimension tiled into
+    near-equal blocks of about 4096.  ``mats``: torch tensors M1..Mn."""
+
+    def __init__(self, mats, paren, block: int = 4096):
+        self.paren = paren
+        self.rels = [Relation.from_dense(m.contiguous(), [chain_blocks(m.shape[0], block),
+                                                          chain_blocks(m.shape[1], block)]) for m in mats]
+        self.steps = []          # (left, right, out) in evaluation order
+        self.flop = 0.0
+        self.out = self._plan(paren)
+
+    def _plan(self, node):
+        if isinstance(node, int):
+            return self.rels[node - 1]
+        left, right = self._plan(node[0]), self._plan(node[1])
+        out = Relation("bf16", (left.dims[0], right.dims[1]), [left.bounds[0], right.bounds[1]],
+                       device=left.storage.device)
+        self.steps.append((left, right, out))
+        self.flop += 2.0 * left.dims[0] * left.dims[1] * right.dims[1]
+        return out
+
+    def run(self, rec: Recorder | None = None):
+        c = rec.call if rec is not None else _direct
+        for i, (l, r, o) in enumerate(self.steps):
+            c(f"chain.{i}", lambda l=l, r=r, o=o: joinagg("ij,jk->ik", [l, r], "sum", "product", out=o))
+        return self.out
 
 
 class LlamaBlock:
