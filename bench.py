@@ -583,6 +583,11 @@ def profile_case(name: str, reps: int):
         ch = AttentionChain(Relation.from_dense(q, [1, 32, 1, 1]), Relation.from_dense(k, [1, 32, 4, 1]),
                             Relation.from_dense(v, [1, 32, 4, 1]))
         fn = ch.run
+    elif name == "c1":  # fp32 matmul join-agg 256^3, i, j, k in 4 blocks each (64 tuples)
+        A = Relation.from_dense(synth.make_torch("f32", (256, 256), "uniform", 1, -1, 1, device=dev), [4, 4])
+        B = Relation.from_dense(synth.make_torch("f32", (256, 256), "uniform", 2, -1, 1, device=dev), [4, 4])
+        C = Relation("f32", (256, 256), [4, 4], device=dev)
+        fn = lambda: joinagg("ij,jk->ik", [A, B], out=C)  # noqa: E731
     elif name == "attn_fused":  # fused causal attention b4 s2048 h32 d128 token-major, s and t in 4 blocks
         from tensor_relational_einsum_gb300.relation import attention
         q, k, v = (Relation.from_dense(synth.make_torch("bf16", (4, 2048, 32, 128), "normal", sd, 0, 1, device=dev),
@@ -627,7 +632,7 @@ def profile_case(name: str, reps: int):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["gemm", "attn", "attn_fused", "exchange", "norm", "ffn_ew"], default=None)
+    ap.add_argument("--profile-case", choices=["gemm", "attn", "attn_fused", "c1", "exchange", "norm", "ffn_ew"], default=None)
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)

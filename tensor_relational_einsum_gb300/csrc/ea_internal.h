@@ -203,6 +203,7 @@ struct CtParams {
     int a_dtype, b_dtype, c_dtype;
     float scale;
     int pred_mode;                     // 0 none; 1 mask n > m; 2 mask m > n
+    int tile;                          // output tile edge: 64, or 32 when 64-wide tiles would leave SMs idle
 };
 cudaError_t launch_contract_simt(const CtParams &p, cudaStream_t st);
 

@@ -592,13 +592,13 @@ static int pred_mode_of(const JoinCtx &j, const ContractionViews &cv, int *kpred
 }
 
 static ea_status build_simt(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cudaStream_t st, DevPlan *p) {
-    (void)c;
     int kpred = 0;
     int mode = pred_mode_of(j, cv, &kpred);
     if (mode < 0) return set_error(EA_ERR_UNSUPPORTED, "contraction: predicate letters must be output letters");
     std::vector<CtGroup> groups;
     std::vector<CtTuple> tuples;
     std::vector<CtTile> tiles;
+    std::vector<std::pair<int32_t, CtGroup>> gtiles;  // groups with work, for the tiles
     for (size_t g = 0; g < j.wl.groups.size(); g++) {
         CtGroup G;
         memset(&G, 0, sizeof G);
@@ -640,11 +640,17 @@ static ea_status build_simt(JoinCtx &j, const ContractionViews &cv, DevCtx *c, c
         G.t1 = (int32_t)tuples.size();
         int32_t gid = (int32_t)groups.size();
         groups.push_back(G);
-        for (int64_t bb = 0; bb < G.nb; bb++)
-            for (int64_t n0 = 0; n0 < G.N; n0 += 64)
-                for (int64_t m0 = 0; m0 < G.M; m0 += 64)
-                    tiles.push_back(CtTile{gid, (int32_t)bb, (int32_t)m0, (int32_t)n0});
+        gtiles.push_back({gid, G});
     }
+    // 64-wide output tiles, or 32-wide when the 64-wide ones would leave SMs idle
+    int64_t n64 = 0;
+    for (auto &g : gtiles) n64 += g.second.nb * ((g.second.M + 63) / 64) * ((g.second.N + 63) / 64);
+    const int tsz = n64 < 2 * (int64_t)c->num_sms ? 32 : 64;
+    for (auto &g : gtiles)
+        for (int64_t bb = 0; bb < g.second.nb; bb++)
+            for (int64_t n0 = 0; n0 < g.second.N; n0 += tsz)
+                for (int64_t m0 = 0; m0 < g.second.M; m0 += tsz)
+                    tiles.push_back(CtTile{g.first, (int32_t)bb, (int32_t)m0, (int32_t)n0});
     Blob b;
     size_t og = b.add_vec(groups), ou = b.add_vec(tuples), ot = b.add_vec(tiles);
     ea_status s = upload(b, st, p);
@@ -663,6 +669,7 @@ static ea_status build_simt(JoinCtx &j, const ContractionViews &cv, DevCtx *c, c
     q.c_dtype = j.out->dtype;
     q.scale = j.scale;
     q.pred_mode = mode;
+    q.tile = tsz;
     return EA_OK;
 }
 

@@ -18,76 +18,95 @@ namespace ea {
 
 namespace {
 
-constexpr int kT = 64;   // output tile
-constexpr int kK = 16;   // k chunk
-constexpr int kThreads = 256;
+constexpr int kK = 64;  // k chunk
 
-__global__ void __launch_bounds__(kThreads) simt_contract_kernel(const CtParams p) {
-    __shared__ float As[kK][kT + 4];
-    __shared__ float Bs[kK][kT + 4];
+// One CTA per TT x TT output tile, MT x MT outputs per thread; the next k
+// chunk is read into registers while the current one is multiplied from
+// shared memory, so each chunk costs one global round trip overlapped with
+// math.
+template <int TT, int MT>
+__global__ void __launch_bounds__((TT / MT) * (TT / MT)) simt_contract_kernel(const CtParams p) {
+    constexpr int NT = (TT / MT) * (TT / MT);
+    constexpr int PER = kK * TT / NT;  // elements of each operand a thread stages per chunk
+    __shared__ float As[kK][TT + 4];
+    __shared__ float Bs[kK][TT + 4];
     const CtTile tile = p.tiles[blockIdx.x];
     const CtGroup G = p.groups[tile.group];
-    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-    float acc[4][4];
+    const int tx = threadIdx.x % (TT / MT), ty = threadIdx.x / (TT / MT);
+    float acc[MT][MT];
 #pragma unroll
-    for (int i = 0; i < 4; i++)
+    for (int i = 0; i < MT; i++)
 #pragma unroll
-        for (int j = 0; j < 4; j++) acc[i][j] = 0.0f;
+        for (int j = 0; j < MT; j++) acc[i][j] = 0.0f;
     const int64_t m0 = tile.m0, n0 = tile.n0, bb = tile.batch;
-    for (int t = G.t0; t < G.t1; t++) {
-        const CtTuple U = p.tuples[t];
+    float ra[PER], rb[PER];
+    // stage chunk (t, k0) of both operands into registers
+    auto fetch = [&](const CtTuple &U, int64_t k0) {
         const bool a_m_fast = U.a_sk != 1 && U.a_sm == 1;
         const bool b_n_fast = !(U.b_sk == 1 && U.b_sn != 1);
-        for (int64_t k0 = 0; k0 < U.K; k0 += kK) {
-            for (int i = threadIdx.x; i < kK * kT; i += kThreads) {
-                int m, k;
-                if (a_m_fast) {
-                    m = i % kT;
-                    k = i / kT;
-                } else {
-                    m = i / kK;
-                    k = i % kK;
-                }
-                int64_t gm = m0 + m, gk = k0 + k;
-                As[k][m] = (gm < G.M && gk < U.K)
-                               ? ld_elem(p.a, p.a_dtype, U.a_base + gm * U.a_sm + gk * U.a_sk + bb * U.a_sb)
-                               : 0.0f;
-                int n, k2;
-                if (b_n_fast) {
-                    n = i % kT;
-                    k2 = i / kT;
-                } else {
-                    n = i / kK;
-                    k2 = i % kK;
-                }
-                int64_t gn = n0 + n, gk2 = k0 + k2;
-                Bs[k2][n] = (gn < G.N && gk2 < U.K)
-                                ? ld_elem(p.b, p.b_dtype, U.b_base + gk2 * U.b_sk + gn * U.b_sn + bb * U.b_sb)
-                                : 0.0f;
-            }
-            __syncthreads();
 #pragma unroll
-            for (int k = 0; k < kK; k++) {
-                float a[4], b[4];
-#pragma unroll
-                for (int i = 0; i < 4; i++) a[i] = As[k][ty * 4 + i];
-#pragma unroll
-                for (int j = 0; j < 4; j++) b[j] = Bs[k][tx * 4 + j];
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-#pragma unroll
-                    for (int j = 0; j < 4; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-            }
-            __syncthreads();
+        for (int q = 0; q < PER; q++) {
+            const int i = threadIdx.x + q * NT;
+            const int m = a_m_fast ? i % TT : i / kK, k = a_m_fast ? i / TT : i % kK;
+            const int64_t gm = m0 + m, gk = k0 + k;
+            ra[q] = (gm < G.M && gk < U.K) ? ld_elem(p.a, p.a_dtype, U.a_base + gm * U.a_sm + gk * U.a_sk + bb * U.a_sb)
+                                           : 0.0f;
+            const int n = b_n_fast ? i % TT : i / kK, k2 = b_n_fast ? i / TT : i % kK;
+            const int64_t gn = n0 + n, gk2 = k0 + k2;
+            rb[q] = (gn < G.N && gk2 < U.K) ? ld_elem(p.b, p.b_dtype, U.b_base + gk2 * U.b_sk + gn * U.b_sn + bb * U.b_sb)
+                                            : 0.0f;
         }
+    };
+    auto stash = [&](const CtTuple &U) {
+        const bool a_m_fast = U.a_sk != 1 && U.a_sm == 1;
+        const bool b_n_fast = !(U.b_sk == 1 && U.b_sn != 1);
+#pragma unroll
+        for (int q = 0; q < PER; q++) {
+            const int i = threadIdx.x + q * NT;
+            const int m = a_m_fast ? i % TT : i / kK, k = a_m_fast ? i / TT : i % kK;
+            As[k][m] = ra[q];
+            const int n = b_n_fast ? i % TT : i / kK, k2 = b_n_fast ? i / TT : i % kK;
+            Bs[k2][n] = rb[q];
+        }
+    };
+    int t = G.t0;
+    int64_t k0 = 0;
+    if (t < G.t1) fetch(p.tuples[t], 0);
+    while (t < G.t1) {
+        const CtTuple U = p.tuples[t];
+        stash(U);
+        __syncthreads();
+        // the next chunk: the rest of this tuple, else the next tuple's first
+        int tn = t;
+        int64_t kn = k0 + kK;
+        if (kn >= U.K) {
+            tn = t + 1;
+            kn = 0;
+        }
+        if (tn < G.t1) fetch(p.tuples[tn], kn);
+#pragma unroll
+        for (int k = 0; k < kK; k++) {
+            float a[MT], b[MT];
+#pragma unroll
+            for (int i = 0; i < MT; i++) a[i] = As[k][ty * MT + i];
+#pragma unroll
+            for (int j = 0; j < MT; j++) b[j] = Bs[k][tx * MT + j];
+#pragma unroll
+            for (int i = 0; i < MT; i++)
+#pragma unroll
+                for (int j = 0; j < MT; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+        t = tn;
+        k0 = kn;
     }
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        int64_t gm = m0 + ty * 4 + i;
+    for (int i = 0; i < MT; i++) {
+        int64_t gm = m0 + ty * MT + i;
         if (gm >= G.M) continue;
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            int64_t gn = n0 + tx * 4 + j;
+        for (int j = 0; j < MT; j++) {
+            int64_t gn = n0 + tx * MT + j;
             if (gn >= G.N) continue;
             float v = acc[i][j] * p.scale;
             if (p.pred_mode == 1 && G.n_lo + gn > G.m_lo + gm) v = -INFINITY;
@@ -100,7 +119,8 @@ __global__ void __launch_bounds__(kThreads) simt_contract_kernel(const CtParams 
 }  // namespace
 
 cudaError_t launch_contract_simt(const CtParams &p, cudaStream_t st) {
-    simt_contract_kernel<<<(unsigned)p.ntiles, kThreads, 0, st>>>(p);
+    if (p.tile == 32) simt_contract_kernel<32, 2><<<(unsigned)p.ntiles, 256, 0, st>>>(p);
+    else simt_contract_kernel<64, 4><<<(unsigned)p.ntiles, 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 
