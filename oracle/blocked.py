@@ -68,3 +68,55 @@ def joinagg_blocked(spec: str, arrays, bounds: dict, map: str = "product", agg: 
         osl = tuple(slice(bounds[l][oiv[l]], bounds[l][oiv[l] + 1]) for l in out)
         res[osl] = acc
     return res
+
+
+def joinagg_partials(spec: str, arrays, bounds: dict, map: str = "product", tier: str = "idx") -> np.ndarray:
+    """Definition 3.7 without its aggregation step: every output block keeps
+    one unaggregated copy per function specification of its group, copy q
+    holding the q-th in canonical order (the contracted letters' block ids,
+    outer first).  Returns [m, *output extents], m the common group size --
+    the m partial copies that an exchange with aggregation later combines
+    ("Every Kernel Is a Join", Section 5.3 and Example 5.4, where the copies
+    of C1 are X and Y)."""
+    ins, out = parse(spec)
+    arrays = [np.asarray(a, dtype=np.float64) for a in arrays]
+    ext = letter_extents(spec, [a.shape for a in arrays])
+    letters = letters_in_order(spec)
+    nblk = {l: len(bounds[l]) - 1 for l in letters}
+    wl = worklist(spec, bounds)
+    sizes = {wl["grp_ptr"][g + 1] - wl["grp_ptr"][g] for g in range(len(wl["groups"]))}
+    if len(sizes) != 1:
+        raise ValueError("partials need the same number of function specifications in every group")
+    m = sizes.pop()
+    res = np.full((m,) + tuple(ext[l] for l in out), np.nan)
+
+    def decode(term, bid):
+        iv = {}
+        for l in reversed(term):
+            iv[l] = bid % nblk[l]
+            bid //= nblk[l]
+        return iv
+
+    for g, ob in enumerate(wl["groups"]):
+        oiv = decode(out, ob)
+        osl = tuple(slice(bounds[l][oiv[l]], bounds[l][oiv[l] + 1]) for l in out)
+        for q, tup in enumerate(wl["tuples"][wl["grp_ptr"][g]:wl["grp_ptr"][g + 1]]):
+            iv = {}
+            for term, bid in zip(ins, tup):
+                iv.update(decode(term, bid))
+            proj = [a[tuple(slice(bounds[l][iv[l]], bounds[l][iv[l] + 1]) for l in term)]
+                    for term, a in zip(ins, arrays)]
+            lo = {l: bounds[l][iv[l]] for l in iv}
+            res[(q,) + osl] = joinagg(spec, proj, map=map, agg="sum", tier=tier, lo=lo)
+    return res
+
+
+def aggregate_copies(parts: np.ndarray, agg: str) -> np.ndarray:
+    """x[...] = parts[0, ...] (+) parts[1, ...] (+) ... in copy order, (+) the
+    SUM or MAX of the producer's aggregation: the "X1 + Y1" of the exchange
+    with aggregation ("Every Kernel Is a Join", Example 5.4).  fp64."""
+    parts = np.asarray(parts, dtype=np.float64)
+    acc = parts[0].copy()
+    for q in range(1, parts.shape[0]):
+        acc = _combine(agg, acc, parts[q])
+    return acc

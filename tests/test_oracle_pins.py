@@ -467,3 +467,78 @@ def test_pins_catch_planted_mistakes():
     c1 = chains.softmax_attention(x, x, x, causal=True)["O"]
     c2 = chains.softmax_attention(x2, x2, x2, causal=True)["O"]
     assert np.array_equal(c1[0, 0, :3], c2[0, 0, :3])
+
+
+# -------------------------------------------- partial copies and their (+)
+
+def test_ex54_preamble_partials():
+    """Example 5.4: the copies the producer's GPUs hold and the preamble's
+    X_j + Y_j, written out with numpy matmul on the page's slices."""
+    g = gold("ex5_4_preamble.json")
+    r = rng(54)
+    A = r.standard_normal((g["i"], g["j"]))
+    B = r.standard_normal((g["j"], g["k"]))
+    ib, jb = g["i_bounds"], g["j_bounds"]
+    P = blocked.joinagg_partials("ij,jk->ik", [A, B], {"i": ib, "j": jb, "k": g["k_bounds"]})
+    assert P.shape == (2, g["i"], g["k"])
+
+    def held(gpu):  # the output block F(m,n) writes, computed from its slices alone
+        m, n = g["spec_of_gpu"][gpu]
+        rows = slice(ib[m - 1], ib[m])
+        cols = slice(jb[n - 1], jb[n])
+        return rows, n - 1, A[rows, cols] @ B[cols, :]
+
+    for gpu in range(4):
+        rows, copy, val = held(gpu)
+        assert np.allclose(P[copy, rows], val, rtol=1e-12, atol=1e-12)
+    cb = g["consumer_i_bounds"]
+    S = blocked.aggregate_copies(P, "sum")
+    for j, (x, y) in enumerate(g["out"]):
+        rows = slice(cb[j], cb[j + 1])
+        parts = []
+        for atom in (x, y):
+            prow, copy, val = held(g["in"][atom])
+            parts.append(val[cb[j] - prow.start:cb[j + 1] - prow.start])
+        assert np.allclose(S[rows], parts[0] + parts[1], rtol=1e-12, atol=1e-12)
+    assert np.allclose(S, A @ B, rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("spec,shapes,bounds", [
+    ("ij,jk->ik", [(7, 9), (9, 6)], {"i": [0, 3, 7], "j": [0, 2, 5, 9], "k": [0, 4, 6]}),
+    ("bij,bjk->bik", [(2, 5, 8), (2, 8, 3)], {"b": [0, 1, 2], "i": [0, 5], "j": [0, 1, 4, 6, 8], "k": [0, 3]}),
+    ("ij,kj->ik", [(4, 10), (3, 10)], {"i": [0, 2, 4], "j": [0, 5, 10], "k": [0, 1, 3]}),
+])
+def test_partials_brute_force_and_sum(spec, shapes, bounds):
+    """Copy q of every block is the contraction over the q-th block of the
+    aggregated letter alone (brute force over cells); SUM over the copies is
+    numpy.einsum of the whole; MAX over the copies is numpy's max."""
+    r = rng(7)
+    arrs = [r.standard_normal(s) for s in shapes]
+    P = blocked.joinagg_partials(spec, arrs, bounds)
+    agg_letter = "j"
+    nq = len(bounds[agg_letter]) - 1
+    assert P.shape[0] == nq
+    ins, out = spec.split("->")
+    ta, tb = ins.split(",")
+    for q in range(nq):
+        lo, hi = bounds[agg_letter][q], bounds[agg_letter][q + 1]
+        want = np.zeros(P.shape[1:])
+        ext = dict(zip(ta, arrs[0].shape)) | dict(zip(tb, arrs[1].shape))
+        for cell in itertools.product(*[range(ext[l]) for l in out]):
+            env = dict(zip(out, cell))
+            s = 0.0
+            for jj in range(lo, hi):
+                env[agg_letter] = jj
+                s += arrs[0][tuple(env[l] for l in ta)] * arrs[1][tuple(env[l] for l in tb)]
+            want[cell] = s
+        assert np.allclose(P[q], want, rtol=1e-12, atol=1e-12)
+    assert np.allclose(blocked.aggregate_copies(P, "sum"), np.einsum(spec, *arrs), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(blocked.aggregate_copies(P, "max"), P.max(axis=0))
+
+
+def test_aggregate_copies_order_and_single_copy():
+    x = rng(3).standard_normal((1, 4, 5))
+    assert np.array_equal(blocked.aggregate_copies(x, "sum"), x[0])
+    # copy order: ((a + b) + c), visible where it changes the fp64 rounding
+    P = np.array([[1e16], [1.0], [-1e16]])
+    assert blocked.aggregate_copies(P, "sum")[0] == (1e16 + 1.0) - 1e16
