@@ -318,6 +318,25 @@ def bench_components(peaks, device):
         ex[name] = {"us": round(med * 1e3, 1), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
         del Y
     out["exchange_bf16_8192sq_from_8x1"] = ex
+    del X
+
+    # exchange with aggregation: the FFN down projection with its 4 k-blocks
+    # left as 4 unaggregated fp32 copies, SUM-exchanged into 16x16 tiles
+    from tensor_relational_einsum_gb300.relation import exchange_agg
+    h = Relation.from_dense(synth.make_torch("bf16", (8192, 11008), "normal", 21, 0, 1, device=device), [1, 4])
+    wd = Relation.from_dense(synth.make_torch("bf16", (11008, 4096), "normal", 24, 0, 0.02, device=device), [4, 1])
+    P = Relation("f32", (4, 8192, 4096), [4, 1, 1], device=device)
+    S = Relation("f32", (8192, 4096), [16, 16], device=device)
+    pmed, _ = timed(lambda: joinagg("ij,jk->ik", [h, wd], out=P, partials=True), reps=5, warm=3)
+    xmed, xmn = timed(lambda: exchange_agg(P, "sum", out=S), reps=10, warm=3)
+    xb = (4 + 1) * 8192 * 4096 * 4
+    gbs = xb / (xmed * 1e-3) / 1e9
+    tf = 2.0 * 8192 * 11008 * 4096 / (pmed * 1e-3) / 1e12
+    out["exchange_agg_ffn_down_4_copies_f32"] = {
+        "partials_ms": round(pmed, 4), "partials_TFLOP/s": round(tf, 1),
+        "exchange_agg_us": round(xmed * 1e3, 1), "exchange_agg_min_us": round(xmn * 1e3, 1),
+        "alg_bytes_GB": round(xb / 1e9, 3), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+    del h, wd, P, S
     return out
 
 
@@ -594,6 +613,11 @@ def profile_case(name: str, reps: int):
                                        [4, 4, 1, 1]) for sd in (1, 2, 3))
         o = Relation("bf16", (4, 2048, 32, 128), [4, 4, 1, 1], device=dev)
         fn = lambda: attention("bshd,bthd,bthd->bshd", q, k, v, causal=True, out=o)  # noqa: E731
+    elif name == "exchange_agg":  # 4 fp32 copies of [8192, 4096] -> SUM into 16x16 tiles
+        from tensor_relational_einsum_gb300.relation import exchange_agg
+        P = Relation.from_dense(synth.make_torch("f32", (4, 8192, 4096), "normal", 35, 0, 1, device=dev), [4, 1, 1])
+        S = Relation("f32", (8192, 4096), [16, 16], device=dev)
+        fn = lambda: exchange_agg(P, "sum", out=S)  # noqa: E731
     elif name == "exchange":  # bf16 8192^2: 8x1 row blocks -> 16x16 tiles
         X = Relation.from_dense(synth.make_torch("bf16", (8192, 8192), "uniform", 31, -1, 1, device=dev), [8, 1])
         Y = Relation("bf16", (8192, 8192), [16, 16], device=dev)
@@ -632,7 +656,7 @@ def profile_case(name: str, reps: int):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["gemm", "attn", "attn_fused", "c1", "exchange", "norm", "ffn_ew"], default=None)
+    ap.add_argument("--profile-case", choices=["gemm", "attn", "attn_fused", "c1", "exchange", "exchange_agg", "norm", "ffn_ew"], default=None)
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define EA_ABI_VERSION 2
+#define EA_ABI_VERSION 3
 
 typedef int ea_status;
 #define EA_OK 0
@@ -171,7 +171,14 @@ typedef struct {
  *              rsqrt(row_rms[r] + eps) before the epilogue join.  This is
  *              RMSNorm's apply join pushed through the SUM over the
  *              contracted letter (sum_d x[r,d] s[r] W[d,e] = s[r] sum_d
- *              x[r,d] W[d,e]); a gain over d belongs in the weight.        */
+ *              x[r,d] W[d,e]); a gain over d belongs in the weight.
+ *   partials   a contraction run without its aggregation ("Every Kernel Is
+ *              a Join", Definition 3.7 before step (2); Section 5.3): the
+ *              output relation has one more, leading dimension of extent m,
+ *              tiled into m unit blocks, and copy q receives the output block
+ *              of the q-th function specification of each group (canonical
+ *              order); every group must have m specifications.  The copies
+ *              are aggregated later, e.g. by ea_exchange_agg.                */
 typedef struct {
     int32_t out_dtype;
     float scale;
@@ -187,6 +194,8 @@ typedef struct {
     int32_t epi_map;
     int32_t rope_dim;
     ea_relation row_rms;
+    int32_t partials;
+    int32_t reserved1;
 } ea_opts;
 
 /* ------------------------------------------------------------ basics */
@@ -323,9 +332,24 @@ ea_status ea_attention_run(const char *spec, ea_relation q, ea_relation k, ea_re
  * memory with `in`. */
 ea_status ea_exchange(ea_relation in, const ea_dim_part *new_parts, void *stream, ea_relation *out);
 
+/* The exchange with aggregation ("Every Kernel Is a Join", Section 5.3 and
+ * Example 5.4): `in` holds m unaggregated copies of a relation along its
+ * first dimension (extent m, tiled into m unit blocks, copy q = in[q, ...],
+ * e.g. the partials of a join-agg); every cell x of `out` receives the
+ * aggregate (+)_q in[q, x] of its m copies, re-blocked into out's tiling
+ * through the overlay of the two tilings (each atom's copies are read and
+ * combined once, in copy order, in fp32, and written once).  agg:
+ * EA_AGG_SUM or EA_AGG_MAX.  *out == NULL: the call creates the output with
+ * in's dtype, extents in->dims[1..] and tiling new_parts (rank in->rank - 1);
+ * otherwise *out must have them (new_parts may then be NULL).  Errors:
+ * EA_ERR_SHAPE (extents or rank), EA_ERR_PARTITION (in's first dimension not
+ * in unit blocks, out's tiling unlike new_parts), EA_ERR_ARG (agg, overlap). */
+ea_status ea_exchange_agg(ea_relation in, ea_agg agg, const ea_dim_part *new_parts, void *stream, ea_relation *out);
+
 /* What the last ea_joinagg_run / ea_exchange of the calling host thread
  * launched: kernel class (0 exchange, 1 elementwise, 2 row reduction,
- * 3 SIMT contraction, 4 tcgen05 contraction, 5 attention), kernel launches, work tiles,
+ * 3 SIMT contraction, 4 tcgen05 contraction, 5 attention, 6 exchange with
+ * aggregation), kernel launches, work tiles,
  * aggregation groups and function specifications (tuples).  Any pointer
  * may be NULL. */
 ea_status ea_last_plan(int32_t *kernel_class, int32_t *launches, int64_t *tiles, int64_t *groups, int64_t *tuples);

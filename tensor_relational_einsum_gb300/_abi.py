@@ -43,7 +43,8 @@ class Opts(ctypes.Structure):
                 ("pred_lo", ctypes.c_char), ("pred_hi", ctypes.c_char), ("rope_pos", ctypes.c_char),
                 ("epi_pair", ctypes.c_char), ("rope_table", ctypes.c_void_p), ("rope_npos", ctypes.c_int64),
                 ("out2", ctypes.c_void_p), ("epi_in", ctypes.c_void_p), ("epi_map", ctypes.c_int32),
-                ("rope_dim", ctypes.c_int32), ("row_rms", ctypes.c_void_p)]
+                ("rope_dim", ctypes.c_int32), ("row_rms", ctypes.c_void_p), ("partials", ctypes.c_int32),
+                ("reserved1", ctypes.c_int32)]
 
 
 class AttnOpts(ctypes.Structure):
@@ -91,13 +92,14 @@ def lib():
         L.ea_overlay_atoms.argtypes = [ctypes.c_int, P64, ctypes.POINTER(DimPart), ctypes.POINTER(DimPart), P64]
         L.ea_last_plan.argtypes = [P32, P32, P64, P64, P64]
         L.ea_exchange_noalloc.argtypes = [VP, VP, VP]
+        L.ea_exchange_agg.argtypes = [VP, ctypes.c_int, ctypes.POINTER(DimPart), VP, ctypes.POINTER(VP)]
         L.ea_attention_run.argtypes = [ctypes.c_char_p, VP, VP, VP, ctypes.POINTER(AttnOpts), VP, ctypes.POINTER(VP)]
         for name in ("ea_check", "ea_plan_cache_clear", "ea_relation_create", "ea_relation_destroy",
                      "ea_relation_info", "ea_relation_block", "ea_relation_data", "ea_relation_bounds",
                      "ea_joinagg_run", "ea_exchange", "ea_plan_worklist", "ea_exchange_permutation",
-                     "ea_overlay_atoms", "ea_last_plan", "ea_exchange_noalloc", "ea_attention_run"):
+                     "ea_overlay_atoms", "ea_last_plan", "ea_exchange_noalloc", "ea_attention_run", "ea_exchange_agg"):
             getattr(L, name).restype = ctypes.c_int
-        if L.ea_abi_version() != 2:
+        if L.ea_abi_version() != 3:
             raise ImportError("libea.so ABI version mismatch")
         _lib = L
         return _lib
@@ -156,7 +158,7 @@ def index_parts(parts: dict | None):
     return arr, len(parts), keep
 
 
-KERNEL_CLASS = {0: "exchange", 1: "elementwise", 2: "rowreduce", 3: "contract_simt", 4: "contract_tc", 5: "attention"}
+KERNEL_CLASS = {0: "exchange", 1: "elementwise", 2: "rowreduce", 3: "contract_simt", 4: "contract_tc", 5: "attention", 6: "exchange_agg"}
 
 
 def last_plan():

@@ -212,6 +212,7 @@ struct JoinCtx {
     int rope_dim;                // ROPE: pair period along the last letter (0 = its extent)
     const ea_relation_s *row_rms;  // contraction row scale rsqrt(row_rms[row] + eps), or null
     char row_letter;             // the output letter of input 0 only (rows of the contraction)
+    char copy_letter;            // partials: the letter of the copies (leading output letter), or 0
     char epi_pair;               // EA_MAP_SILU_MUL: the paired letter (innermost in the planned output)
     ea_relation_s *user_out;     // the output relation (out is its pre-epilogue view when paired)
 };
@@ -927,6 +928,7 @@ ea_status launch_plan(DevPlan *p, DevCtx *c, cudaStream_t st) {
     case kSimt: t_last.tiles = p->ct.ntiles; t_last.launches = p->ct.ntiles > 0; break;
     case kTc: t_last.tiles = p->tc.ntiles; t_last.launches = p->tc.ntiles > 0; break;
     case kAttn: t_last.tiles = p->n_groups; t_last.launches = p->at.ncta > 0; break;
+    case kExchangeAgg: t_last.tiles = p->nxtiles; t_last.launches = p->nxtiles > 0; break;
     }
     switch (p->kind) {
     case kExchange:
@@ -951,12 +953,47 @@ ea_status launch_plan(DevPlan *p, DevCtx *c, cudaStream_t st) {
         p->at.err = c->err;
         if (p->at.ncta) e = launch_attention(p->at, st);
         break;
+    case kExchangeAgg:
+        if (p->nxtiles)
+            e = launch_exchange_agg(p->segs, p->xtiles, p->nxtiles, p->xsrc, p->xdst, p->xdtype, p->xagg, p->xcopies,
+                                    p->xcopy_stride, c->num_sms, st);
+        break;
     }
     if (e != cudaSuccess) return cuda_error(e, "kernel launch");
     return EA_OK;
 }
 
 static bool same_tiling(const ea_relation_s *r, int d, const Tiling &t) { return r->bounds[d] == t.b; }
+
+// Partials: the copy letter leads the output and joins with every tuple, so
+// group (q, b) lists all the function specifications of output block b; it
+// keeps only the q-th (canonical order), whose output block copy q receives.
+static ea_status keep_copy_tuples(JoinCtx &j) {
+    const WorkList &w = j.wl;
+    const int n_in = j.sp.n_in;
+    const int64_t m = j.lt.t[j.copy_letter - 'a'].extent;
+    int64_t per_copy = 1;  // output blocks per copy
+    for (size_t d = 1; d < j.sp.out.size(); d++) per_copy *= j.lt.t[j.sp.out[d] - 'a'].nblocks();
+    WorkList nw;
+    nw.grp_ptr.push_back(0);
+    for (size_t g = 0; g < w.groups.size(); g++) {
+        const int64_t q = w.groups[g] / per_copy;
+        const int64_t nt = w.grp_ptr[g + 1] - w.grp_ptr[g];
+        if (nt != m)
+            return set_error(EA_ERR_SHAPE, "partials: an output block has %lld function specifications, not %lld",
+                             (long long)nt, (long long)m);
+        const int64_t t = w.grp_ptr[g] + q;
+        nw.groups.push_back(w.groups[g]);
+        for (int k = 0; k < n_in; k++) nw.tuples.push_back(w.tuples[t * n_in + k]);
+        for (int l = 0; l < 26; l++) nw.tuple_iv.push_back(w.tuple_iv[t * 26 + l]);
+        nw.grp_ptr.push_back((int64_t)nw.groups.size());
+    }
+    j.wl.groups.swap(nw.groups);
+    j.wl.grp_ptr.swap(nw.grp_ptr);
+    j.wl.tuples.swap(nw.tuples);
+    j.wl.tuple_iv.swap(nw.tuple_iv);
+    return EA_OK;
+}
 
 }  // namespace ea
 
@@ -970,9 +1007,7 @@ ea_status ea_exchange(ea_relation in, const ea_dim_part *new_parts, void *stream
     set_error(EA_OK, "");
     if (!in || !out) return set_error(EA_ERR_ARG, "ea_exchange: NULL argument");
     std::lock_guard<std::mutex> lk(g_mu);
-    DevCtx *c;
-    ea_status s = get_ctx(&c);
-    if (s) return s;
+    ea_status s = EA_OK;
     Tiling src[kMaxRank], dst[kMaxRank];
     for (int d = 0; d < in->rank; d++) {
         src[d].extent = in->dims[d];
@@ -1005,6 +1040,12 @@ ea_status ea_exchange(ea_relation in, const ea_dim_part *new_parts, void *stream
         s = ea_relation_create((ea_dtype)in->dtype, in->rank, in->dims, parts, nullptr, &o);
         if (s) return s;
     }
+    DevCtx *c;
+    s = get_ctx(&c);
+    if (s) {
+        if (!*out) ea_relation_destroy(o);
+        return s;
+    }
     Key k;
     k.str("X");
     k.rel(in);
@@ -1030,6 +1071,111 @@ ea_status ea_exchange(ea_relation in, const ea_dim_part *new_parts, void *stream
                 p->xsrc = in->arena;
                 p->xdst = o->arena;
                 p->esize = (int)elem_size(in->dtype);
+                g_cache[k.s] = p;
+            } else {
+                free_plan(p);
+            }
+        }
+        if (s) {
+            if (!*out) ea_relation_destroy(o);
+            return s;
+        }
+    }
+    s = launch_plan(p, c, st);
+    if (s) {
+        if (!*out) ea_relation_destroy(o);
+        return s;
+    }
+    *out = o;
+    return EA_OK;
+}
+
+ea_status ea_exchange_agg(ea_relation in, ea_agg agg, const ea_dim_part *new_parts, void *stream, ea_relation *out) {
+    set_error(EA_OK, "");
+    if (!in || !out) return set_error(EA_ERR_ARG, "ea_exchange_agg: NULL argument");
+    if (agg != EA_AGG_SUM && agg != EA_AGG_MAX) return set_error(EA_ERR_ARG, "ea_exchange_agg: agg must be SUM or MAX");
+    if (in->rank < 2) return set_error(EA_ERR_SHAPE, "ea_exchange_agg: the input needs a copy dimension and one more");
+    const int rank = in->rank - 1;
+    const int64_t m = in->dims[0];
+    if ((int64_t)in->bounds[0].size() != m + 1)
+        return set_error(EA_ERR_PARTITION, "ea_exchange_agg: the copy dimension must be tiled into unit blocks");
+    std::lock_guard<std::mutex> lk(g_mu);
+    ea_status s = EA_OK;
+    Tiling src[kMaxRank], dst[kMaxRank];
+    int64_t dims[kMaxRank];
+    for (int d = 0; d < rank; d++) {
+        dims[d] = in->dims[d + 1];
+        src[d].extent = dims[d];
+        src[d].b = in->bounds[d + 1];
+    }
+    ea_relation o = *out;
+    if (new_parts) {
+        for (int d = 0; d < rank; d++) {
+            s = make_tiling(dims[d], new_parts[d].nblocks, new_parts[d].bounds, &dst[d]);
+            if (s) return s;
+        }
+    } else {
+        if (!o) return set_error(EA_ERR_ARG, "ea_exchange_agg: need new_parts or an output relation");
+        if (o->rank != rank) return set_error(EA_ERR_SHAPE, "ea_exchange_agg: output rank");
+        for (int d = 0; d < rank; d++) {
+            dst[d].extent = o->dims[d];
+            dst[d].b = o->bounds[d];
+        }
+    }
+    if (o) {
+        if (o->dtype != in->dtype || o->rank != rank) return set_error(EA_ERR_SHAPE, "ea_exchange_agg: output dtype/rank");
+        for (int d = 0; d < rank; d++) {
+            if (o->dims[d] != dims[d]) return set_error(EA_ERR_SHAPE, "ea_exchange_agg: output extents differ");
+            if (!same_tiling(o, d, dst[d])) return set_error(EA_ERR_PARTITION, "ea_exchange_agg: output tiling differs");
+        }
+        if (o->bytes && in->bytes && o->arena < in->arena + in->bytes && in->arena < o->arena + o->bytes)
+            return set_error(EA_ERR_ARG, "ea_exchange_agg: input and output arenas overlap");
+    } else {
+        ea_dim_part parts[kMaxRank];
+        for (int d = 0; d < rank; d++) parts[d] = ea_dim_part{dst[d].nblocks(), 0, dst[d].b.data()};
+        s = ea_relation_create((ea_dtype)in->dtype, rank, dims, parts, nullptr, &o);
+        if (s) return s;
+    }
+    DevCtx *c;
+    s = get_ctx(&c);
+    if (s) {
+        if (!*out) ea_relation_destroy(o);
+        return s;
+    }
+    Key k;
+    k.str("XA");
+    k.rel(in);
+    k.rel(o);
+    k.v((int)agg);
+    cudaStream_t st = (cudaStream_t)stream;
+    DevPlan *p;
+    auto it = g_cache.find(k.s);
+    if (it != g_cache.end()) {
+        p = it->second;
+    } else {
+        ExchangePlan xp;
+        s = plan_exchange(rank, dims, src, dst, (int)elem_size(in->dtype), &xp);
+        // copy q lies q * copy_stride elements on: 16-byte chunks stay aligned
+        // in every copy only if that stride is a multiple of 16 bytes
+        if (((in->blk_off.back() / m) * (int64_t)elem_size(in->dtype)) % 16)
+            for (XSeg &g : xp.segs) g.vec = 0;
+        if (!s) {
+            p = new DevPlan();
+            Blob b;
+            size_t os = b.add_vec(xp.segs), ot = b.add_vec(xp.tiles);
+            s = upload(b, st, p);
+            if (!s) {
+                p->kind = kExchangeAgg;
+                p->segs = (XSeg *)(p->dev + os);
+                p->xtiles = (XTile *)(p->dev + ot);
+                p->nxtiles = (int64_t)xp.tiles.size();
+                p->xsrc = in->arena;
+                p->xdst = o->arena;
+                p->esize = (int)elem_size(in->dtype);
+                p->xdtype = in->dtype;
+                p->xagg = agg;
+                p->xcopies = (int)m;
+                p->xcopy_stride = in->blk_off.back() / m;
                 g_cache[k.s] = p;
             } else {
                 free_plan(p);
@@ -1121,6 +1267,29 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
         return set_error(EA_ERR_ARG, "ROPE needs rope_pos, a letter of the spec");
     if (map == EA_MAP_ROPE && j.rope_dim && j.rope_dim != j.lt.t[j.sp.out.back() - 'a'].extent)
         return set_error(EA_ERR_UNSUPPORTED, "the elementwise ROPE join takes pairs over the whole last letter");
+    // Partials: the output gains a leading copy letter (unit blocks), and each
+    // group keeps only its copy's function specification (see below).
+    j.copy_letter = 0;
+    if (o.partials) {
+        if (!(map == EA_MAP_PRODUCT && agg == EA_AGG_SUM && n_inputs == 2))
+            return set_error(EA_ERR_UNSUPPORTED, "partials need a contraction (SUM of PRODUCT, two inputs)");
+        if (o.epi_map || o.row_rms || j.pred_lo)
+            return set_error(EA_ERR_UNSUPPORTED, "partials do not combine with an epilogue, row_rms or a predicate");
+        if (!*out) return set_error(EA_ERR_ARG, "partials need the output relation (its first extent is the copy count)");
+        for (char ch = 'a'; ch <= 'z' && !j.copy_letter; ch++)
+            if (j.lt.t[ch - 'a'].extent < 0) j.copy_letter = ch;
+        if (!j.copy_letter) return set_error(EA_ERR_SPEC, "partials: no letter left for the copies");
+        const ea_relation_s *ro = *out;
+        const int64_t m = ro->rank > 0 ? ro->dims[0] : 0;
+        if (ro->rank != (int)j.sp.out.size() + 1 || m < 1)
+            return set_error(EA_ERR_SHAPE, "partials: the output needs a leading copy dimension");
+        if ((int64_t)ro->bounds[0].size() != m + 1)
+            return set_error(EA_ERR_PARTITION, "partials: the copy dimension must be tiled into unit blocks");
+        Tiling tc;
+        make_tiling(m, (int32_t)m, nullptr, &tc);
+        j.lt.t[j.copy_letter - 'a'] = tc;
+        j.sp.out.insert(j.sp.out.begin(), j.copy_letter);
+    }
     // Output relation.
     int odt = o.out_dtype == 0 ? inputs[0]->dtype : o.out_dtype - 1;
     if (odt != EA_F32 && odt != EA_BF16) return set_error(EA_ERR_DTYPE, "unknown out_dtype %d", o.out_dtype);
@@ -1297,6 +1466,7 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
     key.v(j.epi_pair);
     key.v(j.rope_dim);
     if (j.row_rms) key.rel(j.row_rms);
+    key.v(j.copy_letter);
     if (j.epi_in) key.rel(j.epi_in);
     cudaStream_t st = (cudaStream_t)stream;
     DevPlan *p = nullptr;
@@ -1305,6 +1475,7 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
         p = it->second;
     } else {
         s = plan_worklist(j.sp, j.lt, j.pred_lo, j.pred_hi, &j.wl);
+        if (!s && j.copy_letter) s = keep_copy_tuples(j);
         if (!s) {
             p = new DevPlan();
             if (kind == kEwise) s = build_ewise(j, c, st, p);

@@ -38,7 +38,7 @@ struct Blob {
     }
 };
 
-enum PlanKind { kExchange = 0, kEwise, kRowReduce, kSimt, kTc, kAttn };
+enum PlanKind { kExchange = 0, kEwise, kRowReduce, kSimt, kTc, kAttn, kExchangeAgg };
 
 struct DevPlan {
     int kind = 0;
@@ -55,6 +55,8 @@ struct DevPlan {
     const char *xsrc = nullptr;
     char *xdst = nullptr;
     int esize = 0;
+    int xdtype = 0, xagg = 0, xcopies = 1;  // exchange with aggregation
+    int64_t xcopy_stride = 0;
     // kernels
     EwParams ew{};
     RrParams rr{};

@@ -132,6 +132,34 @@ def exchange(rel: Relation, parts, out: Relation | None = None, stream=None) -> 
     return out
 
 
+def exchange_agg(rel: Relation, agg: str, parts=None, out: Relation | None = None, stream=None) -> Relation:
+    """Aggregate the m copies along ``rel``'s leading (copy) dimension with
+    ``agg`` ("sum" or "max", in copy order) and re-block the result into the
+    tiling ``parts`` of the remaining dimensions: the exchange with
+    aggregation of "Every Kernel Is a Join", Section 5.3 / Example 5.4."""
+    if out is None:
+        out = Relation(rel.dtype, rel.dims[1:], parts, device=rel.storage.device)
+    h = ctypes.c_void_p(out.handle.value)
+    check_status(lib().ea_exchange_agg(rel.handle, AGGS[agg], None, ctypes.c_void_p(_stream_ptr(stream)),
+                                       ctypes.byref(h)))
+    return out
+
+
+def copy_count(spec: str, inputs) -> int:
+    """Function specifications per output block of a contraction: the
+    product of the block counts of its aggregated letters."""
+    terms, outl = _parse(spec)
+    nb = {}
+    for term, r in zip(terms, inputs):
+        for l, b in zip(term, r.bounds):
+            nb.setdefault(l, len(b) - 1)
+    m = 1
+    for l, n in nb.items():
+        if l not in outl:
+            m *= n
+    return m
+
+
 def _parse(spec: str):
     lhs, out = spec.split("->")
     return lhs.split(","), out
@@ -153,7 +181,7 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
             parts: dict | None = None, rope_table: torch.Tensor | None = None, rope_pos: str | None = None,
             out2: Relation | None = None, epi_map: str | None = None, epi_in: Relation | None = None,
             epi_pair: str | None = None, rope_dim: int = 0, row_rms: Relation | None = None,
-            stream=None) -> Relation:
+            partials: bool = False, stream=None) -> Relation:
     """Run one join-agg ("Every Kernel Is a Join", Definition 3.7) with
     libea.so.  ``pred="ts"`` keeps joined tuples with t <= s.  With
     ``agg="max_sumexp"`` the output receives the MAX and ``out2`` the SUM
@@ -163,9 +191,15 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
     ``rope_pos`` the row letter, pairs of period ``rope_dim``);
     ``row_rms=ms`` multiplies every row r by rsqrt(ms[r] + eps) first;
     ``epi_map="silu_mul", epi_pair="c"`` plans letter c (extent 2, second
-    input only) as the innermost output letter and stores SiLU(c=0) * (c=1)."""
+    input only) as the innermost output letter and stores SiLU(c=0) * (c=1).
+    ``partials=True`` runs a contraction without its aggregation: the output
+    gains a leading copy dimension of m unit blocks, copy q holding each
+    block's q-th function specification alone (``exchange_agg`` sums them)."""
     if out is None:
         dims, bounds = output_layout(spec, inputs)
+        if partials:
+            m = copy_count(spec, inputs)
+            dims, bounds = [m] + list(dims), [list(range(m + 1))] + list(bounds)
         out = Relation(out_dtype or inputs[0].dtype, dims, bounds, device=inputs[0].storage.device)
     handles = (ctypes.c_void_p * len(inputs))(*[r.handle.value for r in inputs])
     ip, n_parts, keep = _abi.index_parts(parts)
@@ -184,6 +218,7 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
         o.out2 = out2.handle.value
     if row_rms is not None:
         o.row_rms = row_rms.handle.value
+    o.partials = 1 if partials else 0
     if epi_map is not None:
         o.epi_map = MAPS[epi_map]
         if epi_in is not None:

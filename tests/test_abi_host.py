@@ -29,7 +29,7 @@ def test_exports_every_declared_symbol(L):
     assert {"ea_relation_create", "ea_joinagg_run", "ea_exchange"} <= names
     for n in sorted(names):
         assert hasattr(L, n), n
-    assert L.ea_abi_version() == 2
+    assert L.ea_abi_version() == 3
 
 
 def plan(L, spec, shapes, parts, pred=None):
@@ -277,3 +277,50 @@ def test_epilogue_join_errors_without_gpu(L):
     assert L.ea_joinagg_run(b"td,dfc->tfc", hs, 2, None, 0, 1, 0, ctypes.byref(o3), None, ctypes.byref(out3)) == 8
     for r in (x, w, h, wrong, h3, r3):
         L.ea_relation_destroy(r)
+
+
+def test_exchange_agg_and_partials_errors_without_gpu(L):
+    """ea_exchange_agg checks the copy dimension, the aggregation and the
+    output before any GPU work; a contraction's partials option checks its
+    output's leading copy dimension and refuses epilogues."""
+    F32 = 0
+    _, p = _fake_rel(L, F32, (2, 256, 64), [2, 2, 1], 1 << 24)
+    _, o = _fake_rel(L, F32, (256, 64), [4, 1], 1 << 26)
+    out = ctypes.c_void_p(o.value)
+    assert L.ea_exchange_agg(None, 1, None, None, ctypes.byref(out)) == 7
+    assert L.ea_exchange_agg(p, 0, None, None, ctypes.byref(out)) == 7           # NONE is no aggregation
+    assert L.ea_exchange_agg(p, 3, None, None, ctypes.byref(out)) == 7           # MAX_SUMEXP neither
+    _, blocked = _fake_rel(L, F32, (2, 256, 64), [1, 2, 1], 1 << 27)
+    assert L.ea_exchange_agg(blocked, 1, None, None, ctypes.byref(out)) == 3     # copies not in unit blocks
+    _, flat = _fake_rel(L, F32, (256,), [2], 1 << 28)
+    assert L.ea_exchange_agg(flat, 1, None, None, ctypes.byref(out)) == 2        # no dimension besides the copies
+    _, wide = _fake_rel(L, F32, (256, 65), [4, 1], 1 << 29)
+    w = ctypes.c_void_p(wide.value)
+    assert L.ea_exchange_agg(p, 1, None, None, ctypes.byref(w)) == 2             # extents differ
+    _, bf = _fake_rel(L, 1, (256, 64), [4, 1], 1 << 30)
+    b = ctypes.c_void_p(bf.value)
+    assert L.ea_exchange_agg(p, 1, None, None, ctypes.byref(b)) == 2             # dtype differs
+    _, ov = _fake_rel(L, F32, (256, 64), [4, 1], (1 << 24) + 4096)
+    v = ctypes.c_void_p(ov.value)
+    assert L.ea_exchange_agg(p, 1, None, None, ctypes.byref(v)) == 7             # arenas overlap
+    # partials of "ij,jk->ik" with j in 2 blocks: output [2, i, k], copies in unit blocks
+    _, a = _fake_rel(L, 1, (256, 128), [2, 2], 1 << 31)
+    _, bb = _fake_rel(L, 1, (128, 64), [2, 1], 1 << 32)
+    hs = (ctypes.c_void_p * 2)(a.value, bb.value)
+    po = _abi.Opts()
+    po.partials = 1
+    none = ctypes.c_void_p()
+    assert L.ea_joinagg_run(b"ij,jk->ik", hs, 2, None, 0, 1, 0, ctypes.byref(po), None, ctypes.byref(none)) == 7
+    _, o2 = _fake_rel(L, F32, (256, 64), [2, 1], 1 << 33)
+    x = ctypes.c_void_p(o2.value)
+    assert L.ea_joinagg_run(b"ij,jk->ik", hs, 2, None, 0, 1, 0, ctypes.byref(po), None, ctypes.byref(x)) == 2
+    _, o3 = _fake_rel(L, F32, (2, 256, 64), [1, 2, 1], 1 << 34)
+    x = ctypes.c_void_p(o3.value)
+    assert L.ea_joinagg_run(b"ij,jk->ik", hs, 2, None, 0, 1, 0, ctypes.byref(po), None, ctypes.byref(x)) == 3
+    _, o4 = _fake_rel(L, F32, (2, 256, 64), [2, 2, 1], 1 << 35)
+    x = ctypes.c_void_p(o4.value)
+    assert L.ea_joinagg_run(b"ij,jk->ik", hs, 2, None, 0, 2, 0, ctypes.byref(po), None, ctypes.byref(x)) == 8  # MAX
+    po.epi_map = 3  # an epilogue join (ADD)
+    assert L.ea_joinagg_run(b"ij,jk->ik", hs, 2, None, 0, 1, 0, ctypes.byref(po), None, ctypes.byref(x)) == 8
+    for h in (p, o, blocked, flat, wide, bf, ov, a, bb, o2, o3, o4):
+        L.ea_relation_destroy(h)
