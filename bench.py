@@ -373,7 +373,7 @@ class CpuSample:
 def run_reference(args, world, rank, dist):
     if rank != 0:
         return 0
-    tokens = args.cpu_tokens
+    tokens = args.ref_tokens
     sample = CpuSample(tokens)
     times = []
     for i in range(args.warmup + args.steps):
@@ -662,7 +662,10 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-tokens", type=int, default=32)
+    ap.add_argument("--cpu-tokens", type=int, default=128,
+                    help="tokens of the oracle's CPU-baseline sample (about 10-15 s on 16 cores)")
+    ap.add_argument("--ref-tokens", type=int, default=32,
+                    help="tokens per step of the reference arm (the oracle), so K + W steps end in minutes")
     ap.add_argument("--no-components", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
