@@ -400,18 +400,28 @@ def config_dict():
             "l2": "inputs larger than L2 (block touches ~10 GB per step)"}
 
 
+def contraction_source_hash() -> str:
+    """sha256 (16 hex digits) of what fixes the tcgen05 contraction's launches:
+    its kernel sources and the planner function that builds its tiles
+    (build_tc in joinagg.cpp, up to the generic launcher)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "tensor_relational_einsum_gb300", "csrc")
+    ja = open(os.path.join(csrc, "joinagg.cpp"), "rb").read()
+    lo = ja.index(b"static ea_status build_tc(")
+    hi = ja.index(b"ea_status launch_plan(", lo)
+    return hashlib.sha256(open(os.path.join(csrc, "kernels", "contract_tc.cu"), "rb").read() +
+                          open(os.path.join(csrc, "kernels", "tc_common.cuh"), "rb").read() +
+                          ja[lo:hi]).hexdigest()[:16]
+
+
 def traffic_from_profiles():
     """DRAM bytes per launch of the dominant kernel (the gate+up contraction)
     from the committed ncu summary, if it was taken on the current kernel
-    and planner sources; else None."""
-    import hashlib
-    csrc = os.path.join(ROOT, "tensor_relational_einsum_gb300", "csrc")
+    sources and tile planner; else None."""
     prof = os.path.join(ROOT, "profiles", "contract_tc_ffn_gate_up.md")
     if not os.path.exists(prof):
         return None
-    h = hashlib.sha256(open(os.path.join(csrc, "kernels", "contract_tc.cu"), "rb").read() +
-                       open(os.path.join(csrc, "kernels", "tc_common.cuh"), "rb").read() +
-                       open(os.path.join(csrc, "joinagg.cpp"), "rb").read()).hexdigest()[:16]
+    h = contraction_source_hash()
     want, val = None, None
     for line in open(prof):
         if line.startswith("source_sha256_16:"):
@@ -591,12 +601,14 @@ def profile_case(name: str, reps: int):
     from tensor_relational_einsum_gb300.relation import Relation, check, exchange, joinagg
     build()
     dev = torch.device("cuda", 0)
-    if name == "gemm":   # FFN gate+up contraction with SiLU * up in its epilogue: x[8192,4096] . W[4096, 11008, 2]
+    if name == "gemm":   # FFN gate+up contraction, RMSNorm row scale and SiLU * up in its epilogue: x[8192,4096] . W[4096, 11008, 2]
         x = Relation.from_dense(synth.make_torch("bf16", (8192, 4096), "normal", 21, 0, 1, device=dev), [1, 4])
         w = Relation.from_dense(synth.make_torch("bf16", (4096, 11008, 2), "normal", 22, 0, 0.02, device=dev),
                                 [4, 4, 1])
         y = Relation("bf16", (8192, 11008), [1, 4], device=dev)
-        fn = lambda: joinagg("td,dfc->tf", [x, w], out=y, epi_map="silu_mul", epi_pair="c")  # noqa: E731
+        ms = Relation.from_dense(torch.ones(8192, dtype=torch.float32, device=dev), [1])
+        fn = lambda: joinagg("td,dfc->tf", [x, w], out=y, epi_map="silu_mul", epi_pair="c",  # noqa: E731
+                             row_rms=ms, eps=1e-6)
     elif name == "attn":  # attention chain b1 h32 s=t=2048 d128, t in 4 blocks
         q, k, v = (synth.make_torch("bf16", (1, 32, 2048, 128), "normal", sd, 0, 1, device=dev) for sd in (1, 2, 3))
         ch = AttentionChain(Relation.from_dense(q, [1, 32, 1, 1]), Relation.from_dense(k, [1, 32, 4, 1]),

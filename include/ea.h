@@ -214,14 +214,30 @@ ea_status ea_check(void *stream);
  * device first.  Plans are otherwise kept for the life of the process. */
 ea_status ea_plan_cache_clear(void);
 
+/* Device memory the library takes for itself: the arenas of relations
+ * created with dev_ptr == NULL and the device copies of cached plans (work
+ * lists, tensor maps, exchange segments).  By default cudaMalloc/cudaFree;
+ * ea_set_allocator(alloc, free, ctx) routes later allocations through
+ * alloc(bytes, ctx) and their release through free(ptr, ctx) (for instance
+ * a framework's caching allocator).  alloc must return device memory of
+ * the current device, 16-byte aligned, or NULL (the call that needed it
+ * then fails with EA_ERR_ALLOC).  Memory is released through the pair that
+ * allocated it, even after the allocator has been changed.  Both NULL:
+ * back to cudaMalloc/cudaFree.  Exactly one NULL: EA_ERR_ARG.  Not called
+ * concurrently with other ea_* calls that allocate.  This is the library's
+ * own memory only; ea_exchange_noalloc never allocates. */
+typedef void *(*ea_alloc_fn)(size_t bytes, void *ctx);
+typedef void (*ea_free_fn)(void *ptr, void *ctx);
+ea_status ea_set_allocator(ea_alloc_fn alloc, ea_free_fn free_fn, void *ctx);
+
 /* ------------------------------------------------------------ relations */
 
 /* Create a relation: a tensor of `dtype` and extents dims[0..rank-1]
  * (1 <= rank <= 8) tiled by parts[0..rank-1] (Definitions 3.1, 3.2).
  * dev_ptr: an existing device arena of at least prod(dims) * elemsize bytes
  * in the layout described above, borrowed (the caller keeps it alive and
- * frees it); NULL: the library allocates the arena with cudaMalloc and
- * frees it in ea_relation_destroy.  The arena must be 16-byte aligned.
+ * frees it); NULL: the library allocates the arena (cudaMalloc, or the
+ * allocator given to ea_set_allocator) and frees it in ea_relation_destroy.  The arena must be 16-byte aligned.
  * *out receives the handle. */
 ea_status ea_relation_create(ea_dtype dtype, int rank, const int64_t *dims, const ea_dim_part *parts, void *dev_ptr,
                              ea_relation *out);

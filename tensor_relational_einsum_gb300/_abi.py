@@ -59,6 +59,8 @@ _lock = threading.Lock()
 P64 = ctypes.POINTER(ctypes.c_int64)
 P32 = ctypes.POINTER(ctypes.c_int32)
 VP = ctypes.c_void_p
+ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p)
+FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p)
 
 
 def lib():
@@ -93,11 +95,13 @@ def lib():
         L.ea_last_plan.argtypes = [P32, P32, P64, P64, P64]
         L.ea_exchange_noalloc.argtypes = [VP, VP, VP]
         L.ea_exchange_agg.argtypes = [VP, ctypes.c_int, ctypes.POINTER(DimPart), VP, ctypes.POINTER(VP)]
+        L.ea_set_allocator.argtypes = [ALLOC_FN, FREE_FN, VP]
         L.ea_attention_run.argtypes = [ctypes.c_char_p, VP, VP, VP, ctypes.POINTER(AttnOpts), VP, ctypes.POINTER(VP)]
         for name in ("ea_check", "ea_plan_cache_clear", "ea_relation_create", "ea_relation_destroy",
                      "ea_relation_info", "ea_relation_block", "ea_relation_data", "ea_relation_bounds",
                      "ea_joinagg_run", "ea_exchange", "ea_plan_worklist", "ea_exchange_permutation",
-                     "ea_overlay_atoms", "ea_last_plan", "ea_exchange_noalloc", "ea_attention_run", "ea_exchange_agg"):
+                     "ea_overlay_atoms", "ea_last_plan", "ea_exchange_noalloc", "ea_attention_run", "ea_exchange_agg",
+                     "ea_set_allocator"):
             getattr(L, name).restype = ctypes.c_int
         if L.ea_abi_version() != 3:
             raise ImportError("libea.so ABI version mismatch")

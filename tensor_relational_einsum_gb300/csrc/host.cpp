@@ -16,6 +16,52 @@
 namespace ea {
 
 std::mutex g_mu;
+
+// ------------------------------------------------------------- allocator
+
+namespace {
+std::mutex g_alloc_mu;
+ea_alloc_fn g_alloc_fn = nullptr;
+ea_free_fn g_free_fn = nullptr;
+void *g_alloc_ctx = nullptr;
+}  // namespace
+
+ea_status dev_alloc(size_t bytes, void **ptr, DevFree *rel, const char *what) {
+    ea_alloc_fn fa;
+    DevFree r;
+    {
+        std::lock_guard<std::mutex> lk(g_alloc_mu);
+        fa = g_alloc_fn;
+        r.fn = g_free_fn;
+        r.ctx = g_alloc_ctx;
+    }
+    *ptr = nullptr;
+    if (!fa) {
+        r = DevFree{};
+        cudaError_t e = cudaMalloc(ptr, bytes);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            *ptr = nullptr;
+            return set_error(EA_ERR_ALLOC, "%s: cudaMalloc(%zu) failed: %s", what, bytes, cudaGetErrorString(e));
+        }
+    } else {
+        *ptr = fa(bytes, r.ctx);
+        if (!*ptr) return set_error(EA_ERR_ALLOC, "%s: the allocator returned NULL for %zu bytes", what, bytes);
+        if ((uintptr_t)*ptr % 16) {
+            r.fn(*ptr, r.ctx);
+            *ptr = nullptr;
+            return set_error(EA_ERR_ALLOC, "%s: the allocator returned memory not 16-byte aligned", what);
+        }
+    }
+    *rel = r;
+    return EA_OK;
+}
+
+void dev_free(void *ptr, const DevFree &rel) {
+    if (!ptr) return;
+    if (rel.fn) rel.fn(ptr, rel.ctx);
+    else cudaFree(ptr);
+}
 static thread_local char t_err[1024];
 
 ea_status set_error(ea_status code, const char *fmt, ...) {
@@ -342,6 +388,17 @@ using namespace ea;
 
 extern "C" {
 
+ea_status ea_set_allocator(ea_alloc_fn alloc, ea_free_fn free_fn, void *ctx) {
+    t_err[0] = 0;
+    if ((alloc == nullptr) != (free_fn == nullptr))
+        return set_error(EA_ERR_ARG, "ea_set_allocator: give both functions or neither");
+    std::lock_guard<std::mutex> lk(ea::g_alloc_mu);
+    ea::g_alloc_fn = alloc;
+    ea::g_free_fn = free_fn;
+    ea::g_alloc_ctx = alloc ? ctx : nullptr;
+    return EA_OK;
+}
+
 int ea_abi_version(void) { return EA_ABI_VERSION; }
 
 const char *ea_last_error(void) { return t_err; }
@@ -373,12 +430,10 @@ ea_status ea_relation_create(ea_dtype dtype, int rank, const int64_t *dims, cons
     if (dev_ptr) {
         r->arena = (char *)dev_ptr;
     } else if (r->bytes > 0) {
-        cudaError_t e = cudaMalloc((void **)&r->arena, r->bytes);
-        if (e != cudaSuccess) {
+        ea_status st = dev_alloc(r->bytes, (void **)&r->arena, &r->release, "ea_relation_create");
+        if (st) {
             delete r;
-            cudaGetLastError();
-            return set_error(EA_ERR_ALLOC, "ea_relation_create: cudaMalloc(%zu) failed: %s", r->bytes,
-                             cudaGetErrorString(e));
+            return st;
         }
         r->owned = true;
     }
@@ -389,7 +444,7 @@ ea_status ea_relation_create(ea_dtype dtype, int rank, const int64_t *dims, cons
 ea_status ea_relation_destroy(ea_relation rel) {
     t_err[0] = 0;
     if (!rel) return EA_OK;
-    if (rel->owned && rel->arena) cudaFree(rel->arena);
+    if (rel->owned && rel->arena) dev_free(rel->arena, rel->release);
     delete rel;
     return EA_OK;
 }

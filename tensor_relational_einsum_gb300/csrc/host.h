@@ -10,6 +10,15 @@
 
 #include "ea_internal.h"
 
+namespace ea {
+// How to release a block of device memory the library took: through the
+// allocator pair that was current when it was taken (fn == NULL: cudaFree).
+struct DevFree {
+    ea_free_fn fn = nullptr;
+    void *ctx = nullptr;
+};
+}  // namespace ea
+
 struct ea_relation_s {
     int dtype = 0;
     int rank = 0;
@@ -20,11 +29,16 @@ struct ea_relation_s {
     char *arena = nullptr;
     size_t bytes = 0;
     bool owned = false;
+    ea::DevFree release;  // owned arenas: how to free them
 };
 
 namespace ea {
 
 ea_status set_error(ea_status code, const char *fmt, ...);
+// Device memory through the allocator of ea_set_allocator (else cudaMalloc);
+// *rel receives the matching release.  EA_ERR_ALLOC on failure.
+ea_status dev_alloc(size_t bytes, void **ptr, DevFree *rel, const char *what);
+void dev_free(void *ptr, const DevFree &rel);
 ea_status cuda_error(cudaError_t e, const char *what);
 size_t elem_size(int dtype);
 

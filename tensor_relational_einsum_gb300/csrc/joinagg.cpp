@@ -56,12 +56,9 @@ std::unordered_map<std::string, DevPlan *> g_cache;
 
 ea_status upload(const Blob &b, cudaStream_t st, DevPlan *p) {
     p->bytes = b.h.size();
-    cudaError_t e = cudaMalloc((void **)&p->dev, p->bytes);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return set_error(EA_ERR_ALLOC, "plan upload: cudaMalloc(%zu): %s", p->bytes, cudaGetErrorString(e));
-    }
-    e = cudaMallocHost((void **)&p->pinned, p->bytes);
+    ea_status s = dev_alloc(p->bytes, (void **)&p->dev, &p->dev_release, "plan upload");
+    if (s) return s;
+    cudaError_t e = cudaMallocHost((void **)&p->pinned, p->bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return set_error(EA_ERR_ALLOC, "plan upload: cudaMallocHost(%zu): %s", p->bytes, cudaGetErrorString(e));
@@ -79,7 +76,7 @@ ea_status upload(const Blob &b, cudaStream_t st, DevPlan *p) {
 
 void free_plan(DevPlan *p) {
     if (!p) return;
-    if (p->dev) cudaFree(p->dev);
+    if (p->dev) dev_free(p->dev, p->dev_release);
     if (p->pinned) cudaFreeHost(p->pinned);
     if (p->ready) cudaEventDestroy(p->ready);
     delete p;

@@ -43,6 +43,7 @@ enum PlanKind { kExchange = 0, kEwise, kRowReduce, kSimt, kTc, kAttn, kExchangeA
 struct DevPlan {
     int kind = 0;
     char *dev = nullptr;
+    DevFree dev_release;  // how `dev` is freed (the allocator that took it)
     char *pinned = nullptr;
     size_t bytes = 0;
     cudaEvent_t ready = nullptr;

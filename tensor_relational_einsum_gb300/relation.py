@@ -261,6 +261,35 @@ def attention(spec: str, q: Relation, k: Relation, v: Relation, scale: float = 0
     return out
 
 
+# Callbacks handed to ea_set_allocator stay referenced for the life of the
+# process: memory taken through them is released through them, possibly
+# after the allocator has been switched back.
+_allocators = []
+
+
+def use_torch_allocator(enable: bool = True):
+    """Route the library's own device memory (arenas of relations it creates
+    with no storage given, device copies of cached plans) through torch's
+    caching allocator on the current stream; ``enable=False`` goes back to
+    cudaMalloc.  Relations built from Python always borrow torch storage."""
+    if not enable:
+        check_status(lib().ea_set_allocator(_abi.ALLOC_FN(), _abi.FREE_FN(), None))
+        return
+
+    def _alloc(n, ctx):
+        try:
+            return torch.cuda.caching_allocator_alloc(max(int(n), 1))
+        except Exception:  # out of memory: the library reports EA_ERR_ALLOC
+            return None
+
+    def _free(p, ctx):
+        torch.cuda.caching_allocator_delete(p)
+
+    pair = (_abi.ALLOC_FN(_alloc), _abi.FREE_FN(_free))
+    _allocators.append(pair)
+    check_status(lib().ea_set_allocator(pair[0], pair[1], None))
+
+
 def check(stream=None):
     """Synchronise the stream and raise on an asynchronous CUDA error or a
     raised device error flag."""

@@ -324,3 +324,51 @@ def test_exchange_agg_and_partials_errors_without_gpu(L):
     assert L.ea_joinagg_run(b"ij,jk->ik", hs, 2, None, 0, 1, 0, ctypes.byref(po), None, ctypes.byref(x)) == 8
     for h in (p, o, blocked, flat, wide, bf, ov, a, bb, o2, o3, o4):
         L.ea_relation_destroy(h)
+
+
+def test_set_allocator_routes_library_arenas_without_gpu(L):
+    """ea_set_allocator: relations the library creates take their arena from
+    the given allocator and give it back through the matching free, even
+    after the allocator has been switched back; a NULL or misaligned block
+    is EA_ERR_ALLOC.  ea_relation_create touches no memory, so fake device
+    addresses serve here."""
+    calls = []
+
+    def fake_alloc(n, ctx):
+        calls.append(("alloc", n))
+        return 1 << 40
+
+    def fake_free(p, ctx):
+        calls.append(("free", p))
+
+    a, f = _abi.ALLOC_FN(fake_alloc), _abi.FREE_FN(fake_free)
+    assert L.ea_set_allocator(a, _abi.FREE_FN(), None) == 7          # one of the two missing
+    assert L.ea_set_allocator(a, f, None) == 0
+    dims = (64, 32)
+    arr, keep, _ = _abi.dim_parts(dims, [2, 1])
+    h = ctypes.c_void_p()
+    assert L.ea_relation_create(0, 2, _abi.i64(dims), arr, None, ctypes.byref(h)) == 0
+    ptr, nbytes = ctypes.c_void_p(), ctypes.c_size_t()
+    assert L.ea_relation_data(h, ctypes.byref(ptr), ctypes.byref(nbytes)) == 0
+    assert ptr.value == 1 << 40 and nbytes.value == 64 * 32 * 4
+    assert calls == [("alloc", 64 * 32 * 4)]
+    assert L.ea_set_allocator(_abi.ALLOC_FN(), _abi.FREE_FN(), None) == 0   # back to cudaMalloc
+    assert L.ea_relation_destroy(h) == 0
+    assert calls[-1] == ("free", 1 << 40)                              # released by the pair that took it
+
+    def bad_alloc(n, ctx):
+        calls.append(("bad", n))
+        return (1 << 40) + 8
+
+    def null_alloc(n, ctx):
+        return None
+
+    b = _abi.ALLOC_FN(bad_alloc)
+    assert L.ea_set_allocator(b, f, None) == 0
+    h2 = ctypes.c_void_p()
+    assert L.ea_relation_create(0, 2, _abi.i64(dims), arr, None, ctypes.byref(h2)) == 5
+    assert b"aligned" in L.ea_last_error() and calls[-1] == ("free", (1 << 40) + 8)
+    n = _abi.ALLOC_FN(null_alloc)
+    assert L.ea_set_allocator(n, f, None) == 0
+    assert L.ea_relation_create(0, 2, _abi.i64(dims), arr, None, ctypes.byref(h2)) == 5
+    assert L.ea_set_allocator(_abi.ALLOC_FN(), _abi.FREE_FN(), None) == 0

@@ -56,6 +56,12 @@ def test_exchange_bit_exact(dtype, dims, src, dst):
     assert np.array_equal(arena_bits(X).view(flat.dtype), want_dst)
     back = exchange(X, src)
     assert np.array_equal(arena_bits(back).view(flat.dtype), want_src)
+    # composition: src -> dst -> a third tiling equals src -> the third tiling
+    third = [[0, n // 3, n] if n >= 3 else 1 for n in dims]
+    via = exchange(X, third)
+    direct = exchange(R, third)
+    assert np.array_equal(arena_bits(via), arena_bits(direct))
+    assert np.array_equal(arena_bits(direct).view(flat.dtype), oracle.exchange(flat, dims, whole, bounds_of(dims, third)))
 
 
 # ------------------------------------------------------- fp32 contraction (C1)
