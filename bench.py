@@ -674,7 +674,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-tokens", type=int, default=128,
+    ap.add_argument("--cpu-tokens", type=int, default=192,
                     help="tokens of the oracle's CPU-baseline sample (about 10-15 s on 16 cores)")
     ap.add_argument("--ref-tokens", type=int, default=32,
                     help="tokens per step of the reference arm (the oracle), so K + W steps end in minutes")

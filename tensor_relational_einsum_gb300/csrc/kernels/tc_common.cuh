@@ -50,9 +50,11 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
 
 // Wait for the phase of `parity` to complete.  Gives up (returns false) when
 // another role has aborted, or after `limit` ns, raising the abort flag and
-// the device error word with `code`.
-static __device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort, int *err, int code,
-                                       uint64_t limit = kTimeoutNs, bool watch_abort = true) {
+// the device error word with `code`.  Inlined: as a called function the wait
+// cost its caller some 400 cycles of register saves and restores even when
+// the phase had long completed, which stalled the single MMA-issuing thread.
+static __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort, int *err,
+                                                 int code, uint64_t limit = kTimeoutNs, bool watch_abort = true) {
     if (mbar_try(b, parity)) return true;
     const uint64_t t0 = gtime();
     for (uint32_t i = 1;; i++) {
