@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define EA_ABI_VERSION 3
+#define EA_ABI_VERSION 4
 
 typedef int ea_status;
 #define EA_OK 0
@@ -131,7 +131,13 @@ typedef struct {
  *              positions packed end to end); the elementwise join requires
  *              values below rope_npos.
  *   rope_table ROPE: device pointer, fp32 [rope_npos][d/2][2] = (cos, sin)
- *              of angle pos * theta^(-2i/d).  Not owned.
+ *              of angle pos * theta^(-2i/d) (rope_layout 0), or
+ *              [d/2][rope_npos][2] (rope_layout 1, pair-major: consecutive
+ *              positions of one pair are adjacent, which a contraction's
+ *              epilogue, one row per thread, reads coalesced).  Not owned.
+ *   rope_layout ROPE: 0 or 1 as above; the elementwise ROPE join takes 0
+ *              only (EA_ERR_UNSUPPORTED otherwise), any other value is
+ *              EA_ERR_ARG.
  *   rope_dim   ROPE: d, the period of the pairs along the last letter (the
  *              head dimension when that letter merges heads and head dims);
  *              0 = the last letter's extent.
@@ -195,7 +201,7 @@ typedef struct {
     int32_t rope_dim;
     ea_relation row_rms;
     int32_t partials;
-    int32_t reserved1;
+    int32_t rope_layout;
 } ea_opts;
 
 /* ------------------------------------------------------------ basics */

@@ -44,7 +44,7 @@ class Opts(ctypes.Structure):
                 ("epi_pair", ctypes.c_char), ("rope_table", ctypes.c_void_p), ("rope_npos", ctypes.c_int64),
                 ("out2", ctypes.c_void_p), ("epi_in", ctypes.c_void_p), ("epi_map", ctypes.c_int32),
                 ("rope_dim", ctypes.c_int32), ("row_rms", ctypes.c_void_p), ("partials", ctypes.c_int32),
-                ("reserved1", ctypes.c_int32)]
+                ("rope_layout", ctypes.c_int32)]
 
 
 class AttnOpts(ctypes.Structure):
@@ -103,7 +103,7 @@ def lib():
                      "ea_overlay_atoms", "ea_last_plan", "ea_exchange_noalloc", "ea_attention_run", "ea_exchange_agg",
                      "ea_set_allocator"):
             getattr(L, name).restype = ctypes.c_int
-        if L.ea_abi_version() != 3:
+        if L.ea_abi_version() != 4:
             raise ImportError("libea.so ABI version mismatch")
         _lib = L
         return _lib

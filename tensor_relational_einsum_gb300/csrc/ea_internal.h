@@ -225,9 +225,10 @@ struct TcParams {
     const char *epi_in;                // epi 1: the joined relation's arena (output dtype)
     const float *row_rms;              // row scale rsqrt(row_rms[global row] + eps), or null
     float eps;
-    const float *rope_table;           // epi 3: [rope_npos][rope_half][2] = (cos, sin)
+    const float *rope_table;           // epi 3: [rope_npos][rope_half][2] = (cos, sin), or pair-major
     int64_t rope_npos;
     int32_t rope_half;                 // pairs per period along the columns
+    int32_t rope_pm;                   // table pair-major: [rope_half][rope_npos][2]
     int *err;
 };
 cudaError_t launch_contract_tc(const TcParams &p, int num_sms, cudaStream_t st);

@@ -207,6 +207,7 @@ struct JoinCtx {
     int epi_map;                 // epilogue join of a contraction: 0, EA_MAP_ADD or EA_MAP_SILU_MUL
     const ea_relation_s *epi_in; // EA_MAP_ADD: the joined relation (output's extents and tiling)
     int rope_dim;                // ROPE: pair period along the last letter (0 = its extent)
+    int rope_layout;             // ROPE table: 0 position-major, 1 pair-major
     const ea_relation_s *row_rms;  // contraction row scale rsqrt(row_rms[row] + eps), or null
     char row_letter;             // the output letter of input 0 only (rows of the contraction)
     char copy_letter;            // partials: the letter of the copies (leading output letter), or 0
@@ -904,6 +905,7 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
     q.rope_table = j.rope_table;
     q.rope_npos = j.rope_npos;
     q.rope_half = (int32_t)((j.rope_dim ? j.rope_dim : j.lt.t[j.sp.out.back() - 'a'].extent) / 2);
+    q.rope_pm = j.rope_layout;
     q.err = c->err;
     return EA_OK;
 }
@@ -1224,6 +1226,10 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
     j.pred_hi = o.pred_hi;
     j.rope_table = o.rope_table;
     j.rope_npos = o.rope_npos;
+    j.rope_layout = o.rope_layout;
+    if (o.rope_layout != 0 && o.rope_layout != 1) return set_error(EA_ERR_ARG, "rope_layout must be 0 or 1");
+    if (map == EA_MAP_ROPE && o.rope_layout != 0)
+        return set_error(EA_ERR_UNSUPPORTED, "the elementwise ROPE join reads a position-major table (rope_layout 0)");
     j.rope_pos = o.rope_pos;
     j.rope_dim = o.rope_dim;
     j.out2 = agg == EA_AGG_MAX_SUMEXP ? o.out2 : nullptr;
@@ -1458,6 +1464,7 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
     key.v(j.rope_pos);
     key.v(j.rope_table);
     key.v(j.rope_npos);
+    key.v(j.rope_layout);
     if (j.out2) key.rel(j.out2);
     key.v(j.epi_map);
     key.v(j.epi_pair);

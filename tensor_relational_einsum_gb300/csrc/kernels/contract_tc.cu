@@ -301,13 +301,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                 if (p.epi == 3 && T.m0 + ep < G.m_ext) {
                     // epilogue join ROPE: rotate the interleaved column pairs of this row
                     // by the angles of its position (rows = positions, packed sequences)
+                    // (a pair-major table puts the warp's 32 consecutive positions
+                    // of one pair side by side: one 256-byte read per pair)
                     const int64_t pos = (G.r_lo + T.m0 + ep) % p.rope_npos;
-                    const float2 *tab = reinterpret_cast<const float2 *>(p.rope_table) + pos * p.rope_half;
+                    const float2 *tab = reinterpret_cast<const float2 *>(p.rope_table) +
+                                        (p.rope_pm ? pos : pos * p.rope_half);
+                    const int64_t pstride = p.rope_pm ? p.rope_npos : 1;
                     int ip = (int)(((G.c_lo + T.n0 + c0) >> 1) % p.rope_half);
 #pragma unroll
                     for (int q = 0; q < 32; q++) {
                         if (2 * q < CW) {
-                            const float2 cs = __ldg(tab + ip);
+                            const float2 cs = __ldg(tab + ip * pstride);
                             const float x0 = v[2 * q], x1 = v[2 * q + 1];
                             v[2 * q] = x0 * cs.x - x1 * cs.y;
                             v[2 * q + 1] = x0 * cs.y + x1 * cs.x;

@@ -334,6 +334,7 @@ class LlamaBlock:
             self.qr = Relation("bf16", hd, attn_parts, device=dev)
             self.kr = Relation("bf16", hd, attn_parts, device=dev)
         self.table = rope_table(s, self.dh, theta, device=dev)
+        self.table_pm = self.table.transpose(0, 1).contiguous()  # [pairs, positions, 2] for the epilogue
         self.fused_epilogues = fused_epilogues
         self.fused_attention = fused_attention
         if fused_attention:
@@ -368,8 +369,8 @@ class LlamaBlock:
         if self.fused_epilogues:
             c("norm1.sumsq", lambda: joinagg("td->t", [self.x], "sum", "square", out=self.ms1, scale=1.0 / self.D))
             c("qkv", lambda: joinagg("td,dce->cte", [self.x, self.wqk], "sum", "product", out=self.qk_out,
-                                     epi_map="rope", rope_table=self.table, rope_pos="t", rope_dim=self.dh,
-                                     row_rms=self.ms1, eps=self.eps))
+                                     epi_map="rope", rope_table=self.table_pm, rope_layout=1, rope_pos="t",
+                                     rope_dim=self.dh, row_rms=self.ms1, eps=self.eps))
             c("qkv.v", lambda: joinagg("td,de->te", [self.x, self.wv], "sum", "product", out=self.v_out,
                                        row_rms=self.ms1, eps=self.eps))
         else:

@@ -181,14 +181,15 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
             parts: dict | None = None, rope_table: torch.Tensor | None = None, rope_pos: str | None = None,
             out2: Relation | None = None, epi_map: str | None = None, epi_in: Relation | None = None,
             epi_pair: str | None = None, rope_dim: int = 0, row_rms: Relation | None = None,
-            partials: bool = False, stream=None) -> Relation:
+            partials: bool = False, rope_layout: int = 0, stream=None) -> Relation:
     """Run one join-agg ("Every Kernel Is a Join", Definition 3.7) with
     libea.so.  ``pred="ts"`` keeps joined tuples with t <= s.  With
     ``agg="max_sumexp"`` the output receives the MAX and ``out2`` the SUM
     of exp(value - max).  A contraction may fuse an elementwise join into
     its epilogue: ``epi_map="add", epi_in=R`` stores value + R;
     ``epi_map="rope"`` rotates the output's column pairs (``rope_table``,
-    ``rope_pos`` the row letter, pairs of period ``rope_dim``);
+    ``rope_pos`` the row letter, pairs of period ``rope_dim``; a table
+    [pairs, positions, 2] with ``rope_layout=1``);
     ``row_rms=ms`` multiplies every row r by rsqrt(ms[r] + eps) first;
     ``epi_map="silu_mul", epi_pair="c"`` plans letter c (extent 2, second
     input only) as the innermost output letter and stores SiLU(c=0) * (c=1).
@@ -211,9 +212,10 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
         o.pred_lo, o.pred_hi = pred[0].encode(), pred[1].encode()
     if rope_table is not None:
         o.rope_table = rope_table.data_ptr()
-        o.rope_npos = rope_table.shape[0]
+        o.rope_npos = rope_table.shape[1] if rope_layout == 1 else rope_table.shape[0]
         o.rope_pos = rope_pos.encode()
         o.rope_dim = rope_dim
+        o.rope_layout = rope_layout
     if out2 is not None:
         o.out2 = out2.handle.value
     if row_rms is not None:

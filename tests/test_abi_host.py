@@ -29,7 +29,7 @@ def test_exports_every_declared_symbol(L):
     assert {"ea_relation_create", "ea_joinagg_run", "ea_exchange"} <= names
     for n in sorted(names):
         assert hasattr(L, n), n
-    assert L.ea_abi_version() == 3
+    assert L.ea_abi_version() == 4
 
 
 def plan(L, spec, shapes, parts, pred=None):
@@ -372,3 +372,23 @@ def test_set_allocator_routes_library_arenas_without_gpu(L):
     assert L.ea_set_allocator(n, f, None) == 0
     assert L.ea_relation_create(0, 2, _abi.i64(dims), arr, None, ctypes.byref(h2)) == 5
     assert L.ea_set_allocator(_abi.ALLOC_FN(), _abi.FREE_FN(), None) == 0
+
+
+def test_rope_layout_errors_without_gpu(L):
+    """rope_layout: 0 or 1 (else EA_ERR_ARG); the elementwise ROPE join
+    reads only the position-major table (EA_ERR_UNSUPPORTED for 1)."""
+    BF = 1
+    _, x = _fake_rel(L, BF, (4, 64, 2, 128), [1, 1, 1, 1], 1 << 24)
+    _, y = _fake_rel(L, BF, (4, 64, 2, 128), [1, 1, 1, 1], 1 << 26)
+    hs = (ctypes.c_void_p * 1)(x.value)
+    out = ctypes.c_void_p(y.value)
+    o = _abi.Opts()
+    o.rope_table = 1 << 28
+    o.rope_npos = 64
+    o.rope_pos = b"s"
+    o.rope_layout = 2
+    assert L.ea_joinagg_run(b"bshd->bshd", hs, 1, None, 0, 0, 9, ctypes.byref(o), None, ctypes.byref(out)) == 7
+    o.rope_layout = 1
+    assert L.ea_joinagg_run(b"bshd->bshd", hs, 1, None, 0, 0, 9, ctypes.byref(o), None, ctypes.byref(out)) == 8
+    for h in (x, y):
+        L.ea_relation_destroy(h)

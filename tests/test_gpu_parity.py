@@ -214,17 +214,21 @@ def test_tc_epilogue_silu_pairs_clustered_sampled_rows():
     assert rel_frob(got, want) <= BF16_TOL
 
 
-def test_tc_epilogue_rope():
+@pytest.mark.parametrize("layout", [0, 1])
+def test_tc_epilogue_rope(layout):
     # Q,K projection with RoPE in the epilogue: 2 sequences x 160 positions
-    # (tokens in one block per sequence), 2 heads of 128, model dim 128 in 2 blocks
+    # (tokens in one block per sequence), 2 heads of 128, model dim 128 in 2
+    # blocks; the table position-major (layout 0) or pair-major (layout 1)
     from tensor_relational_einsum_gb300.graphs import rope_table
     S, NS, H, DH, DM = 160, 2, 2, 128, 128
     T, E = NS * S, H * DH
     x = synth.make("bf16", (T, DM), "normal", 71, 0, 1)
     w = synth.make("bf16", (DM, 2, E), "normal", 72, 0, 0.1)
     tab = rope_table(S, DH, 10000.0)
+    if layout == 1:
+        tab = tab.transpose(0, 1).contiguous()
     out = joinagg("td,dce->cte", [rel(x, [NS, 2]), rel(w, [2, 2, 1])], epi_map="rope", rope_table=tab, rope_pos="t",
-                  rope_dim=DH)
+                  rope_dim=DH, rope_layout=layout)
     assert last()["kernel"] == "contract_tc"
     got = dense64(out)
     for c in range(2):
