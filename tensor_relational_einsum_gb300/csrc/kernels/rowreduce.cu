@@ -63,6 +63,28 @@ struct RrBatch {
     static constexpr int U = (128 / BYTES) / (NS > 0 ? NS : 1) > 0 ? (128 / BYTES) / (NS > 0 ? NS : 1) : 1;
 };
 
+// Packed two-wide fp32 arithmetic (one instruction for two values).
+__device__ __forceinline__ uint64_t pk2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ float pk2_sum(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo + hi;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 template <int MAP, int AGG, int NIN, int MASK, int DT>
 __device__ __forceinline__ void rr_seg(const RrParams &p, Acc &acc, const int64_t *ioff, const int64_t *iinn,
                                        const float *bc, int64_t len, int64_t cmin, int64_t cmax, bool vec, int sl,
@@ -74,6 +96,40 @@ __device__ __forceinline__ void rr_seg(const RrParams &p, Acc &acc, const int64_
     const int mask = MASK < 0 ? (p.stream_mask | 1) : MASK;
     const bool whole = cmin <= 0 && cmax >= len - 1;
     const int64_t step = (int64_t)lpr * 8;  // cells between a lane's consecutive chunks
+    if constexpr (AGG == EA_AGG_SUM && (MAP == EA_MAP_SQUARE || MAP == EA_MAP_IDENTITY) && kRaw && NS == 1) {
+        // SUM of one streamed input (or of its squares) over whole rows: two
+        // cells per packed f32x2 add or FMA, four running pair-sums, the
+        // map's scale applied once to the row segment's sum
+        if (vec && whole) {
+            int k0 = 0;
+#pragma unroll
+            for (int k = 0; k < NIN; k++)
+                if ((MASK >> k) & 1) k0 = k;
+            uint64_t s2[4] = {0, 0, 0, 0};
+            for (int64_t c0 = (int64_t)sl * 8; c0 < len; c0 += step * U) {
+                uint4 raw[U][kB16 ? 1 : 2];
+#pragma unroll
+                for (int u = 0; u < U; u++) {
+                    const int64_t c = c0 + (int64_t)u * step;
+                    if (c < len) ld_raw<kB16>(p.in[k0], ioff[k0] + c, raw[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < U; u++) {
+                    if (c0 + (int64_t)u * step >= len) continue;
+                    const uint32_t *w = reinterpret_cast<const uint32_t *>(raw[u]);
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const uint64_t x2 = kB16 ? pk2(w[e] << 16, w[e] & 0xFFFF0000u) : pk2(w[2 * e], w[2 * e + 1]);
+                        if constexpr (MAP == EA_MAP_SQUARE) s2[e] = ffma2(x2, x2, s2[e]);
+                        else s2[e] = fadd2(s2[e], x2);
+                    }
+                }
+            }
+            const float srow = pk2_sum(fadd2(fadd2(s2[0], s2[1]), fadd2(s2[2], s2[3])));
+            acc.a += MAP == EA_MAP_SQUARE ? p.scale * srow : srow;
+            return;
+        }
+    }
     if (vec) {
         for (int64_t c0 = (int64_t)sl * 8; c0 < len; c0 += step * U) {
             uint4 raw[kRaw ? U : 1][kRaw ? NS : 1][kB16 ? 1 : 2];
@@ -161,8 +217,11 @@ __device__ __forceinline__ void rr_seg(const RrParams &p, Acc &acc, const int64_
     }
 }
 
+template <int AGG, int MAP, int MASK>
+struct RrMinBlocks;
+
 template <int AGG, int MAP, int NIN, int MASK, int DT>
-__global__ void __launch_bounds__(kThreads, 3) rowreduce_kernel(const RrParams p) {
+__global__ void __launch_bounds__(kThreads, (RrMinBlocks<AGG, MAP, MASK>::value)) rowreduce_kernel(const RrParams p) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int mask = MASK < 0 ? (p.stream_mask | 1) : MASK;
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
@@ -259,8 +318,17 @@ struct TileItem {
     int32_t vec;
 };
 
+// Resident CTAs per SM the register budget is sized for: the packed SUM
+// path (one streamed input, whole rows) keeps eight 16-byte chunks per lane
+// in flight plus its pair-sums, which fits 128 registers but not 80.
+template <int AGG, int MAP, int MASK>
+struct RrMinBlocks {
+    static constexpr int value =
+        (AGG == EA_AGG_SUM && (MAP == EA_MAP_SQUARE || MAP == EA_MAP_IDENTITY) && MASK == 1) ? 2 : 3;
+};
+
 template <int AGG, int MAP, int NIN, int MASK, int DT>
-__global__ void __launch_bounds__(kThreads, 3) rowreduce_tile_kernel(const RrParams p) {
+__global__ void __launch_bounds__(kThreads, (RrMinBlocks<AGG, MAP, MASK>::value)) rowreduce_tile_kernel(const RrParams p) {
     __shared__ TileItem<NIN> ti[kTileItems];
     __shared__ int64_t s_out0, s_ostr;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
