@@ -28,10 +28,11 @@
 // Each K and V tile is loaded once for both, and while one warpgroup works
 // on its scores the tensor cores run the other's products.
 //
-// Roles (320 threads, one CTA per SM, persistent over its list of items):
-//   warp 8     TMA: Q tiles (one buffer per X), K and V tiles into rings of
-//              two and three stages (128-byte swizzle, one [128 x 64] box per
-//              64 head-dim columns).
+// Roles (384 threads, one CTA per SM, persistent over its list of items;
+// warps 10 and 11 only complete the third warpgroup of the register split):
+//   warp 8     TMA: Q tiles (one buffer per X), K and V of a key tile into
+//              one stage of a two-stage ring with one barrier (128-byte
+//              swizzle, one [128 x 64] box per 64 head-dim columns).
 //   warp 9     TMEM owner and MMA issuer (one thread).  Per X and key tile
 //              j: S_X = Q_X K_j^T; after the softmax of X has written P_X,
 //              O_X (+)= P_X V_j with P_X read from TMEM, then at once
@@ -60,15 +61,24 @@ using namespace tc;
 
 constexpr int kRows = 128;  // query rows of a tile (= TMEM lanes)
 constexpr int kKeys = 128;  // keys of a key tile
-constexpr int kAtThreads = 320;
+constexpr int kAtThreads = 384;  // three warpgroups: softmax X = 0, softmax X = 1, TMA + MMA (+2 idle warps)
+// Register split (setmaxnreg): the block is launched with 168 registers a
+// thread (384 x 168 = 64512); the TMA/MMA warpgroup gives up 80 a thread
+// and the two softmax warpgroups take 40 each, so that a softmax thread keeps
+// its row of 128 scores in registers.  The split uses exactly the launch's
+// registers: 2 x 128 x 208 + 128 x 88 = 64512.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtlRegs = 88;
+constexpr int kSoftmaxRegs = 208;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kCtlRegs <= kAtThreads * kLaunchRegs, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;  // first TMEM column of the output accumulators
 constexpr float kLazy = 16.0f;   // log2 of the largest exponential taken against a stale maximum
-constexpr int kVStages = 3;      // V ring depth (K: two stages)
+constexpr int kKvStages = 2;     // K/V ring depth: stage s holds K and V of one key tile
 
 struct AtCtl {
     uint64_t q_full[2], q_empty[2];
-    uint64_t k_full[2], k_empty[2], v_full[3], v_empty[3];
+    uint64_t kv_full[kKvStages], kv_empty[kKvStages];
     uint64_t s_full[2], p_full[2], o_fin[2];
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -80,9 +90,9 @@ struct AtCfg {
     static constexpr int CH = D / 64;            // 64-column (128-byte) chunks of the head dimension
     static constexpr int TILE = kRows * D * 2;   // one [128 x D] bf16 tile
     static constexpr int Q_OFF = 0;              // Q_0, Q_1
-    static constexpr int K_OFF = 2 * TILE;       // two K stages
-    static constexpr int V_OFF = 4 * TILE;       // three V stages
-    static constexpr int CTL_OFF = 7 * TILE;
+    static constexpr int K_OFF = 2 * TILE;       // K of each K/V stage
+    static constexpr int V_OFF = 2 * TILE + kKvStages * TILE;  // V of each K/V stage
+    static constexpr int CTL_OFF = 2 * TILE + 2 * kKvStages * TILE;
     static constexpr int SMEM = 1024 + CTL_OFF + (int)sizeof(AtCtl);
 };
 
@@ -161,15 +171,13 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
         for (int b = 0; b < 2; b++) {
             mbar_init(&ctl->q_full[b], 1);
             mbar_init(&ctl->q_empty[b], 1);
-            mbar_init(&ctl->k_full[b], 1);
-            mbar_init(&ctl->k_empty[b], 1);
             mbar_init(&ctl->s_full[b], 1);
             mbar_init(&ctl->p_full[b], 4);
             mbar_init(&ctl->o_fin[b], 1);
         }
-        for (int b = 0; b < kVStages; b++) {
-            mbar_init(&ctl->v_full[b], 1);
-            mbar_init(&ctl->v_empty[b], 1);
+        for (int b = 0; b < kKvStages; b++) {
+            mbar_init(&ctl->kv_full[b], 1);
+            mbar_init(&ctl->kv_empty[b], 1);
         }
         mbar_init(&ctl->mma_done, 1);
         ctl->abort = 0;
@@ -182,29 +190,15 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
+    if (warp >= 8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
     if (warp == 8) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            // K and V of tile t in that order: O += P V of tile t comes just
-            // before S = Q K^T of tile t + 1 on the tensor pipe.
+            // K and V of key tile t into stage t % kKvStages, one barrier for
+            // both: the stage is released once O += P V of tile t is done.
             uint32_t ct = 0, qx[2] = {0, 0};  // key tiles; items per query slot
-            uint32_t q_armed = 0, q_par = 0, k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
-            const CUtensorMap *pv_map = nullptr;  // V block of the tile being loaded
-            int pv_c1 = 0, pv_c2 = 0, pv_c3 = 0;
+            uint32_t q_armed = 0, q_par = 0, kv_armed = 0, kv_par = 0;
             bool ok = true;
-            auto load_v = [&](uint32_t t) -> bool {
-                const int st = t % kVStages;
-                const uint32_t ph = (t / kVStages) & 1;
-                if (!mbar_wait(&ctl->v_empty[st], ph ^ 1, abort, p.err, kDevTimeoutProducer)) return false;
-                const uint32_t vs = smem_u32(smem + C::V_OFF + st * C::TILE);
-                mbar_expect_tx(&ctl->v_full[st], C::TILE);
-#pragma unroll
-                for (int c = 0; c < C::CH; c++)
-                    tma_load_4d(vs + c * (kKeys * 128), pv_map, &ctl->v_full[st], 64 * c, pv_c1, pv_c2, pv_c3);
-                v_armed |= 1u << st;
-                v_par = (v_par & ~(1u << st)) | (ph << st);
-                return true;
-            };
             for (int ii = i0; ii < i1 && ok; ii++) {
                 const AtItem &it = p.items[ii];
                 const int ntiles = it.ntiles, nq = it.nq;
@@ -229,9 +223,9 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                     const AtRun R = p.runs[r];
                     const CUtensorMap *km = maps + R.k_map, *vm = maps + R.k_map + p.n_kv;
                     for (int k = 0; k < R.ntiles; k++) {
-                        const int st = ct & 1;
-                        const uint32_t ph = (ct >> 1) & 1;
-                        if (!mbar_wait(&ctl->k_empty[st], ph ^ 1, abort, p.err, kDevTimeoutProducer)) {
+                        const int st = ct % kKvStages;
+                        const uint32_t ph = (ct / kKvStages) & 1;
+                        if (!mbar_wait(&ctl->kv_empty[st], ph ^ 1, abort, p.err, kDevTimeoutProducer)) {
                             ok = false;
                             break;
                         }
@@ -240,32 +234,26 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                         const int c2 = R.k_c[1] + (R.pos_slot == 1 ? step : 0);
                         const int c3 = R.k_c[2] + (R.pos_slot == 2 ? step : 0);
                         const uint32_t ks = smem_u32(smem + C::K_OFF + st * C::TILE);
-                        mbar_expect_tx(&ctl->k_full[st], C::TILE);
+                        const uint32_t vs = smem_u32(smem + C::V_OFF + st * C::TILE);
+                        mbar_expect_tx(&ctl->kv_full[st], 2 * C::TILE);
 #pragma unroll
                         for (int c = 0; c < C::CH; c++)
-                            tma_load_4d(ks + c * (kKeys * 128), km, &ctl->k_full[st], 64 * c, c1, c2, c3);
-                        k_armed |= 1u << st;
-                        k_par = (k_par & ~(1u << st)) | (ph << st);
-                        pv_map = vm;
-                        pv_c1 = c1;
-                        pv_c2 = c2;
-                        pv_c3 = c3;
-                        if (!load_v(ct)) {
-                            ok = false;
-                            break;
-                        }
+                            tma_load_4d(ks + c * (kKeys * 128), km, &ctl->kv_full[st], 64 * c, c1, c2, c3);
+#pragma unroll
+                        for (int c = 0; c < C::CH; c++)
+                            tma_load_4d(vs + c * (kKeys * 128), vm, &ctl->kv_full[st], 64 * c, c1, c2, c3);
+                        kv_armed |= 1u << st;
+                        kv_par = (kv_par & ~(1u << st)) | (ph << st);
                         ct++;
                     }
                 }
             }
             if (*abort) {
                 // Let our own copies land before the CTA can exit.
-                for (int s = 0; s < 2; s++) {
+                for (int s = 0; s < 2; s++)
                     if (q_armed & (1u << s)) mbar_wait(&ctl->q_full[s], (q_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
-                    if (k_armed & (1u << s)) mbar_wait(&ctl->k_full[s], (k_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
-                }
-                for (int s = 0; s < kVStages; s++)
-                    if (v_armed & (1u << s)) mbar_wait(&ctl->v_full[s], (v_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
+                for (int s = 0; s < kKvStages; s++)
+                    if (kv_armed & (1u << s)) mbar_wait(&ctl->kv_full[s], (kv_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
             }
         }
     } else if (warp == 9) {
@@ -278,7 +266,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             // S_x = Q_x K_t^T
             auto mma_s = [&](int x, uint32_t t) {
                 const uint32_t qa = smem_u32(smem + C::Q_OFF + x * C::TILE);
-                const uint32_t kb = smem_u32(smem + C::K_OFF + (t & 1) * C::TILE);
+                const uint32_t kb = smem_u32(smem + C::K_OFF + (t % kKvStages) * C::TILE);
                 const uint32_t d = tmem + (uint32_t)(x * kKeys);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++)
@@ -289,7 +277,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             };
             // O_x (+)= P_x V_t, P_x in the first 64 columns of S_x
             auto mma_o = [&](int x, uint32_t t, bool first) {
-                const uint32_t vb = smem_u32(smem + C::V_OFF + (t % kVStages) * C::TILE);
+                const uint32_t vb = smem_u32(smem + C::V_OFF + (t % kKvStages) * C::TILE);
                 const uint32_t pa = tmem + (uint32_t)(x * kKeys);
                 const uint32_t d = tmem + kOCol + (uint32_t)(x * D);
 #pragma unroll
@@ -302,7 +290,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                 const int n = it.ntiles, nq = it.nq;
                 if (n == 0) continue;
                 // first scores of the item
-                if (!mbar_wait(&ctl->k_full[ct & 1], (ct >> 1) & 1, abort, p.err, kDevTimeoutMma)) {
+                if (!mbar_wait(&ctl->kv_full[ct % kKvStages], (ct / kKvStages) & 1, abort, p.err, kDevTimeoutMma)) {
                     ok = false;
                     break;
                 }
@@ -317,12 +305,11 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                     if (n == 1) umma_commit(&ctl->q_empty[x]);
                 }
                 if (!ok) break;
-                umma_commit(&ctl->k_empty[ct & 1]);
                 for (int j = 0; j < n && ok; j++) {
                     const uint32_t t = ct + j;
                     for (int x = 0; x < nq; x++) {
-                        if (!mbar_wait(&ctl->p_full[x], (tx[x] + j) & 1, abort, p.err, kDevTimeoutMma) ||
-                            (x == 0 && !mbar_wait(&ctl->v_full[t % kVStages], (t / kVStages) & 1, abort, p.err, kDevTimeoutMma))) {
+                        // V of tile t arrived with its K (waited for before S of tile t)
+                        if (!mbar_wait(&ctl->p_full[x], (tx[x] + j) & 1, abort, p.err, kDevTimeoutMma)) {
                             ok = false;
                             break;
                         }
@@ -330,8 +317,8 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                         mma_o(x, t, j == 0);
                         if (j == n - 1) umma_commit(&ctl->o_fin[x]);
                         if (j + 1 < n) {
-                            if (x == 0 && !mbar_wait(&ctl->k_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort, p.err,
-                                                     kDevTimeoutMma)) {
+                            if (x == 0 && !mbar_wait(&ctl->kv_full[(t + 1) % kKvStages], ((t + 1) / kKvStages) & 1,
+                                                     abort, p.err, kDevTimeoutMma)) {
                                 ok = false;
                                 break;
                             }
@@ -340,8 +327,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                         }
                     }
                     if (!ok) break;
-                    umma_commit(&ctl->v_empty[t % kVStages]);
-                    if (j + 1 < n) umma_commit(&ctl->k_empty[(t + 1) & 1]);
+                    umma_commit(&ctl->kv_empty[t % kKvStages]);  // K and V of tile t are done
                 }
                 ct += n;
                 for (int x = 0; x < nq; x++) tx[x] += n;
@@ -350,7 +336,8 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             umma_commit(&ctl->mma_done);
             mbar_wait(&ctl->mma_done, 0, abort, p.err, kDevTimeoutMma, kTimeoutNs, false);
         }
-    } else {
+    } else if (warp < 8) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
         // ------------------------------------------------ softmax and output (warps 0-7)
         const int x = warp >> 2;
         const int row = threadIdx.x & (kRows - 1);
@@ -519,6 +506,13 @@ cudaError_t launch_d(const AtParams &p, cudaStream_t st) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64 && !configured[dev]) {
+        // The register split assumes the block starts with kLaunchRegs a
+        // thread: with fewer, setmaxnreg.inc would wait for registers that
+        // never come, so such a build is refused before it can launch.
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, attention_kernel<D>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
         e = cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
