@@ -317,6 +317,16 @@ def bench_components(peaks, device):
         gbs = 2 * nbytes / (med * 1e-3) / 1e9
         ex[name] = {"us": round(med * 1e3, 1), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
         del Y
+    # context: a plain device copy of the same 128 MiB (torch's copy kernel);
+    # the measured peak is taken on 2 GiB, where L2 effects vanish
+    xt = X.arena()
+    yt = torch.empty_like(xt)
+    cmed, _ = timed(lambda: yt.copy_(xt), reps=10, warm=3)
+    ccopy = 2 * nbytes / (cmed * 1e-3) / 1e9
+    for v in ex.values():
+        v["frac_of_same_size_copy"] = round(v["GB/s"] / ccopy, 3)
+    ex["same_size_device_copy_GB/s"] = round(ccopy, 1)
+    del yt
     out["exchange_bf16_8192sq_from_8x1"] = ex
     del X
 

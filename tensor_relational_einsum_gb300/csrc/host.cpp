@@ -260,6 +260,33 @@ static int interval_of(const Tiling &t, int64_t x) {
 
 static void emit_segment(XSeg seg, int nd, const int64_t *ext, const int64_t *ss, const int64_t *ds, int esize,
                          ExchangePlan *xp) {
+    // A run of 16 KiB or more, contiguous on both sides, is cut into rows of
+    // 8 KiB (plus its tail), so that its tiles hold many rows and every warp
+    // of a CTA takes part in copying it.
+    const int64_t w = 8192 / esize;
+    if (seg.inner >= 2 * w && nd < kMaxRank) {
+        const int64_t q = seg.inner / w, rem = seg.inner - q * w;
+        int64_t e2[kMaxRank + 1], s2[kMaxRank + 1], d2[kMaxRank + 1];
+        for (int i = 0; i < nd; i++) {
+            e2[i] = ext[i];
+            s2[i] = ss[i];
+            d2[i] = ds[i];
+        }
+        e2[nd] = q;
+        s2[nd] = w;
+        d2[nd] = w;
+        XSeg body = seg;
+        body.inner = w;
+        emit_segment(body, nd + 1, e2, s2, d2, esize, xp);
+        if (rem > 0) {
+            XSeg tail = seg;
+            tail.inner = rem;
+            tail.src_off += q * w;
+            tail.dst_off += q * w;
+            emit_segment(tail, nd, ext, ss, ds, esize, xp);
+        }
+        return;
+    }
     // Up to 4 outer dims fit one segment; peel the outermost otherwise.
     if (nd > 4) {
         for (int64_t i = 0; i < ext[0]; i++) {
