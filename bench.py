@@ -3,9 +3,10 @@
 
 A step is one forward pass of the LLaMA-7B-shaped block (batch 8 x 2048
 tokens, d 4096, 32 heads x 128, FFN 11008, RMSNorm, RoPE, causal
-attention, bf16) executed as a graph of join-aggs and one exchange -- every
-row of the hot path: contractions with fused SUM, MAX/SUM row reductions,
-elementwise joins, the re-blocking exchange.  ``value`` is the block's
+attention, bf16) executed as a graph of join-aggs -- contractions with
+fused SUM and epilogue joins, SUM row reductions, the fused attention
+join-agg; the end-to-end measure adds the exchanges that bring the tokens
+into the block's tiling and the output back.  ``value`` is the block's
 algorithmic TFLOP/s (projections and FFN dense, attention over the causal
 join); ``ms_per_step`` is the block forward in ms.  The other workloads
 (fp32 matmul join-agg, the attention chain, the SwiGLU FFN, the exchange

@@ -19,11 +19,12 @@ All arithmetic runs in libea.so.
                       join-agg over near-equal blocks.
 * ``LlamaBlock``      pre-norm block: RMSNorm, Q,K contraction with RoPE in its
                       epilogue and V contraction (or fused QKV then RoPE),
-                      causal attention (fused, or the chain), exchange of the attention
-                      output into the O-projection's tiling, O projection
-                      (+ residual in its epilogue), RMSNorm, SwiGLU FFN
-                      (SiLU * up and the second residual in the contraction
-                      epilogues), or the same with every join unfused.
+                      causal attention (fused, or the chain), O projection
+                      reading the attention output in place (+ residual in
+                      its epilogue), RMSNorm, SwiGLU FFN (SiLU * up and the
+                      second residual in the contraction epilogues); or the
+                      same with every join unfused and an exchange of the
+                      attention output into the O projection's tiling.
 """
 from __future__ import annotations
 
@@ -317,7 +318,9 @@ class LlamaBlock:
         else:
             wqkv = torch.stack([W["wq"], W["wk"], W["wv"]], dim=1).contiguous()     # [D, 3, D]
             self.wqkv = Relation.from_dense(wqkv, [db, 3, 1])
-        self.wo = Relation.from_dense(W["wo"].contiguous(), [db, db])
+        # the O projection contracts the whole model dim (one block) when it
+        # reads the attention output in place (fused path), else db blocks
+        self.wo = Relation.from_dense(W["wo"].contiguous(), [1 if fused_epilogues else db, db])
         self.ms1 = Relation("f32", (T,), [tb], device=dev)
         self.n1 = None if fused_epilogues else Relation("bf16", (T, D), [tb, db], device=dev)
         self.qkv = Relation("bf16", (3, T, D), [3, tb, 1], device=dev)
@@ -345,8 +348,13 @@ class LlamaBlock:
                                        qspec="bshd", kspec="bthd", vspec="bthd", ospec="bshd")
         # the attention output, seen as [T, D] in blocks of s / s_blocks tokens x all heads ...
         self.o_tok = view(self.attn.O, 0, (T, D), [b * sb, 1])
-        # ... re-blocked by the exchange into the O projection's contraction tiling
-        self.o_ex = Relation("bf16", (T, D), [tb, db], device=dev)
+        # ... re-blocked by the exchange into the O projection's contraction
+        # tiling (unfused path); with the model dim in one block the same
+        # arena is already a [T, D] relation in blocks of one sequence (the
+        # rows of all heads of a token are contiguous), which the fused path's
+        # O projection reads in place
+        self.o_ex = None if fused_epilogues else Relation("bf16", (T, D), [tb, db], device=dev)
+        self.o_rows = view(self.attn.O, 0, (T, D), [tb, 1])
         self.a = None if fused_epilogues else Relation("bf16", (T, D), [tb, db], device=dev)
         self.h = Relation("bf16", (T, D), [tb, db], device=dev)
         self.ms2 = Relation("f32", (T,), [tb], device=dev)
@@ -381,11 +389,11 @@ class LlamaBlock:
             c("rope.k", lambda: joinagg("bshd->bshd", [self.k], "none", "rope", out=self.kr, rope_table=self.table,
                                         rope_pos="s"))
         self.attn.run(rec)
-        c("exchange.attn_out", lambda: exchange(self.o_tok, None, out=self.o_ex))
         if self.fused_epilogues:
-            c("o_proj", lambda: joinagg("te,ed->td", [self.o_ex, self.wo], "sum", "product", out=self.h,
+            c("o_proj", lambda: joinagg("te,ed->td", [self.o_rows, self.wo], "sum", "product", out=self.h,
                                         epi_map="add", epi_in=self.x))
         else:
+            c("exchange.attn_out", lambda: exchange(self.o_tok, None, out=self.o_ex))
             c("o_proj", lambda: joinagg("te,ed->td", [self.o_ex, self.wo], "sum", "product", out=self.a))
             c("residual1", lambda: joinagg("td,td->td", [self.x, self.a], "none", "add", out=self.h))
         if self.fused_epilogues:
