@@ -510,19 +510,19 @@ def run_ours(args, world, rank, local, dist):
             ent["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 3)
         per_call[name] = ent
     # End to end through host buffers, pipelined as a server runs it: while
-    # step i computes on one stream, a copy stream brings in step i+1's tokens
-    # (pinned host -> device) and returns step i-1's output (device -> host),
-    # with two pinned host buffers and two device stages each way.  Every
-    # step's own copies are inside the timed region.
+    # step i computes on one stream, a copy stream loads step i+1's tokens
+    # from pinned host memory straight into the blocks of one of two input
+    # relations (strided copies, ea_relation_copy_host: no device-side
+    # re-blocking) and offloads step i-1's output relation to pinned host
+    # memory the same way.  Every step's own copies are inside the timed region.
     nbuf = 2
     x_host = [torch.empty((B * S, D), dtype=torch.bfloat16, pin_memory=True) for _ in range(nbuf)]
     xd = x_dev.cpu()
     for h in x_host:
         h.copy_(xd)
     y_host = [torch.empty((B * S, D), dtype=torch.bfloat16, pin_memory=True) for _ in range(nbuf)]
-    x_stage = [torch.empty_like(x_dev) for _ in range(nbuf)]
-    x_whole = [Relation("bf16", (B * S, D), [1, 1], storage=xs.reshape(-1)) for xs in x_stage]
-    y_whole = [Relation("bf16", (B * S, D), [1, 1], device=device) for _ in range(nbuf)]
+    x_rel = [Relation("bf16", (B * S, D), blk.x.bounds, device=device) for _ in range(nbuf)]
+    y_rel = [Relation("bf16", (B * S, D), blk.y.bounds, device=device) for _ in range(nbuf)]
     comp, copy = torch.cuda.Stream(device), torch.cuda.Stream(device)
     h2d = [torch.cuda.Event() for _ in range(nbuf)]
     done = [torch.cuda.Event() for _ in range(nbuf)]
@@ -530,28 +530,26 @@ def run_ours(args, world, rank, local, dist):
 
     def e2e_steps(n):
         with torch.cuda.stream(copy):
-            x_stage[0].copy_(x_host[0], non_blocking=True)
+            x_rel[0].copy_host(x_host[0], to_device=True, stream=copy)
             h2d[0].record(copy)
         for i in range(n):
             b = i % nbuf
-            if i + 1 < n:  # next step's tokens, once step i + 1 - nbuf has read that stage
+            if i + 1 < n:  # next step's tokens, once step i + 1 - nbuf has read that relation
                 nb_ = (i + 1) % nbuf
                 with torch.cuda.stream(copy):
                     if i + 1 >= nbuf:
                         copy.wait_event(done[nb_])
-                    x_stage[nb_].copy_(x_host[nb_], non_blocking=True)
+                    x_rel[nb_].copy_host(x_host[nb_], to_device=True, stream=copy)
                     h2d[nb_].record(copy)
             with torch.cuda.stream(comp):
                 comp.wait_event(h2d[b])
                 if i >= nbuf:
-                    comp.wait_event(d2h[b])  # step i - nbuf's output has left y_whole[b]
-                exchange(x_whole[b], None, out=blk.x)
-                blk.run()
-                exchange(blk.y, None, out=y_whole[b])
+                    comp.wait_event(d2h[b])  # step i - nbuf's output has left y_rel[b]
+                blk.run(x=x_rel[b], y=y_rel[b])
                 done[b].record(comp)
             with torch.cuda.stream(copy):
                 copy.wait_event(done[b])
-                y_host[b].copy_(y_whole[b].arena().reshape(B * S, D), non_blocking=True)
+                y_rel[b].copy_host(y_host[b], to_device=False, stream=copy)
                 d2h[b].record(copy)
 
     n_e2e = max(4, args.steps)
@@ -584,7 +582,7 @@ def run_ours(args, world, rank, local, dist):
     comps = None
     cpu = None
     if rank == 0 and not args.no_components:
-        del blk, x_dev, x_stage, x_whole, y_whole, x_host, y_host, graph
+        del blk, x_dev, x_rel, y_rel, x_host, y_host, graph
         torch.cuda.empty_cache()
         comps = bench_components(peaks, device)
         check()

@@ -263,6 +263,20 @@ ea_status ea_relation_data(ea_relation rel, void **arena, size_t *bytes);
 /* Bounds of dimension `dim` (room for nblocks + 1 values). */
 ea_status ea_relation_bounds(ea_relation rel, int dim, int32_t *nblocks, int64_t *bounds);
 
+/* Load a relation from, or offload it to, a dense row-major tensor in host
+ * memory (the pages' "load NumPy inputs ... offload"): `host` holds the
+ * relation's prod(dims) elements of its dtype in row-major order.
+ * direction EA_TO_DEVICE copies host -> the relation's blocks,
+ * EA_TO_HOST the blocks -> host.  Every block is moved with strided copies
+ * on `stream` (cudaMemcpy2DAsync, one per block and per index of its dims
+ * outside the two innermost non-merged ones), so no device-side re-blocking
+ * is needed; asynchronous with respect to the host only when `host` is
+ * pinned.  The caller keeps `host` alive until the stream has passed the
+ * copies.  Errors: EA_ERR_ARG (NULL, direction), EA_ERR_CUDA. */
+#define EA_TO_HOST 0
+#define EA_TO_DEVICE 1
+ea_status ea_relation_copy_host(ea_relation rel, void *host, int direction, void *stream);
+
 /* ------------------------------------------------------------ join-agg */
 
 /* Run one join-agg (Definition 3.7) on the GPU.

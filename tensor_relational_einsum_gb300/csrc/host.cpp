@@ -468,6 +468,64 @@ ea_status ea_relation_create(ea_dtype dtype, int rank, const int64_t *dims, cons
     return EA_OK;
 }
 
+ea_status ea_relation_copy_host(ea_relation rel, void *host, int direction, void *stream) {
+    t_err[0] = 0;
+    if (!rel || (!host && rel->bytes)) return set_error(EA_ERR_ARG, "ea_relation_copy_host: NULL argument");
+    if (direction != EA_TO_HOST && direction != EA_TO_DEVICE)
+        return set_error(EA_ERR_ARG, "ea_relation_copy_host: direction must be EA_TO_HOST or EA_TO_DEVICE");
+    const int r = rel->rank;
+    const size_t es = elem_size(rel->dtype);
+    int64_t hstr[kMaxRank];  // row-major strides of the dense host tensor (elements)
+    hstr[r - 1] = 1;
+    for (int d = r - 2; d >= 0; d--) hstr[d] = hstr[d + 1] * rel->dims[d + 1];
+    cudaStream_t st = (cudaStream_t)stream;
+    char *hbase = (char *)host;
+    for (int64_t b = 0; b < rel->nblocks; b++) {
+        int64_t iv[kMaxRank], lo[kMaxRank], ext[kMaxRank];
+        block_coords(rel, b, iv);
+        block_box(rel, iv, lo, ext);
+        // k: the innermost dim the block does not span whole (or 0); the
+        // block's cells over dims k.. are then one run, contiguous in the host
+        // tensor and in the block alike
+        int k = r - 1;
+        while (k > 0 && ext[k] == rel->dims[k]) k--;
+        int64_t run = 1;
+        for (int d = k; d < r; d++) run *= ext[d];
+        if (run == 0) continue;
+        // one strided copy per index of dims < k - 1; dim k - 1 (if any) is
+        // the copy's height at the host stride of that dim
+        const int64_t height = k >= 1 ? ext[k - 1] : 1;
+        const int64_t hpitch = k >= 1 ? hstr[k - 1] : 0;
+        const int nout = k >= 1 ? k - 1 : 0;
+        int64_t nouter = 1;
+        for (int d = 0; d < nout; d++) nouter *= ext[d];
+        const size_t wbytes = (size_t)run * es;
+        char *dblock = rel->arena + rel->blk_off[b] * es;
+        for (int64_t o = 0; o < nouter; o++) {
+            int64_t rem = o, hoff = 0;
+            for (int d = nout - 1; d >= 0; d--) {
+                hoff += (lo[d] + rem % ext[d]) * hstr[d];
+                rem /= ext[d];
+            }
+            for (int d = nout; d < r; d++) hoff += lo[d] * hstr[d];
+            char *hp = hbase + hoff * es;
+            char *dp = dblock + (size_t)(o * height * run) * es;
+            cudaError_t e;
+            if (height == 1)
+                e = direction == EA_TO_DEVICE ? cudaMemcpyAsync(dp, hp, wbytes, cudaMemcpyHostToDevice, st)
+                                              : cudaMemcpyAsync(hp, dp, wbytes, cudaMemcpyDeviceToHost, st);
+            else
+                e = direction == EA_TO_DEVICE
+                        ? cudaMemcpy2DAsync(dp, wbytes, hp, (size_t)hpitch * es, wbytes, (size_t)height,
+                                            cudaMemcpyHostToDevice, st)
+                        : cudaMemcpy2DAsync(hp, (size_t)hpitch * es, dp, wbytes, wbytes, (size_t)height,
+                                            cudaMemcpyDeviceToHost, st);
+            if (e != cudaSuccess) return cuda_error(e, "ea_relation_copy_host");
+        }
+    }
+    return EA_OK;
+}
+
 ea_status ea_relation_destroy(ea_relation rel) {
     t_err[0] = 0;
     if (!rel) return EA_OK;

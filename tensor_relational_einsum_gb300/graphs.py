@@ -208,8 +208,9 @@ class SwigluFFN:
         self.Y = out if out is not None else Relation("bf16", (T, D), [tb, x.bounds[1]], device=dev)
         self.T, self.D, self.F = T, D, F
 
-    def run(self, x: Relation | None = None, rec: Recorder | None = None):
+    def run(self, x: Relation | None = None, rec: Recorder | None = None, out: Relation | None = None):
         x = x or self.x
+        Y = out or self.Y
         c = rec.call if rec is not None else _direct
         if self.fused:
             c("ffn.gate_up", lambda: joinagg("td,dfc->tf", [x, self.wgu], "sum", "product", out=self.H,
@@ -218,11 +219,11 @@ class SwigluFFN:
             c("ffn.gate_up", lambda: joinagg("td,dcf->ctf", [x, self.wgu], "sum", "product", out=self.gu))
             c("ffn.silu_mul", lambda: joinagg("tf,tf->tf", [self.G, self.U], "none", "silu_mul", out=self.H))
         if self.residual is not None:
-            c("ffn.down", lambda: joinagg("tf,fd->td", [self.H, self.wd], "sum", "product", out=self.Y,
+            c("ffn.down", lambda: joinagg("tf,fd->td", [self.H, self.wd], "sum", "product", out=Y,
                                           epi_map="add", epi_in=self.residual))
         else:
-            c("ffn.down", lambda: joinagg("tf,fd->td", [self.H, self.wd], "sum", "product", out=self.Y))
-        return self.Y
+            c("ffn.down", lambda: joinagg("tf,fd->td", [self.H, self.wd], "sum", "product", out=Y))
+        return Y
 
     def flops(self) -> float:
         return 2.0 * self.T * self.D * self.F * 3
@@ -372,17 +373,22 @@ class LlamaBlock:
         c(tag + ".sumsq", lambda: joinagg("td->t", [x], "sum", "square", out=ms, scale=1.0 / self.D))
         c(tag + ".apply", lambda: joinagg("td,t,d->td", [x, ms, g], "none", "rms_apply", out=out, eps=self.eps))
 
-    def run(self, rec: Recorder | None = None):
+    def run(self, rec: Recorder | None = None, x: Relation | None = None, y: Relation | None = None):
+        """One block forward on ``x`` (default: the block's own input
+        relation) into ``y`` (default: its own output); both tiled like the
+        block's, e.g. double buffers a pipelined caller fills and drains."""
         c = rec.call if rec is not None else _direct
+        x = x or self.x
+        y = y or self.y
         if self.fused_epilogues:
-            c("norm1.sumsq", lambda: joinagg("td->t", [self.x], "sum", "square", out=self.ms1, scale=1.0 / self.D))
-            c("qkv", lambda: joinagg("td,dce->cte", [self.x, self.wqk], "sum", "product", out=self.qk_out,
+            c("norm1.sumsq", lambda: joinagg("td->t", [x], "sum", "square", out=self.ms1, scale=1.0 / self.D))
+            c("qkv", lambda: joinagg("td,dce->cte", [x, self.wqk], "sum", "product", out=self.qk_out,
                                      epi_map="rope", rope_table=self.table_pm, rope_layout=1, rope_pos="t",
                                      rope_dim=self.dh, row_rms=self.ms1, eps=self.eps))
-            c("qkv.v", lambda: joinagg("td,de->te", [self.x, self.wv], "sum", "product", out=self.v_out,
+            c("qkv.v", lambda: joinagg("td,de->te", [x, self.wv], "sum", "product", out=self.v_out,
                                        row_rms=self.ms1, eps=self.eps))
         else:
-            self.rmsnorm(self.x, self.ms1, self.g1, self.n1, c, "norm1")
+            self.rmsnorm(x, self.ms1, self.g1, self.n1, c, "norm1")
             c("qkv", lambda: joinagg("td,dce->cte", [self.n1, self.wqkv], "sum", "product", out=self.qkv))
             c("rope.q", lambda: joinagg("bshd->bshd", [self.q], "none", "rope", out=self.qr, rope_table=self.table,
                                         rope_pos="s"))
@@ -391,20 +397,20 @@ class LlamaBlock:
         self.attn.run(rec)
         if self.fused_epilogues:
             c("o_proj", lambda: joinagg("te,ed->td", [self.o_rows, self.wo], "sum", "product", out=self.h,
-                                        epi_map="add", epi_in=self.x))
+                                        epi_map="add", epi_in=x))
         else:
             c("exchange.attn_out", lambda: exchange(self.o_tok, None, out=self.o_ex))
             c("o_proj", lambda: joinagg("te,ed->td", [self.o_ex, self.wo], "sum", "product", out=self.a))
-            c("residual1", lambda: joinagg("td,td->td", [self.x, self.a], "none", "add", out=self.h))
+            c("residual1", lambda: joinagg("td,td->td", [x, self.a], "none", "add", out=self.h))
         if self.fused_epilogues:
             c("norm2.sumsq", lambda: joinagg("td->t", [self.h], "sum", "square", out=self.ms2, scale=1.0 / self.D))
-            self.ffn.run(self.h, rec)
+            self.ffn.run(self.h, rec, out=y)
         else:
             self.rmsnorm(self.h, self.ms2, self.g2, self.n2, c, "norm2")
             self.ffn.run(self.n2, rec)
         if not self.fused_epilogues:
-            c("residual2", lambda: joinagg("td,td->td", [self.h, self.ffn_out], "none", "add", out=self.y))
-        return self.y
+            c("residual2", lambda: joinagg("td,td->td", [self.h, self.ffn_out], "none", "add", out=y))
+        return y
 
     def call_bytes(self) -> dict:
         """Algorithmic bytes of each call: every input relation read once,

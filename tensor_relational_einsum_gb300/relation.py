@@ -111,6 +111,21 @@ class Relation:
         exchange(whole, None, out=self, stream=stream)
         return self
 
+    def copy_host(self, host: torch.Tensor, to_device: bool = True, stream=None) -> torch.Tensor:
+        """Load this relation from (``to_device``) or offload it to the dense
+        row-major CPU tensor ``host`` with strided copies straight between
+        host memory and the blocks (no device-side re-blocking).  Pinned host
+        memory makes the copies asynchronous on ``stream``."""
+        n = 1
+        for d in self.dims:
+            n *= d
+        if host.device.type != "cpu" or not host.is_contiguous() or host.dtype != _TORCH[self.dtype] or \
+                host.numel() != n:
+            raise ValueError("host must be a contiguous CPU tensor of the relation's dtype and size")
+        check_status(lib().ea_relation_copy_host(self.handle, ctypes.c_void_p(host.data_ptr()), 1 if to_device else 0,
+                                                 ctypes.c_void_p(_stream_ptr(stream))))
+        return host
+
     def to_dense(self) -> torch.Tensor:
         """The tensor, row-major, as a new CUDA tensor."""
         if all(len(b) == 2 for b in self.bounds):

@@ -392,3 +392,14 @@ def test_rope_layout_errors_without_gpu(L):
     assert L.ea_joinagg_run(b"bshd->bshd", hs, 1, None, 0, 0, 9, ctypes.byref(o), None, ctypes.byref(out)) == 8
     for h in (x, y):
         L.ea_relation_destroy(h)
+
+
+def test_copy_host_errors_without_gpu(L):
+    """ea_relation_copy_host checks its arguments before any copy."""
+    _, r = _fake_rel(L, 0, (8, 6), [2, 2], 1 << 24)
+    host = ctypes.create_string_buffer(8 * 6 * 4)
+    assert L.ea_relation_copy_host(None, host, 1, None) == 7
+    assert L.ea_relation_copy_host(r, None, 1, None) == 7
+    assert L.ea_relation_copy_host(r, host, 2, None) == 7
+    assert L.ea_relation_copy_host(r, host, -1, None) == 7
+    L.ea_relation_destroy(r)

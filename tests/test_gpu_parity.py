@@ -380,3 +380,35 @@ def test_rowreduce_causal_predicate():
 def test_no_device_error_raised():
     from tensor_relational_einsum_gb300.relation import check
     check()
+
+
+# ----------------------------------------------------- host load / offload
+
+@pytest.mark.parametrize("dtype,dims,parts", [
+    ("bf16", (300, 200), [[0, 100, 300], [0, 72, 200]]),
+    ("f32", (64, 8192), [4, 1]),
+    ("bf16", (3, 5, 7, 9), [3, 1, 7, 1]),
+    ("f32", (2, 64, 4, 128), [2, 4, 2, 1]),
+    ("bf16", (1000,), [[0, 7, 1000]]),
+])
+def test_copy_host_bit_exact(dtype, dims, parts):
+    """A relation loaded from a dense host tensor holds the oracle's arena
+    of that tensor bit for bit, and offloading it gives the tensor back."""
+    from tensor_relational_einsum_gb300.relation import Relation
+    t = synth.make(dtype, dims, "uniform", 91, -1, 1)
+    if dtype == "bf16":
+        host = torch.from_numpy(t.host.view(np.int16).copy()).view(torch.bfloat16).reshape(dims)
+    else:
+        host = torch.from_numpy(t.host.copy()).reshape(dims)
+    host = host.contiguous().pin_memory()
+    R = Relation(dtype, dims, parts, device="cuda")
+    R.copy_host(host, to_device=True)
+    torch.cuda.synchronize()
+    flat = t.host.reshape(-1)
+    want = oracle.exchange(flat, dims, [[0, n] for n in dims], bounds_of(dims, parts))
+    assert np.array_equal(arena_bits(R).view(flat.dtype), want)
+    back = torch.empty_like(host).pin_memory()
+    R.copy_host(back, to_device=False)
+    torch.cuda.synchronize()
+    bits = (lambda x: x.view(torch.int16)) if dtype == "bf16" else (lambda x: x.view(torch.int32))
+    assert torch.equal(bits(back), bits(host))
