@@ -378,31 +378,35 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                         break;
                     }
                     tc_fence_after();
+                    // the scores, with the maximum of each 32 of them from the load
                     uint32_t u[kKeys];
-                    tmem_ld32(srow, u);
-                    tmem_ld32(srow + 32, u + 32);
-                    tmem_ld32(srow + 64, u + 64);
-                    tmem_ld32(srow + 96, u + 96);
+                    float hm0, hm1, hm2, hm3;
+                    tmem_ld32_max(srow, u, hm0);
+                    tmem_ld32_max(srow + 32, u + 32, hm1);
+                    tmem_ld32_max(srow + 64, u + 64, hm2);
+                    tmem_ld32_max(srow + 96, u + 96, hm3);
                     tmem_wait_ld();
 
                     const int64_t t0 = R.t_glob0 + (int64_t)kKeys * k;
                     const int nv = min(kKeys, R.nkeys - kKeys * k);
                     const int jlo = (int)max64(0, min64(kKeys, lo_t - t0));
                     const int jhi = (int)max64(-1, min64(nv - 1, hi_t - t0));
+                    float mx = fmaxf(max3(hm0, hm1, hm2), hm3);
                     if (jlo > 0 || jhi < kKeys - 1) {
+                        // a masked tile: drop the removed keys and take the maximum again
 #pragma unroll
                         for (int q = 0; q < kKeys; q++)
                             if (q < jlo || q > jhi) u[q] = __float_as_uint(-INFINITY);
-                    }
-                    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+                        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-                    for (int q = 0; q < kKeys; q += 8) {
-                        mx0 = max3(mx0, __uint_as_float(u[q]), __uint_as_float(u[q + 1]));
-                        mx1 = max3(mx1, __uint_as_float(u[q + 2]), __uint_as_float(u[q + 3]));
-                        mx2 = max3(mx2, __uint_as_float(u[q + 4]), __uint_as_float(u[q + 5]));
-                        mx3 = max3(mx3, __uint_as_float(u[q + 6]), __uint_as_float(u[q + 7]));
+                        for (int q = 0; q < kKeys; q += 8) {
+                            mx0 = max3(mx0, __uint_as_float(u[q]), __uint_as_float(u[q + 1]));
+                            mx1 = max3(mx1, __uint_as_float(u[q + 2]), __uint_as_float(u[q + 3]));
+                            mx2 = max3(mx2, __uint_as_float(u[q + 4]), __uint_as_float(u[q + 5]));
+                            mx3 = max3(mx3, __uint_as_float(u[q + 6]), __uint_as_float(u[q + 7]));
+                        }
+                        mx = fmaxf(max3(mx0, mx1, mx2), mx3);
                     }
-                    const float mx = fmaxf(max3(mx0, mx1, mx2), mx3);
                     m_max = fmaxf(m_max, mx);
                     // move the reference maximum only when exponentials would pass 2^kLazy
                     float alpha = 1.f;
