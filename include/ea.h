@@ -216,6 +216,15 @@ const char *ea_last_error(void);
  * or a bounds check fails.  Returns EA_ERR_CUDA or EA_ERR_DEVICE on error. */
 ea_status ea_check(void *stream);
 
+/* Failure-detection self-test: launch a one-CTA kernel whose thread waits
+ * on an mbarrier phase that nothing completes, through the same bounded
+ * wait the tcgen05 kernels use; after `limit_us` microseconds (1 ..
+ * 1000000) the wait gives up, raises the device error word and the kernel
+ * returns.  The next ea_check on `stream` then reports EA_ERR_DEVICE
+ * ("bounded wait ran out in the wait self-test") and clears the word; the
+ * context stays usable.  Errors: EA_ERR_ARG (limit), EA_ERR_CUDA. */
+ea_status ea_selftest_wait_timeout(int64_t limit_us, void *stream);
+
 /* Free every cached plan (work lists, tensor maps).  Synchronises the
  * device first.  Plans are otherwise kept for the life of the process. */
 ea_status ea_plan_cache_clear(void);

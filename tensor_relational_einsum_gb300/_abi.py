@@ -97,12 +97,13 @@ def lib():
         L.ea_exchange_agg.argtypes = [VP, ctypes.c_int, ctypes.POINTER(DimPart), VP, ctypes.POINTER(VP)]
         L.ea_set_allocator.argtypes = [ALLOC_FN, FREE_FN, VP]
         L.ea_relation_copy_host.argtypes = [VP, VP, ctypes.c_int, VP]
+        L.ea_selftest_wait_timeout.argtypes = [ctypes.c_int64, VP]
         L.ea_attention_run.argtypes = [ctypes.c_char_p, VP, VP, VP, ctypes.POINTER(AttnOpts), VP, ctypes.POINTER(VP)]
         for name in ("ea_check", "ea_plan_cache_clear", "ea_relation_create", "ea_relation_destroy",
                      "ea_relation_info", "ea_relation_block", "ea_relation_data", "ea_relation_bounds",
                      "ea_joinagg_run", "ea_exchange", "ea_plan_worklist", "ea_exchange_permutation",
                      "ea_overlay_atoms", "ea_last_plan", "ea_exchange_noalloc", "ea_attention_run", "ea_exchange_agg",
-                     "ea_set_allocator", "ea_relation_copy_host"):
+                     "ea_set_allocator", "ea_relation_copy_host", "ea_selftest_wait_timeout"):
             getattr(L, name).restype = ctypes.c_int
         if L.ea_abi_version() != 4:
             raise ImportError("libea.so ABI version mismatch")

@@ -22,6 +22,7 @@ enum DeviceErr : int {
     kDevBounds = 4,
     kDevTimeoutSoftmax = 5,
     kDevTimeoutCorrection = 6,
+    kDevTimeoutSelftest = 7,
 };
 
 // ---------------------------------------------------------------- exchange
@@ -287,6 +288,7 @@ struct AtParams {
     int *err;
 };
 cudaError_t launch_attention(const AtParams &p, cudaStream_t st);
+cudaError_t launch_wait_timeout(int *err, uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_exchange_agg(const XSeg *segs, const XTile *tiles, int64_t ntiles, const char *src, char *dst,
                                 int dtype, int agg, int ncopies, int64_t copy_stride, int num_sms, cudaStream_t st);
 int attention_smem_bytes(int d);

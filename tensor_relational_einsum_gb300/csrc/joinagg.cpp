@@ -1552,8 +1552,22 @@ ea_status ea_check(void *stream) {
                          : flag == kDevBounds          ? "bounds check"
                          : flag == kDevTimeoutSoftmax  ? "bounded wait ran out in the attention softmax warps"
                          : flag == kDevTimeoutCorrection ? "bounded wait ran out in the attention output warps"
+                         : flag == kDevTimeoutSelftest ? "bounded wait ran out in the wait self-test (expected)"
                                                        : "unknown");
     }
+    return EA_OK;
+}
+
+ea_status ea_selftest_wait_timeout(int64_t limit_us, void *stream) {
+    set_error(EA_OK, "");
+    if (limit_us < 1 || limit_us > 1000000)
+        return set_error(EA_ERR_ARG, "ea_selftest_wait_timeout: limit_us must be in [1, 1000000]");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevCtx *c;
+    ea_status s = get_ctx(&c);
+    if (s) return s;
+    cudaError_t e = launch_wait_timeout(c->err, (uint64_t)limit_us * 1000ull, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_error(e, "ea_selftest_wait_timeout");
     return EA_OK;
 }
 

@@ -403,3 +403,8 @@ def test_copy_host_errors_without_gpu(L):
     assert L.ea_relation_copy_host(r, host, 2, None) == 7
     assert L.ea_relation_copy_host(r, host, -1, None) == 7
     L.ea_relation_destroy(r)
+
+
+def test_selftest_wait_timeout_argument_check_without_gpu(L):
+    assert L.ea_selftest_wait_timeout(0, None) == 7
+    assert L.ea_selftest_wait_timeout(2000000, None) == 7
