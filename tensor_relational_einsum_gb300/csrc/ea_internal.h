@@ -205,6 +205,8 @@ struct CtParams {
     float scale;
     int pred_mode;                     // 0 none; 1 mask n > m; 2 mask m > n
     int tile;                          // output tile edge: 64, or 32 when 64-wide tiles would leave SMs idle
+    int split;                         // fp32, 32-wide tiles, <= 4 tuples of K <= 64 per group: one warp
+                                       // group per tuple, the tuples' products summed in canonical order
 };
 cudaError_t launch_contract_simt(const CtParams &p, cudaStream_t st);
 

@@ -669,6 +669,11 @@ static ea_status build_simt(JoinCtx &j, const ContractionViews &cv, DevCtx *c, c
     q.scale = j.scale;
     q.pred_mode = mode;
     q.tile = tsz;
+    // small groups of fp32 blocks: every tuple of a group at once (split)
+    bool split = tsz == 32 && q.a_dtype == EA_F32 && q.b_dtype == EA_F32;
+    for (const CtGroup &G : groups) split = split && G.t1 - G.t0 <= 4;
+    for (const CtTuple &T : tuples) split = split && T.K <= 64;
+    q.split = split ? 1 : 0;
     return EA_OK;
 }
 
