@@ -54,7 +54,7 @@ typedef int ea_status;
 #define EA_ERR_ALLOC 5       /* device or host allocation failed                   */
 #define EA_ERR_CUDA 6        /* a CUDA runtime call failed (message has the name)  */
 #define EA_ERR_ARG 7         /* NULL pointer, bad count, bad enum value            */
-#define EA_ERR_UNSUPPORTED 8 /* valid join-agg this build has no kernel for        */
+#define EA_ERR_UNSUPPORTED 8 /* valid join-agg the library has no kernel for      */
 #define EA_ERR_DEVICE 9      /* a kernel raised the device error flag (ea_check)   */
 
 typedef struct ea_relation_s *ea_relation; /* opaque handle */
