@@ -190,6 +190,7 @@ struct RrParams {
     int stream_mask;                   // bit k: input k runs along the row (else broadcast)
     int max_items;                     // most tuples in one group
     int tile_linear;                   // 1: no tile crosses a run of the innermost row dim
+    int row_batch;                     // 1: every group has <= 4 tuples, vectorisable, of one length, no predicate
     int *err;
 };
 cudaError_t launch_rowreduce(const RrParams &p, int num_sms, cudaStream_t st);

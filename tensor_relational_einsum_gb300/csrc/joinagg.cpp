@@ -528,6 +528,12 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
     r.pred = j.pred_lo ? 1 : 0;
     r.max_items = (int)max_items;
     r.tile_linear = 1;
+    {
+        bool rb = !j.pred_lo && max_items <= 4;
+        for (const RrGroup &G : groups)
+            for (int32_t i = G.i0; i < G.i1 && rb; i++) rb = items[i].vec && items[i].len == items[G.i0].len;
+        r.row_batch = rb ? 1 : 0;
+    }
     r.stream_mask = 0;
     for (int k = 0; k < n_in; k++)
         if (sp.term[k].find(red.back()) != std::string::npos) r.stream_mask |= 1 << k;

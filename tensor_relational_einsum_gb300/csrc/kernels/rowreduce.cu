@@ -439,8 +439,90 @@ __global__ void __launch_bounds__(kThreads, (RrMinBlocks<AGG, MAP, MASK>::value)
     }
 }
 
+// SUM (or SUM of squares) of one input over rows whose segments lie in at
+// most four blocks of one length (no predicate): a warp (or a slice of one)
+// requests a row's segments in all its blocks together, 64 bytes per lane
+// per segment, then sums them -- one memory round trip per
+// batch instead of one per block.  Packed f32x2 sums; the map's scale on the
+// row's sum.
+template <int MAP, int DT>
+__global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_kernel(const RrParams p) {
+    constexpr bool kB16 = DT == 1;
+    constexpr int kRowU = kB16 ? 4 : 2;  // 64 bytes per lane per segment in flight
+    __shared__ int64_t s_off[4], s_rstr[4], s_out0, s_ostr, s_len;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        const RrTile T = p.tiles[t];
+        const RrGroup G = p.groups[T.group];
+        const int n = G.i1 - G.i0;
+        __syncthreads();
+        if (threadIdx.x < n) {
+            const EwItem &it = p.items[G.i0 + threadIdx.x];
+            int64_t cd[kViewDims];
+            decode_row(it, T.row0, cd);
+            const int last = it.nd - 1;
+            int64_t o = it.in_base[0];
+            for (int d = 0; d < it.nd; d++) o += cd[d] * it.istr[0][d];
+            s_off[threadIdx.x] = o;
+            s_rstr[threadIdx.x] = last >= 0 ? it.istr[0][last] : 0;
+            if (threadIdx.x == 0) {
+                int64_t oo = it.out_base;
+                for (int d = 0; d < it.nd; d++) oo += cd[d] * it.ostr[d];
+                s_out0 = oo;
+                s_ostr = last >= 0 ? it.ostr[last] : 0;
+                s_len = it.len;
+            }
+        }
+        __syncthreads();
+        const int64_t len = s_len, chunks = len / 8;
+        int lpb = 32;
+        while (lpb > 1 && (int64_t)lpb * kRowU > chunks) lpb /= 2;
+        const int rpb = 32 / lpb, subb = lane / lpb, slb = lane % lpb;
+        const int64_t step = (int64_t)lpb * 8;
+        const int64_t pad = (T.nrows + rpb - 1) / rpb * rpb;
+        for (int64_t rr0 = (int64_t)warp * rpb; rr0 < pad; rr0 += (int64_t)kWarps * rpb) {
+            const int64_t rr = rr0 + subb;
+            const bool live = rr < T.nrows;  // lanes past the tile still join the shuffles
+            const int64_t dr = live ? rr : T.nrows - 1;
+            uint64_t s2[4] = {0, 0, 0, 0};
+            for (int64_t c0 = (int64_t)slb * 8; c0 < len; c0 += step * kRowU) {
+                uint4 raw[4][kRowU][kB16 ? 1 : 2];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    if (i >= n) continue;
+                    const int64_t off = s_off[i] + dr * s_rstr[i];
+#pragma unroll
+                    for (int u = 0; u < kRowU; u++) {
+                        const int64_t c = c0 + (int64_t)u * step;
+                        if (c < len) ld_raw<kB16>(p.in[0], off + c, raw[i][u]);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    if (i >= n) continue;
+#pragma unroll
+                    for (int u = 0; u < kRowU; u++) {
+                        if (c0 + (int64_t)u * step >= len) continue;
+                        const uint32_t *w = reinterpret_cast<const uint32_t *>(raw[i][u]);
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            const uint64_t x2 = kB16 ? pk2(w[e] << 16, w[e] & 0xFFFF0000u) : pk2(w[2 * e], w[2 * e + 1]);
+                            if constexpr (MAP == EA_MAP_SQUARE) s2[e] = ffma2(x2, x2, s2[e]);
+                            else s2[e] = fadd2(s2[e], x2);
+                        }
+                    }
+                }
+            }
+            float a = pk2_sum(fadd2(fadd2(s2[0], s2[1]), fadd2(s2[2], s2[3])));
+            if (MAP == EA_MAP_SQUARE) a *= p.scale;
+            for (int o = lpb / 2; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if (slb == 0 && live) st_elem(p.out, p.out_dtype, s_out0 + dr * s_ostr, a);
+        }
+    }
+}
+
 template <int AGG, int MAP, int NIN, int MASK>
-cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st) {
+cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st, int num_sms) {
     int dt = -1;
     for (int k = 0; k < NIN; k++) {
         if (MASK >= 0 && !((MASK >> k) & 1)) continue;
@@ -448,6 +530,15 @@ cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st) {
         dt = dt < 0 ? d : (dt == d ? dt : 0);
     }
     const bool tile = p.tile_linear && p.max_items <= kTileItems;
+    if constexpr (AGG == EA_AGG_SUM && (MAP == EA_MAP_SQUARE || MAP == EA_MAP_IDENTITY) && NIN == 1 && MASK == 1) {
+        if (tile && p.row_batch && dt > 0) {
+            // persistent: the CTAs that fit (two per SM) loop over the tiles
+            const unsigned g2 = (unsigned)std::min<int64_t>(p.ntiles, 2 * (int64_t)num_sms);
+            if (dt == 1) rowreduce_rowbatch_kernel<MAP, 1><<<g2, kThreads, 0, st>>>(p);
+            else rowreduce_rowbatch_kernel<MAP, 2><<<g2, kThreads, 0, st>>>(p);
+            return cudaGetLastError();
+        }
+    }
     if (tile) {
         if (MASK < 0 || dt <= 0) rowreduce_tile_kernel<AGG, MAP, NIN, MASK, 0><<<(unsigned)grid, kThreads, 0, st>>>(p);
         else if (dt == 1) rowreduce_tile_kernel<AGG, MAP, NIN, MASK, 1><<<(unsigned)grid, kThreads, 0, st>>>(p);
@@ -461,10 +552,10 @@ cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st) {
 }
 
 template <int AGG>
-cudaError_t generic(const RrParams &p, int64_t grid, cudaStream_t st) {
-    if (p.n_in == 1) return go<AGG, -1, 1, -1>(p, grid, st);
-    if (p.n_in == 2) return go<AGG, -1, 2, -1>(p, grid, st);
-    return go<AGG, -1, 3, -1>(p, grid, st);
+cudaError_t generic(const RrParams &p, int64_t grid, cudaStream_t st, int num_sms) {
+    if (p.n_in == 1) return go<AGG, -1, 1, -1>(p, grid, st, num_sms);
+    if (p.n_in == 2) return go<AGG, -1, 2, -1>(p, grid, st, num_sms);
+    return go<AGG, -1, 3, -1>(p, grid, st, num_sms);
 }
 
 }  // namespace
@@ -476,17 +567,17 @@ cudaError_t launch_rowreduce(const RrParams &p, int num_sms, cudaStream_t st) {
     const int n = p.n_in, m = p.stream_mask | 1;
     switch (p.agg) {
     case EA_AGG_MAX_SUMEXP:
-        if (n == 1 && p.map == EA_MAP_IDENTITY) return go<EA_AGG_MAX_SUMEXP, EA_MAP_IDENTITY, 1, 1>(p, grid, st);
-        return generic<EA_AGG_MAX_SUMEXP>(p, grid, st);
+        if (n == 1 && p.map == EA_MAP_IDENTITY) return go<EA_AGG_MAX_SUMEXP, EA_MAP_IDENTITY, 1, 1>(p, grid, st, num_sms);
+        return generic<EA_AGG_MAX_SUMEXP>(p, grid, st, num_sms);
     case EA_AGG_MAX:
-        if (n == 1 && p.map == EA_MAP_IDENTITY) return go<EA_AGG_MAX, EA_MAP_IDENTITY, 1, 1>(p, grid, st);
-        return generic<EA_AGG_MAX>(p, grid, st);
+        if (n == 1 && p.map == EA_MAP_IDENTITY) return go<EA_AGG_MAX, EA_MAP_IDENTITY, 1, 1>(p, grid, st, num_sms);
+        return generic<EA_AGG_MAX>(p, grid, st, num_sms);
     default:
-        if (n == 1 && p.map == EA_MAP_SQUARE) return go<EA_AGG_SUM, EA_MAP_SQUARE, 1, 1>(p, grid, st);
-        if (n == 1 && p.map == EA_MAP_IDENTITY) return go<EA_AGG_SUM, EA_MAP_IDENTITY, 1, 1>(p, grid, st);
-        if (n == 2 && m == 1 && p.map == EA_MAP_EXP_SUB) return go<EA_AGG_SUM, EA_MAP_EXP_SUB, 2, 1>(p, grid, st);
-        if (n == 2 && m == 3 && p.map == EA_MAP_PRODUCT) return go<EA_AGG_SUM, EA_MAP_PRODUCT, 2, 3>(p, grid, st);
-        return generic<EA_AGG_SUM>(p, grid, st);
+        if (n == 1 && p.map == EA_MAP_SQUARE) return go<EA_AGG_SUM, EA_MAP_SQUARE, 1, 1>(p, grid, st, num_sms);
+        if (n == 1 && p.map == EA_MAP_IDENTITY) return go<EA_AGG_SUM, EA_MAP_IDENTITY, 1, 1>(p, grid, st, num_sms);
+        if (n == 2 && m == 1 && p.map == EA_MAP_EXP_SUB) return go<EA_AGG_SUM, EA_MAP_EXP_SUB, 2, 1>(p, grid, st, num_sms);
+        if (n == 2 && m == 3 && p.map == EA_MAP_PRODUCT) return go<EA_AGG_SUM, EA_MAP_PRODUCT, 2, 3>(p, grid, st, num_sms);
+        return generic<EA_AGG_SUM>(p, grid, st, num_sms);
     }
 }
 
