@@ -69,6 +69,7 @@ CASES = [
     ((2, 7, 5), [2, 1, 1], [[0, 3, 7], [0, 2, 5]]),                  # copy stride of 35 elements: no vector path
     ((5, 64, 1000), [5, 2, 3], [1, 1]),                              # gather into one block
     ((1, 50, 40), [1, 2, 2], [3, 3]),                                # a single copy is a plain exchange
+    ((2, 3, 9000), [2, 1, 1], [1, [0, 4500, 9000]]),                 # long runs: cut into 8 KiB rows + a tail
 ]
 
 
