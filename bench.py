@@ -379,6 +379,20 @@ class CpuSample:
         return time.time() - t0, block_flops(b=1, s=self.tokens), oracle.threads()
 
 
+def cpu_one_core(sample: "CpuSample"):
+    """The same oracle sample with the oracle's worker threads capped at one
+    (its C kernels read ORC_THREADS per call): (seconds, flops, cores)."""
+    old = os.environ.get("ORC_THREADS")
+    os.environ["ORC_THREADS"] = "1"
+    try:
+        return sample.run()
+    finally:
+        if old is None:
+            del os.environ["ORC_THREADS"]
+        else:
+            os.environ["ORC_THREADS"] = old
+
+
 # ------------------------------------------------------------------- arms
 
 def run_reference(args, world, rank, dist):
@@ -590,6 +604,9 @@ def run_ours(args, world, rank, local, dist):
         dt, fl, cores = CpuSample(args.cpu_tokens).run()
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": f"one sequence, first {args.cpu_tokens} tokens, full-width block; {dt:.1f} s"}
+        one = cpu_one_core(CpuSample(args.cpu_one_core_tokens))
+        cpu["one_core"] = {"value": one[1] / one[0] / 1e12, "unit": "TFLOP/s", "cores": one[2],
+                           "sample": f"one sequence, first {args.cpu_one_core_tokens} tokens; {one[0]:.1f} s"}
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -691,6 +708,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-tokens", type=int, default=192,
                     help="tokens of the oracle's CPU-baseline sample (about 10-15 s on 16 cores)")
+    ap.add_argument("--cpu-one-core-tokens", type=int, default=4,
+                    help="tokens of the one-core oracle sample (about 10 s)")
     ap.add_argument("--ref-tokens", type=int, default=32,
                     help="tokens per step of the reference arm (the oracle), so K + W steps end in minutes")
     ap.add_argument("--no-components", action="store_true")

@@ -492,6 +492,9 @@ static void *idx_worker(void *arg) {
 
 static int hw_threads(int want) {
     if (want > 0) return want;
+    /* ORC_THREADS caps the default (the benchmark's one-core baseline) */
+    const char *env = getenv("ORC_THREADS");
+    if (env && atoi(env) > 0) return atoi(env);
     long n = sysconf(_SC_NPROCESSORS_ONLN);
     return n > 0 ? (int)n : 1;
 }
