@@ -117,6 +117,8 @@ X_CASES = [
     ((2, 16, 4, 8), [2, 1, 1, 1], [2, 1, 4, 1]),
     ((2, 3, 5, 7, 3), [2, 3, 1, 2, 1], [1, 1, 5, 1, 3]),
     ((8192, 8), [8, 1], [16, 1]),
+    ((4, 50000), [2, 1], [1, 1]),                                   # long runs: cut into rows + a tail
+    ((3, 40000), [1, [0, 17000, 40000]], [[0, 1, 3], 1]),
 ]
 
 
