@@ -521,6 +521,107 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_kernel(const R
     }
 }
 
+// The softmax statistics (MAX and SUM of exp) of one input over rows whose
+// segments lie in at most four blocks of one length, no predicate: a row's
+// segments in all its blocks are requested together (64 bytes per lane per
+// segment), the batch's maximum is merged into the running one once per
+// batch, and the lanes' (m, l) pairs are merged by shuffles.
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_stats_kernel(const RrParams p) {
+    constexpr bool kB16 = DT == 1;
+    constexpr int kRowU = kB16 ? 4 : 2;
+    constexpr int EPC = 8;  // cells per chunk
+    __shared__ int64_t s_off[4], s_rstr[4], s_out0, s_ostr, s_len;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        const RrTile T = p.tiles[t];
+        const RrGroup G = p.groups[T.group];
+        const int n = G.i1 - G.i0;
+        __syncthreads();
+        if (threadIdx.x < n) {
+            const EwItem &it = p.items[G.i0 + threadIdx.x];
+            int64_t cd[kViewDims];
+            decode_row(it, T.row0, cd);
+            const int last = it.nd - 1;
+            int64_t o = it.in_base[0];
+            for (int d = 0; d < it.nd; d++) o += cd[d] * it.istr[0][d];
+            s_off[threadIdx.x] = o;
+            s_rstr[threadIdx.x] = last >= 0 ? it.istr[0][last] : 0;
+            if (threadIdx.x == 0) {
+                int64_t oo = it.out_base;
+                for (int d = 0; d < it.nd; d++) oo += cd[d] * it.ostr[d];
+                s_out0 = oo;
+                s_ostr = last >= 0 ? it.ostr[last] : 0;
+                s_len = it.len;
+            }
+        }
+        __syncthreads();
+        const int64_t len = s_len, chunks = len / EPC;
+        int lpb = 32;
+        while (lpb > 1 && (int64_t)lpb * kRowU > chunks) lpb /= 2;
+        const int rpb = 32 / lpb, subb = lane / lpb, slb = lane % lpb;
+        const int64_t step = (int64_t)lpb * EPC;
+        const int64_t pad = (T.nrows + rpb - 1) / rpb * rpb;
+        for (int64_t rr0 = (int64_t)warp * rpb; rr0 < pad; rr0 += (int64_t)kWarps * rpb) {
+            const int64_t rr = rr0 + subb;
+            const bool live = rr < T.nrows;
+            const int64_t dr = live ? rr : T.nrows - 1;
+            Stats st{-INFINITY, 0.0f};
+            for (int64_t c0 = (int64_t)slb * EPC; c0 < len; c0 += step * kRowU) {
+                uint4 raw[4][kRowU][kB16 ? 1 : 2];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    if (i >= n) continue;
+                    const int64_t off = s_off[i] + dr * s_rstr[i];
+#pragma unroll
+                    for (int u = 0; u < kRowU; u++) {
+                        const int64_t c = c0 + (int64_t)u * step;
+                        if (c < len) ld_raw<kB16>(p.in[0], off + c, raw[i][u]);
+                    }
+                }
+                // the batch maximum, then its exponentials against the running maximum
+                float bm = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    if (i >= n) continue;
+#pragma unroll
+                    for (int u = 0; u < kRowU; u++) {
+                        if (c0 + (int64_t)u * step >= len) continue;
+#pragma unroll
+                        for (int e = 0; e < EPC; e++) bm = fmaxf(bm, raw_at<kB16>(raw[i][u], e));
+                    }
+                }
+                if (bm > st.m) {
+                    st.l *= __expf(st.m - bm);  // exp(-inf) = 0 on the first batch
+                    st.m = bm;
+                }
+                if (st.m != -INFINITY) {
+                    float sum = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        if (i >= n) continue;
+#pragma unroll
+                        for (int u = 0; u < kRowU; u++) {
+                            if (c0 + (int64_t)u * step >= len) continue;
+#pragma unroll
+                            for (int e = 0; e < EPC; e++) sum += __expf(raw_at<kB16>(raw[i][u], e) - st.m);
+                        }
+                    }
+                    st.l += sum;
+                }
+            }
+            for (int o = lpb / 2; o > 0; o >>= 1) {
+                Stats other{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.l, o)};
+                st = stats_merge(st, other);
+            }
+            if (slb == 0 && live) {
+                st_elem(p.out, p.out_dtype, s_out0 + dr * s_ostr, st.m);
+                st_elem(p.out2, p.out2_dtype, s_out0 + dr * s_ostr, st.l);
+            }
+        }
+    }
+}
+
 template <int AGG, int MAP, int NIN, int MASK>
 cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st, int num_sms) {
     int dt = -1;
@@ -530,6 +631,14 @@ cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st, int num_sms) {
         dt = dt < 0 ? d : (dt == d ? dt : 0);
     }
     const bool tile = p.tile_linear && p.max_items <= kTileItems;
+    if constexpr (AGG == EA_AGG_MAX_SUMEXP && MAP == EA_MAP_IDENTITY && NIN == 1 && MASK == 1) {
+        if (tile && p.row_batch && dt > 0) {
+            const unsigned g2 = (unsigned)std::min<int64_t>(p.ntiles, 2 * (int64_t)num_sms);
+            if (dt == 1) rowreduce_rowbatch_stats_kernel<1><<<g2, kThreads, 0, st>>>(p);
+            else rowreduce_rowbatch_stats_kernel<2><<<g2, kThreads, 0, st>>>(p);
+            return cudaGetLastError();
+        }
+    }
     if constexpr (AGG == EA_AGG_SUM && (MAP == EA_MAP_SQUARE || MAP == EA_MAP_IDENTITY) && NIN == 1 && MASK == 1) {
         if (tile && p.row_batch && dt > 0) {
             // persistent: the CTAs that fit (two per SM) loop over the tiles
