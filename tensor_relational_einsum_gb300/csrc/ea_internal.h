@@ -93,6 +93,12 @@ struct RrTile {
     int64_t nrows;
 };
 
+// Flat tile descriptor of the row-batch reductions, kRbWords int64 words:
+// [0, 4) element offset of the tile's first row in each block, [4, 8) row
+// stride in each block, 8 output offset of the first row, 9 output row
+// stride, 10 segment length, 11 rows (low 32 bits) | blocks per row << 32.
+constexpr int kRbWords = 12;
+
 // ------------------------------------------------------------ contraction
 // Generic (SIMT) grouped contraction: C[b][m][n] (+)= A[b][m][k] * B[b][k][n].
 struct CtGroup {
@@ -190,7 +196,8 @@ struct RrParams {
     int stream_mask;                   // bit k: input k runs along the row (else broadcast)
     int max_items;                     // most tuples in one group
     int tile_linear;                   // 1: no tile crosses a run of the innermost row dim
-    int row_batch;                     // 1: every group has <= 4 tuples, vectorisable, of one length, no predicate
+    int row_batch;                     // 1: the row-batch kernels (rb_desc) serve this plan
+    const int64_t *rb_desc;            // kRbWords per tile when row_batch
     int *err;
 };
 cudaError_t launch_rowreduce(const RrParams &p, int num_sms, cudaStream_t st);

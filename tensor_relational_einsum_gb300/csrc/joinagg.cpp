@@ -418,6 +418,11 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
     std::vector<EwItem> items;
     std::vector<RrGroup> groups;
     std::vector<RrTile> tiles;
+    struct GroupRows {
+        int32_t gid;
+        int64_t rows, run, per;
+    };
+    std::vector<GroupRows> grows;
     int64_t max_items = 0;
     int inner_letter = red.size() == 1 ? red[0] - 'a' : -2;
     for (size_t g = 0; g < j.wl.groups.size(); g++) {
@@ -498,12 +503,74 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
         const int64_t pass = 8 * (32 / lpr);
         const int64_t per = rows * (int64_t)j.wl.groups.size() >= 4 * pass * 8 * c->num_sms ? 4 * pass : pass;
         const int64_t run = first.nd > 0 ? first.ext[first.nd - 1] : 1;
-        for (int64_t r0 = 0; r0 < rows; r0 += run)
-            for (int64_t r = r0; r < r0 + run; r += per) tiles.push_back(RrTile{gid, 0, r, std::min(per, r0 + run - r)});
+        grows.push_back(GroupRows{gid, rows, run, per});
         max_items = std::max<int64_t>(max_items, G.i1 - G.i0);
     }
+    // The row-batch kernels (one streamed input, SUM of x or x^2, or the
+    // softmax statistics; at most four blocks of one length per row, no
+    // predicate) take flat tile descriptors: per tile the element offset of
+    // its first row and the row stride in each block, the output offset and
+    // stride, the length and the rows -- a warp reads one with a single load
+    // and needs no CTA barrier.
+    bool rb = !j.pred_lo && max_items <= 4 && n_in == 1 &&
+              ((j.agg == EA_AGG_SUM && (j.map == EA_MAP_SQUARE || j.map == EA_MAP_IDENTITY)) ||
+               (j.agg == EA_AGG_MAX_SUMEXP && j.map == EA_MAP_IDENTITY));
+    for (const RrGroup &G : groups)
+        for (int32_t i = G.i0; i < G.i1 && rb; i++) {
+            const EwItem &it = items[i];
+            rb = it.vec && it.len == items[G.i0].len;
+            if (it.nd > 0)  // row strides held in 32 bits
+                rb = rb && std::llabs(it.istr[0][it.nd - 1]) < (1ll << 31) && std::llabs(it.ostr[it.nd - 1]) < (1ll << 31);
+        }
+    for (const GroupRows &gr : grows) {
+        int64_t per = gr.per;
+        if (rb) {
+            const int64_t row_u = j.in[0]->dtype == EA_BF16 ? 4 : 2;  // 8-element chunks per lane per block
+            const int64_t chunks = items[groups[gr.gid].i0].len / 8;
+            int64_t lpb = 32;
+            while (lpb > 1 && lpb * row_u > chunks) lpb /= 2;
+            // one row pass of the 8 warp slots, or four when there are many rows
+            const int64_t pass = 8 * (32 / lpb);
+            per = gr.rows * (int64_t)groups.size() >= 4 * pass * 8 * c->num_sms ? 4 * pass : pass;
+        }
+        for (int64_t r0 = 0; r0 < gr.rows; r0 += gr.run)
+            for (int64_t r = r0; r < r0 + gr.run; r += per)
+                tiles.push_back(RrTile{gr.gid, 0, r, std::min(per, r0 + gr.run - r)});
+    }
+    std::vector<int64_t> rbd;
+    if (rb) {
+        rbd.assign(tiles.size() * kRbWords, 0);
+        for (size_t t = 0; t < tiles.size(); t++) {
+            const RrTile &T = tiles[t];
+            const RrGroup &G = groups[T.group];
+            int64_t *w = &rbd[t * kRbWords];
+            for (int32_t i = G.i0; i < G.i1; i++) {
+                const EwItem &it = items[i];
+                int64_t cd[kViewDims] = {0, 0, 0, 0, 0, 0};
+                int64_t r = T.row0;
+                for (int d = it.nd - 1; d >= 1; d--) {
+                    cd[d] = r % it.ext[d];
+                    r /= it.ext[d];
+                }
+                if (it.nd > 0) cd[0] = r;
+                const int last = it.nd - 1;
+                int64_t o = it.in_base[0];
+                for (int d = 0; d < it.nd; d++) o += cd[d] * it.istr[0][d];
+                w[i - G.i0] = o;
+                w[4 + i - G.i0] = last >= 0 ? it.istr[0][last] : 0;
+                if (i == G.i0) {
+                    int64_t oo = it.out_base;
+                    for (int d = 0; d < it.nd; d++) oo += cd[d] * it.ostr[d];
+                    w[8] = oo;
+                    w[9] = last >= 0 ? it.ostr[last] : 0;
+                    w[10] = it.len;
+                }
+            }
+            w[11] = (int64_t)(uint32_t)T.nrows | ((int64_t)(G.i1 - G.i0) << 32);
+        }
+    }
     Blob b;
-    size_t oi = b.add_vec(items), og = b.add_vec(groups), ot = b.add_vec(tiles);
+    size_t oi = b.add_vec(items), og = b.add_vec(groups), ot = b.add_vec(tiles), orb = b.add_vec(rbd);
     ea_status s = upload(b, st, p);
     if (s) return s;
     p->kind = kRowReduce;
@@ -511,6 +578,7 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
     r.items = (const EwItem *)(p->dev + oi);
     r.groups = (const RrGroup *)(p->dev + og);
     r.tiles = (const RrTile *)(p->dev + ot);
+    r.rb_desc = rb ? (const int64_t *)(p->dev + orb) : nullptr;
     r.ntiles = (int64_t)tiles.size();
     for (int k = 0; k < n_in; k++) {
         r.in[k] = j.in[k]->arena;
@@ -528,12 +596,7 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
     r.pred = j.pred_lo ? 1 : 0;
     r.max_items = (int)max_items;
     r.tile_linear = 1;
-    {
-        bool rb = !j.pred_lo && max_items <= 4;
-        for (const RrGroup &G : groups)
-            for (int32_t i = G.i0; i < G.i1 && rb; i++) rb = items[i].vec && items[i].len == items[G.i0].len;
-        r.row_batch = rb ? 1 : 0;
-    }
+    r.row_batch = rb ? 1 : 0;
     r.stream_mask = 0;
     for (int k = 0; k < n_in; k++)
         if (sp.term[k].find(red.back()) != std::string::npos) r.stream_mask |= 1 << k;

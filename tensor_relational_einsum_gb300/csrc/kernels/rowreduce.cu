@@ -439,71 +439,82 @@ __global__ void __launch_bounds__(kThreads, (RrMinBlocks<AGG, MAP, MASK>::value)
     }
 }
 
+// The row-batch kernels work in units of one warp pass over a tile (tile
+// t, warp slot w: rows w * rpb + [0, rpb), then every kWarps * rpb further
+// rows of the tile).  The warps of the grid stride over the units with no
+// CTA barrier; a unit's flat descriptor (kRbWords words, lane i holding
+// word i) is loaded while the unit before it is still being reduced.
+struct RbUnit {
+    int64_t off[4], out0, len;
+    int32_t rstr[4], ostr, nrows, n;  // the planner keeps the strides below 2^31
+};
+
+__device__ __forceinline__ int64_t rb_word(const RrParams &p, int64_t unit, int lane) {
+    return lane < kRbWords ? __ldg(p.rb_desc + (unit / kWarps) * kRbWords + lane) : 0;
+}
+
+__device__ __forceinline__ RbUnit rb_unpack(int64_t w) {
+    RbUnit d;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        d.off[i] = __shfl_sync(0xffffffffu, w, i);
+        d.rstr[i] = __shfl_sync(0xffffffffu, (int32_t)w, 4 + i);
+    }
+    d.out0 = __shfl_sync(0xffffffffu, w, 8);
+    d.ostr = __shfl_sync(0xffffffffu, (int32_t)w, 9);
+    d.len = __shfl_sync(0xffffffffu, w, 10);
+    d.nrows = __shfl_sync(0xffffffffu, (int32_t)w, 11);
+    d.n = __shfl_sync(0xffffffffu, (int32_t)(w >> 32), 11);
+    return d;
+}
+
 // SUM (or SUM of squares) of one input over rows whose segments lie in at
 // most four blocks of one length (no predicate): a warp (or a slice of one)
 // requests a row's segments in all its blocks together, 64 bytes per lane
-// per segment, then sums them -- one memory round trip per
-// batch instead of one per block.  Packed f32x2 sums; the map's scale on the
-// row's sum.
+// per segment, then sums them -- one memory round trip per batch instead of
+// one per block.  Packed f32x2 sums; the map's scale on the row's sum.
 template <int MAP, int DT>
 __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_kernel(const RrParams p) {
     constexpr bool kB16 = DT == 1;
     constexpr int kRowU = kB16 ? 4 : 2;  // 64 bytes per lane per segment in flight
-    __shared__ int64_t s_off[4], s_rstr[4], s_out0, s_ostr, s_len;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-        const RrTile T = p.tiles[t];
-        const RrGroup G = p.groups[T.group];
-        const int n = G.i1 - G.i0;
-        __syncthreads();
-        if (threadIdx.x < n) {
-            const EwItem &it = p.items[G.i0 + threadIdx.x];
-            int64_t cd[kViewDims];
-            decode_row(it, T.row0, cd);
-            const int last = it.nd - 1;
-            int64_t o = it.in_base[0];
-            for (int d = 0; d < it.nd; d++) o += cd[d] * it.istr[0][d];
-            s_off[threadIdx.x] = o;
-            s_rstr[threadIdx.x] = last >= 0 ? it.istr[0][last] : 0;
-            if (threadIdx.x == 0) {
-                int64_t oo = it.out_base;
-                for (int d = 0; d < it.nd; d++) oo += cd[d] * it.ostr[d];
-                s_out0 = oo;
-                s_ostr = last >= 0 ? it.ostr[last] : 0;
-                s_len = it.len;
-            }
-        }
-        __syncthreads();
-        const int64_t len = s_len, chunks = len / 8;
+    const int lane = threadIdx.x % 32;
+    const int64_t nunits = p.ntiles * kWarps, nw = (int64_t)gridDim.x * kWarps;
+    int64_t u = (int64_t)blockIdx.x * kWarps + threadIdx.x / 32;
+    int64_t wnext = u < nunits ? rb_word(p, u, lane) : 0;
+    for (; u < nunits; u += nw) {
+        const RbUnit d = rb_unpack(wnext);
+        if (u + nw < nunits) wnext = rb_word(p, u + nw, lane);
+        const int n = d.n;
+        const int64_t len = d.len, chunks = len / 8;
         int lpb = 32;
         while (lpb > 1 && (int64_t)lpb * kRowU > chunks) lpb /= 2;
         const int rpb = 32 / lpb, subb = lane / lpb, slb = lane % lpb;
         const int64_t step = (int64_t)lpb * 8;
-        const int64_t pad = (T.nrows + rpb - 1) / rpb * rpb;
-        for (int64_t rr0 = (int64_t)warp * rpb; rr0 < pad; rr0 += (int64_t)kWarps * rpb) {
+        const int64_t pad = (d.nrows + rpb - 1) / rpb * rpb;
+        for (int64_t rr0 = (u % kWarps) * rpb; rr0 < pad; rr0 += (int64_t)kWarps * rpb) {
             const int64_t rr = rr0 + subb;
-            const bool live = rr < T.nrows;  // lanes past the tile still join the shuffles
-            const int64_t dr = live ? rr : T.nrows - 1;
+            const bool live = rr < d.nrows;  // lanes past the tile still join the shuffles
+            const int64_t dr = live ? rr : d.nrows - 1;
             uint64_t s2[4] = {0, 0, 0, 0};
             for (int64_t c0 = (int64_t)slb * 8; c0 < len; c0 += step * kRowU) {
                 uint4 raw[4][kRowU][kB16 ? 1 : 2];
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     if (i >= n) continue;
-                    const int64_t off = s_off[i] + dr * s_rstr[i];
+                    const int64_t off = d.off[i] + dr * d.rstr[i];
 #pragma unroll
-                    for (int u = 0; u < kRowU; u++) {
-                        const int64_t c = c0 + (int64_t)u * step;
-                        if (c < len) ld_raw<kB16>(p.in[0], off + c, raw[i][u]);
+                    for (int uu = 0; uu < kRowU; uu++) {
+                        const int64_t c = c0 + (int64_t)uu * step;
+                        if (c < len) ld_raw<kB16>(p.in[0], off + c, raw[i][uu]);
                     }
                 }
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     if (i >= n) continue;
 #pragma unroll
-                    for (int u = 0; u < kRowU; u++) {
-                        if (c0 + (int64_t)u * step >= len) continue;
-                        const uint32_t *w = reinterpret_cast<const uint32_t *>(raw[i][u]);
+                    for (int uu = 0; uu < kRowU; uu++) {
+                        if (c0 + (int64_t)uu * step >= len) continue;
+                        const uint32_t *w = reinterpret_cast<const uint32_t *>(raw[i][uu]);
 #pragma unroll
                         for (int e = 0; e < 4; e++) {
                             const uint64_t x2 = kB16 ? pk2(w[e] << 16, w[e] & 0xFFFF0000u) : pk2(w[2 * e], w[2 * e + 1]);
@@ -516,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_kernel(const R
             float a = pk2_sum(fadd2(fadd2(s2[0], s2[1]), fadd2(s2[2], s2[3])));
             if (MAP == EA_MAP_SQUARE) a *= p.scale;
             for (int o = lpb / 2; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-            if (slb == 0 && live) st_elem(p.out, p.out_dtype, s_out0 + dr * s_ostr, a);
+            if (slb == 0 && live) st_elem(p.out, p.out_dtype, d.out0 + dr * d.ostr, a);
         }
     }
 }
@@ -531,52 +542,35 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_stats_kernel(c
     constexpr bool kB16 = DT == 1;
     constexpr int kRowU = kB16 ? 4 : 2;
     constexpr int EPC = 8;  // cells per chunk
-    __shared__ int64_t s_off[4], s_rstr[4], s_out0, s_ostr, s_len;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-        const RrTile T = p.tiles[t];
-        const RrGroup G = p.groups[T.group];
-        const int n = G.i1 - G.i0;
-        __syncthreads();
-        if (threadIdx.x < n) {
-            const EwItem &it = p.items[G.i0 + threadIdx.x];
-            int64_t cd[kViewDims];
-            decode_row(it, T.row0, cd);
-            const int last = it.nd - 1;
-            int64_t o = it.in_base[0];
-            for (int d = 0; d < it.nd; d++) o += cd[d] * it.istr[0][d];
-            s_off[threadIdx.x] = o;
-            s_rstr[threadIdx.x] = last >= 0 ? it.istr[0][last] : 0;
-            if (threadIdx.x == 0) {
-                int64_t oo = it.out_base;
-                for (int d = 0; d < it.nd; d++) oo += cd[d] * it.ostr[d];
-                s_out0 = oo;
-                s_ostr = last >= 0 ? it.ostr[last] : 0;
-                s_len = it.len;
-            }
-        }
-        __syncthreads();
-        const int64_t len = s_len, chunks = len / EPC;
+    const int lane = threadIdx.x % 32;
+    const int64_t nunits = p.ntiles * kWarps, nw = (int64_t)gridDim.x * kWarps;
+    int64_t u = (int64_t)blockIdx.x * kWarps + threadIdx.x / 32;
+    int64_t wnext = u < nunits ? rb_word(p, u, lane) : 0;
+    for (; u < nunits; u += nw) {
+        const RbUnit d = rb_unpack(wnext);
+        if (u + nw < nunits) wnext = rb_word(p, u + nw, lane);
+        const int n = d.n;
+        const int64_t len = d.len, chunks = len / EPC;
         int lpb = 32;
         while (lpb > 1 && (int64_t)lpb * kRowU > chunks) lpb /= 2;
         const int rpb = 32 / lpb, subb = lane / lpb, slb = lane % lpb;
         const int64_t step = (int64_t)lpb * EPC;
-        const int64_t pad = (T.nrows + rpb - 1) / rpb * rpb;
-        for (int64_t rr0 = (int64_t)warp * rpb; rr0 < pad; rr0 += (int64_t)kWarps * rpb) {
+        const int64_t pad = (d.nrows + rpb - 1) / rpb * rpb;
+        for (int64_t rr0 = (u % kWarps) * rpb; rr0 < pad; rr0 += (int64_t)kWarps * rpb) {
             const int64_t rr = rr0 + subb;
-            const bool live = rr < T.nrows;
-            const int64_t dr = live ? rr : T.nrows - 1;
+            const bool live = rr < d.nrows;
+            const int64_t dr = live ? rr : d.nrows - 1;
             Stats st{-INFINITY, 0.0f};
             for (int64_t c0 = (int64_t)slb * EPC; c0 < len; c0 += step * kRowU) {
                 uint4 raw[4][kRowU][kB16 ? 1 : 2];
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     if (i >= n) continue;
-                    const int64_t off = s_off[i] + dr * s_rstr[i];
+                    const int64_t off = d.off[i] + dr * d.rstr[i];
 #pragma unroll
-                    for (int u = 0; u < kRowU; u++) {
-                        const int64_t c = c0 + (int64_t)u * step;
-                        if (c < len) ld_raw<kB16>(p.in[0], off + c, raw[i][u]);
+                    for (int uu = 0; uu < kRowU; uu++) {
+                        const int64_t c = c0 + (int64_t)uu * step;
+                        if (c < len) ld_raw<kB16>(p.in[0], off + c, raw[i][uu]);
                     }
                 }
                 // the batch maximum, then its exponentials against the running maximum
@@ -585,10 +579,10 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_stats_kernel(c
                 for (int i = 0; i < 4; i++) {
                     if (i >= n) continue;
 #pragma unroll
-                    for (int u = 0; u < kRowU; u++) {
-                        if (c0 + (int64_t)u * step >= len) continue;
+                    for (int uu = 0; uu < kRowU; uu++) {
+                        if (c0 + (int64_t)uu * step >= len) continue;
 #pragma unroll
-                        for (int e = 0; e < EPC; e++) bm = fmaxf(bm, raw_at<kB16>(raw[i][u], e));
+                        for (int e = 0; e < EPC; e++) bm = fmaxf(bm, raw_at<kB16>(raw[i][uu], e));
                     }
                 }
                 if (bm > st.m) {
@@ -601,10 +595,10 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_stats_kernel(c
                     for (int i = 0; i < 4; i++) {
                         if (i >= n) continue;
 #pragma unroll
-                        for (int u = 0; u < kRowU; u++) {
-                            if (c0 + (int64_t)u * step >= len) continue;
+                        for (int uu = 0; uu < kRowU; uu++) {
+                            if (c0 + (int64_t)uu * step >= len) continue;
 #pragma unroll
-                            for (int e = 0; e < EPC; e++) sum += __expf(raw_at<kB16>(raw[i][u], e) - st.m);
+                            for (int e = 0; e < EPC; e++) sum += __expf(raw_at<kB16>(raw[i][uu], e) - st.m);
                         }
                     }
                     st.l += sum;
@@ -615,8 +609,8 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_stats_kernel(c
                 st = stats_merge(st, other);
             }
             if (slb == 0 && live) {
-                st_elem(p.out, p.out_dtype, s_out0 + dr * s_ostr, st.m);
-                st_elem(p.out2, p.out2_dtype, s_out0 + dr * s_ostr, st.l);
+                st_elem(p.out, p.out_dtype, d.out0 + dr * d.ostr, st.m);
+                st_elem(p.out2, p.out2_dtype, d.out0 + dr * d.ostr, st.l);
             }
         }
     }
@@ -632,7 +626,7 @@ cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st, int num_sms) {
     }
     const bool tile = p.tile_linear && p.max_items <= kTileItems;
     if constexpr (AGG == EA_AGG_MAX_SUMEXP && MAP == EA_MAP_IDENTITY && NIN == 1 && MASK == 1) {
-        if (tile && p.row_batch && dt > 0) {
+        if (tile && p.row_batch && p.rb_desc && dt > 0) {
             const unsigned g2 = (unsigned)std::min<int64_t>(p.ntiles, 2 * (int64_t)num_sms);
             if (dt == 1) rowreduce_rowbatch_stats_kernel<1><<<g2, kThreads, 0, st>>>(p);
             else rowreduce_rowbatch_stats_kernel<2><<<g2, kThreads, 0, st>>>(p);
@@ -640,7 +634,7 @@ cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st, int num_sms) {
         }
     }
     if constexpr (AGG == EA_AGG_SUM && (MAP == EA_MAP_SQUARE || MAP == EA_MAP_IDENTITY) && NIN == 1 && MASK == 1) {
-        if (tile && p.row_batch && dt > 0) {
+        if (tile && p.row_batch && p.rb_desc && dt > 0) {
             // persistent: the CTAs that fit (two per SM) loop over the tiles
             const unsigned g2 = (unsigned)std::min<int64_t>(p.ntiles, 2 * (int64_t)num_sms);
             if (dt == 1) rowreduce_rowbatch_kernel<MAP, 1><<<g2, kThreads, 0, st>>>(p);
