@@ -441,16 +441,18 @@ __global__ void __launch_bounds__(kThreads, (RrMinBlocks<AGG, MAP, MASK>::value)
 
 // The row-batch kernels work in units of one warp pass over a tile (tile
 // t, warp slot w: rows w * rpb + [0, rpb), then every kWarps * rpb further
-// rows of the tile).  The warps of the grid stride over the units with no
-// CTA barrier; a unit's flat descriptor (kRbWords words, lane i holding
-// word i) is loaded while the unit before it is still being reduced.
+// rows of the tile).  A CTA takes one contiguous range of tiles, so that
+// its warps stream through neighbouring rows of each block; its warp w
+// takes slot w of each, with no CTA barrier, and a tile's flat descriptor
+// (kRbWords words, lane i holding word i) is loaded while the tile before
+// it is still being reduced.
 struct RbUnit {
     int64_t off[4], out0, len;
     int32_t rstr[4], ostr, nrows, n;  // the planner keeps the strides below 2^31
 };
 
-__device__ __forceinline__ int64_t rb_word(const RrParams &p, int64_t unit, int lane) {
-    return lane < kRbWords ? __ldg(p.rb_desc + (unit / kWarps) * kRbWords + lane) : 0;
+__device__ __forceinline__ int64_t rb_word(const RrParams &p, int64_t tile, int lane) {
+    return lane < kRbWords ? __ldg(p.rb_desc + tile * kRbWords + lane) : 0;
 }
 
 __device__ __forceinline__ RbUnit rb_unpack(int64_t w) {
@@ -478,12 +480,13 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_kernel(const R
     constexpr bool kB16 = DT == 1;
     constexpr int kRowU = kB16 ? 4 : 2;  // 64 bytes per lane per segment in flight
     const int lane = threadIdx.x % 32;
-    const int64_t nunits = p.ntiles * kWarps, nw = (int64_t)gridDim.x * kWarps;
-    int64_t u = (int64_t)blockIdx.x * kWarps + threadIdx.x / 32;
-    int64_t wnext = u < nunits ? rb_word(p, u, lane) : 0;
-    for (; u < nunits; u += nw) {
+    const int slot = threadIdx.x / 32;
+    const int64_t t1 = ((int64_t)blockIdx.x + 1) * p.ntiles / gridDim.x;
+    int64_t t = (int64_t)blockIdx.x * p.ntiles / gridDim.x;
+    int64_t wnext = t < t1 ? rb_word(p, t, lane) : 0;
+    for (; t < t1; t++) {
         const RbUnit d = rb_unpack(wnext);
-        if (u + nw < nunits) wnext = rb_word(p, u + nw, lane);
+        if (t + 1 < t1) wnext = rb_word(p, t + 1, lane);
         const int n = d.n;
         const int64_t len = d.len, chunks = len / 8;
         int lpb = 32;
@@ -491,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_kernel(const R
         const int rpb = 32 / lpb, subb = lane / lpb, slb = lane % lpb;
         const int64_t step = (int64_t)lpb * 8;
         const int64_t pad = (d.nrows + rpb - 1) / rpb * rpb;
-        for (int64_t rr0 = (u % kWarps) * rpb; rr0 < pad; rr0 += (int64_t)kWarps * rpb) {
+        for (int64_t rr0 = (int64_t)slot * rpb; rr0 < pad; rr0 += (int64_t)kWarps * rpb) {
             const int64_t rr = rr0 + subb;
             const bool live = rr < d.nrows;  // lanes past the tile still join the shuffles
             const int64_t dr = live ? rr : d.nrows - 1;
@@ -543,12 +546,13 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_stats_kernel(c
     constexpr int kRowU = kB16 ? 4 : 2;
     constexpr int EPC = 8;  // cells per chunk
     const int lane = threadIdx.x % 32;
-    const int64_t nunits = p.ntiles * kWarps, nw = (int64_t)gridDim.x * kWarps;
-    int64_t u = (int64_t)blockIdx.x * kWarps + threadIdx.x / 32;
-    int64_t wnext = u < nunits ? rb_word(p, u, lane) : 0;
-    for (; u < nunits; u += nw) {
+    const int slot = threadIdx.x / 32;
+    const int64_t t1 = ((int64_t)blockIdx.x + 1) * p.ntiles / gridDim.x;
+    int64_t t = (int64_t)blockIdx.x * p.ntiles / gridDim.x;
+    int64_t wnext = t < t1 ? rb_word(p, t, lane) : 0;
+    for (; t < t1; t++) {
         const RbUnit d = rb_unpack(wnext);
-        if (u + nw < nunits) wnext = rb_word(p, u + nw, lane);
+        if (t + 1 < t1) wnext = rb_word(p, t + 1, lane);
         const int n = d.n;
         const int64_t len = d.len, chunks = len / EPC;
         int lpb = 32;
@@ -556,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_stats_kernel(c
         const int rpb = 32 / lpb, subb = lane / lpb, slb = lane % lpb;
         const int64_t step = (int64_t)lpb * EPC;
         const int64_t pad = (d.nrows + rpb - 1) / rpb * rpb;
-        for (int64_t rr0 = (u % kWarps) * rpb; rr0 < pad; rr0 += (int64_t)kWarps * rpb) {
+        for (int64_t rr0 = (int64_t)slot * rpb; rr0 < pad; rr0 += (int64_t)kWarps * rpb) {
             const int64_t rr = rr0 + subb;
             const bool live = rr < d.nrows;
             const int64_t dr = live ? rr : d.nrows - 1;

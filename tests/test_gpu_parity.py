@@ -365,6 +365,41 @@ def test_rowreduce_fused_softmax_stats(parts, pred):
     assert rel_frob(dense64(l), want_l) <= 1e-5
 
 
+@pytest.mark.parametrize("dtype,shape,parts", [("f32", (2, 3, 40, 512), [2, 3, 2, 4]),
+                                               ("bf16", (1, 2, 50, 256), [1, 2, [0, 16, 33, 50], 4])])
+def test_rowreduce_rowbatch_stats(dtype, shape, parts):
+    """The softmax statistics over rows cut into four equal, vectorisable
+    blocks (the row-batch kernel): ragged tiles, and for bf16 64-wide
+    segments with sixteen rows per warp pass."""
+    from tensor_relational_einsum_gb300.relation import Relation
+    S = synth.make(dtype, shape, "normal", 23, 0, 3)
+    m = Relation("f32", shape[:3], parts[:3])
+    l = Relation("f32", shape[:3], parts[:3])
+    joinagg("bhst->bhs", [rel(S, parts)], agg="max_sumexp", map="identity", out=m, out2=l)
+    assert last()["kernel"] == "rowreduce"
+    want_m = oracle.joinagg("bhst->bhs", [S.to_f64()], "identity", "max")
+    E = oracle.joinagg("bhst,bhs->bhst", [S.to_f64(), want_m], "exp_sub", "none")
+    want_l = oracle.joinagg("bhst->bhs", [E], "identity", "sum")
+    assert np.array_equal(dense64(m), want_m)
+    assert rel_frob(dense64(l), want_l) <= 1e-5
+
+
+def test_rowreduce_rowbatch_sum_of_squares_four_pass_tiles():
+    """40960 rows of 4096 bf16 in 8 x 4 blocks: enough rows that the planner
+    cuts row-batch tiles of four row passes (32 rows); 64 sampled rows
+    against the oracle."""
+    from tensor_relational_einsum_gb300.relation import Relation
+    x = synth.make_torch("bf16", (40960, 4096), "normal", 24, 0, 1, device="cuda")
+    ms = joinagg("td->t", [Relation.from_dense(x, [8, 4])], agg="sum", map="square", scale=1.0 / 4096,
+                 out_dtype="f32")
+    assert last()["kernel"] == "rowreduce" and last()["tiles"] == 8 * (5120 // 32)
+    rows = [int(i) for i in synth.subset_rows(25, 40960, 64)]
+    xs = x[rows].double().cpu().numpy()
+    want = oracle.joinagg("td->t", [xs], "square", "sum", scale=1.0 / 4096)
+    got = ms.to_dense()[rows].double().cpu().numpy()
+    assert rel_frob(got, want) <= 1e-5
+
+
 def test_rowreduce_causal_predicate():
     S = synth.make("f32", (1, 2, 64, 64), "normal", 18, 0, 2)
     RS = rel(S, [1, 2, 4, 4])
