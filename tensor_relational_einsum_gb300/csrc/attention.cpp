@@ -8,7 +8,10 @@
 // intervals; key-value head floor(h / g)) that the predicate keeps, stored
 // as runs of consecutive tiles of one block.  Two neighbouring query tiles
 // of one head form a work item over the union of their key tiles (a tile
-// only one of them keeps is fully masked for the other).  Items are dealt
+// only one of them keeps is fully masked for the other; the trailing tiles
+// a query tile keeps none of -- under the causal predicate, the later
+// tile's diagonal tile for the earlier one -- are not run for it).  Items
+// are weighted by the key tiles each query tile runs, and dealt
 // to the CTAs by list scheduling in block order: each goes to the CTA with
 // the least work so far, which balances the causal triangle and keeps the
 // items that read the same K/V blocks running at the same time (their
@@ -251,6 +254,7 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
                         khi = std::max(khi, thi_k[xq]);
                     }
                     it.r0 = (int32_t)runs.size();
+                    int64_t last_kept[2] = {-1, -1};  // per query slot: its last kept tile in the item
                     const int ntb = (int)k->bounds[ksd].size() - 1;
                     for (int tb = 0; tb < ntb; tb++) {
                         kiv[ksd] = tb;
@@ -267,6 +271,11 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
                             last = kt;
                         }
                         if (first < 0) continue;
+                        for (int64_t kt = first; kt <= last; kt++) {
+                            const int64_t t0 = tlo + kt * kTileRows, t1 = std::min<int64_t>(thi, t0 + kTileRows) - 1;
+                            for (int xq = 0; xq < it.nq; xq++)
+                                if (!(t1 < tlo_k[xq] || t0 > thi_k[xq])) last_kept[xq] = it.ntiles + (kt - first);
+                        }
                         const int64_t kb = block_id(k, kiv);
                         const BlockMap &km = maps[kmap0 + kb];
                         AtRun R{};
@@ -286,6 +295,9 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
                     (void)klo;
                     (void)khi;
                     it.r1 = (int32_t)runs.size();
+                    // a query slot skips the trailing key tiles it keeps none of
+                    for (int xq = 0; xq < it.nq; xq++)
+                        it.nt[xq] = last_kept[xq] >= 0 ? (int32_t)(last_kept[xq] + 1) : it.ntiles;
                     items.push_back(it);
                 }
             }
@@ -302,7 +314,8 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
             Load l = heap.top();
             heap.pop();
             per[l.second].push_back((int32_t)i);
-            l.first += 4 * (int64_t)items[i].ntiles + 2;  // a key tile ~ 4 units, an item's set-up ~ 2
+            // a key tile of one query slot ~ 2 units, an item's set-up ~ 2
+            l.first += 2 * (int64_t)(items[i].nt[0] + (items[i].nq > 1 ? items[i].nt[1] : 0)) + 2;
             heap.push(l);
         }
     }
@@ -315,7 +328,7 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
     }
     int64_t ntup = 0, ngroups = 0;
     for (const AtItem &it : items) {
-        ntup += (int64_t)it.ntiles * it.nq;
+        ntup += (int64_t)it.nt[0] + (it.nq > 1 ? it.nt[1] : 0);
         ngroups += it.nq;
     }
 

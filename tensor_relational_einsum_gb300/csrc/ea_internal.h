@@ -268,6 +268,8 @@ struct AtItem {
     int32_t nq;        // query tiles of the item: 1 or 2
     int32_t r0, r1;    // key-tile runs [r0, r1), shared by the query tiles
     int32_t ntiles;    // key tiles over all runs
+    int32_t nt[2];     // query slot x runs the first nt[x] key tiles (its later ones are all masked)
+    int32_t pad;
 };
 
 struct AtRun {

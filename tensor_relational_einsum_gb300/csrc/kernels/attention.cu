@@ -34,7 +34,8 @@
 //              one stage of a two-stage ring with one barrier (128-byte
 //              swizzle, one [128 x 64] box per 64 head-dim columns).
 //   warp 9     TMEM owner and MMA issuer (one thread).  Per X and key tile
-//              j: S_X = Q_X K_j^T; after the softmax of X has written P_X,
+//              j (the first nt[X] tiles of the item: X stops after the last
+//              tile it keeps): S_X = Q_X K_j^T; after the softmax of X has written P_X,
 //              O_X (+)= P_X V_j with P_X read from TMEM, then at once
 //              S_X = Q_X K_{j+1}^T (in order on the tensor pipe, so the
 //              next scores land after P_X has been read).
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             // ------------------------------------------------ TMA producer
             // K and V of key tile t into stage t % kKvStages, one barrier for
             // both: the stage is released once O += P V of tile t is done.
-            uint32_t ct = 0, qx[2] = {0, 0};  // key tiles; items per query slot
+            uint32_t ct = 0, qx0 = 0, qx1 = 0;  // key tiles; items per query slot
             uint32_t q_armed = 0, q_par = 0, kv_armed = 0, kv_par = 0;
             bool ok = true;
             for (int ii = i0; ii < i1 && ok; ii++) {
@@ -204,7 +205,8 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                 const int ntiles = it.ntiles, nq = it.nq;
                 if (ntiles == 0) continue;
                 for (int x = 0; x < nq && ok; x++) {
-                    if (!mbar_wait(&ctl->q_empty[x], (qx[x] & 1) ^ 1, abort, p.err, kDevTimeoutProducer)) {
+                    const uint32_t qn = x == 0 ? qx0 : qx1;
+                    if (!mbar_wait(&ctl->q_empty[x], (qn & 1) ^ 1, abort, p.err, kDevTimeoutProducer)) {
                         ok = false;
                         break;
                     }
@@ -216,8 +218,9 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                     for (int c = 0; c < C::CH; c++)
                         tma_load_4d(qs + c * (kRows * 128), qm, &ctl->q_full[x], 64 * c, Q.q_c[0], Q.q_c[1], Q.q_c[2]);
                     q_armed |= 1u << x;
-                    q_par = (q_par & ~(1u << x)) | ((qx[x] & 1) << x);
-                    qx[x]++;
+                    q_par = (q_par & ~(1u << x)) | ((qn & 1) << x);
+                    if (x == 0) qx0++;
+                    else qx1++;
                 }
                 for (int r = it.r0; r < it.r1 && ok; r++) {
                     const AtRun R = p.runs[r];
@@ -261,7 +264,8 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             // ------------------------------------------------ MMA issuer
             const uint32_t idesc_s = make_idesc(kRows, kKeys, 0, 0);  // Q (K-major) x K (K-major)
             const uint32_t idesc_o = make_idesc(kRows, D, 0, 1);      // P (TMEM) x V (MN-major)
-            uint32_t ct = 0, qx[2] = {0, 0}, tx[2] = {0, 0};  // key tiles; items and tiles per query slot
+            // key tiles; items and tiles per query slot (scalars: no local-memory arrays)
+            uint32_t ct = 0, qx0 = 0, qx1 = 0, tx0 = 0, tx1 = 0;
             bool ok = true;
             // S_x = Q_x K_t^T
             auto mma_s = [&](int x, uint32_t t) {
@@ -289,48 +293,57 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                 const AtItem &it = p.items[ii];
                 const int n = it.ntiles, nq = it.nq;
                 if (n == 0) continue;
+                const int nt0 = it.nt[0], nt1 = nq > 1 ? it.nt[1] : 0;  // scalars: no local-memory array
                 // first scores of the item
                 if (!mbar_wait(&ctl->kv_full[ct % kKvStages], (ct / kKvStages) & 1, abort, p.err, kDevTimeoutMma)) {
                     ok = false;
                     break;
                 }
                 for (int x = 0; x < nq && ok; x++) {
-                    if (!mbar_wait(&ctl->q_full[x], qx[x] & 1, abort, p.err, kDevTimeoutMma)) {
+                    if (!mbar_wait(&ctl->q_full[x], (x == 0 ? qx0 : qx1) & 1, abort, p.err, kDevTimeoutMma)) {
                         ok = false;
                         break;
                     }
-                    qx[x]++;
+                    if (x == 0) qx0++;
+                    else qx1++;
                     tc_fence_after();
                     mma_s(x, ct);
-                    if (n == 1) umma_commit(&ctl->q_empty[x]);
+                    if ((x == 0 ? nt0 : nt1) == 1) umma_commit(&ctl->q_empty[x]);
                 }
                 if (!ok) break;
                 for (int j = 0; j < n && ok; j++) {
                     const uint32_t t = ct + j;
+                    bool kv_next = false;  // K and V of tile t + 1 have landed
                     for (int x = 0; x < nq; x++) {
+                        const int ntx = x == 0 ? nt0 : nt1;
+                        if (j >= ntx) continue;  // the rest of the item is masked for x
                         // V of tile t arrived with its K (waited for before S of tile t)
-                        if (!mbar_wait(&ctl->p_full[x], (tx[x] + j) & 1, abort, p.err, kDevTimeoutMma)) {
+                        if (!mbar_wait(&ctl->p_full[x], ((x == 0 ? tx0 : tx1) + j) & 1, abort, p.err, kDevTimeoutMma)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         mma_o(x, t, j == 0);
-                        if (j == n - 1) umma_commit(&ctl->o_fin[x]);
-                        if (j + 1 < n) {
-                            if (x == 0 && !mbar_wait(&ctl->kv_full[(t + 1) % kKvStages], ((t + 1) / kKvStages) & 1,
-                                                     abort, p.err, kDevTimeoutMma)) {
-                                ok = false;
-                                break;
+                        if (j == ntx - 1) umma_commit(&ctl->o_fin[x]);
+                        if (j + 1 < ntx) {
+                            if (!kv_next) {
+                                if (!mbar_wait(&ctl->kv_full[(t + 1) % kKvStages], ((t + 1) / kKvStages) & 1, abort,
+                                               p.err, kDevTimeoutMma)) {
+                                    ok = false;
+                                    break;
+                                }
+                                kv_next = true;
                             }
                             mma_s(x, t + 1);
-                            if (j + 1 == n - 1) umma_commit(&ctl->q_empty[x]);
+                            if (j + 1 == ntx - 1) umma_commit(&ctl->q_empty[x]);
                         }
                     }
                     if (!ok) break;
                     umma_commit(&ctl->kv_empty[t % kKvStages]);  // K and V of tile t are done
                 }
                 ct += n;
-                for (int x = 0; x < nq; x++) tx[x] += n;
+                tx0 += nt0;
+                tx1 += nt1;
             }
             // Every MMA this thread issued has completed once mma_done flips.
             umma_commit(&ctl->mma_done);
@@ -349,8 +362,8 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
         bool ok = true;
         for (int ii = i0; ii < i1 && ok; ii++) {
             const AtItem &it = p.items[ii];
-            const int n = it.ntiles;
             if (x >= it.nq) continue;
+            const int n = it.nt[x];  // key tiles of this query slot: a prefix of the item's
             const AtQTile &Q = it.q[x];
             const int nrows = Q.nrows;
             const int64_t s_g = Q.s_glob0 + row;
@@ -369,9 +382,9 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             if (p.causal) hi_t = s_g < hi_t ? s_g : hi_t;
             float m_ref = -INFINITY, m_max = -INFINITY, l = 0.f;  // raw score units
             int j = 0;
-            for (int r = it.r0; r < it.r1 && ok; r++) {
+            for (int r = it.r0; r < it.r1 && ok && j < n; r++) {
                 const AtRun R = p.runs[r];
-                for (int k = 0; k < R.ntiles; k++, j++) {
+                for (int k = 0; k < R.ntiles && j < n; k++, j++) {
                     const uint32_t t = ct + j;
                     if (!warp_wait(&ctl->s_full[x], t & 1, abort, p.err, kDevTimeoutSoftmax)) {
                         ok = false;
