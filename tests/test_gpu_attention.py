@@ -114,6 +114,23 @@ def test_repeat_is_bit_identical_and_plan_cached():
     assert torch.equal(a, O1.arena())
 
 
+@pytest.mark.parametrize("causal,want", [(True, 2 * 3 * (4 + 3 + 2 + 1)), (False, 2 * 3 * 4 * 4)])
+def test_causal_pairs_run_only_kept_key_tiles(causal, want):
+    """s = t = 512 (four tiles of 128), 2 x 3 heads, t in 2 blocks: with the
+    causal predicate a query tile runs only the key tiles up to its
+    diagonal -- the earlier tile of a pair skips the later one's diagonal
+    tile, all masked for it -- so the (query tile, key tile) steps are
+    4 + 3 + 2 + 1 per head instead of 4 + 4 + 2 + 2; without it, all 16."""
+    from tensor_relational_einsum_gb300 import _abi
+    from tensor_relational_einsum_gb300.relation import attention
+    Q, K, V = (synth.make("bf16", (2, 3, 512, 128), "normal", sd, 0, 1) for sd in (64, 65, 66))
+    q, k, v = rel(Q, [2, 3, 1, 1]), rel(K, [2, 3, 2, 1]), rel(V, [2, 3, 2, 1])
+    attention("bhsd,bhtd,bhtd->bhsd", q, k, v, causal=causal)
+    plan = _abi.last_plan()  # read before anything else launches
+    assert plan["kernel"] == "attention" and plan["tuples"] == want
+    _run("bhsd,bhtd,bhtd->bhsd", Q, K, V, [2, 3, 1, 1], [2, 3, 2, 1], "bhsd", causal=causal, stats=False)
+
+
 def test_value_closed_forms():
     # V = 1 everywhere: every kept row averages ones, O = 1 exactly up to bf16
     from tensor_relational_einsum_gb300.relation import Relation, attention
