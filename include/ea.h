@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define EA_ABI_VERSION 4
+#define EA_ABI_VERSION 5
 
 typedef int ea_status;
 #define EA_OK 0
@@ -56,6 +56,7 @@ typedef int ea_status;
 #define EA_ERR_ARG 7         /* NULL pointer, bad count, bad enum value            */
 #define EA_ERR_UNSUPPORTED 8 /* valid join-agg the library has no kernel for      */
 #define EA_ERR_DEVICE 9      /* a kernel raised the device error flag (ea_check)   */
+#define EA_ERR_BOUNDS 10     /* a plan descriptor addresses memory outside its arena */
 
 typedef struct ea_relation_s *ea_relation; /* opaque handle */
 
@@ -184,7 +185,15 @@ typedef struct {
  *              tiled into m unit blocks, and copy q receives the output block
  *              of the q-th function specification of each group (canonical
  *              order); every group must have m specifications.  The copies
- *              are aggregated later, e.g. by ea_exchange_agg.                */
+ *              are aggregated later, e.g. by ea_exchange_agg.
+ *   simt_bf16  a bf16 contraction that the tcgen05 kernel cannot take (an
+ *              operand or output whose rows are not 16-byte aligned for
+ *              TMA, an operand with neither its row nor its contracted
+ *              dimension contiguous, a block edge or a predicate it does
+ *              not handle) returns EA_ERR_UNSUPPORTED unless this is
+ *              nonzero; nonzero lets it run on the SIMT contraction kernel
+ *              (fp32 FMA, a small fraction of the tensor-core rate).
+ *              fp32 contractions always run on the SIMT kernel.             */
 typedef struct {
     int32_t out_dtype;
     float scale;
@@ -202,6 +211,7 @@ typedef struct {
     ea_relation row_rms;
     int32_t partials;
     int32_t rope_layout;
+    int32_t simt_bf16;
 } ea_opts;
 
 /* ------------------------------------------------------------ basics */
@@ -399,6 +409,13 @@ ea_status ea_exchange_agg(ea_relation in, ea_agg agg, const ea_dim_part *new_par
  * may be NULL. */
 ea_status ea_last_plan(int32_t *kernel_class, int32_t *launches, int64_t *tiles, int64_t *groups, int64_t *tuples);
 
+/* How many CTAs shared one MMA tile in that launch: 1, or 2 when the
+ * tcgen05 contraction ran as CTA pairs (tcgen05 cta_group::2: one 256-row
+ * tile over two SMs, each SM loading its own A rows and half of the B tile;
+ * chosen when the work has at least two tiles per SM).  1 for every other
+ * kernel.  Errors: EA_ERR_ARG (NULL). */
+ea_status ea_last_plan_cluster(int32_t *ctas);
+
 /* The exchange for callers that must not allocate device memory.  This
  * call has no counterpart in the paper.  ea_exchange and ea_joinagg_run
  * upload their plans into memory they take from cudaMalloc; a process
@@ -414,11 +431,14 @@ ea_status ea_last_plan(int32_t *kernel_class, int32_t *launches, int64_t *tiles,
  * than that (about 6000 overlay atoms, or more than 2048 split points in
  * one dimension) is rejected with EA_ERR_UNSUPPORTED before anything is
  * launched.  The first call on each device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  The plan is copied into the array with
- * cudaMemcpyAsync on `stream`, then the kernel runs on `stream`.  Every
- * call shares the one array, so calls whose work overlaps on the GPU
- * (different streams with no ordering between them) race on it. */
+ * address (cudaGetSymbolAddress) with that device current.  The plan is
+ * staged in a static host buffer and copied into the array with
+ * cudaMemcpyAsync on `stream`, then the kernel runs on `stream`.  A call on
+ * a stream that is being captured into a CUDA graph returns
+ * EA_ERR_UNSUPPORTED (a replayed copy would read whatever plan a later call
+ * left in the host buffer).  Every call shares the one array, so calls
+ * whose work overlaps on the GPU (different streams with no ordering
+ * between them) race on it. */
 ea_status ea_exchange_noalloc(ea_relation in, ea_relation out, void *stream);
 
 /* ------------------------------------------------ host-only planning hooks */
@@ -447,6 +467,34 @@ ea_status ea_plan_worklist(const char *spec, const int64_t *shapes, const ea_ind
  * source arena of the element at position i of the destination arena. */
 ea_status ea_exchange_permutation(int rank, const int64_t *dims, const ea_dim_part *src_parts,
                                   const ea_dim_part *dst_parts, int64_t *perm);
+
+/* The plan check on hand-made exchange descriptors (no GPU needed).  Every
+ * plan the library builds passes the same check before it is uploaded; a
+ * plan with a descriptor outside its arenas is rejected with EA_ERR_BOUNDS
+ * and nothing is launched.  An exchange plan is a list of segments, each
+ * rows of a contiguous run (16 int64 words per segment: source offset,
+ * destination offset, run length, number of outer dimensions nd <= 4,
+ * ext[4], source strides[4], destination strides[4]; elements, outermost
+ * first, only the first nd of each group used), and tiles that cut the
+ * segments (5 words per tile: segment index, first row, rows, first
+ * element of the run, elements).  Returns EA_OK if every segment's source
+ * and destination elements lie in [0, src_elems) and [0, dst_elems) and
+ * every tile inside its segment, else EA_ERR_BOUNDS (message names the
+ * first offending descriptor); EA_ERR_ARG for bad counts or pointers. */
+ea_status ea_plan_check_exchange(const int64_t *seg_words, int64_t nseg, const int64_t *tile_words, int64_t ntiles,
+                                 int64_t src_elems, int64_t dst_elems);
+
+/* 1 if this library was built with EA_DEBUG_BOUNDS, else 0.  In that build
+ * every kernel also checks, before it touches a tile (an exchange segment's
+ * rows, an elementwise or row-reduction view, a contraction's operand and
+ * output blocks, the residual and row-scale rows of a contraction's
+ * epilogue, an attention query tile's output rows), that the tile's element
+ * range lies inside its arena; if not it raises the device error word,
+ * which ea_check reports as EA_ERR_DEVICE, and skips the tile (the
+ * allocation-free exchange, which has no error word, only skips it).  The
+ * default build leaves these checks out; both builds check every plan on
+ * the host before upload (EA_ERR_BOUNDS). */
+int ea_debug_bounds(void);
 
 /* Number of atoms of the overlay of two tilings (Section 5.3). */
 ea_status ea_overlay_atoms(int rank, const int64_t *dims, const ea_dim_part *src_parts, const ea_dim_part *dst_parts,

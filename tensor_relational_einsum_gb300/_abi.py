@@ -12,7 +12,8 @@ import os
 import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libea.so")
+# EA_BOUNDS_CHECK=1 loads the bounds-checking build (EA_DEBUG_BOUNDS).
+LIB_PATH = os.path.join(PKG, "libea_bounds.so" if os.environ.get("EA_BOUNDS_CHECK", "") == "1" else "libea.so")
 
 F32, BF16 = 0, 1
 DTYPES = {"f32": F32, "bf16": BF16}
@@ -20,7 +21,8 @@ AGGS = {"none": 0, "sum": 1, "max": 2, "max_sumexp": 3}
 MAPS = {"product": 0, "identity": 1, "silu_mul": 2, "add": 3, "exp_sub": 4, "div": 5, "square": 6,
         "rms_apply": 7, "exp_sub_div": 8, "rope": 9}
 STATUS = {0: "EA_OK", 1: "EA_ERR_SPEC", 2: "EA_ERR_SHAPE", 3: "EA_ERR_PARTITION", 4: "EA_ERR_DTYPE",
-          5: "EA_ERR_ALLOC", 6: "EA_ERR_CUDA", 7: "EA_ERR_ARG", 8: "EA_ERR_UNSUPPORTED", 9: "EA_ERR_DEVICE"}
+          5: "EA_ERR_ALLOC", 6: "EA_ERR_CUDA", 7: "EA_ERR_ARG", 8: "EA_ERR_UNSUPPORTED", 9: "EA_ERR_DEVICE",
+          10: "EA_ERR_BOUNDS"}
 
 
 class EaError(RuntimeError):
@@ -44,7 +46,7 @@ class Opts(ctypes.Structure):
                 ("epi_pair", ctypes.c_char), ("rope_table", ctypes.c_void_p), ("rope_npos", ctypes.c_int64),
                 ("out2", ctypes.c_void_p), ("epi_in", ctypes.c_void_p), ("epi_map", ctypes.c_int32),
                 ("rope_dim", ctypes.c_int32), ("row_rms", ctypes.c_void_p), ("partials", ctypes.c_int32),
-                ("rope_layout", ctypes.c_int32)]
+                ("rope_layout", ctypes.c_int32), ("simt_bf16", ctypes.c_int32)]
 
 
 class AttnOpts(ctypes.Structure):
@@ -73,6 +75,7 @@ def lib():
             raise ImportError(f"{LIB_PATH} is missing: build it with tensor_relational_einsum_gb300.build.build()")
         L = ctypes.CDLL(LIB_PATH)
         L.ea_abi_version.restype = ctypes.c_int
+        L.ea_debug_bounds.restype = ctypes.c_int
         L.ea_last_error.restype = ctypes.c_char_p
         L.ea_check.argtypes = [VP]
         L.ea_plan_cache_clear.argtypes = []
@@ -93,19 +96,21 @@ def lib():
         L.ea_exchange_permutation.argtypes = [ctypes.c_int, P64, ctypes.POINTER(DimPart), ctypes.POINTER(DimPart), P64]
         L.ea_overlay_atoms.argtypes = [ctypes.c_int, P64, ctypes.POINTER(DimPart), ctypes.POINTER(DimPart), P64]
         L.ea_last_plan.argtypes = [P32, P32, P64, P64, P64]
+        L.ea_last_plan_cluster.argtypes = [P32]
         L.ea_exchange_noalloc.argtypes = [VP, VP, VP]
         L.ea_exchange_agg.argtypes = [VP, ctypes.c_int, ctypes.POINTER(DimPart), VP, ctypes.POINTER(VP)]
         L.ea_set_allocator.argtypes = [ALLOC_FN, FREE_FN, VP]
         L.ea_relation_copy_host.argtypes = [VP, VP, ctypes.c_int, VP]
         L.ea_selftest_wait_timeout.argtypes = [ctypes.c_int64, VP]
+        L.ea_plan_check_exchange.argtypes = [P64, ctypes.c_int64, P64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
         L.ea_attention_run.argtypes = [ctypes.c_char_p, VP, VP, VP, ctypes.POINTER(AttnOpts), VP, ctypes.POINTER(VP)]
         for name in ("ea_check", "ea_plan_cache_clear", "ea_relation_create", "ea_relation_destroy",
                      "ea_relation_info", "ea_relation_block", "ea_relation_data", "ea_relation_bounds",
                      "ea_joinagg_run", "ea_exchange", "ea_plan_worklist", "ea_exchange_permutation",
-                     "ea_overlay_atoms", "ea_last_plan", "ea_exchange_noalloc", "ea_attention_run", "ea_exchange_agg",
-                     "ea_set_allocator", "ea_relation_copy_host", "ea_selftest_wait_timeout"):
+                     "ea_overlay_atoms", "ea_last_plan", "ea_last_plan_cluster", "ea_exchange_noalloc", "ea_attention_run", "ea_exchange_agg",
+                     "ea_set_allocator", "ea_relation_copy_host", "ea_selftest_wait_timeout", "ea_plan_check_exchange"):
             getattr(L, name).restype = ctypes.c_int
-        if L.ea_abi_version() != 4:
+        if L.ea_abi_version() != 5:
             raise ImportError("libea.so ABI version mismatch")
         _lib = L
         return _lib
@@ -173,5 +178,7 @@ def last_plan():
     t, g, u = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
     check_status(lib().ea_last_plan(ctypes.byref(k), ctypes.byref(n), ctypes.byref(t), ctypes.byref(g),
                                     ctypes.byref(u)))
+    c = ctypes.c_int32()
+    check_status(lib().ea_last_plan_cluster(ctypes.byref(c)))
     return {"kernel": KERNEL_CLASS.get(k.value, None), "launches": n.value, "tiles": t.value, "groups": g.value,
-            "tuples": u.value}
+            "tuples": u.value, "cta_pair": c.value == 2}

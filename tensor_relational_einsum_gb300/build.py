@@ -20,6 +20,14 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libea.so")
+# The bounds-checking build (EA_DEBUG_BOUNDS: every kernel checks each
+# tile's element range against its arena before touching it).  The binding
+# loads it instead of libea.so when the environment sets EA_BOUNDS_CHECK=1.
+LIB_BOUNDS = os.path.join(PKG, "libea_bounds.so")
+
+
+def bounds_variant() -> bool:
+    return os.environ.get("EA_BOUNDS_CHECK", "") == "1"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -48,22 +56,29 @@ def headers():
             [os.path.join(INCLUDE, "ea.h")])
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in sources() + headers() + [__file__])
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_flags=(), bounds: bool | None = None) -> str:
+    """Build libea.so (or, with bounds=True -- by default when EA_BOUNDS_CHECK=1
+    -- the bounds-checking libea_bounds.so) if a source is newer; return its path."""
+    if bounds is None:
+        bounds = bounds_variant()
+    lib = LIB_BOUNDS if bounds else LIB
+    if not force and not _stale(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
-    common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC, *extra_flags]
+    objdir = os.path.join(BUILD, "bounds") if bounds else BUILD
+    os.makedirs(objdir, exist_ok=True)
+    common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC, *extra_flags,
+              *(["-DEA_DEBUG_BOUNDS"] if bounds else [])]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.relpath(src, CSRC).replace(os.sep, "_") + ".o")
+        obj = os.path.join(objdir, os.path.relpath(src, CSRC).replace(os.sep, "_") + ".o")
         if src.endswith(".cu"):
             cmd = [nvcc, *ARCH, "-lineinfo", *common, "-c", src, "-o", obj]
         else:
@@ -78,17 +93,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp.{os.getpid()}"
+    tmp = lib + f".tmp.{os.getpid()}"
     libdir = _cuda_lib_dir(nvcc)
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, "-L", libdir, "-Xlinker",
            f"-rpath,{libdir}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True,
-                extra_flags=(["-Xptxas", "-v"] if "--ptxas" in sys.argv else [])))
+                extra_flags=(["-Xptxas", "-v"] if "--ptxas" in sys.argv else []),
+                bounds=True if "--bounds" in sys.argv else None))

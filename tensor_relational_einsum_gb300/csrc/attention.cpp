@@ -302,7 +302,18 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
                 }
             }
     }
-    (void)D;
+    // the plan check: every query tile's output rows and statistics rows
+    // inside their arenas (Q, K and V are read through tensor maps over
+    // whole blocks, which the block offsets keep inside the arenas)
+    for (size_t i = 0; i < items.size(); i++)
+        for (int x = 0; x < items[i].nq; x++) {
+            const AtQTile &Q = items[i].q[x];
+            const int64_t e[2] = {Q.nrows, D}, st2[2] = {Q.o_rstr, 1};
+            ea_status cs = check_block(Q.o_off, 2, e, st2, rel_elems(j.o), "attention output rows", i);
+            const int64_t me[1] = {Q.nrows}, ms[1] = {Q.ml_rstr};
+            if (!cs && j.m) cs = check_block(Q.ml_off, 1, me, ms, rel_elems(j.m), "attention statistics rows", i);
+            if (cs) return cs;
+        }
     // List scheduling: each group, in order, to the CTA with the least work.
     const int ncta = (int)std::min<int64_t>((int64_t)c->num_sms, (int64_t)items.size());
     std::vector<std::vector<int32_t>> per(std::max(ncta, 1));
@@ -347,6 +358,8 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
     P.runs = (const AtRun *)(p->dev + orr);
     P.seq_ends = j.ends.empty() ? nullptr : (const int64_t *)(p->dev + oe);
     P.o = j.o->arena;
+    P.o_elems = rel_elems(j.o);
+    P.ml_elems = j.m ? rel_elems(j.m) : 0;
     P.m_out = j.m ? (float *)j.m->arena : nullptr;
     P.l_out = j.l ? (float *)j.l->arena : nullptr;
     P.ncta = ncta;

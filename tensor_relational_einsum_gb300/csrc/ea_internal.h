@@ -153,8 +153,10 @@ struct TcTile {
 // Each returns cudaSuccess or the launch error.  All take a device error
 // word (int*) for bounded-wait / bounds failures.
 
+// src_elems, dst_elems: arena sizes in elements (checked per tile by a
+// library built with EA_DEBUG_BOUNDS, which raises `err` on a violation).
 cudaError_t launch_exchange(const XSeg *segs, const XTile *tiles, int64_t ntiles, const char *src, char *dst,
-                            int esize, int num_sms, cudaStream_t st);
+                            int esize, int num_sms, cudaStream_t st, int64_t src_elems, int64_t dst_elems, int *err);
 
 struct EwParams {
     const EwItem *items;
@@ -174,6 +176,7 @@ struct EwParams {
     int has_vec, has_scalar;           // which kernel variants have tiles
     int stream_mask;                   // bit k: input k runs along the row (else broadcast)
     int *err;
+    int64_t in_elems[kMaxIn], out_elems;  // arena sizes (elements), for EA_DEBUG_BOUNDS checks
 };
 cudaError_t launch_ewise(const EwParams &p, int num_sms, cudaStream_t st);
 
@@ -199,6 +202,7 @@ struct RrParams {
     int row_batch;                     // 1: the row-batch kernels (rb_desc) serve this plan
     const int64_t *rb_desc;            // kRbWords per tile when row_batch
     int *err;
+    int64_t in_elems[kMaxIn], out_elems;  // arena sizes (elements), for EA_DEBUG_BOUNDS checks
 };
 cudaError_t launch_rowreduce(const RrParams &p, int num_sms, cudaStream_t st);
 
@@ -215,6 +219,8 @@ struct CtParams {
     int tile;                          // output tile edge: 64, or 32 when 64-wide tiles would leave SMs idle
     int split;                         // fp32, 32-wide tiles, <= 4 tuples of K <= 64 per group: one warp
                                        // group per tuple, the tuples' products summed in canonical order
+    int64_t a_elems, b_elems, c_elems;  // arena sizes (elements), for EA_DEBUG_BOUNDS checks
+    int *err;
 };
 cudaError_t launch_contract_simt(const CtParams &p, cudaStream_t st);
 
@@ -229,8 +235,8 @@ struct TcParams {
     float scale;
     int32_t pred_mode;
     int32_t bn;                        // 128 or 256
-    int32_t cluster;                   // CTAs per cluster sharing each B tile (1 or 2): tiles
-                                       // 2 p and 2 p + 1 have the same group, batch and n0
+    int32_t cluster;                   // 1, or 2: CTA pairs (cta_group::2); tiles 2 p and 2 p + 1
+                                       // have the same group, batch and n0, and m0 128 apart
     int32_t epi;                       // epilogue join: 0 none, 1 ADD epi_in, 2 SiLU(g) * u of column pairs,
                                        // 3 ROPE rotation of column pairs
     const char *epi_in;                // epi 1: the joined relation's arena (output dtype)
@@ -241,9 +247,9 @@ struct TcParams {
     int32_t rope_half;                 // pairs per period along the columns
     int32_t rope_pm;                   // table pair-major: [rope_half][rope_npos][2]
     int *err;
+    int64_t epi_elems, rms_elems;      // arena sizes of epi_in and row_rms (elements), for EA_DEBUG_BOUNDS
 };
 cudaError_t launch_contract_tc(const TcParams &p, int num_sms, cudaStream_t st);
-int tc_smem_bytes(int bn);
 
 // --------------------------------------------------------------- attention
 // Flash attention as one join-agg: an aggregation group is one tile of 128
@@ -298,11 +304,13 @@ struct AtParams {
     float scale_log2;        // scale * log2(e)
     int32_t d;               // head dimension: 64 or 128
     int *err;
+    int64_t o_elems, ml_elems;  // arena sizes of O and of m / l (elements), for EA_DEBUG_BOUNDS
 };
 cudaError_t launch_attention(const AtParams &p, cudaStream_t st);
 cudaError_t launch_wait_timeout(int *err, uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_exchange_agg(const XSeg *segs, const XTile *tiles, int64_t ntiles, const char *src, char *dst,
-                                int dtype, int agg, int ncopies, int64_t copy_stride, int num_sms, cudaStream_t st);
+                                int dtype, int agg, int ncopies, int64_t copy_stride, int num_sms, cudaStream_t st,
+                                int64_t src_elems, int64_t dst_elems, int *err);
 int attention_smem_bytes(int d);
 
 }  // namespace ea

@@ -91,6 +91,24 @@ struct ExchangePlan {
 ea_status plan_exchange(int rank, const int64_t *dims, const Tiling *src, const Tiling *dst, int esize,
                         ExchangePlan *xp);
 
+// The plan check (bounds.cpp): every descriptor's element range inside the
+// arena it addresses, else EA_ERR_BOUNDS.  copies / copy_stride: the
+// exchange with aggregation reads copy q at q * copy_stride elements on.
+ea_status check_exchange_plan(const XSeg *segs, size_t nseg, const XTile *tiles, size_t ntiles, int64_t src_elems,
+                              int64_t dst_elems, int64_t copies, int64_t copy_stride);
+ea_status check_view_items(const EwItem *items, size_t n, int n_in, const int64_t *in_elems, int64_t out_elems,
+                           const char *what);
+ea_status check_ew_tiles(const EwTile *tiles, size_t nt, const EwItem *items, size_t n);
+ea_status check_rr_tiles(const RrTile *tiles, size_t nt, const RrGroup *groups, size_t ng, const EwItem *items,
+                         size_t n);
+ea_status check_rb_desc(const int64_t *w, size_t ntiles, int64_t in_elems, int64_t out_elems);
+ea_status check_simt_plan(const CtGroup *groups, size_t ng, const CtTuple *tuples, size_t nt, int64_t a_elems,
+                          int64_t b_elems, int64_t c_elems);
+inline int64_t rel_elems(const ea_relation_s *r) { return r->blk_off.empty() ? 0 : r->blk_off.back(); }
+// base + sum_i c_i str_i (0 <= c_i < ext_i) inside [0, elems).
+ea_status check_block(int64_t base, int n, const int64_t *ext, const int64_t *str, int64_t elems, const char *what,
+                      size_t index);
+
 // Arena offsets of a tiling (row-major blocks, consecutive).
 void tiling_offsets(int rank, const Tiling *t, std::vector<int64_t> *off);
 

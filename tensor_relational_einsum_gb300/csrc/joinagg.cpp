@@ -212,6 +212,7 @@ struct JoinCtx {
     char row_letter;             // the output letter of input 0 only (rows of the contraction)
     char copy_letter;            // partials: the letter of the copies (leading output letter), or 0
     char epi_pair;               // EA_MAP_SILU_MUL: the paired letter (innermost in the planned output)
+    int simt_bf16;               // a bf16 contraction may run on the SIMT kernel
     ea_relation_s *user_out;     // the output relation (out is its pre-epilogue view when paired)
 };
 
@@ -359,6 +360,11 @@ static ea_status build_ewise(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan *p)
     }
     (void)es_out;
     (void)c;
+    int64_t in_el[kMaxIn];
+    for (int k = 0; k < n_in; k++) in_el[k] = rel_elems(j.in[k]);
+    ea_status cs = check_view_items(items.data(), items.size(), n_in, in_el, rel_elems(j.out), "elementwise view");
+    if (!cs) cs = check_ew_tiles(tiles.data(), tiles.size(), items.data(), items.size());
+    if (cs) return cs;
     Blob b;
     size_t oi = b.add_vec(items), ot = b.add_vec(tiles);
     ea_status s = upload(b, st, p);
@@ -374,6 +380,8 @@ static ea_status build_ewise(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan *p)
     }
     e.out = j.out->arena;
     e.out_dtype = j.out->dtype;
+    e.out_elems = rel_elems(j.out);
+    for (int k = 0; k < n_in; k++) e.in_elems[k] = rel_elems(j.in[k]);
     e.n_in = n_in;
     e.map = j.map;
     e.scale = j.scale;
@@ -569,6 +577,12 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
             w[11] = (int64_t)(uint32_t)T.nrows | ((int64_t)(G.i1 - G.i0) << 32);
         }
     }
+    int64_t in_el[kMaxIn];
+    for (int k = 0; k < n_in; k++) in_el[k] = rel_elems(j.in[k]);
+    ea_status cs = check_view_items(items.data(), items.size(), n_in, in_el, rel_elems(j.out), "row-reduction view");
+    if (!cs) cs = check_rr_tiles(tiles.data(), tiles.size(), groups.data(), groups.size(), items.data(), items.size());
+    if (!cs && rb) cs = check_rb_desc(rbd.data(), tiles.size(), in_el[0], rel_elems(j.out));
+    if (cs) return cs;
     Blob b;
     size_t oi = b.add_vec(items), og = b.add_vec(groups), ot = b.add_vec(tiles), orb = b.add_vec(rbd);
     ea_status s = upload(b, st, p);
@@ -586,6 +600,8 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
     }
     r.out = j.out->arena;
     r.out_dtype = j.out->dtype;
+    r.out_elems = rel_elems(j.out);
+    for (int k = 0; k < n_in; k++) r.in_elems[k] = rel_elems(j.in[k]);
     r.out2 = j.out2 ? j.out2->arena : nullptr;
     r.out2_dtype = j.out2 ? j.out2->dtype : 0;
     r.n_in = n_in;
@@ -719,6 +735,9 @@ static ea_status build_simt(JoinCtx &j, const ContractionViews &cv, DevCtx *c, c
             for (int64_t n0 = 0; n0 < g.second.N; n0 += tsz)
                 for (int64_t m0 = 0; m0 < g.second.M; m0 += tsz)
                     tiles.push_back(CtTile{g.first, (int32_t)bb, (int32_t)m0, (int32_t)n0});
+    ea_status cs = check_simt_plan(groups.data(), groups.size(), tuples.data(), tuples.size(), rel_elems(j.in[0]),
+                                   rel_elems(j.in[1]), rel_elems(j.out));
+    if (cs) return cs;
     Blob b;
     size_t og = b.add_vec(groups), ou = b.add_vec(tuples), ot = b.add_vec(tiles);
     ea_status s = upload(b, st, p);
@@ -732,6 +751,10 @@ static ea_status build_simt(JoinCtx &j, const ContractionViews &cv, DevCtx *c, c
     q.a = j.in[0]->arena;
     q.b = j.in[1]->arena;
     q.c = j.out->arena;
+    q.a_elems = rel_elems(j.in[0]);
+    q.b_elems = rel_elems(j.in[1]);
+    q.c_elems = rel_elems(j.out);
+    q.err = c->err;
     q.a_dtype = j.in[0]->dtype;
     q.b_dtype = j.in[1]->dtype;
     q.c_dtype = j.out->dtype;
@@ -863,8 +886,8 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
     if (tg_ops.empty()) return EA_ERR_UNSUPPORTED;
     const int bn = maxN <= 128 ? 128 : 256;
     if (mode && swap) mode = 3 - mode;  // the mask is stated in the swapped roles
-    // Clusters of two CTAs share each B tile (multicast) when there are
-    // enough tiles to keep every SM busy in pairs.
+    // CTA pairs (one 256-row MMA over two SMs, each loading half of the B
+    // tile) when there are enough tiles to keep every SM busy in pairs.
     int64_t est_tiles = 0;
     for (const GroupGeom &G : gg) est_tiles += G.nb * ((G.M + 127) / 128) * ((G.N + bn - 1) / bn);
     const int cl = est_tiles >= 2 * (int64_t)c->num_sms ? 2 : 1;
@@ -880,6 +903,11 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
         if (it != cache.end()) {
             *id = it->second;
             return EA_OK;
+        }
+        {
+            const int64_t e[3] = {o.M, o.K, o.nb}, st3[3] = {o.s_m, o.s_k, o.s_b};
+            ea_status cs = check_block(o.base, 3, e, st3, rel_elems(o.rel), "contraction operand block", maps.size());
+            if (cs) return cs;
         }
         CUtensorMap m;
         int64_t row = outer_stride(o, mn);
@@ -928,6 +956,16 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
         TG.e_sb = G.c_sb / h;
         TG.r_lo = G.r_lo;
         TG.c_lo = G.e_lo;
+        {
+            // the stored output block, the residual block read by an ADD
+            // epilogue (same geometry) and the rows of the row scale
+            const int64_t e[3] = {G.N / h, G.M, G.nb}, st3[3] = {1, G.c_sm / h, G.c_sb / h};
+            ea_status cs = check_block(G.c_base / h, 3, e, st3, rel_elems(j.user_out), "contraction output block", g);
+            if (!cs && j.epi_in) cs = check_block(TG.e_base, 3, e, st3, rel_elems(j.epi_in), "epilogue input block", g);
+            const int64_t re[1] = {G.M}, rs[1] = {1};
+            if (!cs && j.row_rms) cs = check_block(G.r_lo, 1, re, rs, rel_elems(j.row_rms), "row-scale block", g);
+            if (cs) return cs;
+        }
         CUtensorMap m;
         const void *cptr = j.out->arena + (G.c_base / h) * esc;
         ea_status s = encode_map(c, &m, j.out->dtype, cptr, G.N / h, G.M, G.nb, (G.c_sm / h) * esc,
@@ -939,7 +977,7 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
         groups.push_back(TG);
         // Grouped raster: bands of kBand m-tiles, each band swept across all
         // n-tiles with m fastest, so the tiles in flight at once share a
-        // small set of A rows and B columns that stays in L2.  With clusters
+        // small set of A rows and B columns that stays in L2.  With CTA pairs
         // the tiles come in pairs of the same n-tile (consecutive m-tiles; a
         // band with an odd count gets a padding tile past the block's rows).
         // A band's A rows take about 32 MiB: B is re-read once per band, and
@@ -960,6 +998,15 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
                 }
     }
     if (tiles.size() > (size_t)INT32_MAX) return EA_ERR_UNSUPPORTED;
+    if (cl == 2) {
+        // a CTA pair computes tiles 2u and 2u + 1 as one 256-row MMA tile
+        if (tiles.size() % 2) return set_error(EA_ERR_UNSUPPORTED, "contraction: odd tile count for CTA pairs");
+        for (size_t u = 0; u < tiles.size(); u += 2) {
+            const TcTile &t0 = tiles[u], &t1 = tiles[u + 1];
+            if (t0.group != t1.group || t0.batch != t1.batch || t0.n0 != t1.n0 || t1.m0 != t0.m0 + 128)
+                return set_error(EA_ERR_UNSUPPORTED, "contraction: tiles of a CTA pair are not M-adjacent");
+        }
+    }
     Blob b;
     size_t om = b.add(maps.data(), maps.size() * sizeof(CUtensorMap), 128);
     size_t og = b.add_vec(groups), ou = b.add_vec(tuples), ot = b.add_vec(tiles);
@@ -982,6 +1029,8 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
     q.epi = j.epi_map == EA_MAP_ADD ? 1 : j.epi_map == EA_MAP_SILU_MUL ? 2 : j.epi_map == EA_MAP_ROPE ? 3 : 0;
     q.epi_in = j.epi_in ? j.epi_in->arena : nullptr;
     q.row_rms = j.row_rms ? (const float *)j.row_rms->arena : nullptr;
+    q.epi_elems = j.epi_in ? rel_elems(j.epi_in) : 0;
+    q.rms_elems = j.row_rms ? rel_elems(j.row_rms) : 0;
     q.eps = j.eps;
     q.rope_table = j.rope_table;
     q.rope_npos = j.rope_npos;
@@ -1006,13 +1055,19 @@ ea_status launch_plan(DevPlan *p, DevCtx *c, cudaStream_t st) {
     case kEwise: t_last.tiles = p->ew.ntiles; t_last.launches = p->ew.has_vec + p->ew.has_scalar; break;
     case kRowReduce: t_last.tiles = p->rr.ntiles; t_last.launches = p->rr.ntiles > 0; break;
     case kSimt: t_last.tiles = p->ct.ntiles; t_last.launches = p->ct.ntiles > 0; break;
-    case kTc: t_last.tiles = p->tc.ntiles; t_last.launches = p->tc.ntiles > 0; break;
+    case kTc:
+        t_last.tiles = p->tc.ntiles;
+        t_last.launches = p->tc.ntiles > 0;
+        t_last.cluster = p->tc.cluster;
+        break;
     case kAttn: t_last.tiles = p->n_groups; t_last.launches = p->at.ncta > 0; break;
     case kExchangeAgg: t_last.tiles = p->nxtiles; t_last.launches = p->nxtiles > 0; break;
     }
     switch (p->kind) {
     case kExchange:
-        if (p->nxtiles) e = launch_exchange(p->segs, p->xtiles, p->nxtiles, p->xsrc, p->xdst, p->esize, c->num_sms, st);
+        if (p->nxtiles)
+            e = launch_exchange(p->segs, p->xtiles, p->nxtiles, p->xsrc, p->xdst, p->esize, c->num_sms, st,
+                                p->xsrc_elems, p->xdst_elems, c->err);
         break;
     case kEwise:
         p->ew.err = c->err;
@@ -1023,6 +1078,7 @@ ea_status launch_plan(DevPlan *p, DevCtx *c, cudaStream_t st) {
         if (p->rr.ntiles) e = launch_rowreduce(p->rr, c->num_sms, st);
         break;
     case kSimt:
+        p->ct.err = c->err;
         if (p->ct.ntiles) e = launch_contract_simt(p->ct, st);
         break;
     case kTc:
@@ -1036,7 +1092,7 @@ ea_status launch_plan(DevPlan *p, DevCtx *c, cudaStream_t st) {
     case kExchangeAgg:
         if (p->nxtiles)
             e = launch_exchange_agg(p->segs, p->xtiles, p->nxtiles, p->xsrc, p->xdst, p->xdtype, p->xagg, p->xcopies,
-                                    p->xcopy_stride, c->num_sms, st);
+                                    p->xcopy_stride, c->num_sms, st, p->xsrc_elems, p->xdst_elems, c->err);
         break;
     }
     if (e != cudaSuccess) return cuda_error(e, "kernel launch");
@@ -1138,6 +1194,8 @@ ea_status ea_exchange(ea_relation in, const ea_dim_part *new_parts, void *stream
     } else {
         ExchangePlan xp;
         s = plan_exchange(in->rank, in->dims, src, dst, (int)elem_size(in->dtype), &xp);
+        if (!s) s = check_exchange_plan(xp.segs.data(), xp.segs.size(), xp.tiles.data(), xp.tiles.size(), rel_elems(in),
+                                        rel_elems(o), 1, 0);
         if (!s) {
             p = new DevPlan();
             Blob b;
@@ -1150,6 +1208,8 @@ ea_status ea_exchange(ea_relation in, const ea_dim_part *new_parts, void *stream
                 p->nxtiles = (int64_t)xp.tiles.size();
                 p->xsrc = in->arena;
                 p->xdst = o->arena;
+                p->xsrc_elems = rel_elems(in);
+                p->xdst_elems = rel_elems(o);
                 p->esize = (int)elem_size(in->dtype);
                 g_cache[k.s] = p;
             } else {
@@ -1239,6 +1299,8 @@ ea_status ea_exchange_agg(ea_relation in, ea_agg agg, const ea_dim_part *new_par
         // in every copy only if that stride is a multiple of 16 bytes
         if (((in->blk_off.back() / m) * (int64_t)elem_size(in->dtype)) % 16)
             for (XSeg &g : xp.segs) g.vec = 0;
+        if (!s) s = check_exchange_plan(xp.segs.data(), xp.segs.size(), xp.tiles.data(), xp.tiles.size(), rel_elems(in),
+                                        rel_elems(o), m, in->blk_off.back() / m);
         if (!s) {
             p = new DevPlan();
             Blob b;
@@ -1251,6 +1313,8 @@ ea_status ea_exchange_agg(ea_relation in, ea_agg agg, const ea_dim_part *new_par
                 p->nxtiles = (int64_t)xp.tiles.size();
                 p->xsrc = in->arena;
                 p->xdst = o->arena;
+                p->xsrc_elems = rel_elems(in);
+                p->xdst_elems = rel_elems(o);
                 p->esize = (int)elem_size(in->dtype);
                 p->xdtype = in->dtype;
                 p->xagg = agg;
@@ -1313,6 +1377,7 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
         return set_error(EA_ERR_UNSUPPORTED, "the elementwise ROPE join reads a position-major table (rope_layout 0)");
     j.rope_pos = o.rope_pos;
     j.rope_dim = o.rope_dim;
+    j.simt_bf16 = o.simt_bf16 != 0;
     j.out2 = agg == EA_AGG_MAX_SUMEXP ? o.out2 : nullptr;
     if (agg == EA_AGG_MAX_SUMEXP && !j.out2) return set_error(EA_ERR_ARG, "MAX_SUMEXP needs opts->out2");
     // Letter tilings: from the inputs, which must agree; explicit parts must match.
@@ -1552,6 +1617,7 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
     key.v(j.rope_dim);
     if (j.row_rms) key.rel(j.row_rms);
     key.v(j.copy_letter);
+    key.v(j.simt_bf16);
     if (j.epi_in) key.rel(j.epi_in);
     cudaStream_t st = (cudaStream_t)stream;
     DevPlan *p = nullptr;
@@ -1570,6 +1636,12 @@ ea_status ea_joinagg_run(const char *spec, const ea_relation *inputs, int n_inpu
                 if (s == EA_ERR_UNSUPPORTED && (j.epi_map || j.row_rms)) {
                     s = set_error(EA_ERR_UNSUPPORTED, "an epilogue join needs the tcgen05 contraction path "
                                                       "(bf16 operands that TMA can tile)");
+                } else if (s == EA_ERR_UNSUPPORTED && !j.simt_bf16 &&
+                           std::all_of(j.in, j.in + j.sp.n_in,
+                                       [](const ea_relation_s *r) { return r->dtype == EA_BF16; })) {
+                    s = set_error(EA_ERR_UNSUPPORTED, "this bf16 contraction cannot run on the tcgen05 kernel "
+                                                      "(operand rows TMA cannot tile); opts->simt_bf16 lets it run "
+                                                      "on the SIMT kernel");
                 } else if (s == EA_ERR_UNSUPPORTED) {
                     free_plan(p);
                     p = new DevPlan();
@@ -1606,6 +1678,12 @@ ea_status ea_last_plan(int32_t *kernel_class, int32_t *launches, int64_t *tiles,
     if (tiles) *tiles = t_last.tiles;
     if (groups) *groups = t_last.groups;
     if (tuples) *tuples = t_last.tuples;
+    return EA_OK;
+}
+
+ea_status ea_last_plan_cluster(int32_t *ctas) {
+    if (!ctas) return set_error(EA_ERR_ARG, "ea_last_plan_cluster: NULL pointer");
+    *ctas = t_last.cluster;
     return EA_OK;
 }
 

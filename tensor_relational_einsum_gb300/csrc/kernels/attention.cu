@@ -269,24 +269,25 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             bool ok = true;
             // S_x = Q_x K_t^T
             auto mma_s = [&](int x, uint32_t t) {
-                const uint32_t qa = smem_u32(smem + C::Q_OFF + x * C::TILE);
-                const uint32_t kb = smem_u32(smem + C::K_OFF + (t % kKvStages) * C::TILE);
+                // the operands' descriptors once; each MMA adds a constant offset
+                const uint64_t qd = sdesc(smem_u32(smem + C::Q_OFF + x * C::TILE), 16, 1024);
+                const uint64_t kd = sdesc(smem_u32(smem + C::K_OFF + (t % kKvStages) * C::TILE), 16, 1024);
                 const uint32_t d = tmem + (uint32_t)(x * kKeys);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++)
-                    umma_bf16(d, sdesc(qa + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024),
-                              sdesc(kb + (kk >> 2) * (kKeys * 128) + (kk & 3) * 32, 16, 1024), idesc_s,
+                    umma_bf16(d, qd + (uint64_t)sdesc_off((kk >> 2) * (kRows * 128) + (kk & 3) * 32),
+                              kd + (uint64_t)sdesc_off((kk >> 2) * (kKeys * 128) + (kk & 3) * 32), idesc_s,
                               kk > 0 ? 1u : 0u);
                 umma_commit(&ctl->s_full[x]);
             };
             // O_x (+)= P_x V_t, P_x in the first 64 columns of S_x
             auto mma_o = [&](int x, uint32_t t, bool first) {
-                const uint32_t vb = smem_u32(smem + C::V_OFF + (t % kKvStages) * C::TILE);
+                const uint64_t vd = sdesc(smem_u32(smem + C::V_OFF + (t % kKvStages) * C::TILE), kKeys * 128, 1024);
                 const uint32_t pa = tmem + (uint32_t)(x * kKeys);
                 const uint32_t d = tmem + kOCol + (uint32_t)(x * D);
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; kk++)
-                    umma_bf16_ts(d, pa + kk * 8, sdesc(vb + kk * 2048, kKeys * 128, 1024), idesc_o,
+                    umma_bf16_ts(d, pa + kk * 8, vd + (uint64_t)sdesc_off(kk * 2048), idesc_o,
                                  (!first || kk > 0) ? 1u : 0u);
             };
             for (int ii = i0; ii < i1 && ok; ii++) {
@@ -473,6 +474,14 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                 ci++;
             }
             tc_fence_after();
+            bool in = true;
+            if constexpr (kBoundsCheck) {
+                // the query tile's output rows (and statistics rows) inside their arenas
+                const int64_t nr = nrows, one = 1;
+                in = range_in(Q.o_off, 1, &nr, &Q.o_rstr, D, 1, p.o_elems) &&
+                     (!p.m_out || range_in(Q.ml_off, 1, &nr, &Q.ml_rstr, 1, 0, p.ml_elems));
+                if (!in && row == 0) bounds_fail(p.err);
+            }
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint4 *dst = reinterpret_cast<uint4 *>(p.o + (Q.o_off + (int64_t)(row < nrows ? row : 0) * Q.o_rstr) * 2);
 #pragma unroll
@@ -485,7 +494,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
 #pragma unroll
                     for (int i = 0; i < 32; i++) o[i] = 0u;
                 }
-                if (row < nrows) {
+                if (row < nrows && in) {
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
                         const float *f = reinterpret_cast<const float *>(o + 8 * q);
@@ -499,7 +508,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                 }
             }
             tc_fence_before();
-            if (p.m_out && row < nrows) {
+            if (p.m_out && row < nrows && in) {
                 const int64_t o = Q.ml_off + (int64_t)row * Q.ml_rstr;
                 p.m_out[o] = m_max * p.scale;
                 p.l_out[o] = m_max == -INFINITY ? 0.f : l * ex2((m_ref - m_max) * c);

@@ -24,6 +24,21 @@ constexpr int kK = 64;  // k chunk
 // chunk is read into registers while the current one is multiplied from
 // shared memory, so each chunk costs one global round trip overlapped with
 // math.
+// A CTA's output tile, and every operand block its group's tuples read,
+// inside the arenas (checked by a library built with EA_DEBUG_BOUNDS).
+__device__ __forceinline__ bool ct_in(const CtParams &p, const CtGroup &G) {
+    const int64_t ce[3] = {G.M, G.N, G.nb}, cs[3] = {G.c_sm, G.c_sn, G.c_sb};
+    if (!range_in(G.c_base, 3, ce, cs, 1, 0, p.c_elems)) return false;
+    for (int t = G.t0; t < G.t1; t++) {
+        const CtTuple U = p.tuples[t];
+        const int64_t ae[3] = {G.M, U.K, G.nb}, as[3] = {U.a_sm, U.a_sk, U.a_sb};
+        const int64_t be[3] = {U.K, G.N, G.nb}, bs[3] = {U.b_sk, U.b_sn, U.b_sb};
+        if (!range_in(U.a_base, 3, ae, as, 1, 0, p.a_elems) || !range_in(U.b_base, 3, be, bs, 1, 0, p.b_elems))
+            return false;
+    }
+    return true;
+}
+
 template <int TT, int MT>
 __global__ void __launch_bounds__((TT / MT) * (TT / MT)) simt_contract_kernel(const CtParams p) {
     constexpr int NT = (TT / MT) * (TT / MT);
@@ -32,6 +47,12 @@ __global__ void __launch_bounds__((TT / MT) * (TT / MT)) simt_contract_kernel(co
     __shared__ float Bs[kK][TT + 4];
     const CtTile tile = p.tiles[blockIdx.x];
     const CtGroup G = p.groups[tile.group];
+    if constexpr (kBoundsCheck) {
+        if (!ct_in(p, G)) {
+            if (threadIdx.x == 0) bounds_fail(p.err);
+            return;
+        }
+    }
     const int tx = threadIdx.x % (TT / MT), ty = threadIdx.x / (TT / MT);
     float acc[MT][MT];
 #pragma unroll
@@ -146,6 +167,12 @@ __global__ void __launch_bounds__((TT / MT) * (TT / MT)) simt_ms_kernel(const Ct
     extern __shared__ float sm[];
     const CtTile tile = p.tiles[blockIdx.x];
     const CtGroup G = p.groups[tile.group];
+    if constexpr (kBoundsCheck) {
+        if (!ct_in(p, G)) {
+            if (threadIdx.x == 0) bounds_fail(p.err);
+            return;
+        }
+    }
     const int tx = threadIdx.x % (TT / MT), ty = threadIdx.x / (TT / MT);
     const int64_t m0 = tile.m0, n0 = tile.n0, bb = tile.batch;
     const float *A = reinterpret_cast<const float *>(p.a), *B = reinterpret_cast<const float *>(p.b);
@@ -239,6 +266,12 @@ __global__ void __launch_bounds__(256) simt_split_kernel(const CtParams p) {
     extern __shared__ float sm[];
     const CtTile tile = p.tiles[blockIdx.x];
     const CtGroup G = p.groups[tile.group];
+    if constexpr (kBoundsCheck) {
+        if (!ct_in(p, G)) {
+            if (threadIdx.x == 0) bounds_fail(p.err);
+            return;
+        }
+    }
     const int g = threadIdx.x / 64, lt = threadIdx.x % 64;
     const int tx = lt % 8, ty = lt / 8;
     const int64_t m0 = tile.m0, n0 = tile.n0, bb = tile.batch;

@@ -23,6 +23,16 @@
 //   warps 4-7 epilogue: tcgen05.ld of its 32 rows, scale, predicate mask
 //            (-inf), convert, write 128-byte swizzled rows into a staging
 //            buffer, TMA store (double-buffered).
+// With enough tiles the CTAs run in pairs (clusters of two, tcgen05
+// cta_group::2): a pair computes two M-adjacent tiles of the same output
+// columns as one 256 x BN tile.  Each CTA loads its own 128 A rows and its
+// own half of the B tile (plain TMA loads; the byte counts of both CTAs
+// complete on the even CTA's stage barrier), and the even CTA's MMA thread
+// issues M = 256 MMAs that read both CTAs' shared memory and write both
+// CTAs' TMEM.  L2 and each SM's shared memory serve every B byte once per
+// pair.  The MMA thread's commits signal the stage and accumulator barriers
+// of both CTAs (the odd CTA's through its shared::cluster address), and the
+// odd CTA's epilogue hands an accumulator back by a remote arrive.
 // Every mbarrier wait is bounded (2 s of %globaltimer); on time-out the
 // kernel raises the device error word, the other roles leave their loops,
 // the MMA issuer waits for its own MMAs, TMEM is freed and the CTA exits.
@@ -41,12 +51,13 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 256;
 
-template <int BN>
+template <int BN, bool PAIR>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // this CTA's rows of the B tile
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int STAGES = (192 * 1024) / STAGE;  // 4 or 6 alone, 6 or 8 in a pair
     static constexpr int STAGING = 2 * 16384;
     static constexpr int CTL = 256;
     static constexpr int SMEM = 1024 + STAGES * STAGE + STAGING + CTL;
@@ -66,15 +77,14 @@ struct SmemCtl {
 
 // ------------------------------------------------------------------ kernel
 
-template <int BN, int CL>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams p) {
-    using C = Cfg<BN>;
-    // CL CTAs of a cluster run tiles that share their B tile: each loads
-    // 1/CL of it and multicasts it to all, so L2 serves each B byte once
-    // per cluster; a stage is refilled only when every CTA's MMAs are done
-    // with it (their commits arrive on every CTA's `empty`).
-    constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1);
-    const int rank = CL > 1 ? (int)cluster_rank() : 0;
+    using C = Cfg<BN, PAIR>;
+    static_assert(C::STAGES <= 8, "stage barriers");
+    constexpr int CL = PAIR ? 2 : 1;
+    // In a pair, CTA rank 0 issues the MMAs; tiles 2u and 2u + 1 are rank 0's
+    // and rank 1's rows of unit u.
+    const int rank = PAIR ? (int)cluster_rank() : 0;
     const int nunits = (p.ntiles + CL - 1) / CL, unit0 = blockIdx.x / CL, ustep = gridDim.x / CL;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -88,11 +98,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; s++) {
             mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->empty[s], CL);
+            mbar_init(&ctl->empty[s], 1);
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(&ctl->tfull[a], 1);
-            mbar_init(&ctl->tempty[a], 1);
+            mbar_init(&ctl->tempty[a], CL);  // a pair's accumulator is free once both epilogues are done
         }
         mbar_init(&ctl->mma_done, 1);
         ctl->abort = 0;
@@ -100,10 +110,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
     }
-    if (warp == 2) tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+    if (warp == 2) {
+        if (PAIR) tmem_alloc_pair(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+        else tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+    }
     tc_fence_before();
     __syncthreads();
-    if (CL > 1) cluster_sync();  // every CTA's barriers are initialised before any multicast
+    if (PAIR) cluster_sync();  // both CTAs' barriers are initialised before either signals the other
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
 
@@ -127,14 +140,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                     }
                     const uint32_t sa = smem_u32(stages + stage * C::STAGE), sb = sa + C::A_BYTES;
                     uint64_t *fb = &ctl->full[stage];
-                    mbar_expect_tx(fb, C::STAGE);
-                    if (!p.a_mn_major) {
-                        tma_load_3d(sa, am, fb, kc * BK, T.m0, T.batch);
-                    } else {
-                        tma_load_3d(sa, am, fb, T.m0, kc * BK, T.batch);
-                        tma_load_3d(sa + 8192, am, fb, T.m0 + 64, kc * BK, T.batch);
-                    }
-                    if (CL == 1) {
+                    if (!PAIR) {
+                        mbar_expect_tx(fb, C::STAGE);
+                        if (!p.a_mn_major) {
+                            tma_load_3d(sa, am, fb, kc * BK, T.m0, T.batch);
+                        } else {
+                            tma_load_3d(sa, am, fb, T.m0, kc * BK, T.batch);
+                            tma_load_3d(sa + 8192, am, fb, T.m0 + 64, kc * BK, T.batch);
+                        }
                         if (!p.b_mn_major) {
                             tma_load_3d(sb, bm, fb, kc * BK, T.n0, T.batch);
                         } else {
@@ -143,16 +156,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                                 tma_load_3d(sb + j * 8192, bm, fb, T.n0 + 64 * j, kc * BK, T.batch);
                         }
                     } else {
-                        // this CTA's 1/CL of the B tile, to every CTA of the cluster
-                        constexpr int ROWS = BN / CL;
+                        // this CTA's A rows and its half of the B tile, counted on rank 0's barrier
+                        const uint32_t fc = mapa_u32(smem_u32(fb), 0);
+                        if (rank == 0) mbar_expect_tx(fb, 2 * C::STAGE);
+                        if (!p.a_mn_major) {
+                            tma_load_3d_pair(sa, am, fc, kc * BK, T.m0, T.batch);
+                        } else {
+                            tma_load_3d_pair(sa, am, fc, T.m0, kc * BK, T.batch);
+                            tma_load_3d_pair(sa + 8192, am, fc, T.m0 + 64, kc * BK, T.batch);
+                        }
+                        const int n_half = T.n0 + rank * C::B_ROWS;
                         if (!p.b_mn_major) {
-                            tma_load_3d_mc(sb + rank * ROWS * 128, bm, fb, kc * BK, T.n0 + rank * ROWS, T.batch, kMask);
+                            tma_load_3d_pair(sb, bm, fc, kc * BK, n_half, T.batch);
                         } else {
 #pragma unroll
-                            for (int j = 0; j < ROWS / 64; j++) {
-                                const int jj = rank * (ROWS / 64) + j;
-                                tma_load_3d_mc(sb + jj * 8192, bm, fb, T.n0 + 64 * jj, kc * BK, T.batch, kMask);
-                            }
+                            for (int j = 0; j < C::B_ROWS / 64; j++)
+                                tma_load_3d_pair(sb + j * 8192, bm, fc, n_half + 64 * j, kc * BK, T.batch);
                         }
                     }
                     armed |= 1u << stage;
@@ -167,19 +186,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
         }
         if (*abort) {
             // Let our own copies land before the CTA can exit.
-            for (int s = 0; s < C::STAGES; s++)
-                if (armed & (1u << s)) mbar_wait(&ctl->full[s], (armed_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
+            if (!PAIR || rank == 0) {
+                for (int s = 0; s < C::STAGES; s++)
+                    if (armed & (1u << s))
+                        mbar_wait(&ctl->full[s], (armed_par >> s) & 1, abort, p.err, 0, kDrainNs, false);
+            } else if (armed) {
+                // rank 1's copies complete on rank 0's barriers: give them the drain time
+                const uint64_t t0 = gtime();
+                while (gtime() - t0 < kDrainNs) {
+                }
+            }
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && rank == 0) {
         // ------------------------------------------------ MMA issuer
-        const uint32_t idesc = make_idesc(BM, BN, p.a_mn_major, p.b_mn_major);
+        const uint32_t idesc = make_idesc(CL * BM, BN, p.a_mn_major, p.b_mn_major);
+        // descriptor layout and the address step of one K = 16 slice: a
+        // K-major operand advances 32 bytes inside its 128-byte rows, an
+        // MN-major one 16 rows of 128 bytes
+        const uint32_t a_lbo = p.a_mn_major ? 8192 : 16, b_lbo = p.b_mn_major ? 8192 : 16;
+        const uint64_t a_step = sdesc_off(p.a_mn_major ? 2048 : 32), b_step = sdesc_off(p.b_mn_major ? 2048 : 32);
         int stage = 0, acc = 0;
         uint32_t ph = 0, acc_ph = 0;
         bool ok = true;
         for (int unit = unit0; unit < nunits && ok; unit += ustep) {
             const TcTile T = p.tiles[unit * CL + rank];
             const TcGroup G = p.groups[T.group];
-            if (!mbar_wait(&ctl->tempty[acc], acc_ph ^ 1, abort, p.err, kDevTimeoutMma)) break;
+            if (!mbar_wait<PAIR>(&ctl->tempty[acc], acc_ph ^ 1, abort, p.err, kDevTimeoutMma)) break;
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(acc * BN);
             uint32_t accumulate = 0;
@@ -191,16 +223,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                         break;
                     }
                     tc_fence_after();
+                    // the stage's descriptors once; each MMA adds a constant step
                     const uint32_t sa = smem_u32(stages + stage * C::STAGE), sb = sa + C::A_BYTES;
+                    const uint64_t ad = sdesc(sa, a_lbo, 1024), bd = sdesc(sb, b_lbo, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; kk++) {
-                        const uint64_t ad = p.a_mn_major ? sdesc(sa + kk * 2048, 8192, 1024) : sdesc(sa + kk * 32, 16, 1024);
-                        const uint64_t bd = p.b_mn_major ? sdesc(sb + kk * 2048, 8192, 1024) : sdesc(sb + kk * 32, 16, 1024);
-                        umma_bf16(d, ad, bd, idesc, accumulate);
+                        if (PAIR) umma_bf16_pair(d, ad + kk * a_step, bd + kk * b_step, idesc, accumulate);
+                        else umma_bf16(d, ad + kk * a_step, bd + kk * b_step, idesc, accumulate);
                         accumulate = 1;
                     }
-                    if (CL == 1) umma_commit(&ctl->empty[stage]);
-                    else umma_commit_mc(&ctl->empty[stage], kMask);
+                    if (!PAIR) {
+                        umma_commit(&ctl->empty[stage]);
+                    } else {
+                        umma_commit_pair(smem_u32(&ctl->empty[stage]));
+                        umma_commit_pair(mapa_u32(smem_u32(&ctl->empty[stage]), 1));  // rank 1's
+                    }
                     if (++stage == C::STAGES) {
                         stage = 0;
                         ph ^= 1;
@@ -208,12 +245,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                 }
             }
             if (!ok) break;
-            umma_commit(&ctl->tfull[acc]);
+            if (!PAIR) {
+                umma_commit(&ctl->tfull[acc]);
+            } else {
+                umma_commit_pair(smem_u32(&ctl->tfull[acc]));
+                umma_commit_pair(mapa_u32(smem_u32(&ctl->tfull[acc]), 1));
+            }
             acc ^= 1;
             if (acc == 0) acc_ph ^= 1;
         }
         // Every MMA this thread issued has completed once mma_done flips.
-        umma_commit(&ctl->mma_done);
+        if (PAIR) umma_commit_pair(smem_u32(&ctl->mma_done));
+        else umma_commit(&ctl->mma_done);
         mbar_wait(&ctl->mma_done, 0, abort, p.err, kDevTimeoutMma, kTimeoutNs, false);
     } else if (warp >= 4) {
         // ------------------------------------------------ epilogue
@@ -226,7 +269,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
             const TcTile T = p.tiles[unit * CL + rank];
             const TcGroup G = p.groups[T.group];
             const CUtensorMap *om = maps + G.out_map;
-            const bool store = T.m0 < G.m_ext;  // a padding tile of a cluster is computed, not stored
+            bool store = T.m0 < G.m_ext;  // a padding tile of a CTA pair is computed, not stored
+            if constexpr (kBoundsCheck) {
+                // the rows of the tile the epilogue reads: the residual block
+                // and the row scale (the output goes through its tensor map)
+                const int64_t rows = min64(128, (int64_t)G.m_ext - T.m0), cols = min64(BN, (int64_t)G.n_ext - T.n0);
+                bool in = true;
+                if (store && p.epi == 1)
+                    in = range_in(G.e_base + (int64_t)T.batch * G.e_sb + (int64_t)T.m0 * G.e_sm + T.n0, 1, &rows,
+                                  &G.e_sm, cols, 1, p.epi_elems);
+                const int64_t one = 1;
+                if (store && p.row_rms) in = in && range_in(G.r_lo + T.m0, 1, &rows, &one, 1, 0, p.rms_elems);
+                if (!in) {
+                    if (ep == 0) bounds_fail(p.err);
+                    store = false;
+                }
+            }
             if (ep == 0) ctl->ep_ok = mbar_wait(&ctl->tfull[acc], acc_ph, abort, p.err, kDevTimeoutEpilogue) ? 1 : 0;
             named_bar(1, 128);
             if (!ctl->ep_ok) break;
@@ -234,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
             const uint32_t tb = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * BN);
             const int64_t m_g = G.m_lo + T.m0 + ep;
             // the row's scale: scale, times rsqrt(row_rms + eps) for a fused RMSNorm apply
-            const float sc = (p.row_rms && T.m0 + ep < G.m_ext)
+            const float sc = (p.row_rms && store && T.m0 + ep < G.m_ext)
                                  ? p.scale * rsqrtf(__ldg(p.row_rms + G.r_lo + T.m0 + ep) + p.eps)
                                  : p.scale;
             // epilogue join SiLU(g) * u over column pairs: 128 planned columns -> 64 stored
@@ -385,7 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
             }
             tc_fence_before();
             named_bar(1, 128);
-            if (ep == 0) mbar_arrive(&ctl->tempty[acc]);
+            if (ep == 0) {
+                if (rank == 0) mbar_arrive(&ctl->tempty[acc]);
+                else mbar_arrive_cluster(mapa_u32(smem_u32(&ctl->tempty[acc]), 0));
+            }
             acc ^= 1;
             if (acc == 0) acc_ph ^= 1;
         }
@@ -394,28 +455,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
 
     tc_fence_before();
     __syncthreads();
+    // No CTA of a pair frees TMEM or leaves while the other may still signal
+    // it, or the pair's MMAs may still read its shared memory.
+    if (PAIR) cluster_sync();
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        if (PAIR) tmem_dealloc_pair(tmem, C::TMEM_COLS);
+        else tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    if (CL > 1) cluster_sync();  // no CTA leaves while a peer may still signal or fill its shared memory
 }
 
-template <int BN, int CL>
+template <int BN, bool PAIR>
 cudaError_t launch_bn(const TcParams &p, int num_sms, cudaStream_t st) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, PAIR>;
+    constexpr int CL = PAIR ? 2 : 1;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(tc_contract_kernel<BN, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        e = cudaFuncSetAttribute(tc_contract_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
     const int units = (p.ntiles + CL - 1) / CL;
-    if (CL == 1) {
-        tc_contract_kernel<BN, CL><<<std::min<int>(units, num_sms), kThreads, C::SMEM, st>>>(p);
+    if (!PAIR) {
+        tc_contract_kernel<BN, PAIR><<<std::min<int>(units, num_sms), kThreads, C::SMEM, st>>>(p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -435,25 +500,23 @@ cudaError_t launch_bn(const TcParams &p, int num_sms, cudaStream_t st) {
     const int di = (dev >= 0 && dev < 64) ? dev : 0;
     if (resident[di] == 0) {
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, tc_contract_kernel<BN, CL>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, tc_contract_kernel<BN, PAIR>, &cfg);
         if (e != cudaSuccess) return e;
         resident[di] = n > 0 ? n : std::max(1, num_sms / CL);
     }
     cfg.gridDim = dim3(CL * std::max(1, std::min(units, resident[di])), 1, 1);
-    return cudaLaunchKernelEx(&cfg, tc_contract_kernel<BN, CL>, p);
+    return cudaLaunchKernelEx(&cfg, tc_contract_kernel<BN, PAIR>, p);
 }
 
 }  // namespace
 
-int tc_smem_bytes(int bn) { return bn == 256 ? Cfg<256>::SMEM : Cfg<128>::SMEM; }
-
 cudaError_t launch_contract_tc(const TcParams &p, int num_sms, cudaStream_t st) {
     if (p.cluster == 2) {
-        if (p.bn == 256) return launch_bn<256, 2>(p, num_sms, st);
-        return launch_bn<128, 2>(p, num_sms, st);
+        if (p.bn == 256) return launch_bn<256, true>(p, num_sms, st);
+        return launch_bn<128, true>(p, num_sms, st);
     }
-    if (p.bn == 256) return launch_bn<256, 1>(p, num_sms, st);
-    return launch_bn<128, 1>(p, num_sms, st);
+    if (p.bn == 256) return launch_bn<256, false>(p, num_sms, st);
+    return launch_bn<128, false>(p, num_sms, st);
 }
 
 }  // namespace ea

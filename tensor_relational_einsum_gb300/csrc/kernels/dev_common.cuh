@@ -111,6 +111,57 @@ __device__ __forceinline__ float fmap(float v0, float v1, float v2, float scale,
     else return v0;
 }
 
+// ---- bounds checks of a library built with EA_DEBUG_BOUNDS: before a tile
+// (or segment, view, operand block) is touched, its element range is
+// checked against its arena; outside it, the kernel raises the device error
+// word (kDevBounds) and skips the access.  Compiled out otherwise.
+#ifdef EA_DEBUG_BOUNDS
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+
+// base + sum_i c_i str_i (0 <= c_i < ext_i) + c len_str (0 <= c < len)
+// inside [0, elems); an empty range always is.
+__device__ __forceinline__ bool range_in(int64_t base, int n, const int64_t *ext, const int64_t *str, int64_t len,
+                                         int64_t len_str, int64_t elems) {
+    if (len <= 0) return true;
+    int64_t lo = base, hi = base;
+    for (int i = 0; i < n; i++) {
+        if (ext[i] <= 0) return true;
+        const int64_t span = (ext[i] - 1) * str[i];
+        if (span < 0) lo += span;
+        else hi += span;
+    }
+    const int64_t span = (len - 1) * len_str;
+    if (span < 0) lo += span;
+    else hi += span;
+    return lo >= 0 && hi < elems;
+}
+
+__device__ __forceinline__ bool bounds_fail(int *err) {
+    if (err) atomicCAS(err, 0, (int)kDevBounds);
+    return false;
+}
+
+// A view (elementwise join or row reduction) inside its output and input arenas.
+__device__ __forceinline__ bool view_in(const EwItem &it, int n_in, const int64_t *in_elems, int64_t out_elems) {
+    if (!range_in(it.out_base, it.nd, it.ext, it.ostr, it.len, it.out_inner, out_elems)) return false;
+    for (int k = 0; k < n_in; k++)
+        if (!range_in(it.in_base[k], it.nd, it.ext, it.istr[k], it.len, it.in_inner[k], in_elems[k])) return false;
+    return true;
+}
+
+// An exchange segment's rows inside both arenas (copies: copy q read at
+// q * copy_stride further on).
+__device__ __forceinline__ bool seg_in(const XSeg &g, const XTile &T, int64_t src_elems, int64_t dst_elems,
+                                       int copies = 1, int64_t copy_stride = 0) {
+    if (T.row0 < 0 || T.row0 + T.nrows > g.rows || T.col0 < 0 || T.col0 + T.ncols > g.inner) return false;
+    const int64_t s_hi = (copies - 1) * copy_stride;
+    return range_in(g.src_off, g.nd, g.ext, g.sstr, g.inner, 1, src_elems - s_hi) &&
+           range_in(g.dst_off, g.nd, g.ext, g.dstr, g.inner, 1, dst_elems);
+}
+
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 

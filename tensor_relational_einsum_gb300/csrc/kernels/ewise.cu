@@ -183,6 +183,13 @@ __global__ void __launch_bounds__(kThreads, 3) ewise_kernel(const EwParams p) {
     const int mask = MASK < 0 ? p.stream_mask : MASK;
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const EwTile T = p.tiles[t];
+        if constexpr (kBoundsCheck) {
+            if (!view_in(p.items[T.item], p.n_in, p.in_elems, p.out_elems) || T.row0 < 0 ||
+                T.row0 + T.nrows > p.items[T.item].rows || T.col0 < 0 || T.col0 + T.ncols > p.items[T.item].len) {
+                if (threadIdx.x == 0) bounds_fail(p.err);
+                continue;
+            }
+        }
         __syncthreads();
         if (threadIdx.x == 0) {
             const EwItem &it = p.items[T.item];

@@ -14,7 +14,7 @@
 // stores are marked streaming.
 #include <algorithm>
 
-#include "../ea_internal.h"
+#include "dev_common.cuh"
 
 namespace ea {
 
@@ -40,7 +40,7 @@ __device__ __forceinline__ void seg_row(const XSeg &g, int64_t r, int64_t *so, i
 __global__ void __launch_bounds__(kThreads, 3) exchange_kernel(const XSeg *__restrict__ segs,
                                                             const XTile *__restrict__ tiles, int64_t ntiles,
                                                             const char *__restrict__ src, char *__restrict__ dst,
-                                                            int esize) {
+                                                            int esize, int64_t src_elems, int64_t dst_elems, int *err) {
     __shared__ XSeg sg;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -49,6 +49,12 @@ __global__ void __launch_bounds__(kThreads, 3) exchange_kernel(const XSeg *__res
         if (threadIdx.x < (int)(sizeof(XSeg) / 8))
             reinterpret_cast<int64_t *>(&sg)[threadIdx.x] = reinterpret_cast<const int64_t *>(segs + T.seg)[threadIdx.x];
         __syncthreads();
+        if constexpr (kBoundsCheck) {
+            if (!seg_in(sg, T, src_elems, dst_elems)) {
+                if (threadIdx.x == 0) bounds_fail(err);
+                continue;
+            }
+        }
         if (sg.vec) {
             // a warp (or a slice of one, for short rows) copies a row: each
             // lane keeps kUnroll 16-byte loads in flight before it stores
@@ -98,10 +104,11 @@ __global__ void __launch_bounds__(kThreads, 3) exchange_kernel(const XSeg *__res
 }  // namespace
 
 cudaError_t launch_exchange(const XSeg *segs, const XTile *tiles, int64_t ntiles, const char *src, char *dst,
-                            int esize, int num_sms, cudaStream_t st) {
+                            int esize, int num_sms, cudaStream_t st, int64_t src_elems, int64_t dst_elems, int *err) {
     // Eight resident CTAs of 256 threads per SM; persistent over the tiles.
     int64_t grid = std::min<int64_t>(ntiles, (int64_t)num_sms * 8);
-    exchange_kernel<<<(unsigned)grid, kThreads, 0, st>>>(segs, tiles, ntiles, src, dst, esize);
+    exchange_kernel<<<(unsigned)grid, kThreads, 0, st>>>(segs, tiles, ntiles, src, dst, esize, src_elems, dst_elems,
+                                                         err);
     return cudaGetLastError();
 }
 

@@ -15,7 +15,7 @@
 
 #include <cuda_bf16.h>
 
-#include "../ea_internal.h"
+#include "dev_common.cuh"
 
 namespace ea {
 
@@ -88,7 +88,8 @@ template <bool kBf16, int AGG>
 __global__ void __launch_bounds__(kThreads, 3) exchange_agg_kernel(const XSeg *__restrict__ segs,
                                                                 const XTile *__restrict__ tiles, int64_t ntiles,
                                                                 const char *__restrict__ src, char *__restrict__ dst,
-                                                                int ncopies, int64_t copy_stride) {
+                                                                int ncopies, int64_t copy_stride, int64_t src_elems,
+                                                                int64_t dst_elems, int *err) {
     constexpr int esize = kBf16 ? 2 : 4;
     constexpr int EPC = 16 / esize;  // elements per 16-byte chunk
     __shared__ XSeg sg;
@@ -100,6 +101,12 @@ __global__ void __launch_bounds__(kThreads, 3) exchange_agg_kernel(const XSeg *_
         if (threadIdx.x < (int)(sizeof(XSeg) / 8))
             reinterpret_cast<int64_t *>(&sg)[threadIdx.x] = reinterpret_cast<const int64_t *>(segs + T.seg)[threadIdx.x];
         __syncthreads();
+        if constexpr (kBoundsCheck) {
+            if (!seg_in(sg, T, src_elems, dst_elems, ncopies, copy_stride)) {
+                if (threadIdx.x == 0) bounds_fail(err);
+                continue;
+            }
+        }
         if (sg.vec) {
             const int cpr = (int)(T.ncols * esize / 16);
             int lpr = 32;
@@ -159,22 +166,19 @@ __global__ void __launch_bounds__(kThreads, 3) exchange_agg_kernel(const XSeg *_
 }  // namespace
 
 cudaError_t launch_exchange_agg(const XSeg *segs, const XTile *tiles, int64_t ntiles, const char *src, char *dst,
-                                int dtype, int agg, int ncopies, int64_t copy_stride, int num_sms, cudaStream_t st) {
+                                int dtype, int agg, int ncopies, int64_t copy_stride, int num_sms, cudaStream_t st,
+                                int64_t src_elems, int64_t dst_elems, int *err) {
     const int64_t grid = std::min<int64_t>(ntiles, (int64_t)num_sms * 8);
+    auto go = [&](auto kernel) {
+        kernel<<<(unsigned)grid, kThreads, 0, st>>>(segs, tiles, ntiles, src, dst, ncopies, copy_stride, src_elems,
+                                                    dst_elems, err);
+    };
     if (dtype == EA_BF16) {
-        if (agg == EA_AGG_MAX)
-            exchange_agg_kernel<true, EA_AGG_MAX><<<(unsigned)grid, kThreads, 0, st>>>(segs, tiles, ntiles, src, dst,
-                                                                                       ncopies, copy_stride);
-        else
-            exchange_agg_kernel<true, EA_AGG_SUM><<<(unsigned)grid, kThreads, 0, st>>>(segs, tiles, ntiles, src, dst,
-                                                                                       ncopies, copy_stride);
+        if (agg == EA_AGG_MAX) go(exchange_agg_kernel<true, EA_AGG_MAX>);
+        else go(exchange_agg_kernel<true, EA_AGG_SUM>);
     } else {
-        if (agg == EA_AGG_MAX)
-            exchange_agg_kernel<false, EA_AGG_MAX><<<(unsigned)grid, kThreads, 0, st>>>(segs, tiles, ntiles, src, dst,
-                                                                                        ncopies, copy_stride);
-        else
-            exchange_agg_kernel<false, EA_AGG_SUM><<<(unsigned)grid, kThreads, 0, st>>>(segs, tiles, ntiles, src, dst,
-                                                                                        ncopies, copy_stride);
+        if (agg == EA_AGG_MAX) go(exchange_agg_kernel<false, EA_AGG_MAX>);
+        else go(exchange_agg_kernel<false, EA_AGG_SUM>);
     }
     return cudaGetLastError();
 }

@@ -22,7 +22,10 @@
 // static host buffer and copied into the array with cudaMemcpyAsync on the
 // caller's stream, right before the kernel.  Every call shares the array:
 // two calls whose copies and kernels overlap on the GPU (different streams
-// without ordering between them) race on it.
+// without ordering between them) race on it.  A call on a stream that is
+// being captured into a CUDA graph is refused: a captured copy would read
+// the static host buffer when the graph is replayed, by which time a later
+// call may have put another plan there.
 #include <string.h>
 
 #include <mutex>
@@ -152,10 +155,17 @@ extern "C" ea_status ea_exchange_noalloc(ea_relation in, ea_relation out, void *
         if (in->dims[d] != out->dims[d]) return set_error(EA_ERR_SHAPE, "ea_exchange_noalloc: extents differ");
     if (in->bytes && out->bytes && out->arena < in->arena + in->bytes && in->arena < out->arena + out->bytes)
         return set_error(EA_ERR_ARG, "ea_exchange_noalloc: input and output arenas overlap");
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cap);
+    if (e != cudaSuccess) return cuda_error(e, "ea_exchange_noalloc: cudaStreamIsCapturing");
+    if (cap != cudaStreamCaptureStatusNone)
+        return set_error(EA_ERR_UNSUPPORTED, "ea_exchange_noalloc: the stream is being captured; the plan copy "
+                                             "reads a static host buffer that later calls overwrite");
     std::lock_guard<std::mutex> lk(g_na_mu);
     // -- set-up, once per device, with that device current
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_error(e, "ea_exchange_noalloc: cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return set_error(EA_ERR_ARG, "ea_exchange_noalloc: device %d out of range", dev);
     if (!g_ready[dev]) {
@@ -240,14 +250,20 @@ extern "C" ea_status ea_exchange_noalloc(ea_relation in, ea_relation out, void *
                          "use ea_exchange",
                          kNoAllocScratchBytes, (long long)natoms);
     if (em.ntile == 0) return EA_OK;
+    ea_status cs = check_exchange_plan(reinterpret_cast<const XSeg *>(g_stage.plan), em.nseg, g_stage.tiles, em.ntile,
+                                       rel_elems(in), rel_elems(out), 1, 0);
+    if (cs) return cs;
     memcpy(g_stage.plan + seg_bytes, g_stage.tiles, em.ntile * sizeof(XTile));
     // -- copy the plan into the device array and launch, both on the caller's stream
     char *scratch = static_cast<char *>(g_scratch_dev[dev]);
-    cudaStream_t st = (cudaStream_t)stream;
     e = cudaMemcpyAsync(scratch, g_stage.plan, total, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_error(e, "ea_exchange_noalloc: cudaMemcpyAsync(plan)");
+    // (no device error word: the library's word is taken with cudaMalloc on
+    // a device's first allocating call; the plan was checked above, and a
+    // library built with EA_DEBUG_BOUNDS still skips an out-of-arena tile)
     e = launch_exchange(reinterpret_cast<const XSeg *>(scratch), reinterpret_cast<const XTile *>(scratch + seg_bytes),
-                        (int64_t)em.ntile, in->arena, out->arena, esize, g_sms[dev], st);
+                        (int64_t)em.ntile, in->arena, out->arena, esize, g_sms[dev], st, rel_elems(in),
+                        rel_elems(out), nullptr);
     if (e != cudaSuccess) return cuda_error(e, "ea_exchange_noalloc: kernel launch");
     return EA_OK;
 }

@@ -227,6 +227,16 @@ __global__ void __launch_bounds__(kThreads, (RrMinBlocks<AGG, MAP, MASK>::value)
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const RrTile T = p.tiles[t];
         const RrGroup G = p.groups[T.group];
+        if constexpr (kBoundsCheck) {
+            bool in = true;
+            for (int i = G.i0; i < G.i1 && in; i++)
+                in = view_in(p.items[i], p.n_in, p.in_elems, p.out_elems) && T.row0 >= 0 &&
+                     T.row0 + T.nrows <= p.items[i].rows;
+            if (!in) {
+                if (threadIdx.x == 0) bounds_fail(p.err);
+                continue;
+            }
+        }
         // lanes per row: a power of two giving each lane about U chunks of
         // a row segment; short segments pack several rows to a warp
         constexpr int NSr = MASK < 0 ? NIN : ((MASK & 1) + ((MASK >> 1) & 1) + ((MASK >> 2) & 1));
@@ -338,6 +348,16 @@ __global__ void __launch_bounds__(kThreads, (RrMinBlocks<AGG, MAP, MASK>::value)
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const RrTile T = p.tiles[t];
         const RrGroup G = p.groups[T.group];
+        if constexpr (kBoundsCheck) {
+            bool in = true;
+            for (int i = G.i0; i < G.i1 && in; i++)
+                in = view_in(p.items[i], p.n_in, p.in_elems, p.out_elems) && T.row0 >= 0 &&
+                     T.row0 + T.nrows <= p.items[i].rows;
+            if (!in) {
+                if (threadIdx.x == 0) bounds_fail(p.err);
+                continue;
+            }
+        }
         const int n = G.i1 - G.i0;
         __syncthreads();
         if (threadIdx.x < n) {
@@ -470,6 +490,18 @@ __device__ __forceinline__ RbUnit rb_unpack(int64_t w) {
     return d;
 }
 
+// A row-batch tile's rows inside the input and output arenas (its flat
+// descriptor: first-row offset and row stride per block, output offset and
+// stride, segment length, rows and blocks).
+__device__ __forceinline__ bool rb_in(const RrParams &p, int64_t t) {
+    const int64_t *w = p.rb_desc + t * kRbWords;
+    const int64_t rows = (int64_t)(uint32_t)(w[11] & 0xFFFFFFFF), nb = w[11] >> 32, len = w[10];
+    if (nb < 1 || nb > 4) return false;
+    for (int64_t b = 0; b < nb; b++)
+        if (!range_in(w[b], 1, &rows, &w[4 + b], len, 1, p.in_elems[0])) return false;
+    return range_in(w[8], 1, &rows, &w[9], 1, 0, p.out_elems);
+}
+
 // SUM (or SUM of squares) of one input over rows whose segments lie in at
 // most four blocks of one length (no predicate): a warp (or a slice of one)
 // requests a row's segments in all its blocks together, 64 bytes per lane
@@ -487,6 +519,12 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_kernel(const R
     for (; t < t1; t++) {
         const RbUnit d = rb_unpack(wnext);
         if (t + 1 < t1) wnext = rb_word(p, t + 1, lane);
+        if constexpr (kBoundsCheck) {
+            if (!rb_in(p, t)) {
+                if (lane == 0) bounds_fail(p.err);
+                continue;
+            }
+        }
         const int n = d.n;
         const int64_t len = d.len, chunks = len / 8;
         int lpb = 32;
@@ -553,6 +591,12 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_stats_kernel(c
     for (; t < t1; t++) {
         const RbUnit d = rb_unpack(wnext);
         if (t + 1 < t1) wnext = rb_word(p, t + 1, lane);
+        if constexpr (kBoundsCheck) {
+            if (!rb_in(p, t)) {
+                if (lane == 0) bounds_fail(p.err);
+                continue;
+            }
+        }
         const int n = d.n;
         const int64_t len = d.len, chunks = len / EPC;
         int lpb = 32;

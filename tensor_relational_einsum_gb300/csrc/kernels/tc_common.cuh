@@ -36,15 +36,27 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
 }
 
+// CLUSTER: acquire at cluster scope, for barriers that threads of the other
+// CTA of a pair arrive on.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
-        : "memory");
+    if (CLUSTER)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(b)), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(b)), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
@@ -53,12 +65,13 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
 // the device error word with `code`.  Inlined: as a called function the wait
 // cost its caller some 400 cycles of register saves and restores even when
 // the phase had long completed, which stalled the single MMA-issuing thread.
+template <bool CLUSTER = false>
 static __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort, int *err,
                                                  int code, uint64_t limit = kTimeoutNs, bool watch_abort = true) {
-    if (mbar_try(b, parity)) return true;
+    if (mbar_try<CLUSTER>(b, parity)) return true;
     const uint64_t t0 = gtime();
     for (uint32_t i = 1;; i++) {
-        if (mbar_try(b, parity)) return true;
+        if (mbar_try<CLUSTER>(b, parity)) return true;
         if ((i & 31) == 0) {
             if (watch_abort && *abort) return false;
             if (gtime() - t0 > limit) {
@@ -87,16 +100,65 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *map, uint6
         : "memory");
 }
 
-// The same box delivered to the same shared-memory offset of every CTA of
-// the cluster in `mask`, completing bytes on the mbarrier at `bar`'s offset
-// in each of them.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void *map, uint64_t *bar, int c0, int c1, int c2,
-                                               uint16_t mask) {
+// ---- CTA pairs (tcgen05 cta_group::2): the two CTAs of a cluster of two
+// run one MMA of M = 256 over both CTAs' shared memory and TMEM.
+
+// The shared::cluster address of the same shared-memory offset as `addr` in
+// CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// A tile load into this CTA's shared memory whose byte count completes on
+// the mbarrier at the shared::cluster address `bar_cl`, which may lie in
+// either CTA of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *map, uint32_t bar_cl, int c0, int c1,
+                                                 int c2) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
-        "[%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(map), "r"(bar_cl), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cl) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
+}
+
+// TMEM of a pair: one warp of each CTA allocates (and frees) together; both
+// CTAs get the same columns.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D (+)= A B over the pair, issued by one thread of the even CTA: rows
+// [0, 128) of A and D live in the even CTA, rows [128, 256) in the odd one
+// (same shared-memory and TMEM offsets); B's first N/2 rows come from the
+// even CTA's shared memory, the other N/2 from the odd CTA's.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at the shared::cluster address `bar_cl` (either
+// CTA of the pair) when every pair MMA this thread issued so far is done.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar_cl) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_cl)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -162,15 +224,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
                  : "memory");
 }
 
-// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once all
-// prior MMAs of this thread are done.
-__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                     smem_u32(bar)),
-                 "h"(mask)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -219,6 +272,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
     return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
+
+// The change of a descriptor's start-address field when the operand starts
+// `bytes` further on (the field holds the address >> 4; shared-memory
+// addresses stay below 2^18, so adding to the field never carries out).
+__host__ __device__ constexpr uint32_t sdesc_off(int bytes) { return (uint32_t)bytes >> 4; }
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9, 10-12 = 1), operand majors (bit 15 A, bit 16 B; 1 = MN-major),

@@ -55,6 +55,7 @@ struct DevPlan {
     int64_t nxtiles = 0;
     const char *xsrc = nullptr;
     char *xdst = nullptr;
+    int64_t xsrc_elems = 0, xdst_elems = 0;  // arena sizes (EA_DEBUG_BOUNDS checks)
     int esize = 0;
     int xdtype = 0, xagg = 0, xcopies = 1;  // exchange with aggregation
     int64_t xcopy_stride = 0;
@@ -70,6 +71,7 @@ struct DevPlan {
 struct LastPlan {
     int32_t kind = -1, launches = 0;
     int64_t tiles = 0, groups = 0, tuples = 0;
+    int32_t cluster = 1;  // CTAs that share one MMA tile (tcgen05 contraction: 2 = CTA pairs)
 };
 extern thread_local LastPlan t_last;
 

@@ -196,7 +196,7 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
             parts: dict | None = None, rope_table: torch.Tensor | None = None, rope_pos: str | None = None,
             out2: Relation | None = None, epi_map: str | None = None, epi_in: Relation | None = None,
             epi_pair: str | None = None, rope_dim: int = 0, row_rms: Relation | None = None,
-            partials: bool = False, rope_layout: int = 0, stream=None) -> Relation:
+            partials: bool = False, rope_layout: int = 0, simt_bf16: bool = False, stream=None) -> Relation:
     """Run one join-agg ("Every Kernel Is a Join", Definition 3.7) with
     libea.so.  ``pred="ts"`` keeps joined tuples with t <= s.  With
     ``agg="max_sumexp"`` the output receives the MAX and ``out2`` the SUM
@@ -210,7 +210,9 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
     input only) as the innermost output letter and stores SiLU(c=0) * (c=1).
     ``partials=True`` runs a contraction without its aggregation: the output
     gains a leading copy dimension of m unit blocks, copy q holding each
-    block's q-th function specification alone (``exchange_agg`` sums them)."""
+    block's q-th function specification alone (``exchange_agg`` sums them).
+    A bf16 contraction the tensor-core kernel cannot tile raises unless
+    ``simt_bf16=True`` lets it run on the (much slower) SIMT kernel."""
     if out is None:
         dims, bounds = output_layout(spec, inputs)
         if partials:
@@ -236,6 +238,7 @@ def joinagg(spec: str, inputs, agg: str = "sum", map: str = "product", out: Rela
     if row_rms is not None:
         o.row_rms = row_rms.handle.value
     o.partials = 1 if partials else 0
+    o.simt_bf16 = 1 if simt_bf16 else 0
     if epi_map is not None:
         o.epi_map = MAPS[epi_map]
         if epi_in is not None:

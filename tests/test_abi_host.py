@@ -29,7 +29,7 @@ def test_exports_every_declared_symbol(L):
     assert {"ea_relation_create", "ea_joinagg_run", "ea_exchange"} <= names
     for n in sorted(names):
         assert hasattr(L, n), n
-    assert L.ea_abi_version() == 4
+    assert L.ea_abi_version() == 5
 
 
 def plan(L, spec, shapes, parts, pred=None):
@@ -410,3 +410,77 @@ def test_copy_host_errors_without_gpu(L):
 def test_selftest_wait_timeout_argument_check_without_gpu(L):
     assert L.ea_selftest_wait_timeout(0, None) == 7
     assert L.ea_selftest_wait_timeout(2000000, None) == 7
+
+
+# ---------------------------------------------------------- the plan check
+
+def _check_exchange(L, segs, tiles, src_elems, dst_elems):
+    import numpy as np
+    from tensor_relational_einsum_gb300 import _abi
+    sw = np.array([w for s in segs for w in s], dtype=np.int64) if segs else np.zeros(1, np.int64)
+    tw = np.array([w for t in tiles for w in t], dtype=np.int64) if tiles else np.zeros(1, np.int64)
+    P = ctypes.POINTER(ctypes.c_int64)
+    return L.ea_plan_check_exchange(sw.ctypes.data_as(P), len(segs), tw.ctypes.data_as(P), len(tiles),
+                                    src_elems, dst_elems)
+
+
+def _seg(src, dst, inner, ext=(), sstr=(), dstr=()):
+    nd = len(ext)
+    pad = lambda v, fill: list(v) + [fill] * (4 - nd)  # noqa: E731
+    return [src, dst, inner, nd] + pad(ext, 1) + pad(sstr, 0) + pad(dstr, 0)
+
+
+def test_plan_check_accepts_a_valid_exchange_plan(L):
+    # the re-blocking of a [4, 6] tensor from 2 row blocks to 2 column blocks:
+    # each atom is [2, 3], rows of 3 elements; arenas of 24 elements
+    segs = [_seg(0, 0, 3, (2,), (6,), (3,)), _seg(3, 12, 3, (2,), (6,), (3,)),
+            _seg(12, 6, 3, (2,), (6,), (3,)), _seg(15, 18, 3, (2,), (6,), (3,))]
+    tiles = [[i, 0, 2, 0, 3] for i in range(4)]
+    assert _check_exchange(L, segs, tiles, 24, 24) == 0
+    # the same plan with one element too few in either arena
+    assert _check_exchange(L, segs, tiles, 23, 24) == 10
+    assert _check_exchange(L, segs, tiles, 24, 23) == 10
+
+
+@pytest.mark.parametrize("bad,what", [
+    (lambda s, t: (s[:1] + [_seg(22, 0, 3, (2,), (6,), (3,))] + s[2:], t), "source offset past the end"),
+    (lambda s, t: ([_seg(0, 0, 3, (2,), (22,), (3,))] + s[1:], t), "a source stride that walks off the arena"),
+    (lambda s, t: (s[:3] + [_seg(15, -1, 3, (2,), (6,), (3,))], t), "a negative destination offset"),
+    (lambda s, t: (s, t[:1] + [[1, 1, 2, 0, 3]] + t[2:]), "a tile past its segment's rows"),
+    (lambda s, t: (s, t[:1] + [[1, 0, 2, 1, 3]] + t[2:]), "a tile past its segment's run"),
+    (lambda s, t: (s, t + [[4, 0, 1, 0, 1]]), "a tile naming no segment"),
+    (lambda s, t: ([[0, 0, 3, 5, 2, 1, 1, 1, 6, 0, 0, 0, 3, 0, 0, 0]] + s[1:], t),
+     "a segment with more than four outer dimensions"),
+])
+def test_plan_check_rejects_hand_made_bad_descriptors(L, bad, what):
+    segs = [_seg(0, 0, 3, (2,), (6,), (3,)), _seg(3, 12, 3, (2,), (6,), (3,)),
+            _seg(12, 6, 3, (2,), (6,), (3,)), _seg(15, 18, 3, (2,), (6,), (3,))]
+    tiles = [[i, 0, 2, 0, 3] for i in range(4)]
+    s2, t2 = bad(segs, tiles)
+    assert _check_exchange(L, s2, t2, 24, 24) == 10, what
+    assert b"plan check" in L.ea_last_error()
+
+
+def test_plan_check_argument_errors(L):
+    assert _check_exchange(L, [], [], -1, 0) == 7
+    assert _check_exchange(L, [], [], 0, 0) == 0
+
+
+def test_bounds_checking_build_exports_the_abi():
+    """The EA_DEBUG_BOUNDS build (every kernel checks each tile against its
+    arena) compiles, loads, exports every symbol the header declares, and
+    says which build it is; the default build says it is not."""
+    from tensor_relational_einsum_gb300.build import LIB
+    path = build(bounds=True)
+    assert path.endswith("libea_bounds.so")
+    B = ctypes.CDLL(path)
+    hdr = open(os.path.join(ROOT, "include", "ea.h")).read()
+    names = set(re.findall(r"^(?:ea_status|int|const char \*)\s*(ea_[a-z_]+)\s*\(", hdr, re.M))
+    assert "ea_debug_bounds" in names
+    for n in sorted(names):
+        assert hasattr(B, n), n
+    B.ea_abi_version.restype = ctypes.c_int
+    assert B.ea_abi_version() == 5
+    assert B.ea_debug_bounds() == 1
+    build(bounds=False)
+    assert ctypes.CDLL(LIB).ea_debug_bounds() == 0

@@ -1,6 +1,6 @@
 """GPU parity of the matrix-chain workloads ("Every Kernel Is a Join",
-Section 7, chains A-E): every chain in its fixed parenthesization at 1/128
-of the pages' dimensions (the same shapes of plan, every dimension still in
+Section 7, chains A-E): every chain in its fixed parenthesization at about
+1/128 of the pages' dimensions (the same shapes of plan, every dimension still in
 several blocks) against the oracle's chain of contraction join-aggs, and
 chain C at full size on sampled rows (a row of the product is the row of M1
 carried through the chain, in fp64).
@@ -41,7 +41,9 @@ def _mats(dims, seed0, host=True):
 def test_chain_scaled(name):
     from tensor_relational_einsum_gb300.graphs import CHAINS, MatrixChain
     dims, paren = CHAINS[name]
-    dims = [max(16, d // 128) for d in dims]
+    # 1/128 of each dimension, rounded up to whole 32-wide blocks (64-byte
+    # bf16 rows, which the tensor-core kernel's TMA loads need)
+    dims = [max(32, -(-(d // 128) // 32) * 32) for d in dims]
     mats = _mats(dims, 200)
     ch = MatrixChain([to_device(m) for m in mats], paren, block=32)
     out = ch.run()

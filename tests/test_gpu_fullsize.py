@@ -117,8 +117,10 @@ def test_llama_block_full_size_prefix_sample():
     W = {k: host("bf16", shapes[k], "normal", seeds[k], 0.0, 0.02) for k in seeds}
     x = host("bf16", (B * S, D), "normal", 100, 0.0, 1.0)
     Wg = {k: v.cuda() for k, v in W.items()}
-    Wg["g1"] = torch.ones(D, dtype=torch.bfloat16, device="cuda")
-    Wg["g2"] = torch.ones(D, dtype=torch.bfloat16, device="cuda")
+    # RMSNorm gains ~ N(1, 0.1) (folded into the projection weights by the block)
+    gains = {k: host("bf16", (D,), "normal", sd, 1.0, 0.1) for k, sd in (("g1", 108), ("g2", 109))}
+    Wg["g1"] = gains["g1"].cuda()
+    Wg["g2"] = gains["g2"].cuda()
     blk = LlamaBlock(B, S, D, NH, FF, Wg, eps=1e-6, theta=10000.0)
     del Wg
     blk.x.load(x.cuda())
@@ -129,8 +131,8 @@ def test_llama_block_full_size_prefix_sample():
     seq = pick(303, B, 1)[0]
     n = 16
     Wd = {k: f64(v) for k, v in W.items()}
-    Wd["g1"] = np.ones(D)
-    Wd["g2"] = np.ones(D)
+    Wd["g1"] = f64(gains["g1"])
+    Wd["g2"] = f64(gains["g2"])
     xs = f64(x[seq * S: seq * S + n]).reshape(1, n, D)
     want = chains.llama_block(xs, Wd, n_heads=NH, eps=1e-6, theta=10000.0)
     got_y = y[seq * S: seq * S + n].double().cpu().numpy().reshape(1, n, D)

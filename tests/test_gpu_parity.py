@@ -91,12 +91,17 @@ def test_matmul_fp32_integer_exact_any_partition():
 
 # ----------------------------------------------------- bf16 tensor-core path
 
+_LAST_CASE = {}
+
+
 def _bf16_case(spec, shapes, parts_per_input, out_dtype, seeds=(5, 6), dist=("normal", 0.0, 1.0), pred=None,
-               scale=1.0, expect="contract_tc"):
+               scale=1.0, expect="contract_tc", simt_bf16=False):
     ts = [synth.make("bf16", s, dist[0], sd, dist[1], dist[2]) for s, sd in zip(shapes, seeds)]
     rs = [rel(t, p) for t, p in zip(ts, parts_per_input)]
-    C = joinagg(spec, rs, out_dtype=out_dtype, pred=pred, scale=scale)
+    C = joinagg(spec, rs, out_dtype=out_dtype, pred=pred, scale=scale, simt_bf16=simt_bf16)
     info = last()
+    _LAST_CASE.clear()
+    _LAST_CASE.update(info)  # reading C back runs an exchange, which replaces last()
     assert info["kernel"] == expect, info
     want = oracle.joinagg(spec, [t.to_f64() for t in ts], scale=scale, pred=pred)
     return dense64(C), want, C
@@ -148,17 +153,36 @@ def test_tc_batch_inside_block_and_swapped_roles():
     assert rel_frob(got, want) <= 1e-5
 
 
-@pytest.mark.parametrize("spec,bshape", [("bij,bjk->bik", (16, 256, 1096)), ("bij,bkj->bik", (16, 1096, 256))])
-def test_tc_clusters_with_padding_tiles(spec, bshape):
-    # 16 groups of M = 300 (three m-tiles: a padding tile completes each pair
-    # of a two-CTA cluster), N = 1100 (ragged), K = 256: 320 tiles, enough for
-    # the clustered launch that multicasts each B tile to both CTAs
-    # (B MN-major in the first case, K-major in the second)
-    got, want, _ = _bf16_case(spec, [(16, 300, 256), bshape], [[16, 1, 1], [16, 1, 1]], "f32")
+@pytest.mark.parametrize("spec,bshape", [("bij,bjk->bik", (24, 256, 1096)), ("bij,bkj->bik", (24, 1096, 256))])
+def test_tc_cta_pairs_with_padding_tiles(spec, bshape):
+    # 24 groups of M = 300 (three m-tiles: a padding tile completes each CTA
+    # pair), N = 1096 (five 256-wide tiles, ragged), K = 256: 360 tiles, at
+    # least two per SM, so the launch runs in CTA pairs (one 256-row MMA over
+    # two SMs, each loading half of the B tile) (B MN-major in the first
+    # case, K-major in the second)
+    got, want, _ = _bf16_case(spec, [(24, 300, 256), bshape], [[24, 1, 1], [24, 1, 1]], "f32")
+    assert _LAST_CASE["cta_pair"]
     assert rel_frob(got, want) <= 1e-5
-    got, want, _ = _bf16_case(spec, [(16, 300, 256), bshape], [[16, 1, 1], [16, 1, 1]], "f32",
+    got, want, _ = _bf16_case(spec, [(24, 300, 256), bshape], [[24, 1, 1], [24, 1, 1]], "f32",
                               dist=("int", -2, 2))
     assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("spec,ashape,bshape", [
+    ("bji,bjk->bik", (24, 256, 320), (24, 256, 1096)),   # A MN-major (m contiguous), B MN-major
+    ("bji,bkj->bik", (24, 256, 320), (24, 1096, 256)),   # A MN-major, B K-major
+    ("bij,bkj->bik", (104, 300, 192), (104, 120, 192)),  # N = 120: 128-wide tiles in pairs (M = 256, N = 128)
+])
+def test_tc_cta_pairs_operand_majors(spec, ashape, bshape):
+    # every operand layout through the CTA-pair launch, with padding tiles,
+    # ragged N and a K that is not a multiple of the 64-wide chunk (192 = 3
+    # chunks); integer inputs make the result exact
+    parts = [[ashape[0], 1, 1], [bshape[0], 1, 1]]
+    got, want, _ = _bf16_case(spec, [ashape, bshape], parts, "f32", dist=("int", -2, 2))
+    assert _LAST_CASE["kernel"] == "contract_tc" and _LAST_CASE["cta_pair"]
+    assert np.array_equal(got, want)
+    got, want, _ = _bf16_case(spec, [ashape, bshape], parts, "bf16")
+    assert rel_frob(got, want) <= 5e-3
 
 
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
@@ -175,13 +199,14 @@ def test_tc_epilogue_add(out_dtype):
     assert rel_frob(dense64(C), want) <= (1e-5 if out_dtype == "f32" else 5e-3)
 
 
-def test_tc_epilogue_add_clustered_integer_exact():
-    # 16 groups (cluster launch, padding tiles): C = A B + R exactly in integer mode
-    A = synth.make("bf16", (16, 300, 256), "int", 64, -2, 2)
-    B = synth.make("bf16", (16, 256, 1096), "int", 65, -2, 2)
-    R = synth.make("f32", (16, 300, 1096), "int", 66, -100, 100)
-    C = joinagg("bij,bjk->bik", [rel(A, [16, 1, 1]), rel(B, [16, 1, 1])], out_dtype="f32", epi_map="add",
-                epi_in=rel(R, [16, 1, 1]))
+def test_tc_epilogue_add_cta_pairs_integer_exact():
+    # 24 groups (CTA pairs, padding tiles): C = A B + R exactly in integer mode
+    A = synth.make("bf16", (24, 300, 256), "int", 64, -2, 2)
+    B = synth.make("bf16", (24, 256, 1096), "int", 65, -2, 2)
+    R = synth.make("f32", (24, 300, 1096), "int", 66, -100, 100)
+    RA, RB, RR = rel(A, [24, 1, 1]), rel(B, [24, 1, 1]), rel(R, [24, 1, 1])
+    C = joinagg("bij,bjk->bik", [RA, RB], out_dtype="f32", epi_map="add", epi_in=RR)
+    assert last()["cta_pair"]
     P = oracle.joinagg("bij,bjk->bik", [A.to_f64(), B.to_f64()])
     want = oracle.joinagg("bik,bik->bik", [P, R.to_f64()], "add", "none")
     assert np.array_equal(dense64(C), want)
@@ -265,8 +290,16 @@ def test_tc_row_rms(epi):
     assert rel_frob(dense64(out), want) <= tol
 
 
-def test_tc_unaligned_falls_back_to_simt():
-    got, want, _ = _bf16_case("ij,jk->ik", [(70, 45), (45, 33)], [[2, 3], [3, 1]], "f32", expect="contract_simt")
+def test_tc_unaligned_bf16_needs_explicit_simt():
+    # block rows of 45 and 33 bf16 elements are not 16-byte aligned, so TMA
+    # cannot tile the operands: refused unless the SIMT kernel is asked for
+    from tensor_relational_einsum_gb300._abi import EaError
+    A = synth.make("bf16", (70, 45), "normal", 5, 0, 1)
+    B = synth.make("bf16", (45, 33), "normal", 6, 0, 1)
+    with pytest.raises(EaError, match="simt_bf16"):
+        joinagg("ij,jk->ik", [rel(A, [2, 3]), rel(B, [3, 1])], out_dtype="f32")
+    got, want, _ = _bf16_case("ij,jk->ik", [(70, 45), (45, 33)], [[2, 3], [3, 1]], "f32", expect="contract_simt",
+                              simt_bf16=True)
     assert rel_frob(got, want) <= 1e-5
 
 

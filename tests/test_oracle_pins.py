@@ -328,6 +328,87 @@ def test_rmsnorm_invariant():
     np.testing.assert_allclose((out["y"] ** 2).mean(axis=1), ms / (ms + eps), rtol=1e-12)
 
 
+def test_rmsnorm_gain_closed_form():
+    """Rows whose cells all have magnitude c normalise (eps = 0) to
+    sign(x) * gamma: with a gain far from 1 this fixes that the gain
+    multiplies (a dropped or inverted gain fails)."""
+    r = rng(42)
+    D = 12
+    g = 1.0 + 0.1 * r.standard_normal(D)
+    signs = np.where(r.random((4, D)) < 0.5, -1.0, 1.0)
+    c = np.array([[0.5], [1.0], [3.0], [7.25]])
+    out = chains.rmsnorm(c * signs, g, 0.0)
+    np.testing.assert_allclose(out["ms"], c[:, 0] ** 2, rtol=1e-15)
+    np.testing.assert_allclose(out["y"], signs * g, rtol=1e-14)
+    # with eps > 0 the same rows shrink by c / sqrt(c^2 + eps) exactly
+    eps = 0.25
+    out = chains.rmsnorm(c * signs, g, eps)
+    np.testing.assert_allclose(out["y"], signs * g * c / np.sqrt(c ** 2 + eps), rtol=1e-14)
+
+
+def test_rmsnorm_gain_random_rows():
+    r = rng(43)
+    x = r.standard_normal((6, 20)) * 2.0
+    g = 1.0 + 0.1 * r.standard_normal(20)
+    out = chains.rmsnorm(x, g, 1e-6)
+    ms = np.mean(x * x, axis=1, keepdims=True)
+    np.testing.assert_allclose(out["y"], x / np.sqrt(ms + 1e-6) * g[None, :], rtol=1e-13)
+
+
+def test_add_join_values():
+    """The residual ADD join on non-zero operands: IEEE fp64 sums cell by
+    cell (a difference v0 - v1 fails the doubling check)."""
+    r = rng(44)
+    a, b = r.standard_normal((4, 5)), r.standard_normal((4, 5))
+    np.testing.assert_array_equal(oracle.joinagg("td,td->td", [a, b], "add", "none"), a + b)
+    np.testing.assert_array_equal(oracle.joinagg("td,td->td", [a, a], "add", "none"), 2.0 * a)
+    np.testing.assert_array_equal(oracle.joinagg("td,td->td", [a, b], "add", "none", tier="lit"), a + b)
+
+
+def _swiglu_closed_form_case():
+    """Inputs whose SwiGLU output has a closed form: x in [0.5, 1.5), a gate
+    of 50 x (SiLU(G) = G to 1e-10 since G >= 25), an up projection that
+    copies column 0 of x into every column, and a down projection that is a
+    6-cycle permutation (not its own transpose)."""
+    r = rng(45)
+    T, D = 5, 6
+    x = 0.5 + r.random((T, D))
+    w_gate = 50.0 * np.eye(D)
+    w_up = np.zeros((D, D))
+    w_up[0, :] = 1.0
+    perm = np.array([1, 2, 3, 4, 5, 0])
+    w_down = np.eye(D)[perm]              # row f is e_perm[f]: Y[:, perm[f]] = H[:, f]
+    H = (50.0 * x) * x[:, :1]
+    Y = np.empty_like(H)
+    Y[:, perm] = H
+    return x, w_gate, w_up, w_down, H, Y
+
+
+def test_swiglu_ffn_closed_form():
+    """H = SiLU(gate) * up and Y = H w_down: the closed form tells the gate
+    from the up projection (the swapped map SiLU(U) * G gives
+    SiLU(x0) * 50 x) and fixes w_down's orientation (its transpose is the
+    inverse permutation)."""
+    x, wg, wu, wd, H, Y = _swiglu_closed_form_case()
+    out = chains.swiglu_ffn(x, wg, wu, wd)
+    np.testing.assert_allclose(out["G"], 50.0 * x, rtol=1e-15)
+    np.testing.assert_allclose(out["U"], np.repeat(x[:, :1], x.shape[1], axis=1), rtol=1e-15)
+    np.testing.assert_allclose(out["H"], H, rtol=1e-9)
+    np.testing.assert_allclose(out["Y"], Y, rtol=1e-9)
+
+
+def test_swiglu_ffn_random_against_numpy():
+    r = rng(46)
+    x = r.standard_normal((7, 9))
+    wg, wu = r.standard_normal((9, 11)), r.standard_normal((9, 11))
+    wd = r.standard_normal((11, 9))
+    out = chains.swiglu_ffn(x, wg, wu, wd)
+    g = x @ wg
+    h = g / (1.0 + np.exp(-g)) * (x @ wu)
+    np.testing.assert_allclose(out["H"], h, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(out["Y"], h @ wd, rtol=1e-12, atol=1e-12)
+
+
 def test_rope_invariants():
     r = rng(11)
     b, s, h, d = 1, 9, 2, 8
@@ -467,6 +548,23 @@ def test_pins_catch_planted_mistakes():
     c1 = chains.softmax_attention(x, x, x, causal=True)["O"]
     c2 = chains.softmax_attention(x2, x2, x2, causal=True)["O"]
     assert np.array_equal(c1[0, 0, :3], c2[0, 0, :3])
+    # SwiGLU with gate and up swapped (SiLU(U) * G) misses the closed form
+    xs, wg, wu, wd, H, _ = _swiglu_closed_form_case()
+    G = oracle.joinagg("ij,kj->ik", [xs, np.ascontiguousarray(wg.T)])
+    U = oracle.joinagg("ij,kj->ik", [xs, np.ascontiguousarray(wu.T)])
+    assert not np.allclose(oracle.joinagg("ik,ik->ik", [U, G], "silu_mul", "none"), H, rtol=1e-3)
+    # ... and a transposed w_down misses Y
+    assert not np.allclose(chains.swiglu_ffn(xs, wg, wu, np.ascontiguousarray(wd.T))["Y"],
+                           _swiglu_closed_form_case()[5], rtol=1e-3)
+    # RMSNorm with the gain dropped, or divided instead of multiplied
+    g = 1.0 + 0.1 * rng(20).standard_normal(8)
+    xr = np.where(rng(21).random((3, 8)) < 0.5, -2.0, 2.0)
+    want = np.sign(xr) * g
+    assert not np.allclose(chains.rmsnorm(xr, np.ones(8), 0.0)["y"], want, rtol=1e-3)
+    assert not np.allclose(chains.rmsnorm(xr, 1.0 / g, 0.0)["y"], want, rtol=1e-3)
+    # ADD written as a difference misses the doubling
+    a = rng(22).standard_normal((2, 3))
+    assert not np.array_equal(a - a, 2.0 * a)
 
 
 # -------------------------------------------- partial copies and their (+)
