@@ -90,7 +90,7 @@ struct BlockMap {
 };
 
 ea_status encode_block(DevCtx *c, const ea_relation_s *r, int64_t bid, const std::string &term, char pos,
-                       const std::string &shared, BlockMap *bm) {
+                       const std::string &shared, BlockMap *bm, int box_rows = kTileRows) {
     const int rank = r->rank;
     int64_t iv[kMaxRank], lo[kMaxRank], ext[kMaxRank], str[kMaxRank];
     block_coords(r, bid, iv);
@@ -118,7 +118,7 @@ ea_status encode_block(DevCtx *c, const ea_relation_s *r, int64_t bid, const std
         gdim[i + 1] = (cuuint64_t)std::max<int64_t>(dims[i].ext, 1);
         gstr[i] = (cuuint64_t)(std::max<int64_t>(dims[i].str, 1) * 2);
         if (gstr[i] % 16) return set_error(EA_ERR_UNSUPPORTED, "attention: a block stride is not a multiple of 16 bytes");
-        if (dims[i].role == 0) box[i + 1] = kTileRows;
+        if (dims[i].role == 0) box[i + 1] = (cuuint32_t)box_rows;
         bm->slot[dims[i].role] = i;
     }
     if (!c->encode) return set_error(EA_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
@@ -150,6 +150,10 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
     const int rank = q->rank;
     const int ds = pos_in(a.qt, a.s), dq_d = rank - 1;
     const int D = (int)q->dims[dq_d];
+    // Head dim 128 runs on CTA pairs: each CTA of a pair loads half of every
+    // K tile (64 keys: K maps with 64-key boxes) and half of every V tile's
+    // head dims, and holds one query tile of the pair's two.
+    const bool pair = D == 128;
     std::vector<BlockMap> maps;
     maps.reserve(q->nblocks + 2 * k->nblocks);
     for (int64_t b = 0; b < q->nblocks; b++) {
@@ -162,7 +166,7 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
     for (const ea_relation_s *r : {j.k, j.v})
         for (int64_t b = 0; b < k->nblocks; b++) {
             BlockMap bm;
-            ea_status s = encode_block(c, r, b, a.kt, a.t, a.shared, &bm);
+            ea_status s = encode_block(c, r, b, a.kt, a.t, a.shared, &bm, pair && r == j.k ? kTileRows / 2 : kTileRows);
             if (s) return s;
             maps.push_back(bm);
         }
@@ -298,6 +302,14 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
                     // a query slot skips the trailing key tiles it keeps none of
                     for (int xq = 0; xq < it.nq; xq++)
                         it.nt[xq] = last_kept[xq] >= 0 ? (int32_t)(last_kept[xq] + 1) : it.ntiles;
+                    if (pair && it.nq == 1) {
+                        // the second CTA of the pair holds a padding tile: no rows,
+                        // its Q box past the block's positions (read as zeros)
+                        it.q[1] = it.q[0];
+                        it.q[1].nrows = 0;
+                        it.q[1].q_c[qm.slot[0]] = (int32_t)ns;
+                        it.nt[1] = 0;
+                    }
                     items.push_back(it);
                 }
             }
@@ -314,8 +326,10 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
             if (!cs && j.m) cs = check_block(Q.ml_off, 1, me, ms, rel_elems(j.m), "attention statistics rows", i);
             if (cs) return cs;
         }
-    // List scheduling: each group, in order, to the CTA with the least work.
-    const int ncta = (int)std::min<int64_t>((int64_t)c->num_sms, (int64_t)items.size());
+    // List scheduling: each item, in order, to the CTA (or CTA pair) with the
+    // least work so far.
+    const int ncta = (int)std::min<int64_t>(pair ? attention_pair_clusters(c->num_sms) : (int64_t)c->num_sms,
+                                            (int64_t)items.size());
     std::vector<std::vector<int32_t>> per(std::max(ncta, 1));
     if (ncta > 0) {
         typedef std::pair<int64_t, int> Load;  // (work, cta)
@@ -325,16 +339,29 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
             Load l = heap.top();
             heap.pop();
             per[l.second].push_back((int32_t)i);
-            // a key tile of one query slot ~ 2 units, an item's set-up ~ 2
-            l.first += 2 * (int64_t)(items[i].nt[0] + (items[i].nq > 1 ? items[i].nt[1] : 0)) + 2;
+            // a key tile of one query slot ~ 2 units, an item's set-up ~ 2 (a
+            // pair runs every key tile of the item once for both query tiles)
+            l.first += pair ? 2 * (int64_t)items[i].ntiles + 1
+                            : 2 * (int64_t)(items[i].nt[0] + (items[i].nq > 1 ? items[i].nt[1] : 0)) + 2;
             heap.push(l);
         }
     }
+    // items in the order each CTA (pair) runs them, their runs renumbered in
+    // the same order: a CTA's runs are one contiguous range
     std::vector<AtItem> ordered;
+    std::vector<AtRun> oruns;
     std::vector<int32_t> cta_ptr(1, 0);
     ordered.reserve(items.size());
+    oruns.reserve(runs.size());
     for (int x = 0; x < ncta; x++) {
-        for (int32_t i : per[x]) ordered.push_back(items[i]);
+        for (int32_t i : per[x]) {
+            AtItem it = items[i];
+            const int32_t r0 = (int32_t)oruns.size();
+            for (int32_t r = it.r0; r < it.r1; r++) oruns.push_back(runs[r]);
+            it.r1 = r0 + (it.r1 - it.r0);
+            it.r0 = r0;
+            ordered.push_back(it);
+        }
         cta_ptr.push_back((int32_t)ordered.size());
     }
     int64_t ntup = 0, ngroups = 0;
@@ -347,7 +374,7 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
     for (size_t i = 0; i < maps.size(); i++) raw[i] = maps[i].map;
     Blob b;
     const size_t om = b.add(raw.data(), raw.size() * sizeof(CUtensorMap), 128);
-    const size_t oi = b.add_vec(ordered), op = b.add_vec(cta_ptr), orr = b.add_vec(runs), oe = b.add_vec(j.ends);
+    const size_t oi = b.add_vec(ordered), op = b.add_vec(cta_ptr), orr = b.add_vec(oruns), oe = b.add_vec(j.ends);
     ea_status s = upload(b, st, p);
     if (s) return s;
     p->kind = kAttn;
@@ -362,7 +389,8 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
     P.ml_elems = j.m ? rel_elems(j.m) : 0;
     P.m_out = j.m ? (float *)j.m->arena : nullptr;
     P.l_out = j.l ? (float *)j.l->arena : nullptr;
-    P.ncta = ncta;
+    P.ncta = pair ? 2 * ncta : ncta;  // in pairs: cta_ptr indexes pairs
+    P.pair = pair ? 1 : 0;
     P.n_kv = n_kv;
     P.nseq = (int32_t)j.ends.size();
     P.causal = j.causal ? 1 : 0;

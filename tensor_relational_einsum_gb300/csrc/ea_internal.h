@@ -303,10 +303,15 @@ struct AtParams {
     float scale;             // score scale (> 0)
     float scale_log2;        // scale * log2(e)
     int32_t d;               // head dimension: 64 or 128
+    int32_t pair;            // 1: CTA pairs (head dim 128): cta_ptr indexes pairs, ncta = 2 x pairs, items hold
+                             // two query tiles (q[1] a padding tile of no rows when the head has an odd count),
+                             // K maps have 64-key boxes
     int *err;
     int64_t o_elems, ml_elems;  // arena sizes of O and of m / l (elements), for EA_DEBUG_BOUNDS
 };
 cudaError_t launch_attention(const AtParams &p, cudaStream_t st);
+cudaError_t launch_attention_pair(const AtParams &p, cudaStream_t st);
+int attention_pair_clusters(int num_sms);  // CTA pairs of the attention kernel resident at once
 cudaError_t launch_wait_timeout(int *err, uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_exchange_agg(const XSeg *segs, const XTile *tiles, int64_t ntiles, const char *src, char *dst,
                                 int dtype, int agg, int ncopies, int64_t copy_stride, int num_sms, cudaStream_t st,

@@ -16,10 +16,15 @@
 //
 // The reference maximum of a row is only moved when a tile's maximum
 // exceeds it by more than 2^kLazy in exp: until then the exponentials are
-// taken against the older, smaller maximum (values up to 2^kLazy, exact in
-// fp32 and well inside bf16's range), and A and l stay consistent with it,
-// so A / l is unchanged.  Moving it rescales the row of A in TMEM, which is
-// rare after the first tiles.
+// taken against the older, smaller maximum, and A and l stay consistent
+// with it, so A / l is unchanged.  With kLazy = 64 the exponentials stay
+// below 2^64; fp32 and bf16 both have 8 exponent bits, so P, l and A (a sum
+// of fewer than 2^31 keys' products with |v| < 2^32) stay far below the
+// overflow at 2^128, and their relative rounding does not depend on the
+// magnitude.  Moving the maximum rescales the row of A in TMEM; with a
+// threshold this wide it happens on a row's first tile and almost never
+// after, even where the scores spread over tens of units (unscaled scores
+// of 128-wide heads).
 //
 // A work item is one or two groups that share their key tiles: two query
 // tiles of the same head, X = 0 and X = 1, each with its own softmax
@@ -51,6 +56,7 @@
 // flight are waited for and TMEM is freed before the CTA exits.
 #include <algorithm>
 
+#include "attn_common.cuh"
 #include "dev_common.cuh"
 #include "tc_common.cuh"
 
@@ -59,6 +65,7 @@ namespace ea {
 namespace {
 
 using namespace tc;
+using namespace attn;
 
 constexpr int kRows = 128;  // query rows of a tile (= TMEM lanes)
 constexpr int kKeys = 128;  // keys of a key tile
@@ -74,7 +81,7 @@ constexpr int kSoftmaxRegs = 208;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kCtlRegs <= kAtThreads * kLaunchRegs, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;  // first TMEM column of the output accumulators
-constexpr float kLazy = 16.0f;   // log2 of the largest exponential taken against a stale maximum
+constexpr float kLazy = 64.0f;   // log2 of the largest exponential taken against a stale maximum
 constexpr int kKvStages = 2;     // K/V ring depth: stage s holds K and V of one key tile
 
 struct AtCtl {
@@ -96,66 +103,6 @@ struct AtCfg {
     static constexpr int CTL_OFF = 2 * TILE + 2 * kKvStages * TILE;
     static constexpr int SMEM = 1024 + CTL_OFF + (int)sizeof(AtCtl);
 };
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Packed two-wide fp32 arithmetic (one instruction for two values).
-__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ uint64_t pack_u32x2(uint32_t lo, uint32_t hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-    return r;
-}
-__device__ __forceinline__ float lo_f32(uint64_t v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return lo;
-}
-__device__ __forceinline__ float hi_f32(uint64_t v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return hi;
-}
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-// Maximum of three (the inputs hold no NaN).
-__device__ __forceinline__ float max3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// A wait taken by lane 0 for the whole warp; the outcome is the same in
-// every lane, and the warp's later reads are ordered after the wait.
-__device__ __forceinline__ bool warp_wait(uint64_t *b, uint32_t parity, volatile int *abort, int *err, int code) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(b, parity, abort, err, code) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
-}
 
 template <int D>
 __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams p) {
@@ -477,7 +424,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             bool in = true;
             if constexpr (kBoundsCheck) {
                 // the query tile's output rows (and statistics rows) inside their arenas
-                const int64_t nr = nrows, one = 1;
+                const int64_t nr = nrows;
                 in = range_in(Q.o_off, 1, &nr, &Q.o_rstr, D, 1, p.o_elems) &&
                      (!p.m_out || range_in(Q.ml_off, 1, &nr, &Q.ml_rstr, 1, 0, p.ml_elems));
                 if (!in && row == 0) bounds_fail(p.err);
@@ -553,6 +500,7 @@ int attention_smem_bytes(int d) { return d == 64 ? AtCfg<64>::SMEM : AtCfg<128>:
 
 cudaError_t launch_attention(const AtParams &p, cudaStream_t st) {
     if (p.ncta <= 0) return cudaSuccess;
+    if (p.pair) return launch_attention_pair(p, st);
     if (p.d == 64) return launch_d<64>(p, st);
     return launch_d<128>(p, st);
 }

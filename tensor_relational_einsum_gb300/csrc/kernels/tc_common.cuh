@@ -123,9 +123,17 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *map, 
         : "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
+// Arrive on an mbarrier of another CTA of the cluster.  Every such arrive
+// in these kernels publishes TMEM accesses (tcgen05.st of P, tcgen05.ld of
+// an accumulator) that tcgen05.wait has completed and
+// tcgen05.fence::before_thread_sync has ordered before the arrive; no
+// generic-proxy write of the arriving thread is consumed across the pair.
+// So the arrive keeps the default semantics (release at CTA scope): a
+// release at cluster scope would also wait until the thread's earlier
+// writes are performed cluster-wide, which cost ~1300 cycles per arrive,
+// on the critical path of every key tile of the pair attention kernel.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cl) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
 }
 
 // TMEM of a pair: one warp of each CTA allocates (and frees) together; both
@@ -154,11 +162,34 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
         : "memory");
 }
 
+// The pair MMA with A read from TMEM: each CTA's rows of A in its own TMEM
+// at the same columns (`a_tmem`), B from shared memory as above.
+__device__ __forceinline__ void umma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on the mbarrier at the shared::cluster address `bar_cl` (either
 // CTA of the pair) when every pair MMA this thread issued so far is done.
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar_cl) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_cl)
                  : "memory");
+}
+
+// One lane of the (converged) warp: true in exactly one lane.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
