@@ -1,6 +1,5 @@
 // attn_common.cuh -- helpers shared by the attention join-agg kernels:
-// packed two-wide fp32 arithmetic, the base-2 exponential, bf16 packing and
-// a warp-wide bounded wait.
+// packed two-wide fp32 arithmetic, the base-2 exponential and bf16 packing.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -51,23 +50,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// A wait for the whole warp; the outcome is the same in every lane, and
-// the warp's later reads are ordered after the wait.  Fast path: every lane
-// tries the phase once (each lane's own acquire) and the warp votes, ~40
-// cycles when the phase has completed; otherwise lane 0 takes the bounded
-// wait and shares its outcome (a lane-0 wait alone, with its shuffle and
-// reconvergence, cost ~210 cycles even on a completed phase).
-// CLUSTER: acquire at cluster scope.
-template <bool CLUSTER = false>
-__device__ __forceinline__ bool warp_wait(uint64_t *b, uint32_t parity, volatile int *abort, int *err, int code) {
-    if (__all_sync(0xffffffffu, tc::mbar_try<CLUSTER>(b, parity))) return true;
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait<CLUSTER>(b, parity, abort, err, code) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
 }
 
 }  // namespace attn

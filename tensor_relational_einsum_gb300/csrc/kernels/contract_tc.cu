@@ -197,8 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                 }
             }
         }
-    } else if (warp == 1 && lane == 0 && rank == 0) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == 1 && rank == 0) {
+        // ------------------------------------------------ MMA warp
+        // The whole warp runs the issue loop (warp-uniform waits, cursors
+        // and descriptors); one elected lane issues each stage's MMAs and
+        // commits.
         const uint32_t idesc = make_idesc(CL * BM, BN, p.a_mn_major, p.b_mn_major);
         // descriptor layout and the address step of one K = 16 slice: a
         // K-major operand advances 32 bytes inside its 128-byte rows, an
@@ -211,14 +214,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
         for (int unit = unit0; unit < nunits && ok; unit += ustep) {
             const TcTile T = p.tiles[unit * CL + rank];
             const TcGroup G = p.groups[T.group];
-            if (!mbar_wait<PAIR>(&ctl->tempty[acc], acc_ph ^ 1, abort, p.err, kDevTimeoutMma)) break;
+            if (!warp_wait(&ctl->tempty[acc], acc_ph ^ 1, abort, p.err, kDevTimeoutMma)) break;
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(acc * BN);
             uint32_t accumulate = 0;
             for (int t = G.t0; t < G.t1 && ok; t++) {
                 const TcTuple U = p.tuples[t];
                 for (int kc = 0; kc < U.kchunks; kc++) {
-                    if (!mbar_wait(&ctl->full[stage], ph, abort, p.err, kDevTimeoutMma)) {
+                    if (!warp_wait(&ctl->full[stage], ph, abort, p.err, kDevTimeoutMma)) {
                         ok = false;
                         break;
                     }
@@ -226,18 +229,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                     // the stage's descriptors once; each MMA adds a constant step
                     const uint32_t sa = smem_u32(stages + stage * C::STAGE), sb = sa + C::A_BYTES;
                     const uint64_t ad = sdesc(sa, a_lbo, 1024), bd = sdesc(sb, b_lbo, 1024);
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; kk++) {
-                        if (PAIR) umma_bf16_pair(d, ad + kk * a_step, bd + kk * b_step, idesc, accumulate);
-                        else umma_bf16(d, ad + kk * a_step, bd + kk * b_step, idesc, accumulate);
-                        accumulate = 1;
+                        for (int kk = 0; kk < BK / 16; kk++) {
+                            const uint32_t acc_in = (accumulate | (uint32_t)kk) ? 1u : 0u;
+                            if (PAIR) umma_bf16_pair(d, ad + kk * a_step, bd + kk * b_step, idesc, acc_in);
+                            else umma_bf16(d, ad + kk * a_step, bd + kk * b_step, idesc, acc_in);
+                        }
+                        if (!PAIR) {
+                            umma_commit(&ctl->empty[stage]);
+                        } else {
+                            umma_commit_pair(smem_u32(&ctl->empty[stage]));
+                            umma_commit_pair(mapa_u32(smem_u32(&ctl->empty[stage]), 1));  // rank 1's
+                        }
                     }
-                    if (!PAIR) {
-                        umma_commit(&ctl->empty[stage]);
-                    } else {
-                        umma_commit_pair(smem_u32(&ctl->empty[stage]));
-                        umma_commit_pair(mapa_u32(smem_u32(&ctl->empty[stage]), 1));  // rank 1's
-                    }
+                    __syncwarp();
+                    accumulate = 1;
                     if (++stage == C::STAGES) {
                         stage = 0;
                         ph ^= 1;
@@ -245,19 +252,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_contract_kernel(const TcParams
                 }
             }
             if (!ok) break;
-            if (!PAIR) {
-                umma_commit(&ctl->tfull[acc]);
-            } else {
-                umma_commit_pair(smem_u32(&ctl->tfull[acc]));
-                umma_commit_pair(mapa_u32(smem_u32(&ctl->tfull[acc]), 1));
+            if (elect_one()) {
+                if (!PAIR) {
+                    umma_commit(&ctl->tfull[acc]);
+                } else {
+                    umma_commit_pair(smem_u32(&ctl->tfull[acc]));
+                    umma_commit_pair(mapa_u32(smem_u32(&ctl->tfull[acc]), 1));
+                }
             }
+            __syncwarp();
             acc ^= 1;
             if (acc == 0) acc_ph ^= 1;
         }
-        // Every MMA this thread issued has completed once mma_done flips.
-        if (PAIR) umma_commit_pair(smem_u32(&ctl->mma_done));
-        else umma_commit(&ctl->mma_done);
-        mbar_wait(&ctl->mma_done, 0, abort, p.err, kDevTimeoutMma, kTimeoutNs, false);
+        // Every MMA this warp issued has completed once mma_done flips.
+        if (elect_one()) {
+            if (PAIR) umma_commit_pair(smem_u32(&ctl->mma_done));
+            else umma_commit(&ctl->mma_done);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_wait(&ctl->mma_done, 0, abort, p.err, kDevTimeoutMma, kTimeoutNs, false);
+        __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------ epilogue
         const int ep = threadIdx.x - 128;  // = TMEM lane = row of the tile

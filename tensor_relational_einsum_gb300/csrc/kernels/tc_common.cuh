@@ -181,6 +181,23 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar_cl) {
                  : "memory");
 }
 
+// A wait for the whole warp; the outcome is the same in every lane, and
+// the warp's later reads are ordered after the wait.  Fast path: every lane
+// tries the phase once (each lane's own acquire) and the warp votes, ~40
+// cycles when the phase has completed; otherwise lane 0 takes the bounded
+// wait and shares its outcome (a lane-0 wait alone, with its shuffle and
+// reconvergence, cost ~210 cycles even on a completed phase).
+// CLUSTER: acquire at cluster scope.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool warp_wait(uint64_t *b, uint32_t parity, volatile int *abort, int *err, int code) {
+    if (__all_sync(0xffffffffu, mbar_try<CLUSTER>(b, parity))) return true;
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait<CLUSTER>(b, parity, abort, err, code) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
 // One lane of the (converged) warp: true in exactly one lane.
 __device__ __forceinline__ bool elect_one() {
     uint32_t pred;
