@@ -823,6 +823,12 @@ def profile_case(name: str, reps: int):
                                        [4, 4, 1, 1]) for sd in (1, 2, 3))
         o = Relation("bf16", (4, 2048, 32, 128), [4, 4, 1, 1], device=dev)
         fn = lambda: attention("bshd,bthd,bthd->bshd", q, k, v, causal=True, out=o)  # noqa: E731
+    elif name == "attn_c2":  # fused attention b4 h32 s=t=2048 d128 head-major, scale 1, t in 4 blocks (CTA pairs)
+        from tensor_relational_einsum_gb300.relation import attention
+        q, k, v = (Relation.from_dense(synth.make_torch("bf16", (4, 32, 2048, 128), "normal", sd, 0, 1, device=dev),
+                                       [4, 32, 4 if sd > 11 else 1, 1]) for sd in (11, 12, 13))
+        o = Relation("bf16", (4, 32, 2048, 128), [4, 32, 1, 1], device=dev)
+        fn = lambda: attention("bhsd,bhtd,bhtd->bhsd", q, k, v, scale=1.0, out=o)  # noqa: E731
     elif name == "exchange_agg":  # 4 fp32 copies of [8192, 4096] -> SUM into 16x16 tiles
         from tensor_relational_einsum_gb300.relation import exchange_agg
         P = Relation.from_dense(synth.make_torch("f32", (4, 8192, 4096), "normal", 35, 0, 1, device=dev), [4, 1, 1])
@@ -866,7 +872,7 @@ def profile_case(name: str, reps: int):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["gemm", "attn", "attn_fused", "c1", "exchange", "exchange_agg", "norm", "ffn_ew"], default=None)
+    ap.add_argument("--profile-case", choices=["gemm", "attn", "attn_fused", "attn_c2", "c1", "exchange", "exchange_agg", "norm", "ffn_ew"], default=None)
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
