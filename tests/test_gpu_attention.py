@@ -141,6 +141,22 @@ def test_value_closed_forms():
     assert torch.allclose(O.to_dense().float(), torch.ones(1, 4, 300, 128, device="cuda"), atol=2e-3)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_reference_maximum_moves(d):
+    """Key rows grow along t (key t scaled by 1 + t/64, scale 1): a query row's
+    maximum score rises from key tile to key tile by tens of units, more than
+    2^64 in exp every tile or two, so the lazily kept reference maximum moves
+    and each chain's row of A is rescaled in TMEM many times (head dim 64 on
+    the single-CTA kernel, 128 on CTA pairs).  Ragged query and key tiles."""
+    Q = synth.make("bf16", (1, 4, 300, d), "normal", 81, 0, 1)
+    K0 = synth.make("bf16", (1, 4, 700, d), "normal", 82, 0, 1)
+    V = synth.make("bf16", (1, 4, 700, d), "normal", 83, 0, 1)
+    grow = 1.0 + np.arange(700) / 64.0
+    k = K0.to_f64() * grow[None, None, :, None]
+    K = synth.Tensor(synth.f32_to_bf16_bits(synth.f64_to_f32(k)).ravel(), "bf16", K0.shape)
+    _run("bhsd,bhtd,bhtd->bhsd", Q, K, V, [1, 4, 1, 1], [1, 4, 2, 1], "bhsd", scale=1.0)
+
+
 def test_full_size_head_major_sampled_heads():
     """Q, K, V bf16 [4, 32, 2048, 128], (b, h) unit intervals, t in 4 blocks,
     scale 1, no mask: two seeded (b, h) pairs in full against the oracle."""
