@@ -232,10 +232,14 @@ def bench_components(peaks, device):
     from tensor_relational_einsum_gb300.relation import Relation, exchange, joinagg
     hbm = peaks["hbm_gbs"]
     out = {}
-    # Written before every timed call: it flushes L2 (1 GiB > 129 MB), and
-    # the device is still busy with it while the host enqueues the call, so
-    # the events time the call's kernels and not the host's launch latency.
+    # Written, then read, before every timed call: the write flushes L2
+    # (1 GiB > 129 MB), and the read leaves L2 holding clean lines, so the
+    # timed kernels do not pay for writing back the flush's own dirty lines
+    # (a write alone cost the RMSNorm sum of squares ~10% of its time); the
+    # device is still busy with the flush while the host enqueues the call,
+    # so the events time the call's kernels and not the host's launch latency.
     flush = torch.empty(1 << 28, dtype=torch.float32, device=device)
+    sink = torch.empty((), dtype=torch.float32, device=device)
 
     def timed(fn, reps=5, warm=3):
         for _ in range(warm):
@@ -243,7 +247,8 @@ def bench_components(peaks, device):
         torch.cuda.synchronize()
         ts = []
         for _ in range(reps):
-            flush.zero_()
+            flush.fill_(1.0)
+            sink.copy_(flush.sum())
             s = torch.cuda.Event(enable_timing=True)
             e = torch.cuda.Event(enable_timing=True)
             s.record()
@@ -306,6 +311,17 @@ def bench_components(peaks, device):
                                          "alg_bytes_GB": round(4 * qkv_b / 1e9, 3),
                                          "speedup_vs_chain": round(med / fmed, 2)}
     del fa
+
+    # RMSNorm's sum of squares as in the block: x [16384, 4096] bf16, tokens in
+    # 8 blocks (one per sequence), model dim in 4 blocks -> ms [16384] f32
+    x = Relation.from_dense(synth.make_torch("bf16", (16384, 4096), "normal", 5, 0, 1, device=device), [8, 4])
+    ms = Relation("f32", (16384,), [8], device=device)
+    med, mn = timed(lambda: joinagg("td->t", [x], "sum", "square", out=ms, scale=1.0 / 4096), reps=20)
+    nb = 16384 * 4096 * 2 + 16384 * 4
+    out["rmsnorm_sumsq_16384x4096"] = {"us": round(med * 1e3, 1), "min_us": round(mn * 1e3, 1),
+                                       "GB/s": round(nb / (med * 1e-3) / 1e9, 1),
+                                       "frac_hbm": round(nb / (med * 1e-3) / 1e9 / hbm, 3)}
+    del x, ms
 
     # SwiGLU FFN join-aggs, x[8192, 4096], contracted dims in 4 blocks
     x = synth.make_torch("bf16", (8192, 4096), "normal", 21, 0, 1, device=device)
@@ -564,8 +580,8 @@ def config_dict(gains="one"):
             "rmsnorm_gains": "1" if gains == "one" else "N(0, 0.02)",
             "batch": B, "seq_len": S, "d_model": D, "heads": NH, "d_ff": FF, "tilings":
             "tokens: 1 block per sequence; model dim 4 blocks; heads as a batch letter; s, t: 4 blocks",
-            "l2": "block step: inputs larger than L2 (it touches ~10 GB per step); components: a 1 GiB write "
-                  "flushes L2 before every timed call"}
+            "l2": "block step: inputs larger than L2 (it touches ~10 GB per step); components: a 1 GiB write, "
+                  "then a read of it, flushes L2 before every timed call"}
 
 
 def contraction_source_hash() -> str:

@@ -23,6 +23,7 @@ enum DeviceErr : int {
     kDevTimeoutSoftmax = 5,
     kDevTimeoutCorrection = 6,
     kDevTimeoutSelftest = 7,
+    kDevTimeoutReduce = 8,
 };
 
 // ---------------------------------------------------------------- exchange
@@ -98,6 +99,11 @@ struct RrTile {
 // stride in each block, 8 output offset of the first row, 9 output row
 // stride, 10 segment length, 11 rows (low 32 bits) | blocks per row << 32.
 constexpr int kRbWords = 12;
+// The row-batch reductions' bulk-copy path: a tile has at most kRbBulkRows
+// rows, and its rows of one block (one contiguous range) at most
+// kRbBulkBytes bytes.
+constexpr int kRbBulkRows = 8;
+constexpr int kRbBulkBytes = 16384;
 
 // ------------------------------------------------------------ contraction
 // Generic (SIMT) grouped contraction: C[b][m][n] (+)= A[b][m][k] * B[b][k][n].
@@ -200,6 +206,8 @@ struct RrParams {
     int max_items;                     // most tuples in one group
     int tile_linear;                   // 1: no tile crosses a run of the innermost row dim
     int row_batch;                     // 1: the row-batch kernels (rb_desc) serve this plan
+    int row_bulk;                      // 1: ... through bulk copies (every tile's block segment one contiguous,
+                                       //    16-byte aligned range of at most 8 rows and 16 KB)
     const int64_t *rb_desc;            // kRbWords per tile when row_batch
     int *err;
     int64_t in_elems[kMaxIn], out_elems;  // arena sizes (elements), for EA_DEBUG_BOUNDS checks

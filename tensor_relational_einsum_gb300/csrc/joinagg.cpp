@@ -522,7 +522,7 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
     // and needs no CTA barrier.
     bool rb = !j.pred_lo && max_items <= 4 && n_in == 1 &&
               ((j.agg == EA_AGG_SUM && (j.map == EA_MAP_SQUARE || j.map == EA_MAP_IDENTITY)) ||
-               (j.agg == EA_AGG_MAX_SUMEXP && j.map == EA_MAP_IDENTITY));
+               (j.agg == EA_AGG_MAX_SUMEXP && j.map == EA_MAP_IDENTITY && j.scale == 1.0f));  // its kernel takes v as is
     for (const RrGroup &G : groups)
         for (int32_t i = G.i0; i < G.i1 && rb; i++) {
             const EwItem &it = items[i];
@@ -530,9 +530,32 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
             if (it.nd > 0)  // row strides held in 32 bits
                 rb = rb && std::llabs(it.istr[0][it.nd - 1]) < (1ll << 31) && std::llabs(it.ostr[it.nd - 1]) < (1ll << 31);
         }
+    // The bulk-copy path of the row-batch SUM: every block's rows stored back
+    // to back (innermost row stride = segment length), every offset and
+    // stride 16-byte aligned, a row segment at most 2 KB (a chunk of 8 rows
+    // of one block fits a 16 KB stage).  Its tiles are cut to about six per
+    // CTA, in multiples of 8 rows.
+    const int64_t esz = j.in[0]->dtype == EA_BF16 ? 2 : 4;
+    bool bulk = rb && j.agg == EA_AGG_SUM;
+    for (const RrGroup &G : groups)
+        for (int32_t i = G.i0; i < G.i1 && bulk; i++) {
+            const EwItem &it = items[i];
+            const int64_t rowb = it.len * esz;
+            bulk = it.nd >= 1 && it.istr[0][it.nd - 1] == it.len && rowb % 16 == 0 &&
+                   rowb <= kRbBulkBytes / kRbBulkRows && (it.in_base[0] * esz) % 16 == 0;
+            for (int d = 0; d < it.nd && bulk; d++) bulk = (it.istr[0][d] * esz) % 16 == 0;
+        }
+    int64_t bulk_rows = kRbBulkRows;
+    if (bulk) {
+        int64_t all_rows = 0;
+        for (const GroupRows &gr : grows) all_rows += gr.rows;
+        while (bulk_rows < 64 && all_rows / (2 * bulk_rows) >= 6 * (int64_t)c->num_sms) bulk_rows *= 2;
+    }
     for (const GroupRows &gr : grows) {
         int64_t per = gr.per;
-        if (rb) {
+        if (bulk) {
+            per = bulk_rows;
+        } else if (rb) {
             const int64_t row_u = j.in[0]->dtype == EA_BF16 ? 4 : 2;  // 8-element chunks per lane per block
             const int64_t chunks = items[groups[gr.gid].i0].len / 8;
             int64_t lpb = 32;
@@ -613,6 +636,7 @@ static ea_status build_rowreduce(JoinCtx &j, DevCtx *c, cudaStream_t st, DevPlan
     r.max_items = (int)max_items;
     r.tile_linear = 1;
     r.row_batch = rb ? 1 : 0;
+    r.row_bulk = bulk ? 1 : 0;
     r.stream_mask = 0;
     for (int k = 0; k < n_in; k++)
         if (sp.term[k].find(red.back()) != std::string::npos) r.stream_mask |= 1 << k;
@@ -1712,6 +1736,7 @@ ea_status ea_check(void *stream) {
                          : flag == kDevTimeoutSoftmax  ? "bounded wait ran out in the attention softmax warps"
                          : flag == kDevTimeoutCorrection ? "bounded wait ran out in the attention output warps"
                          : flag == kDevTimeoutSelftest ? "bounded wait ran out in the wait self-test (expected)"
+                         : flag == kDevTimeoutReduce   ? "bounded wait ran out in the row-reduction warps"
                                                        : "unknown");
     }
     return EA_OK;

@@ -24,6 +24,7 @@
 #include <math.h>
 
 #include "dev_common.cuh"
+#include "tc_common.cuh"
 
 namespace ea {
 
@@ -126,7 +127,7 @@ __device__ __forceinline__ void rr_seg(const RrParams &p, Acc &acc, const int64_
                 }
             }
             const float srow = pk2_sum(fadd2(fadd2(s2[0], s2[1]), fadd2(s2[2], s2[3])));
-            acc.a += MAP == EA_MAP_SQUARE ? p.scale * srow : srow;
+            acc.a += p.scale * srow;  // IDENTITY and SQUARE both carry the map's scale
             return;
         }
     }
@@ -566,10 +567,160 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_kernel(const R
                 }
             }
             float a = pk2_sum(fadd2(fadd2(s2[0], s2[1]), fadd2(s2[2], s2[3])));
-            if (MAP == EA_MAP_SQUARE) a *= p.scale;
+            a *= p.scale;  // the map's scale (IDENTITY: scale v, SQUARE: scale v^2)
             for (int o = lpb / 2; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
             if (slb == 0 && live) st_elem(p.out, p.out_dtype, d.out0 + dr * d.ostr, a);
         }
+    }
+}
+
+// SUM (or SUM of squares) of one input over rows whose segments lie in at
+// most four blocks, where the rows of each block are stored back to back
+// (16-byte aligned, at most 2 KB a row segment): one thread streams chunks
+// of 8 rows of one block (8 x the segment, at most 16 KB) into a ring of 8
+// shared-memory stages with bulk copies that complete on the stage's
+// mbarrier -- a tile's rows in groups of 8, each group's blocks in order --
+// so up to 128 KB of each SM's input is in flight with no per-lane loads
+// outstanding; eight warps reduce them, warp w row w of each chunk, keeping
+// the row's packed f32x2 partial sums across its blocks.  Tile descriptors
+// are loaded two tiles ahead.
+constexpr int kBulkStages = 8;
+constexpr int kBulkStage = kRbBulkBytes;  // bytes of one chunk at most
+constexpr int kBulkRows = kRbBulkRows;    // rows of a chunk (= consumer warps)
+constexpr int kBulkThreads = 32 * (kBulkRows + 1);  // the consumer warps + the producer warp
+
+struct BulkCtl {
+    uint64_t full[kBulkStages], empty[kBulkStages];
+    int abort;
+};
+
+constexpr int kBulkSmem = 128 + kBulkStages * kBulkStage + (int)sizeof(BulkCtl);
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+                 : "memory");
+}
+
+template <int MAP, int DT>
+__global__ void __launch_bounds__(kBulkThreads, 1) rowreduce_bulk_kernel(const RrParams p) {
+    constexpr bool kB16 = DT == 1;
+    constexpr int kEs = kB16 ? 2 : 4;
+    extern __shared__ uint8_t bulk_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>(((uintptr_t)bulk_raw + 127) & ~(uintptr_t)127);
+    BulkCtl *ctl = reinterpret_cast<BulkCtl *>(ring + kBulkStages * kBulkStage);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t t1 = ((int64_t)blockIdx.x + 1) * p.ntiles / gridDim.x;
+    const int64_t tb = (int64_t)blockIdx.x * p.ntiles / gridDim.x;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kBulkStages; s++) {
+            tc::mbar_init(&ctl->full[s], 1);
+            tc::mbar_init(&ctl->empty[s], kBulkRows);
+        }
+        ctl->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tc::fence_proxy_async();
+    }
+    __syncthreads();
+    volatile int *abort = &ctl->abort;
+    // this CTA's tile descriptors, lane i holding word i, two tiles ahead
+    int64_t wa = tb < t1 ? rb_word(p, tb, lane) : 0, wb = tb + 1 < t1 ? rb_word(p, tb + 1, lane) : 0;
+    uint32_t k = 0;  // chunks so far
+    if (warp == kBulkRows) {
+        // ------------------------------------------------ producer (lane 0 issues)
+        uint32_t armed = 0, par = 0;
+        bool ok = true;
+        for (int64_t t = tb; t < t1 && ok; t++) {
+            const RbUnit d = rb_unpack(wa);
+            wa = wb;
+            if (t + 2 < t1) wb = rb_word(p, t + 2, lane);
+            if constexpr (kBoundsCheck) {
+                if (!rb_in(p, t)) continue;  // the consumers skip it too
+            }
+            for (int r0 = 0; r0 < d.nrows && ok; r0 += kBulkRows) {
+                const int rows = min(kBulkRows, d.nrows - r0);
+                const uint32_t bytes = (uint32_t)(rows * d.len * kEs);
+                for (int i = 0; i < d.n && ok; i++, k++) {
+                    const int s = (int)(k % kBulkStages);
+                    if (lane == 0) {
+                        if (k >= kBulkStages && !tc::mbar_wait(&ctl->empty[s], (k / kBulkStages - 1) & 1, abort, p.err,
+                                                                kDevTimeoutProducer))
+                            ok = false;
+                        if (ok) {
+                            tc::mbar_expect_tx(&ctl->full[s], bytes);
+                            bulk_load(tc::smem_u32(ring + s * kBulkStage),
+                                      p.in[0] + (d.off[i] + (int64_t)r0 * d.rstr[i]) * kEs, bytes, &ctl->full[s]);
+                            armed |= 1u << s;
+                            par = (par & ~(1u << s)) | (((k / kBulkStages) & 1) << s);
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                }
+            }
+        }
+        if (lane == 0 && *abort) {
+            // let this CTA's copies land before it can exit
+            for (int s = 0; s < kBulkStages; s++)
+                if (armed & (1u << s)) tc::mbar_wait(&ctl->full[s], (par >> s) & 1, abort, p.err, 0, tc::kDrainNs, false);
+        }
+    } else {
+        // ------------------------------------------------ consumers: warp w reduces row w of each chunk
+        bool ok = true;
+        for (int64_t t = tb; t < t1 && ok; t++) {
+            const RbUnit d = rb_unpack(wa);
+            wa = wb;
+            if (t + 2 < t1) wb = rb_word(p, t + 2, lane);
+            if constexpr (kBoundsCheck) {
+                if (!rb_in(p, t)) {
+                    if (warp == 0 && lane == 0) bounds_fail(p.err);
+                    continue;
+                }
+            }
+            const int units = (int)(d.len * kEs / 16);  // 16-byte units of a row segment
+            for (int r0 = 0; r0 < d.nrows && ok; r0 += kBulkRows) {
+                const bool live = r0 + warp < d.nrows;
+                uint64_t s2[4] = {0, 0, 0, 0};
+                for (int i = 0; i < d.n; i++, k++) {
+                    const int s = (int)(k % kBulkStages);
+                    if (!tc::warp_wait(&ctl->full[s], (k / kBulkStages) & 1, abort, p.err, kDevTimeoutReduce)) {
+                        ok = false;
+                        break;
+                    }
+                    if (live) {
+                        const uint32_t row = tc::smem_u32(ring + s * kBulkStage) + (uint32_t)(warp * units * 16);
+                        for (int u = lane; u < units; u += 32) {
+                            uint32_t w[4];
+                            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                                         : "r"(row + (uint32_t)(u * 16)));
+                            if constexpr (kB16) {
+#pragma unroll
+                                for (int e = 0; e < 4; e++) {
+                                    const uint64_t x2 = pk2(w[e] << 16, w[e] & 0xFFFF0000u);
+                                    if constexpr (MAP == EA_MAP_SQUARE) s2[e] = ffma2(x2, x2, s2[e]);
+                                    else s2[e] = fadd2(s2[e], x2);
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 2; e++) {
+                                    const uint64_t x2 = pk2(w[2 * e], w[2 * e + 1]);
+                                    if constexpr (MAP == EA_MAP_SQUARE) s2[e] = ffma2(x2, x2, s2[e]);
+                                    else s2[e] = fadd2(s2[e], x2);
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&ctl->empty[s]);
+                }
+                if (!ok) break;
+                float a = pk2_sum(fadd2(fadd2(s2[0], s2[1]), fadd2(s2[2], s2[3])));
+                a *= p.scale;  // the map's scale (IDENTITY: scale v, SQUARE: scale v^2)
+                for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+                if (lane == 0 && live) st_elem(p.out, p.out_dtype, d.out0 + (int64_t)(r0 + warp) * d.ostr, a);
+            }
+        }
+        if (!ok) *abort = 1;
     }
 }
 
@@ -664,6 +815,20 @@ __global__ void __launch_bounds__(kThreads, 2) rowreduce_rowbatch_stats_kernel(c
     }
 }
 
+// The bulk kernel's shared memory is above the default 48 KB: raise the
+// limit once per device.
+template <int MAP, int DT>
+cudaError_t bulk_configure() {
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(rowreduce_bulk_kernel<MAP, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    return e;
+}
+
 template <int AGG, int MAP, int NIN, int MASK>
 cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st, int num_sms) {
     int dt = -1;
@@ -682,6 +847,15 @@ cudaError_t go(const RrParams &p, int64_t grid, cudaStream_t st, int num_sms) {
         }
     }
     if constexpr (AGG == EA_AGG_SUM && (MAP == EA_MAP_SQUARE || MAP == EA_MAP_IDENTITY) && NIN == 1 && MASK == 1) {
+        if (tile && p.row_batch && p.row_bulk && p.rb_desc && dt > 0) {
+            // one CTA per SM (its 128 KB ring), each over a contiguous range of tiles
+            const unsigned g1 = (unsigned)std::min<int64_t>(p.ntiles, (int64_t)num_sms);
+            cudaError_t e = dt == 1 ? bulk_configure<MAP, 1>() : bulk_configure<MAP, 2>();
+            if (e != cudaSuccess) return e;
+            if (dt == 1) rowreduce_bulk_kernel<MAP, 1><<<g1, kBulkThreads, kBulkSmem, st>>>(p);
+            else rowreduce_bulk_kernel<MAP, 2><<<g1, kBulkThreads, kBulkSmem, st>>>(p);
+            return cudaGetLastError();
+        }
         if (tile && p.row_batch && p.rb_desc && dt > 0) {
             // persistent: the CTAs that fit (two per SM) loop over the tiles
             const unsigned g2 = (unsigned)std::min<int64_t>(p.ntiles, 2 * (int64_t)num_sms);

@@ -417,10 +417,27 @@ def test_rowreduce_rowbatch_stats(dtype, shape, parts):
     assert rel_frob(dense64(l), want_l) <= 1e-5
 
 
+def test_rowreduce_scaled_softmax_stats():
+    """MAX_SUMEXP of scale * S with scale 0.25 over row-batch-shaped blocks:
+    m = MAX_t (scale S), l = SUM_t exp(scale S - m) against the oracle."""
+    from tensor_relational_einsum_gb300.relation import Relation
+    S = synth.make("f32", (2, 3, 40, 512), "normal", 27, 0, 3)
+    m = Relation("f32", (2, 3, 40), [2, 3, 2])
+    l = Relation("f32", (2, 3, 40), [2, 3, 2])
+    joinagg("bhst->bhs", [rel(S, [2, 3, 2, 4])], agg="max_sumexp", map="identity", out=m, out2=l, scale=0.25)
+    assert last()["kernel"] == "rowreduce"
+    want_m = oracle.joinagg("bhst->bhs", [S.to_f64()], "identity", "max", scale=0.25)
+    E = oracle.joinagg("bhst,bhs->bhst", [0.25 * S.to_f64(), want_m], "exp_sub", "none")
+    want_l = oracle.joinagg("bhst->bhs", [E], "identity", "sum")
+    assert rel_frob(dense64(m), want_m) <= 1e-6
+    assert rel_frob(dense64(l), want_l) <= 1e-5
+
+
 def test_rowreduce_rowbatch_sum_of_squares_four_pass_tiles():
-    """40960 rows of 4096 bf16 in 8 x 4 blocks: enough rows that the planner
-    cuts row-batch tiles of four row passes (32 rows); 64 sampled rows
-    against the oracle."""
+    """40960 rows of 4096 bf16 in 8 x 4 blocks (2 KB row segments stored
+    back to back: the bulk-copy kernel): enough rows that the planner cuts
+    tiles of 32 rows, four 8-row chunks per block; 64 sampled rows against
+    the oracle."""
     from tensor_relational_einsum_gb300.relation import Relation
     x = synth.make_torch("bf16", (40960, 4096), "normal", 24, 0, 1, device="cuda")
     ms = joinagg("td->t", [Relation.from_dense(x, [8, 4])], agg="sum", map="square", scale=1.0 / 4096,
@@ -431,6 +448,27 @@ def test_rowreduce_rowbatch_sum_of_squares_four_pass_tiles():
     want = oracle.joinagg("td->t", [xs], "square", "sum", scale=1.0 / 4096)
     got = ms.to_dense()[rows].double().cpu().numpy()
     assert rel_frob(got, want) <= 1e-5
+
+
+@pytest.mark.parametrize("dtype,map_,shape,parts", [
+    ("bf16", "square", (300, 1024), [[0, 100, 213, 300], 4]),   # 512-byte segments, ragged 8-row chunks
+    ("f32", "identity", (77, 2048), [[0, 40, 77], 4]),           # 2 KB fp32 segments, one block of odd rows
+    ("bf16", "identity", (90, 8192), [3, 4]),                    # 4 KB segments: the row-batch kernel
+    ("f32", "square", (50, 4096), [2, 2]),                       # 8 KB segments: the row-batch kernel
+    ("f32", "identity", (64, 4096), [2, 8]),                     # eight blocks a row: the tile kernel
+])
+def test_rowreduce_rowbatch_sum_paths(dtype, map_, shape, parts):
+    """SUM (of scale x or scale x^2) over whole rows, every row against the
+    oracle: in at most four equal blocks with row segments of at most 2 KB
+    stored back to back the bulk-copy kernel serves it (chunks of 8 rows of
+    one block, the last chunk of a block ragged), with longer segments the
+    row-batch kernel, with eight blocks the tile kernel's packed row sums.
+    The scale is not 1, so each path must apply it for both maps."""
+    x = synth.make(dtype, shape, "normal", 26, 0, 1)
+    got = joinagg("td->t", [rel(x, parts)], agg="sum", map=map_, scale=1.0 / shape[1], out_dtype="f32")
+    assert last()["kernel"] == "rowreduce"
+    want = oracle.joinagg("td->t", [x.to_f64()], map_, "sum", scale=1.0 / shape[1])
+    assert rel_frob(dense64(got), want) <= 1e-5
 
 
 def test_rowreduce_causal_predicate():
