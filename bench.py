@@ -823,6 +823,14 @@ def profile_case(name: str, reps: int):
         ms = Relation.from_dense(torch.ones(8192, dtype=torch.float32, device=dev), [1])
         fn = lambda: joinagg("td,dfc->tf", [x, w], out=y, epi_map="silu_mul", epi_pair="c",  # noqa: E731
                              row_rms=ms, eps=1e-6)
+    elif name == "gemm_block":  # the block's gate+up launch: x[16384,4096] in 8 x 4 blocks . W[4096, 11008, 2] in 4 x 4 x 1
+        x = Relation.from_dense(synth.make_torch("bf16", (16384, 4096), "normal", 21, 0, 1, device=dev), [8, 4])
+        w = Relation.from_dense(synth.make_torch("bf16", (4096, 11008, 2), "normal", 22, 0, 0.02, device=dev),
+                                [4, 4, 1])
+        y = Relation("bf16", (16384, 11008), [8, 4], device=dev)
+        ms = Relation.from_dense(torch.ones(16384, dtype=torch.float32, device=dev), [8])
+        fn = lambda: joinagg("td,dfc->tf", [x, w], out=y, epi_map="silu_mul", epi_pair="c",  # noqa: E731
+                             row_rms=ms, eps=1e-6)
     elif name == "attn":  # attention chain b1 h32 s=t=2048 d128, t in 4 blocks
         q, k, v = (synth.make_torch("bf16", (1, 32, 2048, 128), "normal", sd, 0, 1, device=dev) for sd in (1, 2, 3))
         ch = AttentionChain(Relation.from_dense(q, [1, 32, 1, 1]), Relation.from_dense(k, [1, 32, 4, 1]),
@@ -888,7 +896,7 @@ def profile_case(name: str, reps: int):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["gemm", "attn", "attn_fused", "attn_c2", "c1", "exchange", "exchange_agg", "norm", "ffn_ew"], default=None)
+    ap.add_argument("--profile-case", choices=["gemm", "gemm_block", "attn", "attn_fused", "attn_c2", "c1", "exchange", "exchange_agg", "norm", "ffn_ew"], default=None)
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)

@@ -14,6 +14,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <map>
 #include <unordered_map>
 
 #include "plan.h"
@@ -917,6 +918,13 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
     const int cl = est_tiles >= 2 * (int64_t)c->num_sms ? 2 : 1;
     // ---- pass 2: tensor maps, tuples, tiles
     std::vector<CUtensorMap> maps;
+    struct Rast {
+        int32_t gid;
+        int64_t nb, nm, nn, band;
+        std::vector<int32_t> key;   // M, batch count, first row, the A tensor map of each tuple
+        std::vector<int32_t> ckey;  // N, batch count, first column, the B tensor map of each tuple
+    };
+    std::vector<Rast> rast;
     std::vector<TcGroup> groups;
     std::vector<TcTuple> tuples;
     std::vector<TcTile> tiles;
@@ -999,27 +1007,134 @@ static ea_status build_tc(JoinCtx &j, const ContractionViews &cv, DevCtx *c, cud
         maps.push_back(m);
         int32_t gid = (int32_t)groups.size();
         groups.push_back(TG);
-        // Grouped raster: bands of kBand m-tiles, each band swept across all
-        // n-tiles with m fastest, so the tiles in flight at once share a
-        // small set of A rows and B columns that stays in L2.  With CTA pairs
-        // the tiles come in pairs of the same n-tile (consecutive m-tiles; a
-        // band with an odd count gets a padding tile past the block's rows).
-        // A band's A rows take about 32 MiB: B is re-read once per band, and
-        // a larger band no longer stays in L2 beside the B columns in flight
-        // (FFN gate+up, 8192 tokens: DRAM reads 907 MB with bands of 16,
-        // 668 MB with 32, 1271 MB with 64).
+        // The group's raster: bands of `band` m-tiles (about 32 MiB of A rows:
+        // B is re-read once per band, and a larger band no longer stays in
+        // L2 beside the B columns in flight -- FFN gate+up, 8192 tokens: DRAM
+        // reads 907 MB with bands of 16, 668 MB with 32, 1271 MB with 64);
+        // the tiles are laid out below, once every group is known.
         const int64_t a_row_bytes = 128 * std::max<int64_t>(1, k_total) * (int64_t)elem_size(j.in[0]->dtype);
-        const int64_t kBand = std::max<int64_t>(8, std::min<int64_t>(64, ((32ll << 20) / a_row_bytes) & ~1ll));
-        const int64_t nm = (G.M + 127) / 128, nn = (G.N + bn - 1) / bn;
-        for (int64_t bb = 0; bb < G.nb; bb++)
-            for (int64_t mb = 0; mb < nm; mb += kBand)
-                for (int64_t ni = 0; ni < nn; ni++) {
-                    const int64_t me = std::min(nm, mb + kBand);
-                    for (int64_t mi = mb; mi < me; mi++)
-                        tiles.push_back(TcTile{gid, (int32_t)bb, (int32_t)(mi * 128), (int32_t)(ni * bn)});
-                    if (cl == 2 && ((me - mb) & 1))
-                        tiles.push_back(TcTile{gid, (int32_t)bb, (int32_t)(me * 128), (int32_t)(ni * bn)});
+        Rast R;
+        R.gid = gid;
+        R.nb = G.nb;
+        R.nm = (G.M + 127) / 128;
+        R.nn = (G.N + bn - 1) / bn;
+        R.band = std::max<int64_t>(8, std::min<int64_t>(64, ((32ll << 20) / a_row_bytes) & ~1ll));
+        R.key.assign(1, (int32_t)G.M);
+        R.key.push_back((int32_t)G.nb);
+        R.key.push_back((int32_t)G.m_lo);
+        for (int32_t t = TG.t0; t < TG.t1; t++) R.key.push_back(tuples[t].a_map);
+        R.ckey.assign(1, (int32_t)G.N);
+        R.ckey.push_back((int32_t)G.nb);
+        R.ckey.push_back((int32_t)G.n_lo);
+        for (int32_t t = TG.t0; t < TG.t1; t++) R.ckey.push_back(tuples[t].b_map);
+        rast.push_back(R);
+    }
+    // Grouped raster over the grid of groups: a group's row key is what it
+    // reads of A (its tuples' A blocks), its column key what it reads of B.
+    // Row keys are taken in order into bands of about 32 MiB of A rows
+    // (whole row keys while they fit, a long one cut into several bands);
+    // each band is swept across every column key's n-tiles with m fastest,
+    // so the tiles in flight at once share a band of A rows and a few B
+    // columns that stay in L2: A is read from DRAM about once, and B once per
+    // band instead of once per row key (FFN gate+up of the block, x in 8 row
+    // blocks: W read 4 times, not 8).  With CTA pairs the tiles come in pairs
+    // of the same n-tile (consecutive m-tiles of one row key; a segment with
+    // an odd count gets a padding tile past the block's rows).
+    {
+        std::map<std::vector<int32_t>, int32_t> row_of, col_of;
+        std::vector<std::vector<size_t>> rows_g;  // row key -> its groups
+        std::vector<int64_t> col_nn;              // column key -> n-tiles
+        std::vector<int32_t> gcol(rast.size());
+        for (size_t r = 0; r < rast.size(); r++) {
+            auto ir = row_of.find(rast[r].key);
+            if (ir == row_of.end()) {
+                row_of.emplace(rast[r].key, (int32_t)rows_g.size());
+                rows_g.push_back(std::vector<size_t>(1, r));
+            } else {
+                rows_g[ir->second].push_back(r);
+            }
+            auto ic = col_of.find(rast[r].ckey);
+            if (ic == col_of.end()) {
+                gcol[r] = (int32_t)col_nn.size();
+                col_of.emplace(rast[r].ckey, gcol[r]);
+                col_nn.push_back(rast[r].nn);
+            } else {
+                gcol[r] = ic->second;
+            }
+        }
+        struct Seg {
+            int32_t row;     // row key
+            int64_t m0, m1;  // its m-tiles [m0, m1)
+        };
+        std::vector<std::vector<Seg>> bands;
+        {
+            std::vector<Seg> cur;
+            int64_t used = 0, budget = 0;
+            for (size_t rk = 0; rk < rows_g.size(); rk++) {
+                const Rast &R = rast[rows_g[rk][0]];
+                for (int64_t m0 = 0; m0 < R.nm;) {
+                    if (cur.empty()) budget = R.band;
+                    int64_t take = std::min(R.nm - m0, budget - used);
+                    // with CTA pairs a segment that stops inside the row key has
+                    // an even count (its padding tile would be a real tile)
+                    if (cl == 2 && m0 + take < R.nm) take &= ~1ll;
+                    if (take <= 0) {
+                        bands.push_back(cur);
+                        cur.clear();
+                        used = 0;
+                        continue;
+                    }
+                    cur.push_back(Seg{(int32_t)rk, m0, m0 + take});
+                    used += take;
+                    m0 += take;
                 }
+            }
+            if (!cur.empty()) bands.push_back(cur);
+        }
+        // (row key, column key) -> the group; per band, the column keys its
+        // groups use, in order of first appearance
+        const int64_t ncol = (int64_t)col_nn.size();
+        std::unordered_map<int64_t, std::vector<size_t>> at;
+        for (size_t rk = 0; rk < rows_g.size(); rk++)
+            for (size_t r : rows_g[rk]) at[(int64_t)rk * ncol + gcol[r]].push_back(r);
+        int64_t nb_max = 0;
+        for (const Rast &R : rast) nb_max = std::max(nb_max, R.nb);
+        std::vector<char> seen(col_nn.size(), 0);
+        std::vector<int32_t> cols;
+        for (int64_t bb = 0; bb < nb_max; bb++)
+            for (const std::vector<Seg> &band : bands) {
+                cols.clear();
+                for (const Seg &sg : band)
+                    for (size_t r : rows_g[sg.row])
+                        if (bb < rast[r].nb && !seen[gcol[r]]) {
+                            seen[gcol[r]] = 1;
+                            cols.push_back(gcol[r]);
+                        }
+                for (int32_t ck : cols) {
+                    seen[ck] = 0;
+                    for (int64_t ni = 0; ni < col_nn[ck]; ni++)
+                        for (const Seg &sg : band) {
+                            const auto it = at.find((int64_t)sg.row * ncol + ck);
+                            if (it == at.end()) continue;
+                            for (size_t r : it->second) {
+                                if (bb >= rast[r].nb) continue;
+                                const int32_t gid = rast[r].gid;
+                                for (int64_t mi = sg.m0; mi < sg.m1; mi++)
+                                    tiles.push_back(TcTile{gid, (int32_t)bb, (int32_t)(mi * 128), (int32_t)(ni * bn)});
+                                if (cl == 2 && ((sg.m1 - sg.m0) & 1))
+                                    tiles.push_back(TcTile{gid, (int32_t)bb, (int32_t)(sg.m1 * 128), (int32_t)(ni * bn)});
+                            }
+                        }
+                }
+            }
+        // every group's tiles are laid out exactly once (padding tiles aside)
+        std::vector<int64_t> got(groups.size(), 0);
+        for (const TcTile &T : tiles)
+            if (T.m0 < groups[T.group].m_ext) got[T.group]++;
+        for (const Rast &R : rast)
+            if (got[R.gid] != R.nb * R.nm * R.nn)
+                return set_error(EA_ERR_UNSUPPORTED, "contraction: raster covers group %d with %lld of %lld tiles",
+                                 R.gid, (long long)got[R.gid], (long long)(R.nb * R.nm * R.nn));
     }
     if (tiles.size() > (size_t)INT32_MAX) return EA_ERR_UNSUPPORTED;
     if (cl == 2) {
