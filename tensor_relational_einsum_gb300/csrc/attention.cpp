@@ -155,7 +155,7 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
     // head dims, and holds one query tile of the pair's two.
     const bool pair = D == 128;
     std::vector<BlockMap> maps;
-    maps.reserve(q->nblocks + 2 * k->nblocks);
+    maps.reserve(2 * q->nblocks + 2 * k->nblocks);
     for (int64_t b = 0; b < q->nblocks; b++) {
         BlockMap bm;
         ea_status s = encode_block(c, q, b, a.qt, a.s, a.shared, &bm);
@@ -171,6 +171,16 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
             maps.push_back(bm);
         }
     const int n_kv = (int)k->nblocks;
+    // CTA pairs store the output through tensor maps over O's blocks (O has
+    // Q's tiling): each softmax warp stores its 32 rows x 64 head dims
+    const int o_map0 = (int)maps.size();
+    if (pair)
+        for (int64_t b = 0; b < q->nblocks; b++) {
+            BlockMap bm;
+            ea_status s = encode_block(c, j.o, b, a.qt, a.s, a.shared, &bm, kTileRows / 4);
+            if (s) return s;
+            maps.push_back(bm);
+        }
     auto seg_of = [&](int64_t pos, int64_t *lo, int64_t *hi) {  // [lo, hi) of the sequence holding pos
         *lo = 0;
         *hi = INT64_MAX;
@@ -248,6 +258,7 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
                         qc[qm.slot[1]] = (int32_t)(nsh > 0 ? x0 : 0);
                         qc[qm.slot[2]] = (int32_t)(nsh > 1 ? x1 : 0);
                         for (int i = 0; i < 3; i++) Q.q_c[i] = qc[i];
+                        Q.pos_slot = qm.slot[0];
                         int64_t a0, a1, b0, b1;
                         seg_of(Q.s_glob0, &a0, &a1);
                         seg_of(Q.s_glob0 + Q.nrows - 1, &b0, &b1);
@@ -392,6 +403,7 @@ ea_status build_attention(const AttnJob &j, DevCtx *c, cudaStream_t st, DevPlan 
     P.ncta = pair ? 2 * ncta : ncta;  // in pairs: cta_ptr indexes pairs
     P.pair = pair ? 1 : 0;
     P.n_kv = n_kv;
+    P.o_map0 = o_map0;
     P.nseq = (int32_t)j.ends.size();
     P.causal = j.causal ? 1 : 0;
     P.scale = j.scale;

@@ -274,7 +274,7 @@ struct AtQTile {
     int32_t q_map;     // tensor map of the Q block
     int32_t q_c[3];    // map coordinates (dims 1..3) of row 0
     int32_t nrows;     // valid query rows (<= 128)
-    int32_t pad;
+    int32_t pos_slot;  // which of q_c is the query position
 };
 
 struct AtItem {
@@ -306,6 +306,7 @@ struct AtParams {
     float *m_out, *l_out;    // optional row statistics (f32 arenas) or null
     int32_t ncta;
     int32_t n_kv;            // number of K (and of V) maps
+    int32_t o_map0;          // CTA pairs: first of the O maps (one per Q block, 32-row boxes), in Q block order
     int32_t nseq;
     int32_t causal;
     float scale;             // score scale (> 0)

@@ -54,10 +54,10 @@
 //              (m, l) are exchanged through shared memory, each thread
 //              stages its 64 values of O = (A_0 a_0 + A_1 a_1) /
 //              (l_0 a_0 + l_1 a_1) in its warp's slice of a staging tile,
-//              and each warp writes its slice as whole 128-byte row
-//              segments.  The query-tile and run descriptors they read sit
-//              in shared memory (copied at the start), so no group start or
-//              end waits on a global load.
+//              and each warp stores its slice (32 rows x 64 head dims) with
+//              one asynchronous TMA tensor store.  The query-tile and run
+//              descriptors they read sit in shared memory (copied at the
+//              start), so no group start or end waits on a global load.
 // Every mbarrier wait is bounded (2 s); on time-out the kernel raises the
 // device error word and every role leaves its loop; no CTA frees TMEM or
 // leaves before the other has finished with it.
@@ -111,7 +111,8 @@ constexpr int kDescItems = 64;
 constexpr int kDescRuns = 256;
 struct DescQ {
     int64_t s_glob0, o_off, o_rstr, ml_off, ml_rstr;
-    int32_t nrows, r0, r1, pad;
+    int32_t nrows, r0, r1, q_map;
+    int32_t q_c[3], pos_slot;  // the tile's map coordinates; which of them is the position
 };
 struct DescRun {
     int64_t t_glob0;
@@ -148,19 +149,23 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void *map, 
         : "memory");
 }
 
+// This warp's staged output rows (a 32-row x 64-column box, 128-byte
+// swizzle) to global memory through the tensor map of the O block.
+__device__ __forceinline__ void tma_store_4d(const void *map, uint32_t src, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(map),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 __device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
-    return v;
-}
-
 // 16-byte unit q of row `row` of a staging tile with 128-byte rows: units
-// are permuted by row mod 8, so that a warp writing one row per lane, and a
-// warp reading four whole rows, both touch every bank once per 128 bytes.
+// are permuted by row mod 8 -- the 128-byte swizzle the output's tensor map
+// reads, with 1024-byte-aligned 8-row atoms -- so a warp writing one row
+// per lane touches every bank once per 128 bytes.
 __device__ __forceinline__ uint32_t sw128_unit(uint32_t tile, int row, int q) {
     return tile + (uint32_t)(row * 128) + (uint32_t)((q ^ (row & 7)) << 4);
 }
@@ -427,7 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_pair_kernel(const AtPar
             d.nrows = Q.nrows;
             d.r0 = it.r0;
             d.r1 = it.r1;
-            d.pad = 0;
+            d.q_map = Q.q_map;
+            for (int i = 0; i < 3; i++) d.q_c[i] = Q.q_c[i];
+            d.pos_slot = Q.pos_slot;
             ctl->dq[t] = d;
         }
         for (int t = (int)threadIdx.x; t < n_dr; t += 256) {
@@ -443,7 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_pair_kernel(const AtPar
             if (ii - i0 >= n_dq) {
                 const AtItem &it = p.items[ii];
                 const AtQTile &G = it.q[rank];
-                if (lane == 0) ctl->dqx[warp] = DescQ{G.s_glob0, G.o_off, G.o_rstr, G.ml_off, G.ml_rstr, G.nrows, it.r0, it.r1, 0};
+                if (lane == 0)
+                    ctl->dqx[warp] = DescQ{G.s_glob0, G.o_off, G.o_rstr, G.ml_off, G.ml_rstr, G.nrows, it.r0, it.r1,
+                                           G.q_map, {G.q_c[0], G.q_c[1], G.q_c[2]}, G.pos_slot};
                 __syncwarp();
                 Qp = &ctl->dqx[warp];
             }
@@ -597,10 +606,13 @@ __global__ void __launch_bounds__(kThreads, 1) attention_pair_kernel(const AtPar
             const float inv = L > 0.f ? 1.f / L : 0.f;
             const float w0 = a0 * inv, w1 = a1 * inv;
             // This thread's 64 output values, staged in its own row of this
-            // warp's slice of the staging tile, then written by the warp as
-            // four rows of 128 contiguous bytes per store instruction.
+            // warp's slice of the staging tile, then written by one tensor
+            // store per warp (asynchronous: the warp moves on to the next
+            // group while the store drains).
             const uint32_t c0row = lane_base + kOCol + (uint32_t)(h * (kD / 2));
             const uint32_t stage = smem_u32(smem + E_OFF + h * (kRows * 128));
+            if (lane == 0) bulk_wait_read0();  // this warp's previous store has read its slice
+            __syncwarp();
 #pragma unroll
             for (int cc = 0; cc < kD / 64; cc++) {
                 uint32_t o0[32], o1[32];
@@ -617,15 +629,20 @@ __global__ void __launch_bounds__(kThreads, 1) attention_pair_kernel(const AtPar
                                  pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
                 }
             }
+            fence_proxy_async();  // each lane's staged row, visible to the bulk store
             __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                const int rr = (warp & 3) * 32 + 4 * i + (lane >> 3), q = lane & 7;
-                const uint4 v = ld_shared_v4(sw128_unit(stage, rr, q));
-                if (rr < nrows && in)
-                    reinterpret_cast<uint4 *>(p.o + (Q.o_off + (int64_t)rr * Q.o_rstr + h * (kD / 2)) * 2)[q] = v;
+            {
+                // one store per warp; rows past the tile are past the O block
+                // (TMA clips them), a warp whose rows all are stores nothing
+                const int r0 = (warp & 3) * 32;
+                if (lane == 0 && r0 < nrows && in) {
+                    int32_t cc[3] = {Q.q_c[0], Q.q_c[1], Q.q_c[2]};
+                    cc[Q.pos_slot] += r0;
+                    tma_store_4d(maps + p.o_map0 + Q.q_map, stage + (uint32_t)(r0 * 128), h * (kD / 2), cc[0], cc[1],
+                                 cc[2]);
+                    bulk_commit();
+                }
             }
-            __syncwarp();
             if (h == 0 && p.m_out && row < nrows && in) {
                 const int64_t o = Q.ml_off + (int64_t)row * Q.ml_rstr;
                 const float mm = fmaxf(c0.z, c1.z);
@@ -641,6 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_pair_kernel(const AtPar
             if (lane == 0) arrive_on_rank0(&ctl->e_done, rank);
             qi++;
         }
+        if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
+        __syncwarp();
         if (!ok) *abort = 1;
     }
 
