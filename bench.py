@@ -112,6 +112,14 @@ class Clocks:
                                          stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        # nvidia-smi takes a while to start: the timed region begins once
+        # the first sample is in (or after 5 s)
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
 
     def stop(self):
         if self.proc is None:
@@ -899,7 +907,7 @@ def main():
     ap.add_argument("--profile-case", choices=["gemm", "gemm_block", "attn", "attn_fused", "attn_c2", "c1", "exchange", "exchange_agg", "norm", "ffn_ew"], default=None)
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-tokens", type=int, default=192,
