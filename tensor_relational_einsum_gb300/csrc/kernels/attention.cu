@@ -38,7 +38,8 @@
 //   warp 8     TMA: Q tiles (one buffer per X), K and V of a key tile into
 //              one stage of a two-stage ring with one barrier (128-byte
 //              swizzle, one [128 x 64] box per 64 head-dim columns).
-//   warp 9     TMEM owner and MMA issuer (one thread).  Per X and key tile
+//   warp 9     TMEM owner and MMA issuer (the whole warp runs the loop with
+//              warp-wide waits; one elected lane issues).  Per X and key tile
 //              j (the first nt[X] tiles of the item: X stops after the last
 //              tile it keeps): S_X = Q_X K_j^T; after the softmax of X has written P_X,
 //              O_X (+)= P_X V_j with P_X read from TMEM, then at once
@@ -207,8 +208,8 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
             }
         }
     } else if (warp == 9) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
+        {
+            // ------------------------------------------------ MMA issuer (the whole warp; one elected lane issues)
             const uint32_t idesc_s = make_idesc(kRows, kKeys, 0, 0);  // Q (K-major) x K (K-major)
             const uint32_t idesc_o = make_idesc(kRows, D, 0, 1);      // P (TMEM) x V (MN-major)
             // key tiles; items and tiles per query slot (scalars: no local-memory arrays)
@@ -220,22 +221,32 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                 const uint64_t qd = sdesc(smem_u32(smem + C::Q_OFF + x * C::TILE), 16, 1024);
                 const uint64_t kd = sdesc(smem_u32(smem + C::K_OFF + (t % kKvStages) * C::TILE), 16, 1024);
                 const uint32_t d = tmem + (uint32_t)(x * kKeys);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; kk++)
-                    umma_bf16(d, qd + (uint64_t)sdesc_off((kk >> 2) * (kRows * 128) + (kk & 3) * 32),
-                              kd + (uint64_t)sdesc_off((kk >> 2) * (kKeys * 128) + (kk & 3) * 32), idesc_s,
-                              kk > 0 ? 1u : 0u);
-                umma_commit(&ctl->s_full[x]);
+                    for (int kk = 0; kk < D / 16; kk++)
+                        umma_bf16(d, qd + (uint64_t)sdesc_off((kk >> 2) * (kRows * 128) + (kk & 3) * 32),
+                                  kd + (uint64_t)sdesc_off((kk >> 2) * (kKeys * 128) + (kk & 3) * 32), idesc_s,
+                                  kk > 0 ? 1u : 0u);
+                    umma_commit(&ctl->s_full[x]);
+                }
+                __syncwarp();
             };
             // O_x (+)= P_x V_t, P_x in the first 64 columns of S_x
             auto mma_o = [&](int x, uint32_t t, bool first) {
                 const uint64_t vd = sdesc(smem_u32(smem + C::V_OFF + (t % kKvStages) * C::TILE), kKeys * 128, 1024);
                 const uint32_t pa = tmem + (uint32_t)(x * kKeys);
                 const uint32_t d = tmem + kOCol + (uint32_t)(x * D);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 16; kk++)
-                    umma_bf16_ts(d, pa + kk * 8, vd + (uint64_t)sdesc_off(kk * 2048), idesc_o,
-                                 (!first || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kKeys / 16; kk++)
+                        umma_bf16_ts(d, pa + kk * 8, vd + (uint64_t)sdesc_off(kk * 2048), idesc_o,
+                                     (!first || kk > 0) ? 1u : 0u);
+                }
+                __syncwarp();
+            };
+            auto commit1 = [&](uint64_t *b) {
+                if (elect_one()) umma_commit(b);
+                __syncwarp();
             };
             for (int ii = i0; ii < i1 && ok; ii++) {
                 const AtItem &it = p.items[ii];
@@ -243,12 +254,12 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                 if (n == 0) continue;
                 const int nt0 = it.nt[0], nt1 = nq > 1 ? it.nt[1] : 0;  // scalars: no local-memory array
                 // first scores of the item
-                if (!mbar_wait(&ctl->kv_full[ct % kKvStages], (ct / kKvStages) & 1, abort, p.err, kDevTimeoutMma)) {
+                if (!warp_wait(&ctl->kv_full[ct % kKvStages], (ct / kKvStages) & 1, abort, p.err, kDevTimeoutMma)) {
                     ok = false;
                     break;
                 }
                 for (int x = 0; x < nq && ok; x++) {
-                    if (!mbar_wait(&ctl->q_full[x], (x == 0 ? qx0 : qx1) & 1, abort, p.err, kDevTimeoutMma)) {
+                    if (!warp_wait(&ctl->q_full[x], (x == 0 ? qx0 : qx1) & 1, abort, p.err, kDevTimeoutMma)) {
                         ok = false;
                         break;
                     }
@@ -256,7 +267,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                     else qx1++;
                     tc_fence_after();
                     mma_s(x, ct);
-                    if ((x == 0 ? nt0 : nt1) == 1) umma_commit(&ctl->q_empty[x]);
+                    if ((x == 0 ? nt0 : nt1) == 1) commit1(&ctl->q_empty[x]);
                 }
                 if (!ok) break;
                 for (int j = 0; j < n && ok; j++) {
@@ -266,16 +277,16 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                         const int ntx = x == 0 ? nt0 : nt1;
                         if (j >= ntx) continue;  // the rest of the item is masked for x
                         // V of tile t arrived with its K (waited for before S of tile t)
-                        if (!mbar_wait(&ctl->p_full[x], ((x == 0 ? tx0 : tx1) + j) & 1, abort, p.err, kDevTimeoutMma)) {
+                        if (!warp_wait(&ctl->p_full[x], ((x == 0 ? tx0 : tx1) + j) & 1, abort, p.err, kDevTimeoutMma)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         mma_o(x, t, j == 0);
-                        if (j == ntx - 1) umma_commit(&ctl->o_fin[x]);
+                        if (j == ntx - 1) commit1(&ctl->o_fin[x]);
                         if (j + 1 < ntx) {
                             if (!kv_next) {
-                                if (!mbar_wait(&ctl->kv_full[(t + 1) % kKvStages], ((t + 1) / kKvStages) & 1, abort,
+                                if (!warp_wait(&ctl->kv_full[(t + 1) % kKvStages], ((t + 1) / kKvStages) & 1, abort,
                                                p.err, kDevTimeoutMma)) {
                                     ok = false;
                                     break;
@@ -283,19 +294,20 @@ __global__ void __launch_bounds__(kAtThreads, 1) attention_kernel(const AtParams
                                 kv_next = true;
                             }
                             mma_s(x, t + 1);
-                            if (j + 1 == ntx - 1) umma_commit(&ctl->q_empty[x]);
+                            if (j + 1 == ntx - 1) commit1(&ctl->q_empty[x]);
                         }
                     }
                     if (!ok) break;
-                    umma_commit(&ctl->kv_empty[t % kKvStages]);  // K and V of tile t are done
+                    commit1(&ctl->kv_empty[t % kKvStages]);  // K and V of tile t are done
                 }
                 ct += n;
                 tx0 += nt0;
                 tx1 += nt1;
             }
             // Every MMA this thread issued has completed once mma_done flips.
-            umma_commit(&ctl->mma_done);
-            mbar_wait(&ctl->mma_done, 0, abort, p.err, kDevTimeoutMma, kTimeoutNs, false);
+            commit1(&ctl->mma_done);
+            if (lane == 0) mbar_wait(&ctl->mma_done, 0, abort, p.err, kDevTimeoutMma, kTimeoutNs, false);
+            __syncwarp();
         }
     } else if (warp < 8) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
