@@ -182,6 +182,43 @@ __device__ __forceinline__ void commit_both(uint64_t *b) {
     umma_commit_pair(mapa_u32(smem_u32(b), 1));
 }
 
+// Drop the keys of a 32-key chunk (chain columns [q0, q0 + 32)) outside
+// this row's visible columns [jlo, jhi]; returns the maximum of the rest.
+__device__ __forceinline__ float mask_chunk(uint32_t *u, int q0, int jlo, int jhi) {
+#pragma unroll
+    for (int q = 0; q < 32; q++)
+        if (q0 + q < jlo || q0 + q > jhi) u[q] = __float_as_uint(-INFINITY);
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 32; q += 8) {
+        m0 = max3(m0, __uint_as_float(u[q]), __uint_as_float(u[q + 1]));
+        m1 = max3(m1, __uint_as_float(u[q + 2]), __uint_as_float(u[q + 3]));
+        m2 = max3(m2, __uint_as_float(u[q + 4]), __uint_as_float(u[q + 5]));
+        m3 = max3(m3, __uint_as_float(u[q + 6]), __uint_as_float(u[q + 7]));
+    }
+    return fmaxf(max3(m0, m1, m2), m3);
+}
+
+// Exponentials of one 32-key chunk, 2^(c s - base), packed two per word into
+// u[Q0, Q0 + 16) (P's bf16 pairs), the pair-sums added into ls.
+template <int Q0>
+__device__ __forceinline__ void exp_chunk(uint32_t *u, uint64_t c2, uint64_t nb2, uint64_t *ls) {
+#pragma unroll
+    for (int q = Q0; q < Q0 + 16; q++) {
+        const uint64_t y = fma_f32x2(pack_u32x2(u[2 * q], u[2 * q + 1]), c2, nb2);
+        const float e0 = ex2(lo_f32(y)), e1 = ex2(hi_f32(y));
+        ls[q & 3] = add_f32x2(ls[q & 3], pack_f32x2(e0, e1));
+        u[q] = pack_bf16(e0, e1);
+    }
+}
+
+// P of a chunk with no visible key: zero.
+template <int Q0>
+__device__ __forceinline__ void zero_chunk(uint32_t *u) {
+#pragma unroll
+    for (int q = Q0; q < Q0 + 16; q++) u[q] = 0u;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attention_pair_kernel(const AtParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -500,22 +537,23 @@ __global__ void __launch_bounds__(kThreads, 1) attention_pair_kernel(const AtPar
                     const int nv = min(kHalf, R.nkeys - kKeys * k - h * kHalf);
                     const int jlo = (int)max64(0, min64(kHalf, lo_t - t0));
                     const int jhi = (int)max64(-1, min64(nv - 1, hi_t - t0));
-                    float mx = fmaxf(hm0, hm1);
-                    if (jlo > 0 || jhi < kHalf - 1) {
-                        // a masked half tile: drop the removed keys and take the maximum again
-#pragma unroll
-                        for (int q = 0; q < kHalf; q++)
-                            if (q < jlo || q > jhi) u[q] = __float_as_uint(-INFINITY);
-                        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-                        for (int q = 0; q < kHalf; q += 8) {
-                            mx0 = max3(mx0, __uint_as_float(u[q]), __uint_as_float(u[q + 1]));
-                            mx1 = max3(mx1, __uint_as_float(u[q + 2]), __uint_as_float(u[q + 3]));
-                            mx2 = max3(mx2, __uint_as_float(u[q + 4]), __uint_as_float(u[q + 5]));
-                            mx3 = max3(mx3, __uint_as_float(u[q + 6]), __uint_as_float(u[q + 7]));
-                        }
-                        mx = fmaxf(max3(mx0, mx1, mx2), mx3);
+                    // Each 32-key chunk is, for the whole warp, all dropped (no exponentials: P is
+                    // zero there), all kept (the maximum comes from the load) or mixed (masked key
+                    // by key and its maximum taken again).  Rows are consecutive positions, so on
+                    // a diagonal tile at most one chunk of a warp is mixed.
+                    bool live0 = true, live1 = true;
+                    const bool masked = __any_sync(0xffffffffu, jlo > 0 || jhi < kHalf - 1);
+                    if (masked) {
+                        live0 = __any_sync(0xffffffffu, jlo < 32 && jhi >= 0);
+                        live1 = __any_sync(0xffffffffu, jlo < kHalf && jhi >= 32);
+                        const bool mix0 = __any_sync(0xffffffffu, jlo > 0 || jhi < 31);
+                        const bool mix1 = __any_sync(0xffffffffu, jlo > 32 || jhi < kHalf - 1);
+                        if (!live0) hm0 = -INFINITY;
+                        else if (mix0) hm0 = mask_chunk(u, 0, jlo, jhi);
+                        if (!live1) hm1 = -INFINITY;
+                        else if (mix1) hm1 = mask_chunk(u + 32, 32, jlo, jhi);
                     }
+                    const float mx = fmaxf(hm0, hm1);
                     m_max = fmaxf(m_max, mx);
                     // move the reference maximum only when exponentials would pass 2^kLazy
                     float alpha = 1.f;
@@ -527,12 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1) attention_pair_kernel(const AtPar
                     // two scores per packed f32x2 FMA and add; four running pair-sums
                     const uint64_t c2 = pack_f32x2(c, c), nb2 = pack_f32x2(-base, -base);
                     uint64_t ls[4] = {0, 0, 0, 0};
-#pragma unroll
-                    for (int q = 0; q < kHalf / 2; q++) {
-                        const uint64_t y = fma_f32x2(pack_u32x2(u[2 * q], u[2 * q + 1]), c2, nb2);
-                        const float e0 = ex2(lo_f32(y)), e1 = ex2(hi_f32(y));
-                        ls[q & 3] = add_f32x2(ls[q & 3], pack_f32x2(e0, e1));
-                        u[q] = pack_bf16(e0, e1);
+                    if (!masked) {
+                        // one straight run of 32 pairs: the common case, scheduled as a whole
+                        exp_chunk<0>(u, c2, nb2, ls);
+                        exp_chunk<16>(u, c2, nb2, ls);
+                    } else {
+                        if (live0) exp_chunk<0>(u, c2, nb2, ls);
+                        else zero_chunk<0>(u);
+                        if (live1) exp_chunk<16>(u, c2, nb2, ls);
+                        else zero_chunk<16>(u);
                     }
                     const uint64_t s01 = add_f32x2(add_f32x2(ls[0], ls[1]), add_f32x2(ls[2], ls[3]));
                     l = fmaf(l, alpha, lo_f32(s01) + hi_f32(s01));
