@@ -27,6 +27,11 @@
 // chain's row moves only when a half tile's maximum exceeds it by more than
 // 2^kLazy in exp (its A row is then rescaled in TMEM); kLazy = 64, as in
 // the single-CTA kernel, for which attention.cu gives the range argument.
+// On a tile the predicate cuts (the causal diagonal, a sequence boundary,
+// the ragged last tile of a run) each 32-key chunk of a warp's scores is,
+// for the warp's 32 rows, all dropped (its P is zero, no exponentials),
+// all kept, or mixed (masked key by key): the diagonal costs little more
+// than a full tile.
 //
 // TMEM of each CTA (512 columns): two score buffers S_0 [0, 128) and
 // S_1 [128, 256) (key tile g's scores go to S_(g mod 2), so the scores of
@@ -180,43 +185,6 @@ __device__ __forceinline__ void arrive_on_rank0(uint64_t *b, int rank) {
 __device__ __forceinline__ void commit_both(uint64_t *b) {
     umma_commit_pair(smem_u32(b));
     umma_commit_pair(mapa_u32(smem_u32(b), 1));
-}
-
-// Drop the keys of a 32-key chunk (chain columns [q0, q0 + 32)) outside
-// this row's visible columns [jlo, jhi]; returns the maximum of the rest.
-__device__ __forceinline__ float mask_chunk(uint32_t *u, int q0, int jlo, int jhi) {
-#pragma unroll
-    for (int q = 0; q < 32; q++)
-        if (q0 + q < jlo || q0 + q > jhi) u[q] = __float_as_uint(-INFINITY);
-    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < 32; q += 8) {
-        m0 = max3(m0, __uint_as_float(u[q]), __uint_as_float(u[q + 1]));
-        m1 = max3(m1, __uint_as_float(u[q + 2]), __uint_as_float(u[q + 3]));
-        m2 = max3(m2, __uint_as_float(u[q + 4]), __uint_as_float(u[q + 5]));
-        m3 = max3(m3, __uint_as_float(u[q + 6]), __uint_as_float(u[q + 7]));
-    }
-    return fmaxf(max3(m0, m1, m2), m3);
-}
-
-// Exponentials of one 32-key chunk, 2^(c s - base), packed two per word into
-// u[Q0, Q0 + 16) (P's bf16 pairs), the pair-sums added into ls.
-template <int Q0>
-__device__ __forceinline__ void exp_chunk(uint32_t *u, uint64_t c2, uint64_t nb2, uint64_t *ls) {
-#pragma unroll
-    for (int q = Q0; q < Q0 + 16; q++) {
-        const uint64_t y = fma_f32x2(pack_u32x2(u[2 * q], u[2 * q + 1]), c2, nb2);
-        const float e0 = ex2(lo_f32(y)), e1 = ex2(hi_f32(y));
-        ls[q & 3] = add_f32x2(ls[q & 3], pack_f32x2(e0, e1));
-        u[q] = pack_bf16(e0, e1);
-    }
-}
-
-// P of a chunk with no visible key: zero.
-template <int Q0>
-__device__ __forceinline__ void zero_chunk(uint32_t *u) {
-#pragma unroll
-    for (int q = Q0; q < Q0 + 16; q++) u[q] = 0u;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attention_pair_kernel(const AtParams p) {
