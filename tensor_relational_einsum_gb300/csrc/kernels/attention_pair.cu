@@ -614,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_pair_kernel(const AtPar
             const float L = c0.y * a0 + c1.y * a1;
             const float inv = L > 0.f ? 1.f / L : 0.f;
             const float w0 = a0 * inv, w1 = a1 * inv;
+            const uint64_t w0x2 = pack_f32x2(w0, w0), w1x2 = pack_f32x2(w1, w1);
             // This thread's 64 output values, staged in its own row of this
             // warp's slice of the staging tile, then written by one tensor
             // store per warp (asynchronous: the warp moves on to the next
@@ -630,12 +631,15 @@ __global__ void __launch_bounds__(kThreads, 1) attention_pair_kernel(const AtPar
                 tmem_wait_ld();
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
-                    float f[8];
+                    uint32_t b[4];  // A_0 a_0 + A_1 a_1, two columns per packed multiply and FMA
 #pragma unroll
-                    for (int e = 0; e < 8; e++)
-                        f[e] = __uint_as_float(o0[8 * q + e]) * w0 + __uint_as_float(o1[8 * q + e]) * w1;
-                    st_shared_v4(sw128_unit(stage, row, 4 * cc + q), pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                                 pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                    for (int e = 0; e < 4; e++) {
+                        const int i = 8 * q + 2 * e;
+                        const uint64_t y = fma_f32x2(pack_u32x2(o1[i], o1[i + 1]), w1x2,
+                                                     mul_f32x2(pack_u32x2(o0[i], o0[i + 1]), w0x2));
+                        b[e] = pack_bf16(lo_f32(y), hi_f32(y));
+                    }
+                    st_shared_v4(sw128_unit(stage, row, 4 * cc + q), b[0], b[1], b[2], b[3]);
                 }
             }
             fence_proxy_async();  // each lane's staged row, visible to the bulk store
