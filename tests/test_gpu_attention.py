@@ -93,6 +93,17 @@ def test_packed_sequences_head_dim_64(causal):
          causal=causal, seq_ends=[100, 260, 512])
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_sequences_head_dim_128(causal):
+    # CTA pairs (d = 128): sequences ending at 100, 260, 333 and 512, so the
+    # boundaries fall inside 32-key chunks and inside warps (rows 96-127 hold
+    # the end of the first sequence and the start of the second); g = 2
+    Q = synth.make("bf16", (1, 512, 4, 128), "normal", 56, 0, 1)
+    K, V = (synth.make("bf16", (1, 512, 2, 128), "normal", sd, 0, 1) for sd in (57, 58))
+    _run("bshd,bthd,bthd->bshd", Q, K, V, [1, 2, 1, 1], [1, [0, 100, 300, 512], 1, 1], "bshd", group=2,
+         causal=causal, seq_ends=[100, 260, 333, 512])
+
+
 def test_rank3_terms():
     from tensor_relational_einsum_gb300.relation import attention
     Q, K, V = (synth.make("bf16", (200, 3, 128), "normal", sd, 0, 1) for sd in (53, 54, 55))
